@@ -1,0 +1,255 @@
+/*
+ * mok.h -- C ABI of the GB300 (sm_103a) MoE layer library, libmok.so.
+ *
+ * The layer is the routed SwiGLU mixture-of-experts layer of the
+ * Mixture-of-Kittens pages, on one GPU: a device-side schedule, dispatch
+ * (gather by expert), expert-grouped GEMMs W1|W3 -> SwiGLU -> W2, a
+ * deterministic weighted combine, and the full backward with the
+ * router-score gradient fused into the SwiGLU backward.  BF16 and MXFP8.
+ *
+ * Citations name the page and its section:
+ *   [MoK]  "Mixture-of-Kittens (MoK)" project summary (English): sections
+ *          "What it is", "Use the functional API", "Core concepts",
+ *          "Limitations / considerations".
+ *   [MTP]  "Cursor Open-Sources Mixture-of-Kittens (MoK): A Deterministic MoE
+ *          Training Megakernel for GB300 NVL72 Racks": section "Three design
+ *          decisions that matter" (paragraphs: communication direction,
+ *          overlap granularity, ring token buffer) and the paragraph after it.
+ *   [NOTE] "Mixture-of-Kittens: our open-source MoE megakernel for NVL72s",
+ *          section 2 (minibatch) and section 3 (ring token buffer).
+ *
+ * Conventions for every call
+ *  - Pointers marked (device) are CUDA device pointers on the current device;
+ *    the library reads or writes them only from kernels enqueued on `stream`
+ *    (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ *  - Ownership: the caller allocates and frees every buffer, including the
+ *    workspace and the forward context ("you manage all tensors yourself",
+ *    [MoK] "Core concepts", ops-layer row).  The library allocates no device
+ *    memory and keeps no per-call global state.
+ *  - Asynchrony: calls only enqueue work; none synchronises or reads device
+ *    data back to the host.
+ *  - Errors found on the host (null pointers, unsupported shapes, too small a
+ *    workspace, comm_sms != 0) return before anything is enqueued.  Errors
+ *    found on the device (an expert id outside [0, E), a bounded wait that
+ *    ran out) are recorded in the workspace's error word and reported by
+ *    mok_check().  Outputs of a call that recorded a device error are
+ *    unspecified.
+ *  - Layouts are row-major and dense.  Shapes: T tokens, H hidden size,
+ *    I expert intermediate size, E experts, k experts per token,
+ *    R = T*k routed rows, flat routed index f = t*k + j.
+ *  - Supported sizes: H % 128 == 0, I % 128 == 0, 1 <= k <= 32,
+ *    1 <= E <= 1024, T >= 1, T*k < 2^31 / max(H, 2I).
+ */
+#ifndef MOK_H_
+#define MOK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOK_OK = 0,
+  MOK_ERR_INVALID_ARG = 1,         /* null pointer, bad shape or config value */
+  MOK_ERR_UNSUPPORTED = 2,         /* a size or mode this build does not support */
+  MOK_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < mok_workspace_size() */
+  MOK_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed */
+  MOK_ERR_BAD_INDEX = 5,           /* device: an expert id outside [0, E) */
+  MOK_ERR_TIMEOUT = 6              /* device: a bounded wait ran out */
+} mok_status;
+
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
+
+typedef struct {
+  int32_t T, H, I, E, k;
+} mok_shape;
+
+/*
+ * Tunable knobs ([MoK] "Core concepts", Config row: communication SM count,
+ * minibatch granularity, macrobatch size, schedule capacity multiplier; the
+ * pages name a fifth knob without saying what it is, so it is not invented).
+ *
+ * minibatch_rows  Routed (expert-sorted, padded) rows per minibatch of the
+ *                 forward ring; a multiple of 128, or 0 for the default:
+ *                 the two-wave floor 2*C*128*256/min(2I, H) ([MTP]
+ *                 overlap-granularity paragraph, [NOTE] section 2) with C
+ *                 the device's SM count, rounded up to a multiple of 128.
+ * ring_slots      Minibatch slots in the ring token buffer (the macrobatch,
+ *                 [MTP] ring-token-buffer paragraph); >= 2, or 0 for 4.
+ * capacity_mult   Schedule capacity multiplier.  On one GPU the schedule is
+ *                 always sized for the worst case (R + E*127 padded rows),
+ *                 so no token is ever dropped; accepted values are 0 (= 1)
+ *                 and >= 1, and values above 1 change nothing.
+ * comm_sms        SMs reserved for inter-GPU transfers.  There are none on
+ *                 one GPU: must be 0.
+ * debug_flags     0 in normal use.  Bit 0 (MOK_DEBUG_SKIP_RING_SIGNAL):
+ *                 the forward ring producer skips one completion signal, so
+ *                 its consumer's bounded wait runs out and the call records
+ *                 MOK_ERR_TIMEOUT -- a host-chosen fault used to test the
+ *                 failure path without faulting the GPU.
+ */
+typedef struct {
+  int32_t minibatch_rows;
+  int32_t ring_slots;
+  float capacity_mult;
+  int32_t comm_sms;
+  int32_t debug_flags;
+} mok_config;
+
+#define MOK_DEBUG_SKIP_RING_SIGNAL 1
+
+/* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
+typedef struct {
+  const uint8_t* q;     /* (device) E4M3 codes, the shape of the source */
+  const uint8_t* scale; /* (device) E8M0 scales, one per 32-element block */
+} mok_mx;
+
+/* Byte offsets of the schedule arrays inside the workspace, for inspection
+ * (all int32, device).  Capacities are host-known upper bounds; the used
+ * lengths are on the device (header words). */
+typedef struct {
+  size_t header;          /* int32[16]: [0] error bits, [1] padded rows used,
+                             [2] M-tiles used */
+  size_t counts;          /* [E]    rows routed to each expert */
+  size_t offsets;         /* [E+1]  exclusive scan of counts */
+  size_t padded_offsets;  /* [E+1]  exclusive scan of ceil(counts/128)*128 */
+  size_t perm;            /* [R]    sorted row r -> flat index f */
+  size_t inv_perm;        /* [R]    f -> r */
+  size_t pad_perm;        /* [pad_capacity] padded row -> f, or -1 */
+  size_t pad_inv;         /* [R]    f -> padded row */
+  size_t tile_expert;     /* [tile_capacity] expert of each 128-row tile */
+  int64_t pad_capacity;   /* rows: (R + E*127) rounded down to 128 */
+  int64_t tile_capacity;  /* pad_capacity / 128 */
+} mok_layout;
+
+/* Bytes of device workspace a layer of this shape/config/precision needs. */
+size_t mok_workspace_size(const mok_shape* shape, const mok_config* cfg, mok_precision prec);
+
+/* Bytes of the forward context (saved activations) forward writes and
+ * backward reads: [h|u] for every padded routed row, bf16. */
+size_t mok_ctx_size(const mok_shape* shape, const mok_config* cfg, mok_precision prec);
+
+/* Offsets of the schedule arrays in the workspace (host-only, no device work). */
+mok_status mok_workspace_layout(const mok_shape* shape, const mok_config* cfg, mok_precision prec,
+                                mok_layout* out);
+
+/*
+ * Build the schedule: the one table that serves forward dispatch and
+ * combine and the backward's reverse combine and reverse dispatch ([MTP]
+ * communication-direction paragraph), on the device with no host readback
+ * ([MTP] ring-token-buffer paragraph: the CPU stays out of the loop).
+ *
+ *   topk_idx  (device) int32 [T, k]: expert of each routed row.
+ * Computes the expert histogram, its exclusive scan, the stable
+ * permutation (key = expert, ties by ascending f), the 128-row padded
+ * offsets, the tile table and the inverse permutations, in the workspace.
+ * An id outside [0, E) records MOK_ERR_BAD_INDEX; that row is routed
+ * nowhere and contributes zero.  Clears the workspace error word first.
+ */
+mok_status mok_build_schedule(const mok_shape* shape, const mok_config* cfg, void* ws, size_t ws_bytes,
+                              const int32_t* topk_idx, void* stream);
+
+/*
+ * Forward ([MoK] "Use the functional API": forward(config, workspace,
+ * schedule, ...) -> (out, fwd_ctx)).  Needs the schedule of the same routing.
+ *
+ *   x       (device) bf16 [T, H]
+ *   scores  (device) f32  [T, k]   router scores s[t, j] (combine weights)
+ *   W1, W3  (device) gate / up projections [E, H, I]:
+ *             MOK_BF16:  const bf16*
+ *             MOK_MXFP8: const mok_mx* (host struct), quantised along H
+ *                        (block_axis 0 of each [H, I] matrix)
+ *   W2      (device) down projection [E, I, H]:
+ *             MOK_BF16:  const bf16*
+ *             MOK_MXFP8: const mok_mx*, quantised along I (block_axis 0)
+ *   out     (device) bf16 [T, H]
+ *           out[t] = sum_{j=0..k-1} s[t,j] * y[t*k+j], summed in f32 in
+ *           increasing j and rounded once, where
+ *           y = (silu(x W1_e) * (x W3_e)) W2_e for e = topk_idx[t, j].
+ *   ctx     (device) mok_ctx_size() bytes, written; read by mok_backward.
+ * Deterministic: bitwise-identical results for identical inputs.
+ */
+mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precision prec, void* ws,
+                       size_t ws_bytes, const void* x, const float* scores, const void* W1, const void* W3,
+                       const void* W2, void* out, void* ctx, void* stream);
+
+/*
+ * Backward ([MoK] "Use the functional API": backward(config, workspace,
+ * schedule, fwd_ctx, ...) -> grads).  The router-score gradient is taken in
+ * the SwiGLU-backward epilogue ([MTP], the paragraph after "Three design
+ * decisions that matter": router gradients fused into the SwiGLU backward).
+ *
+ *   ctx      (device) the forward's context, same routing and inputs
+ *   x, scores, W1, W3, W2   as for mok_forward, except that in MXFP8 mode
+ *            the weights are passed in the orientation the backward GEMMs
+ *            contract over: W1, W3 quantised along I (block_axis 1), W2
+ *            quantised along H (block_axis 1).
+ *   dout     (device) bf16 [T, H]   dL/d out
+ *   dX       (device) bf16 [T, H]   dL/dx
+ *   dW1,dW3  (device) bf16 [E, H, I]; dW2 (device) bf16 [E, I, H].
+ *            Experts with no routed rows get exact zeros.
+ *   dscores  (device) f32 [T, k]    dL/ds[t, j] = <dout_t, y_(t,j)>
+ * Deterministic: fixed reduction orders, no floating-point atomics.
+ */
+mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_precision prec, void* ws,
+                        size_t ws_bytes, const void* ctx, const void* x, const float* scores, const void* W1,
+                        const void* W3, const void* W2, const void* dout, void* dX, void* dW1, void* dW3,
+                        void* dW2, float* dscores, void* stream);
+
+/*
+ * MXFP8 block quantisation ([MoK] "Core concepts", MXFP8 row: weights are
+ * pre-quantised with ops.mxfp8_quantize before the kernel).
+ *
+ *   src    (device) bf16 [batch, rows, cols]
+ *   block_axis 0: blocks of 32 consecutive rows in each column
+ *                 (rows % 32 == 0); scale is [batch, rows/32, cols]
+ *              1: blocks of 32 consecutive columns in each row
+ *                 (cols % 32 == 0); scale is [batch, rows, cols/32]
+ *   q      (device) u8 [batch, rows, cols] E4M3 codes
+ *   scale  (device) u8 E8M0 codes (biased exponent, bias 127)
+ * Rule (OCP MX v1.0): X = floor(log2(amax)) - 8 clamped to [-127, 127]
+ * (X = -127 for an all-zero block); q = RNE(v / 2^X) on the E4M3 grid,
+ * saturating at +-448; a negative value that rounds to zero is 0x80.
+ */
+mok_status mok_mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t block_axis,
+                              uint8_t* q, uint8_t* scale, void* stream);
+
+/*
+ * Dispatch as a standalone copy: xg[r] = x[token of padded row r] for every
+ * padded row of the schedule (zeros for padding rows).  The layer itself
+ * fuses this gather into its GEMMs' loads; this entry point exposes it on
+ * its own ([MTP] communication-direction paragraph: pull-based dispatch).
+ *   x   (device) bf16 [T, H];  xg (device) bf16 [pad_capacity, H]
+ */
+mok_status mok_gather_rows(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                           const void* x, void* xg, void* stream);
+
+/*
+ * The tensor-core GEMM the layer's grouped GEMMs are built on, on one dense
+ * problem (a diagnostic of the core: tile pipeline, operand layouts).
+ *   C (device) f32 [M, N] = A * B
+ *   A (device) bf16: a_mn_major = 0 -> [M, K] row-major; 1 -> [K, M]
+ *   B (device) bf16: b_mn_major = 0 -> [N, K] row-major; 1 -> [K, N]
+ *   scratch (device) >= 256 bytes, caller-owned (tile counter, error word)
+ * M % 128 == 0, N % 128 == 0, K % 64 == 0.
+ */
+mok_status mok_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int32_t a_mn_major, const void* B,
+                         int32_t b_mn_major, float* C, void* scratch, void* stream);
+
+/* Synchronise `stream`, then return (and clear) the status recorded in the
+ * workspace's error word; MOK_OK if none. */
+mok_status mok_check(void* ws, void* stream);
+
+/* Number of SMs of the current device (the C in the minibatch floor). */
+int32_t mok_device_sm_count(void);
+
+const char* mok_status_string(mok_status s);
+const char* mok_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H_ */

@@ -1,0 +1,191 @@
+"""ctypes binding of libmok.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes torch
+tensors for device buffers, and passes their data pointers, sizes and the
+current CUDA stream through the C ABI declared in ``include/mok.h``.  No step
+of the layer runs in Python; if the library is missing the import fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmok.so")
+
+MOK_BF16 = 0
+MOK_MXFP8 = 1
+MOK_DEBUG_SKIP_RING_SIGNAL = 1
+MOK_DEBUG_SERIAL_RING = 2
+
+STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "MOK_ERR_WORKSPACE_TOO_SMALL",
+          4: "MOK_ERR_CUDA", 5: "MOK_ERR_BAD_INDEX", 6: "MOK_ERR_TIMEOUT"}
+
+# every entry point include/mok.h declares
+EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_build_schedule", "mok_forward",
+           "mok_backward", "mok_mxfp8_quantize", "mok_gather_rows", "mok_gemm_bf16", "mok_check",
+           "mok_device_sm_count", "mok_status_string", "mok_version"]
+
+
+class MokError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class MokShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32)]
+
+
+class MokConfig(ctypes.Structure):
+    _fields_ = [("minibatch_rows", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
+                ("capacity_mult", ctypes.c_float), ("comm_sms", ctypes.c_int32), ("debug_flags", ctypes.c_int32)]
+
+
+class MokMx(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+class MokLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("header", "counts", "offsets", "padded_offsets", "perm", "inv_perm",
+                                               "pad_perm", "pad_inv", "tile_expert")] + \
+               [("pad_capacity", ctypes.c_int64), ("tile_capacity", ctypes.c_int64)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run mixture_experts_layer_side_gb300.build.build() "
+                          "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    S = ctypes.POINTER(MokShape)
+    C = ctypes.POINTER(MokConfig)
+    i32, sz = ctypes.c_int32, ctypes.c_size_t
+    sig = {
+        "mok_workspace_size": (sz, [S, C, i32]),
+        "mok_ctx_size": (sz, [S, C, i32]),
+        "mok_workspace_layout": (i32, [S, C, i32, ctypes.POINTER(MokLayout)]),
+        "mok_build_schedule": (i32, [S, C, P, sz, P, P]),
+        "mok_forward": (i32, [S, C, i32, P, sz, P, P, P, P, P, P, P, P]),
+        "mok_backward": (i32, [S, C, i32, P, sz, P, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "mok_mxfp8_quantize": (i32, [P, i32, i32, i32, i32, P, P, P]),
+        "mok_gather_rows": (i32, [S, C, P, sz, P, P, P]),
+        "mok_gemm_bf16": (i32, [i32, i32, i32, P, i32, P, i32, P, P, P]),
+        "mok_check": (i32, [P, P]),
+        "mok_device_sm_count": (i32, []),
+        "mok_status_string": (ctypes.c_char_p, [i32]),
+        "mok_version": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, MokMx):
+        return ctypes.cast(ctypes.pointer(t), ctypes.c_void_p)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ok(status, where):
+    if status != 0:
+        raise MokError(status, where)
+
+
+def shape_of(T, H, I, E, k):
+    return MokShape(T, H, I, E, k)
+
+
+def config(minibatch_rows=0, ring_slots=0, capacity_mult=0.0, comm_sms=0, debug_flags=0):
+    return MokConfig(minibatch_rows, ring_slots, capacity_mult, comm_sms, debug_flags)
+
+
+def mx(q, scale):
+    """MXFP8 tensor descriptor (codes, scales) for mok_forward / mok_backward."""
+    return MokMx(q.data_ptr(), scale.data_ptr())
+
+
+def mok_version():
+    return LIB.mok_version().decode()
+
+
+def mok_status_string(status):
+    return LIB.mok_status_string(status).decode()
+
+
+def mok_device_sm_count():
+    return LIB.mok_device_sm_count()
+
+
+def mok_workspace_size(shape, cfg, prec=MOK_BF16):
+    return LIB.mok_workspace_size(ctypes.byref(shape), ctypes.byref(cfg), prec)
+
+
+def mok_ctx_size(shape, cfg, prec=MOK_BF16):
+    return LIB.mok_ctx_size(ctypes.byref(shape), ctypes.byref(cfg), prec)
+
+
+def mok_workspace_layout(shape, cfg, prec=MOK_BF16):
+    out = MokLayout()
+    _ok(LIB.mok_workspace_layout(ctypes.byref(shape), ctypes.byref(cfg), prec, ctypes.byref(out)),
+        "mok_workspace_layout")
+    return {name: getattr(out, name) for name, _ in MokLayout._fields_}
+
+
+def mok_build_schedule(shape, cfg, ws, topk_idx, stream=None):
+    _ok(LIB.mok_build_schedule(ctypes.byref(shape), ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+                               _ptr(topk_idx), _stream(stream)), "mok_build_schedule")
+
+
+def mok_forward(shape, cfg, prec, ws, x, scores, W1, W3, W2, out, ctx, stream=None):
+    _ok(LIB.mok_forward(ctypes.byref(shape), ctypes.byref(cfg), prec, _ptr(ws), ws.numel() * ws.element_size(),
+                        _ptr(x), _ptr(scores), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(out), _ptr(ctx),
+                        _stream(stream)), "mok_forward")
+
+
+def mok_backward(shape, cfg, prec, ws, ctx, x, scores, W1, W3, W2, dout, dX, dW1, dW3, dW2, dscores, stream=None):
+    _ok(LIB.mok_backward(ctypes.byref(shape), ctypes.byref(cfg), prec, _ptr(ws), ws.numel() * ws.element_size(),
+                         _ptr(ctx), _ptr(x), _ptr(scores), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dout), _ptr(dX),
+                         _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(dscores), _stream(stream)), "mok_backward")
+
+
+def mok_mxfp8_quantize(src, block_axis, q, scale, stream=None):
+    b, r, c = (src.shape if src.dim() == 3 else (1,) + tuple(src.shape))
+    _ok(LIB.mok_mxfp8_quantize(_ptr(src), b, r, c, block_axis, _ptr(q), _ptr(scale), _stream(stream)),
+        "mok_mxfp8_quantize")
+
+
+def mok_gather_rows(shape, cfg, ws, x, xg, stream=None):
+    _ok(LIB.mok_gather_rows(ctypes.byref(shape), ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+                            _ptr(x), _ptr(xg), _stream(stream)), "mok_gather_rows")
+
+
+def mok_gemm_bf16(A, a_mn_major, B, b_mn_major, C, scratch, stream=None):
+    M, N = C.shape
+    K = A.shape[0] if a_mn_major else A.shape[1]
+    _ok(LIB.mok_gemm_bf16(M, N, K, _ptr(A), int(a_mn_major), _ptr(B), int(b_mn_major), _ptr(C), _ptr(scratch),
+                          _stream(stream)), "mok_gemm_bf16")
+
+
+def mok_check(ws, stream=None):
+    """Synchronise and return the device status recorded in the workspace (int)."""
+    return LIB.mok_check(_ptr(ws), _stream(stream))

@@ -1,0 +1,514 @@
+// C ABI of libmok.so: argument checks, workspace layout, tensor maps and the
+// launch sequence of each call.  Everything here runs on the host and only
+// enqueues work on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace mok {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices && cache[dev]) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices) cache[dev] = n;
+  return n;
+}
+
+bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+               const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], es[5] = {1, 1, 1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) s[i] = strides_bytes[i];
+  const CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int effective_minibatch_rows(const mok_shape& s, const mok_config& c, int num_sms) {
+  if (c.minibatch_rows > 0) return c.minibatch_rows;
+  // two full waves of 128 x 256 output tiles over the narrower grouped GEMM
+  const double rows = 2.0 * num_sms * 128.0 * 256.0 / (double)(2 * s.I < s.H ? 2 * s.I : s.H);
+  int m = (int)ceil(rows / kTileRows) * kTileRows;
+  return m < kTileRows ? kTileRows : m;
+}
+
+WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, int num_sms) {
+  WsLayout L;
+  memset(&L, 0, sizeof(L));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const int64_t R = (int64_t)s.T * s.k;
+  L.pad_capacity = (R + (int64_t)s.E * (kTileRows - 1)) / kTileRows * kTileRows;
+  L.tile_capacity = L.pad_capacity / kTileRows;
+  L.nchunks = (R + kSchedChunk - 1) / kSchedChunk;
+  int M = effective_minibatch_rows(s, c, num_sms);
+  if (M > L.pad_capacity) M = (int)L.pad_capacity;
+  L.minibatch_rows = M;
+  L.ring_slots = c.ring_slots > 0 ? c.ring_slots : 4;
+  const size_t I = s.I, H = s.H, P = L.pad_capacity;
+  L.header = take(kHeaderWords * 4);
+  L.counts = take(s.E * 4);
+  L.offsets = take((s.E + 1) * 4);
+  L.padded_offsets = take((s.E + 1) * 4);
+  L.perm = take(R * 4);
+  L.inv_perm = take(R * 4);
+  L.pad_perm = take(P * 4);
+  L.pad_inv = take(R * 4);
+  L.tile_expert = take(L.tile_capacity * 4);
+  L.chunk_hist = take(L.nchunks * s.E * 4);
+  L.chunk_base = take(L.nchunks * s.E * 4);
+  L.ring_flags = take(2 * L.tile_capacity * 4);
+  L.ring = take((size_t)L.ring_slots * M * I * 2);
+  L.yk = take((size_t)R * H * 2);
+  L.dhu = take(P * 2 * I * 2);
+  L.as = take(P * I * 2);
+  L.dsp = take(P * (I / 128) * 4);
+  if (prec == MOK_MXFP8) {
+    L.ring_sf = take((size_t)L.ring_slots * M * (I / 32));
+    L.xq = take((size_t)s.T * H);
+    L.xsf = take((size_t)s.T * (H / 32));
+    L.dq = take((size_t)s.T * H);
+    L.dsf = take((size_t)s.T * (H / 32));
+    L.dhuq = take(P * 2 * I);
+    L.dhusf = take(P * (2 * I / 32));
+  }
+  L.total = off;
+  return L;
+}
+
+}  // namespace mok
+
+using namespace mok;
+
+namespace {
+
+const char* kStatusNames[] = {"MOK_OK",           "MOK_ERR_INVALID_ARG", "MOK_ERR_UNSUPPORTED",
+                              "MOK_ERR_WORKSPACE_TOO_SMALL", "MOK_ERR_CUDA", "MOK_ERR_BAD_INDEX",
+                              "MOK_ERR_TIMEOUT"};
+
+mok_status check_shape(const mok_shape* s) {
+  if (!s) return MOK_ERR_INVALID_ARG;
+  if (s->T < 1 || s->H < 1 || s->I < 1 || s->E < 1 || s->k < 1) return MOK_ERR_INVALID_ARG;
+  if (s->H % 128 || s->I % 128) return MOK_ERR_UNSUPPORTED;
+  if (s->E > 1024 || s->k > 32) return MOK_ERR_UNSUPPORTED;
+  if ((int64_t)s->T * s->k > (1 << 24)) return MOK_ERR_UNSUPPORTED;
+  return MOK_OK;
+}
+
+mok_status check_config(const mok_config* c) {
+  if (!c) return MOK_ERR_INVALID_ARG;
+  if (c->comm_sms != 0) return MOK_ERR_INVALID_ARG;
+  if (c->minibatch_rows < 0 || c->minibatch_rows % 128) return MOK_ERR_INVALID_ARG;
+  if (c->ring_slots < 0 || c->ring_slots == 1) return MOK_ERR_INVALID_ARG;
+  if (!(c->capacity_mult == 0.0f || c->capacity_mult >= 1.0f)) return MOK_ERR_INVALID_ARG;
+  return MOK_OK;
+}
+
+mok_status check_prec(mok_precision p) {
+  if (p == MOK_BF16) return MOK_OK;
+  if (p == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
+  return MOK_ERR_INVALID_ARG;
+}
+
+#define MOK_TRY(expr)                       \
+  do {                                      \
+    const mok_status st_ = (expr);          \
+    if (st_ != MOK_OK) return st_;          \
+  } while (0)
+
+#define MOK_CUDA(expr)                          \
+  do {                                          \
+    if ((expr) != cudaSuccess) return MOK_ERR_CUDA; \
+  } while (0)
+
+const CUtensorMapDataType kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+// bf16 [rows, cols] row-major, box {64, box_rows}.
+bool map2d(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t str[1] = {cols * 2};
+  const uint32_t box[2] = {64, box_rows};
+  return make_tmap(m, kBF16, 2, p, dims, str, box, true);
+}
+
+// bf16 [E, rows, cols], box {64, box_rows, 1}.
+bool map3d(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows, uint64_t E, uint32_t box_rows) {
+  const uint64_t dims[3] = {cols, rows, E};
+  const uint64_t str[2] = {cols * 2, cols * rows * 2};
+  const uint32_t box[3] = {64, box_rows, 1};
+  return make_tmap(m, kBF16, 3, p, dims, str, box, true);
+}
+
+// bf16 [rows, cols] row-major read four whole rows at a time (tile::gather4):
+// box {64, 1}.
+bool map_gather(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t str[1] = {cols * 2};
+  const uint32_t box[2] = {64, 1};
+  return make_tmap(m, kBF16, 2, p, dims, str, box, true);
+}
+
+int gemm_grid(long items) {
+  const int sms = device_sm_count();
+  if (items < 1) items = 1;
+  return (int)(items < sms ? items : sms);
+}
+
+void base_params(GemmParams& g, const mok_shape& s, const WsLayout& L, uint8_t* ws) {
+  memset(&g, 0, sizeof(g));
+  g.T = s.T;
+  g.H = s.H;
+  g.I = s.I;
+  g.E = s.E;
+  g.k = s.k;
+  g.hdr = reinterpret_cast<int32_t*>(ws + L.header);
+  g.tile_expert = reinterpret_cast<const int32_t*>(ws + L.tile_expert);
+  g.pad_perm = reinterpret_cast<const int32_t*>(ws + L.pad_perm);
+  g.padded_offsets = reinterpret_cast<const int32_t*>(ws + L.padded_offsets);
+}
+
+mok_status reset_counters(uint8_t* ws, const WsLayout& L, cudaStream_t st) {
+  // the abort word and the tile counters (words [3, 48)); the error word,
+  // the used-row count and the used-tile count are kept
+  MOK_CUDA(cudaMemsetAsync(ws + L.header + kHdrAbort * 4, 0, (kHdrCounters + kNumCounters - kHdrAbort) * 4, st));
+  return MOK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mok_version(void) { return "mok-gb300 0.1.0 (sm_103a)"; }
+
+const char* mok_status_string(mok_status s) {
+  if ((int)s < 0 || (int)s > 6) return "MOK_ERR_UNKNOWN";
+  return kStatusNames[(int)s];
+}
+
+int32_t mok_device_sm_count(void) { return device_sm_count(); }
+
+size_t mok_workspace_size(const mok_shape* shape, const mok_config* cfg, mok_precision prec) {
+  if (check_shape(shape) != MOK_OK || check_config(cfg) != MOK_OK) return 0;
+  if (prec != MOK_BF16 && prec != MOK_MXFP8) return 0;
+  return ws_layout(*shape, *cfg, prec, device_sm_count()).total;
+}
+
+size_t mok_ctx_size(const mok_shape* shape, const mok_config* cfg, mok_precision prec) {
+  if (check_shape(shape) != MOK_OK || check_config(cfg) != MOK_OK) return 0;
+  if (prec != MOK_BF16 && prec != MOK_MXFP8) return 0;
+  const WsLayout L = ws_layout(*shape, *cfg, prec, device_sm_count());
+  return (size_t)L.pad_capacity * 2 * shape->I * 2;
+}
+
+mok_status mok_workspace_layout(const mok_shape* shape, const mok_config* cfg, mok_precision prec,
+                                mok_layout* out) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  if (!out || (prec != MOK_BF16 && prec != MOK_MXFP8)) return MOK_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*shape, *cfg, prec, device_sm_count());
+  out->header = L.header;
+  out->counts = L.counts;
+  out->offsets = L.offsets;
+  out->padded_offsets = L.padded_offsets;
+  out->perm = L.perm;
+  out->inv_perm = L.inv_perm;
+  out->pad_perm = L.pad_perm;
+  out->pad_inv = L.pad_inv;
+  out->tile_expert = L.tile_expert;
+  out->pad_capacity = L.pad_capacity;
+  out->tile_capacity = L.tile_capacity;
+  return MOK_OK;
+}
+
+mok_status mok_build_schedule(const mok_shape* shape, const mok_config* cfg, void* ws, size_t ws_bytes,
+                              const int32_t* topk_idx, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  if (!ws || !topk_idx) return MOK_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
+  // the schedule part of the layout is the same for both precisions
+  if (ws_bytes < L.chunk_base + align256(L.nchunks * shape->E * 4)) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  MOK_CUDA(launch_schedule(*shape, L, static_cast<uint8_t*>(ws), topk_idx, static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precision prec, void* ws,
+                       size_t ws_bytes, const void* x, const float* scores, const void* W1, const void* W3,
+                       const void* W2, void* out, void* ctx, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  MOK_TRY(check_prec(prec));
+  if (!ws || !x || !scores || !W1 || !W3 || !W2 || !out || !ctx) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  const WsLayout L = ws_layout(s, *cfg, prec, device_sm_count());
+  if (ws_bytes < L.total) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  MOK_TRY(reset_counters(w, L, st));
+  MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 2 * L.tile_capacity * 4, st));
+
+  const int M = L.minibatch_rows, S = L.ring_slots;
+  const int bn2 = (s.H % 256 == 0) ? 256 : 128;
+  GemmParams g;
+  base_params(g, s, L, w);
+  g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
+  g.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);
+  g.ring_rows = M;
+  g.ring_slots = S;
+  g.ring_flags = reinterpret_cast<uint32_t*>(w + L.ring_flags);
+  g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
+  g.debug_flags = cfg->debug_flags;
+
+  TmapSet maps;
+  memset(&maps, 0, sizeof(maps));
+  if (!map_gather(&maps.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
+  if (!map3d(&maps.m[1], W1, s.I, s.H, s.E, 64) || !map3d(&maps.m[2], W3, s.I, s.H, s.E, 64)) return MOK_ERR_CUDA;
+
+  const bool serial = (cfg->debug_flags & 2) != 0;
+  if (!serial) {
+    // one persistent launch: GEMM1 and GEMM2 interleaved through the ring
+    if (!map2d(&maps.m[3], g.ring, s.I, (uint64_t)S * M, 128) || !map3d(&maps.m[4], W2, s.H, s.I, s.E, 64))
+      return MOK_ERR_CUDA;
+    g.nmaps = 5;
+    g.bn = bn2;
+    g.n_tiles = s.H / bn2;
+    g.g1_tiles = s.I / 128;
+    g.m_tiles = (int)L.tile_capacity;
+    g.counter = 0;
+    MOK_CUDA(launch_gemm(GM_FWD_RING, maps, g, gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles)), st));
+  } else {
+    // minibatch by minibatch in stream order (same ring, no device flags)
+    TmapSet m2;
+    memset(&m2, 0, sizeof(m2));
+    if (!map2d(&m2.m[0], g.ring, s.I, (uint64_t)S * M, 128) || !map3d(&m2.m[1], W2, s.H, s.I, s.E, 64))
+      return MOK_ERR_CUDA;
+    maps.m[3] = m2.m[0];
+    const int Mt = M / kTileRows;
+    const int nmb = (int)((L.tile_capacity + Mt - 1) / Mt);
+    int counter = 0;
+    for (int b = 0; b < nmb; ++b) {
+      GemmParams g1 = g;
+      g1.nmaps = 3;
+      g1.bn = 256;
+      g1.n_tiles = s.I / 128;
+      g1.m_tile_begin = b * Mt;
+      g1.m_tile_end = (b + 1) * Mt;
+      g1.counter = counter++ % kNumCounters;
+      if (g1.counter == 0 && b > 0) MOK_TRY(reset_counters(w, L, st));
+      MOK_CUDA(launch_gemm(GM_FWD1, maps, g1, gemm_grid((long)Mt * g1.n_tiles), st));
+      GemmParams g2 = g1;
+      g2.nmaps = 2;
+      g2.bn = bn2;
+      g2.n_tiles = s.H / bn2;
+      g2.counter = counter++ % kNumCounters;
+      MOK_CUDA(launch_gemm(GM_FWD2, m2, g2, gemm_grid((long)Mt * g2.n_tiles), st));
+    }
+  }
+  MOK_CUDA(launch_combine(s, L, w, g.yk, scores, static_cast<__nv_bfloat16*>(out), st));
+  return MOK_OK;
+}
+
+mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_precision prec, void* ws,
+                        size_t ws_bytes, const void* ctx, const void* x, const float* scores, const void* W1,
+                        const void* W3, const void* W2, const void* dout, void* dX, void* dW1, void* dW3,
+                        void* dW2, float* dscores, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  MOK_TRY(check_prec(prec));
+  if (!ws || !ctx || !x || !scores || !W1 || !W3 || !W2 || !dout || !dX || !dW1 || !dW3 || !dW2 || !dscores)
+    return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  const WsLayout L = ws_layout(s, *cfg, prec, device_sm_count());
+  if (ws_bytes < L.total) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  MOK_TRY(reset_counters(w, L, st));
+  const uint64_t P = L.pad_capacity;
+  const int bn_i = (s.I % 256 == 0) ? 256 : 128;
+  const int bn_h = (s.H % 256 == 0) ? 256 : 128;
+
+  GemmParams g;
+  base_params(g, s, L, w);
+  g.ctx_hu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(ctx));
+  g.dhu = reinterpret_cast<__nv_bfloat16*>(w + L.dhu);
+  g.as = reinterpret_cast<__nv_bfloat16*>(w + L.as);
+  g.dsp = reinterpret_cast<float*>(w + L.dsp);
+  g.scores = scores;
+  g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
+
+  // dA' = gather(dout) W2^T, SwiGLU backward + router-score partials
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map_gather(&m.m[0], dout, s.H, s.T)) return MOK_ERR_CUDA;
+    if (!map3d(&m.m[1], W2, s.H, s.I, s.E, bn_i)) return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 2;
+    q.bn = bn_i;
+    q.n_tiles = s.I / bn_i;
+    q.m_tile_begin = 0;
+    q.m_tile_end = (int)L.tile_capacity;
+    q.counter = 0;
+    MOK_CUDA(launch_gemm(GM_BWD_DA, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    MOK_CUDA(launch_ds_reduce(s, L, w, dscores, q.n_tiles, st));
+  }
+  // dX parts = [dh|du] [W1|W3]^T scattered to token order, then summed over k
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map2d(&m.m[0], g.dhu, 2 * (uint64_t)s.I, P, 128) || !map3d(&m.m[1], W1, s.I, s.H, s.E, bn_h) ||
+        !map3d(&m.m[2], W3, s.I, s.H, s.E, bn_h))
+      return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 3;
+    q.bn = bn_h;
+    q.n_tiles = s.H / bn_h;
+    q.m_tile_begin = 0;
+    q.m_tile_end = (int)L.tile_capacity;
+    q.counter = 1;
+    MOK_CUDA(launch_gemm(GM_BWD_DX, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));
+  }
+  // dW1 | dW3 = gather(x)^T [dh|du], per expert
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map_gather(&m.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
+    if (!map2d(&m.m[1], g.dhu, 2 * (uint64_t)s.I, P, 64)) return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 2;
+    q.bn = 256;
+    q.n_tiles = 2 * s.I / 256;
+    q.m_tiles = s.H / 128;
+    q.counter = 2;
+    q.dw0 = static_cast<__nv_bfloat16*>(dW1);
+    q.dw1 = static_cast<__nv_bfloat16*>(dW3);
+    MOK_CUDA(launch_gemm(GM_WG13, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
+  }
+  // dW2 = (s a)^T gather(dout), per expert
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map2d(&m.m[0], g.as, s.I, P, 64) || !map_gather(&m.m[1], dout, s.H, s.T)) return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 2;
+    q.bn = bn_h;
+    q.n_tiles = s.H / bn_h;
+    q.m_tiles = s.I / 128;
+    q.counter = 3;
+    q.dw0 = static_cast<__nv_bfloat16*>(dW2);
+    MOK_CUDA(launch_gemm(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
+  }
+  return MOK_OK;
+}
+
+mok_status mok_mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int32_t cols, int32_t block_axis,
+                              uint8_t* q, uint8_t* scale, void* stream) {
+  if (!src || !q || !scale) return MOK_ERR_INVALID_ARG;
+  if (batch < 1 || rows < 1 || cols < 1) return MOK_ERR_INVALID_ARG;
+  if (block_axis != 0 && block_axis != 1) return MOK_ERR_INVALID_ARG;
+  if (block_axis == 0 && rows % 32) return MOK_ERR_UNSUPPORTED;
+  if (block_axis == 1 && cols % 32) return MOK_ERR_UNSUPPORTED;
+  MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(src), batch, rows, cols, block_axis, q, scale,
+                                 static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+mok_status mok_gather_rows(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                           const void* x, void* xg, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  if (!ws || !x || !xg) return MOK_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
+  if (ws_bytes < L.chunk_base) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  MOK_CUDA(launch_gather_rows(*shape, L, static_cast<const uint8_t*>(ws), static_cast<const __nv_bfloat16*>(x),
+                              static_cast<__nv_bfloat16*>(xg), static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+mok_status mok_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int32_t a_mn_major, const void* B,
+                         int32_t b_mn_major, float* C, void* scratch, void* stream) {
+  if (!A || !B || !C || !scratch) return MOK_ERR_INVALID_ARG;
+  if (M < 128 || N < 128 || K < 64 || M % 128 || N % 128 || K % 64) return MOK_ERR_UNSUPPORTED;
+  const int bn = (N % 256 == 0) ? 256 : 128;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* hdr = static_cast<int32_t*>(scratch);
+  MOK_CUDA(cudaMemsetAsync(hdr, 0, kHeaderWords * 4, st));
+  TmapSet m;
+  memset(&m, 0, sizeof(m));
+  bool ok = a_mn_major ? map2d(&m.m[0], A, M, K, 64) : map2d(&m.m[0], A, K, M, 128);
+  ok = ok && (b_mn_major ? map2d(&m.m[1], B, N, K, 64) : map2d(&m.m[1], B, K, N, bn));
+  if (!ok) return MOK_ERR_CUDA;
+  GemmParams g;
+  memset(&g, 0, sizeof(g));
+  g.nmaps = 2;
+  g.bn = bn;
+  g.n_tiles = N / bn;
+  g.m_tiles = M / 128;
+  g.k_iters = K / 64;
+  g.hdr = hdr;
+  g.out_f32 = C;
+  g.ld_out = N;
+  g.a_mn = a_mn_major ? 1 : 0;
+  g.b_mn = b_mn_major ? 1 : 0;
+  MOK_CUDA(launch_gemm(GM_DENSE, m, g, gemm_grid((long)g.m_tiles * g.n_tiles), st));
+  return MOK_OK;
+}
+
+mok_status mok_check(void* ws, void* stream) {
+  if (!ws) return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOK_CUDA(cudaStreamSynchronize(st));
+  int32_t word = 0;
+  MOK_CUDA(cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost));
+  MOK_CUDA(cudaMemset(ws, 0, sizeof(word)));
+  if (word & MOK_ERRBIT_TIMEOUT) return MOK_ERR_TIMEOUT;
+  if (word & MOK_ERRBIT_BAD_INDEX) return MOK_ERR_BAD_INDEX;
+  return MOK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,636 @@
+// Expert-grouped GEMMs of the MoE layer on sm_103a tensor cores.
+//
+// One persistent, warp-specialised kernel family:
+//   warp 0      TMA producer.  Plain tiles come in with cp.async.bulk.tensor;
+//               the dispatch gather (sorted row -> token) is fused into the
+//               load path with cp.async.bulk.tensor ... tile::gather4, four
+//               token rows per instruction, one instruction per lane.
+//   warp 1      MMA issuer: tcgen05.mma (BF16 in, FP32 accumulate in TMEM),
+//               128 x N tiles, N = 128 or 256; TMEM holds two accumulators so
+//               the epilogue of one tile overlaps the main loop of the next.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, then the fused
+//               per-mode work (SwiGLU, scatter to token order, SwiGLU
+//               backward with the router-score partial sums, weight-gradient
+//               stores).
+// Work items (output tiles) are taken from a device counter in increasing
+// order, so a CTA only ever waits on items taken before its own; the
+// numerics of a tile never depend on which CTA computes it (fixed K order,
+// no split-K, no atomics on data), which keeps every output bitwise
+// reproducible.
+//
+// Pages: expert-grouped GEMM and SwiGLU ("Cursor Open-Sources
+// Mixture-of-Kittens (MoK)", "Three design decisions that matter",
+// overlap-granularity paragraph, and the paragraph after that list);
+// pull dispatch / push combine mapped to gather-in-load and
+// scatter-in-epilogue (same section, communication-direction paragraph);
+// the ring token buffer consumed per minibatch (ring-token-buffer paragraph);
+// router gradient fused into the SwiGLU backward (paragraph after the list).
+#include "gemm.cuh"
+#include "tc.cuh"
+
+namespace mok {
+
+namespace {
+
+struct Ctl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t qfull[kQueue];
+  uint64_t qempty[kQueue];
+  int q[kQueue];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// A decoded work item.
+struct Item {
+  int type;     // effective mode of this item (GM_FWD1 / GM_FWD2 inside the ring kernel)
+  int m;        // 128-row tile index (row-tiled modes) or M tile inside the expert (wgrad)
+  int n;        // N tile
+  int e;        // expert
+  int row0;     // first padded row of the tile (row-tiled) or of the expert (wgrad)
+  int k_iters;  // K iterations of 128 bytes
+};
+
+__device__ __forceinline__ int used_tiles(const GemmParams& p) { return p.hdr[kHdrTiles]; }
+
+// Number of work items of a launch (device-side: depends on the schedule).
+template <int MODE>
+__device__ int count_items(const GemmParams& p) {
+  if constexpr (MODE == GM_DENSE) {
+    return p.m_tiles * p.n_tiles;
+  } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
+    return p.E * p.m_tiles * p.n_tiles;
+  } else if constexpr (MODE == GM_FWD_RING) {
+    return used_tiles(p) * (p.g1_tiles + p.n_tiles);
+  } else {
+    const int end = min(p.m_tile_end, used_tiles(p));
+    return max(end - p.m_tile_begin, 0) * p.n_tiles;
+  }
+}
+
+// Ring kernel: item w -> (type, tile, n).  Sequence of steps: step 0 is
+// GEMM1 of minibatch 0; step s >= 1 is GEMM1 of minibatch s followed by
+// GEMM2 of minibatch s-1; the last step is GEMM2 of the last minibatch.
+__device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& n) {
+  const int Mt = p.ring_rows / kTileRows;
+  const int tiles = used_tiles(p);
+  const int nb = (tiles + Mt - 1) / Mt;
+  const int g1 = p.g1_tiles, g2 = p.n_tiles;
+  auto mt_of = [&](int b) { return min(Mt, tiles - b * Mt); };
+  auto emit = [&](int t, int b, int r, int nt) {
+    type = t;
+    m = b * Mt + r / nt;
+    n = r % nt;
+  };
+  // step 0
+  const int s10 = mt_of(0) * g1;
+  if (w < s10) return emit(GM_FWD1, 0, w, g1);
+  w -= s10;
+  const int full_steps = max(nb - 2, 0);
+  const int F = Mt * (g1 + g2);
+  if (w < full_steps * F) {
+    const int s = 1 + w / F;
+    const int r = w % F;
+    if (r < Mt * g1) return emit(GM_FWD1, s, r, g1);
+    return emit(GM_FWD2, s - 1, r - Mt * g1, g2);
+  }
+  w -= full_steps * F;
+  if (nb >= 2) {
+    const int a = mt_of(nb - 1) * g1;
+    if (w < a) return emit(GM_FWD1, nb - 1, w, g1);
+    w -= a;
+    const int b2 = Mt * g2;
+    if (w < b2) return emit(GM_FWD2, nb - 2, w, g2);
+    w -= b2;
+  }
+  return emit(GM_FWD2, nb - 1, w, g2);
+}
+
+template <int MODE>
+__device__ Item decode(const GemmParams& p, int w) {
+  Item it;
+  if constexpr (MODE == GM_DENSE) {
+    it.type = MODE;
+    it.m = w / p.n_tiles;
+    it.n = w % p.n_tiles;
+    it.e = 0;
+    it.row0 = it.m * kTileRows;
+    it.k_iters = p.k_iters;
+  } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
+    const int per_e = p.m_tiles * p.n_tiles;
+    it.type = MODE;
+    it.e = w / per_e;
+    const int r = w % per_e;
+    it.m = r / p.n_tiles;
+    it.n = r % p.n_tiles;
+    const int a = p.padded_offsets[it.e];
+    const int b = p.padded_offsets[it.e + 1];
+    it.row0 = a;
+    it.k_iters = (b - a) / 64;
+  } else {
+    int type = MODE, m, n;
+    if constexpr (MODE == GM_FWD_RING) {
+      decode_ring(p, w, type, m, n);
+    } else {
+      m = p.m_tile_begin + w / p.n_tiles;
+      n = w % p.n_tiles;
+    }
+    it.type = type;
+    it.m = m;
+    it.n = n;
+    it.e = p.tile_expert[m];
+    it.row0 = m * kTileRows;
+    it.k_iters = (type == GM_FWD1 || type == GM_BWD_DA) ? p.H / 64
+                 : (type == GM_FWD2)                   ? p.I / 64
+                                                       : 2 * p.I / 64;  // GM_BWD_DX
+  }
+  return it;
+}
+
+__device__ __forceinline__ int item_bn(const GemmParams& p, int type) { return type == GM_FWD1 ? 256 : p.bn; }
+
+__device__ __forceinline__ int tok_of(const GemmParams& p, int prow) {
+  const int f = p.pad_perm[prow];
+  return f >= 0 ? f / p.k : p.T;  // row T is outside the tensor: TMA fills zeros
+}
+
+__device__ __forceinline__ int ring_row(const GemmParams& p, int prow) {
+  const int mb = prow / p.ring_rows;
+  return (mb % p.ring_slots) * p.ring_rows + (prow - mb * p.ring_rows);
+}
+
+// ------------------------------------------------------------------ producer
+// All 32 lanes of warp 0 call this for one K stage; lane 0 has already armed
+// the stage's full barrier with the stage's byte count.
+template <int MODE>
+__device__ __forceinline__ void issue_loads(const TmapSet& mp, const GemmParams& p, const Item& it, int kk,
+                                            uint8_t* a, uint8_t* b, uint64_t* bar, int lane, const int (&tok)[4]) {
+  const int type = it.type;
+  if (MODE == GM_DENSE) {
+    if (lane == 0) {
+      if (p.a_mn) {
+        for (int c = 0; c < 2; ++c) tma_load_2d(a + c * 8192, &mp.m[0], bar, it.m * 128 + c * 64, kk * 64);
+      } else {
+        tma_load_2d(a, &mp.m[0], bar, kk * 64, it.m * 128);
+      }
+      if (p.b_mn) {
+        for (int c = 0; c < p.bn / 64; ++c) tma_load_2d(b + c * 8192, &mp.m[1], bar, it.n * p.bn + c * 64, kk * 64);
+      } else {
+        tma_load_2d(b, &mp.m[1], bar, kk * 64, it.n * p.bn);
+      }
+    }
+  } else if (type == GM_FWD1) {
+    // A: gathered token rows of x (K-major); B: W1 and W3 column blocks (N-major)
+    tma_gather4(a + lane * 512, &mp.m[0], bar, kk * 64, tok[0], tok[1], tok[2], tok[3]);
+    if (lane == 0) {
+      for (int c = 0; c < 2; ++c) tma_load_3d(b + c * 8192, &mp.m[1], bar, it.n * 128 + c * 64, kk * 64, it.e);
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(b + (2 + c) * 8192, &mp.m[2], bar, it.n * 128 + c * 64, kk * 64, it.e);
+    }
+  } else if (type == GM_FWD2) {
+    if (lane == 0) {
+      const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
+      const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
+      tma_load_2d(a, &mp.m[mslot], bar, kk * 64, ring_row(p, it.row0));
+      for (int c = 0; c < p.bn / 64; ++c)
+        tma_load_3d(b + c * 8192, &mp.m[wmap], bar, it.n * p.bn + c * 64, kk * 64, it.e);
+    }
+  } else if (type == GM_BWD_DA) {
+    tma_gather4(a + lane * 512, &mp.m[0], bar, kk * 64, tok[0], tok[1], tok[2], tok[3]);
+    if (lane == 0) tma_load_3d(b, &mp.m[1], bar, kk * 64, it.n * p.bn, it.e);
+  } else if (type == GM_BWD_DX) {
+    if (lane == 0) {
+      tma_load_2d(a, &mp.m[0], bar, kk * 64, it.row0);
+      const int ki = p.I / 64;
+      if (kk < ki)
+        tma_load_3d(b, &mp.m[1], bar, kk * 64, it.n * p.bn, it.e);
+      else
+        tma_load_3d(b, &mp.m[2], bar, (kk - ki) * 64, it.n * p.bn, it.e);
+    }
+  } else if (type == GM_WG13 || type == GM_WG2) {
+    // 64 routed rows of the expert per stage: K dimension, gathered by token
+    const int r0 = it.row0 + kk * 64 + 4 * (lane & 15);
+    const int t0 = tok_of(p, r0), t1 = tok_of(p, r0 + 1), t2 = tok_of(p, r0 + 2), t3 = tok_of(p, r0 + 3);
+    const int c = lane >> 4;
+    if (type == GM_WG13) {
+      // A = x^T (M = H, MN-major), B = [dh|du] (N = 2I, MN-major)
+      tma_gather4(a + c * 8192 + (lane & 15) * 512, &mp.m[0], bar, it.m * 128 + c * 64, t0, t1, t2, t3);
+      if (lane == 0)
+        for (int cc = 0; cc < p.bn / 64; ++cc)
+          tma_load_2d(b + cc * 8192, &mp.m[1], bar, it.n * p.bn + cc * 64, it.row0 + kk * 64);
+    } else {
+      // A = (s a)^T (M = I, MN-major), B = dout (N = H, MN-major, gathered)
+      for (int cc = c; cc < p.bn / 64; cc += 2)
+        tma_gather4(b + cc * 8192 + (lane & 15) * 512, &mp.m[1], bar, it.n * p.bn + cc * 64, t0, t1, t2, t3);
+      if (lane == 0)
+        for (int ca = 0; ca < 2; ++ca)
+          tma_load_2d(a + ca * 8192, &mp.m[0], bar, it.m * 128 + ca * 64, it.row0 + kk * 64);
+    }
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ bool a_mn_major(const GemmParams& p, int type) {
+  if (MODE == GM_DENSE) return p.a_mn != 0;
+  return type == GM_WG13 || type == GM_WG2;
+}
+
+template <int MODE>
+__device__ __forceinline__ bool b_mn_major(const GemmParams& p, int type) {
+  if (MODE == GM_DENSE) return p.b_mn != 0;
+  return type == GM_FWD1 || type == GM_FWD2 || type == GM_WG13 || type == GM_WG2;
+}
+
+// ------------------------------------------------------------------ epilogues
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 q = s[i];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+      const float2 f = __bfloat1622float2(b2);
+      v[8 * i + 2 * j] = f.x;
+      v[8 * i + 2 * j + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ float sigmoidf_(float h) { return 1.0f / (1.0f + __expf(-h)); }
+
+// GEMM1: columns [0,128) of the tile are h, [128,256) are u, for
+// intermediate columns [n*128, n*128+128).  a = silu(h) * u from the bf16
+// values that are saved for the backward.
+__device__ void epi_fwd1(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
+  const long prow = (long)it.row0 + row;
+  const int i0 = it.n * 128;
+  __nv_bfloat16* hrow = p.ctx_hu + prow * 2 * p.I + i0;
+  __nv_bfloat16* urow = hrow + p.I;
+  __nv_bfloat16* arow = p.ring + (long)ring_row(p, (int)prow) * p.I + i0;
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    float h[32], u[32];
+    tmem_ld32(tbase + c, h);
+    tmem_ld32(tbase + 128 + c, u);
+    uint32_t hw[16], uw[16], aw[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float h0 = bf16_round(h[2 * i]), h1 = bf16_round(h[2 * i + 1]);
+      const float u0 = bf16_round(u[2 * i]), u1 = bf16_round(u[2 * i + 1]);
+      hw[i] = pack_bf16x2(h0, h1);
+      uw[i] = pack_bf16x2(u0, u1);
+      aw[i] = pack_bf16x2(h0 * sigmoidf_(h0) * u0, h1 * sigmoidf_(h1) * u1);
+    }
+    store32_bf16(hrow + c, hw);
+    store32_bf16(urow + c, uw);
+    store32_bf16(arow + c, aw);
+  }
+}
+
+// Scatter a tile row to token order: row f of dst (skipped for padding rows;
+// every lane still takes part in the warp-collective TMEM loads).
+__device__ void epi_scatter(const GemmParams& p, const Item& it, uint32_t tbase, int row, int bn) {
+  const int prow = it.row0 + row;
+  const int f = p.pad_perm[prow];
+  __nv_bfloat16* dst = p.yk + (long)max(f, 0) * p.H + it.n * bn;
+#pragma unroll 1
+  for (int c = 0; c < bn; c += 32) {
+    float v[32];
+    tmem_ld32(tbase + c, v);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    if (f >= 0) store32_bf16(dst + c, w);
+  }
+}
+
+// SwiGLU backward.  Accumulator = dA' = dout_t W2_e^T for intermediate
+// columns [n*bn, n*bn+bn).  With s the row's router score:
+//   ds partial = sum_i dA'_i a_i          (router-score gradient)
+//   dA = s dA',  dh = dA u sig(h) (1 + h (1 - sig(h))),  du = dA silu(h)
+//   A_s = s a  (the left operand of dW2)
+__device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
+  const long prow = (long)it.row0 + row;
+  const int f = p.pad_perm[prow];
+  const float s = f >= 0 ? p.scores[f] : 0.0f;
+  const int bn = p.bn;
+  const __nv_bfloat16* hrow = p.ctx_hu + prow * 2 * p.I + it.n * bn;
+  const __nv_bfloat16* urow = hrow + p.I;
+  __nv_bfloat16* dhrow = p.dhu + prow * 2 * p.I + it.n * bn;
+  __nv_bfloat16* durow = dhrow + p.I;
+  __nv_bfloat16* asrow = p.as + prow * p.I + it.n * bn;
+  float dsum = 0.0f;
+#pragma unroll 1
+  for (int c = 0; c < bn; c += 32) {
+    float g[32], h[32], u[32];
+    tmem_ld32(tbase + c, g);
+    load32_bf16(hrow + c, h);
+    load32_bf16(urow + c, u);
+    uint32_t dhw[16], duw[16], asw[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float r[2][3];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float hh = h[2 * i + j], uu = u[2 * i + j], gg = g[2 * i + j];
+        const float sg = sigmoidf_(hh);
+        const float sl = hh * sg;
+        const float a = sl * uu;
+        dsum = fmaf(gg, a, dsum);
+        const float dA = s * gg;
+        r[j][0] = dA * uu * sg * (1.0f + hh * (1.0f - sg));
+        r[j][1] = dA * sl;
+        r[j][2] = s * a;
+      }
+      dhw[i] = pack_bf16x2(r[0][0], r[1][0]);
+      duw[i] = pack_bf16x2(r[0][1], r[1][1]);
+      asw[i] = pack_bf16x2(r[0][2], r[1][2]);
+    }
+    store32_bf16(dhrow + c, dhw);
+    store32_bf16(durow + c, duw);
+    store32_bf16(asrow + c, asw);
+  }
+  p.dsp[prow * p.n_tiles + it.n] = dsum;
+}
+
+// Weight gradients: tile rows are rows of dW (H rows of dW1/dW3, I rows of
+// dW2), columns are its columns.  An expert with no routed rows has no
+// accumulation and gets exact zeros.
+__device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
+  const int r = it.m * 128 + row;
+  const int bn = p.bn;
+#pragma unroll 1
+  for (int c = 0; c < bn; c += 32) {
+    float v[32];
+    if (it.k_iters > 0) {
+      tmem_ld32(tbase + c, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    const int col = it.n * bn + c;
+    __nv_bfloat16* dst;
+    if (it.type == GM_WG13) {
+      dst = (col < p.I) ? p.dw0 + ((long)it.e * p.H + r) * p.I + col
+                        : p.dw1 + ((long)it.e * p.H + r) * p.I + (col - p.I);
+    } else {
+      dst = p.dw0 + ((long)it.e * p.I + r) * p.H + col;
+    }
+    store32_bf16(dst, w);
+  }
+}
+
+__device__ void epi_dense(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
+  float* dst = p.out_f32 + (long)(it.m * 128 + row) * p.ld_out + it.n * p.bn;
+#pragma unroll 1
+  for (int c = 0; c < p.bn; c += 32) {
+    float v[32];
+    tmem_ld32(tbase + c, v);
+    float4* d = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ TmapSet maps,
+                                                                const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + kStages * kAStage;
+  Ctl* ctl = reinterpret_cast<Ctl*>(sB + kStages * kBStage);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtx wc{&ctl->abort, &p.hdr[kHdrAbort], &p.hdr[kHdrError]};
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->tfull[i], 1);
+      mbar_init(&ctl->tempty[i], 4);
+    }
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(&ctl->qfull[i], 1);
+      mbar_init(&ctl->qempty[i], 5);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0)
+    for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int num_items = count_items<MODE>(p);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
+    uint32_t* counter = reinterpret_cast<uint32_t*>(&p.hdr[kHdrCounters + p.counter]);
+    bool ok = true;
+    while (ok) {
+      int w = 0;
+      if (lane == 0) {
+        ok = mbar_wait(&ctl->qempty[qs], qp ^ 1, wc);
+        w = (int)atomicAdd(counter, 1u);
+        if (w >= num_items) w = -1;
+        ctl->q[qs] = ok ? w : -1;
+        mbar_arrive(&ctl->qfull[qs]);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (++qs == kQueue) { qs = 0; qp ^= 1; }
+      if (!ok || w < 0) break;
+      const Item it = decode<MODE>(p, w);
+      int tok[4] = {0, 0, 0, 0};
+      if (it.type == GM_FWD1 || it.type == GM_BWD_DA) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tok[q] = tok_of(p, it.row0 + lane * 4 + q);
+      }
+      if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
+        // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all of
+        // its GEMM1 column tiles are done, then order the async-proxy loads
+        // after the acquire.
+        if (lane == 0) {
+          ok = wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc);
+          fence_proxy_async_global();
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      const uint32_t bytes = kAStage + item_bn(p, it.type) * 128;
+      for (int kk = 0; kk < it.k_iters; ++kk) {
+        if (lane == 0) {
+          ok = mbar_wait(&ctl->empty[stage], phase ^ 1, wc);
+          if (ok) mbar_arrive_expect_tx(&ctl->full[stage], bytes);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        issue_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, &ctl->full[stage], lane,
+                          tok);
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, qs = 0, qp = 0, tcount = 0;
+    while (true) {
+      if (!mbar_wait(&ctl->qfull[qs], qp, wc)) break;
+      const int w = ctl->q[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
+      if (++qs == kQueue) { qs = 0; qp ^= 1; }
+      if (w < 0) break;
+      const Item it = decode<MODE>(p, w);
+      const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
+      if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)) break;
+      tc_fence_after();
+      const int bn = item_bn(p, it.type);
+      const bool amn = a_mn_major<MODE>(p, it.type), bmn = b_mn_major<MODE>(p, it.type);
+      const uint32_t idesc = idesc_bf16(128, bn, amn ? 1 : 0, bmn ? 1 : 0);
+      const uint32_t d = tmem + buf * 256;
+      bool ok = true;
+      for (int kk = 0; kk < it.k_iters; ++kk) {
+        if (!mbar_wait(&ctl->full[stage], phase, wc)) { ok = false; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBStage);
+#pragma unroll
+          for (int k16 = 0; k16 < 4; ++k16) {
+            const uint64_t ad = amn ? sdesc_sw128(a0 + k16 * 2048, 8192, 1024) : sdesc_sw128(a0 + k16 * 32, 16, 1024);
+            const uint64_t bd = bmn ? sdesc_sw128(b0 + k16 * 2048, 8192, 1024) : sdesc_sw128(b0 + k16 * 32, 16, 1024);
+            mma_bf16(d, ad, bd, idesc, (kk | k16) != 0 ? 1u : 0u);
+          }
+          mma_commit(&ctl->empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&ctl->tfull[buf]);
+      __syncwarp();
+      ++tcount;
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    uint32_t qs = 0, qp = 0, tcount = 0;
+    while (true) {
+      if (!mbar_wait(&ctl->qfull[qs], qp, wc)) break;
+      const int w = ctl->q[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
+      if (++qs == kQueue) { qs = 0; qp ^= 1; }
+      if (w < 0) break;
+      const Item it = decode<MODE>(p, w);
+      const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
+      if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * 256;
+      if (MODE == GM_FWD_RING && it.type == GM_FWD2 && warp == 2 && lane == 0) {
+        // the accumulator is complete, so every load of this tile's ring
+        // rows has landed: release the rows for reuse
+        red_release_gpu_add(&p.ring_flags[p.m_tiles + it.m], 1u);
+      }
+      bool ok = true;
+      if (MODE == GM_FWD_RING && it.type == GM_FWD1) {
+        // the ring slot rows this tile writes were last read by GEMM2 of the
+        // tile ring_slots minibatches back; each warp waits on its own (no
+        // CTA-level barrier on a path that a bounded wait can abandon)
+        const int back = it.m - p.ring_slots * (p.ring_rows / kTileRows);
+        if (back >= 0) {
+          if (lane == 0) ok = wait_flag_geq(&p.ring_flags[p.m_tiles + back], (uint32_t)p.n_tiles, wc);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+      }
+      if (!ok) break;
+      switch (it.type) {
+        case GM_DENSE: epi_dense(p, it, tbase, row); break;
+        case GM_FWD1: epi_fwd1(p, it, tbase, row); break;
+        case GM_FWD2: epi_scatter(p, it, tbase, row, p.bn); break;
+        case GM_BWD_DA: epi_bwd_da(p, it, tbase, row); break;
+        case GM_BWD_DX: epi_scatter(p, it, tbase, row, p.bn); break;
+        default: epi_wgrad(p, it, tbase, row); break;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+      if (MODE == GM_FWD_RING && it.type == GM_FWD1) {
+        // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
+        // read by TMA): each epilogue warp adds 1, so a tile is complete when
+        // its counter reaches 4 * (GEMM1 column tiles)
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) {
+          const bool skip = (p.debug_flags & MOK_DEBUG_SKIP_RING_SIGNAL) && it.m == 0 && it.n == 0 && warp == 2;
+          __threadfence();
+          if (!skip) red_release_gpu_add(&p.ring_flags[it.m], 1u);
+        }
+      }
+      ++tcount;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
+  const size_t smem = gemm_smem_bytes();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  gemm_kernel<MODE><<<grid, kGemmThreads, smem, st>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return 1024 + kStages * (kAStage + kBStage) + sizeof(Ctl); }
+
+cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
+  switch (mode) {
+    case GM_DENSE: return launch_mode<GM_DENSE>(maps, p, grid, st);
+    case GM_FWD1: return launch_mode<GM_FWD1>(maps, p, grid, st);
+    case GM_FWD2: return launch_mode<GM_FWD2>(maps, p, grid, st);
+    case GM_BWD_DA: return launch_mode<GM_BWD_DA>(maps, p, grid, st);
+    case GM_BWD_DX: return launch_mode<GM_BWD_DX>(maps, p, grid, st);
+    case GM_WG13: return launch_mode<GM_WG13>(maps, p, grid, st);
+    case GM_WG2: return launch_mode<GM_WG2>(maps, p, grid, st);
+    case GM_FWD_RING: return launch_mode<GM_FWD_RING>(maps, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mok

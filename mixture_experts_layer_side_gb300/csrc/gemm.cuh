@@ -1,0 +1,69 @@
+// Expert-grouped GEMM kernel family (tcgen05 + TMEM + TMA), shared declarations.
+#pragma once
+
+#include "mok_internal.cuh"
+
+namespace mok {
+
+// What one launch of the grouped GEMM computes.
+enum GemmMode : int {
+  GM_DENSE = 0,   // C[M,N] f32 = A * B, A [M,K] or [K,M], B [N,K] or [K,N] (diagnostic)
+  GM_FWD1 = 1,    // [h|u] = gather(x) * [W1|W3];  epilogue SwiGLU -> ring (a), ctx (h, u)
+  GM_FWD2 = 2,    // y = ring(a) * W2;             epilogue scatter y -> Yk[f]
+  GM_BWD_DA = 3,  // dA' = gather(dout) * W2^T;    epilogue SwiGLU backward, s*a, ds partials
+  GM_BWD_DX = 4,  // dx = [dh|du] * [W1|W3]^T;     epilogue scatter -> dXk[f]
+  GM_WG13 = 5,    // [dW1|dW3]_e = gather(x)_e^T * [dh|du]_e
+  GM_WG2 = 6,     // dW2_e = (s a)_e^T * gather(dout)_e
+  GM_FWD_RING = 7 // GM_FWD1 and GM_FWD2 interleaved through the minibatch ring in one launch
+};
+
+constexpr int kStages = 4;
+constexpr int kAStage = 128 * 128;  // 128 rows x 128 bytes
+constexpr int kBStage = 256 * 128;  // up to 256 rows x 128 bytes
+constexpr int kQueue = 4;           // depth of the work-item queue in smem
+constexpr int kGemmThreads = 192;   // warp 0 TMA producer, warp 1 MMA, warps 2-5 epilogue
+
+constexpr int kMaxMaps = 6;
+struct TmapSet {
+  CUtensorMap m[kMaxMaps];
+};
+
+struct GemmParams {
+  int bn;         // N tile (128 or 256)
+  int n_tiles;    // N tiles per M tile
+  int k_iters;    // K iterations of 128 bytes (row-tiled and dense modes)
+  int m_tiles;    // dense: M/128; weight-gradient modes: M/128 per expert
+  int m_tile_begin, m_tile_end;  // row-tiled modes: range of 128-row tiles
+  int T, H, I, E, k;
+  int32_t* hdr;   // workspace header: error word, used rows/tiles, counters
+  int counter;    // index of this launch's dynamic tile counter
+  const int32_t* tile_expert;
+  const int32_t* pad_perm;
+  const int32_t* padded_offsets;
+  // epilogue operands
+  float* out_f32;
+  long ld_out;
+  __nv_bfloat16* ctx_hu;   // [pad, 2I]
+  __nv_bfloat16* ring;     // [ring_slots * ring_rows, I]
+  int ring_rows, ring_slots;
+  uint32_t* ring_flags;    // [2 * tile_capacity]
+  __nv_bfloat16* yk;       // [R, H]
+  __nv_bfloat16* dhu;      // [pad, 2I]
+  __nv_bfloat16* as;       // [pad, I]
+  float* dsp;              // [pad, n_tiles]
+  const float* scores;     // [R]
+  __nv_bfloat16* dw0;      // dW1 (WG13) or dW2 (WG2)
+  __nv_bfloat16* dw1;      // dW3 (WG13)
+  int a_mn, b_mn;          // dense: operand major-ness (1 = M/N-major)
+  int g1_tiles;            // ring: GEMM1 N tiles per M tile
+  int debug_flags;
+  int nmaps;               // tensor maps in use (prefetched at start)
+  // Ring launch: m_tiles holds the tile capacity; ring_flags[m] counts the
+  // epilogue warps (4 per column tile) that published GEMM1 rows of tile m,
+  // ring_flags[m_tiles + m] counts the GEMM2 column tiles that consumed them.
+};
+
+size_t gemm_smem_bytes();
+cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
+
+}  // namespace mok

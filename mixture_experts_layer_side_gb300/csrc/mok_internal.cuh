@@ -1,0 +1,72 @@
+// Definitions shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mok.h"
+
+// Device error bits of the workspace error word (header word 0).
+#define MOK_ERRBIT_BAD_INDEX 1
+#define MOK_ERRBIT_TIMEOUT 2
+
+namespace mok {
+
+constexpr int kTileRows = 128;      // padded expert segments and GEMM M tile
+constexpr int kSchedChunk = 1024;   // routed rows per schedule warp
+constexpr int kHeaderWords = 64;    // int32 words of the workspace header
+// header word indices
+constexpr int kHdrError = 0;
+constexpr int kHdrPaddedRows = 1;
+constexpr int kHdrTiles = 2;
+constexpr int kHdrAbort = 3;       // launch-wide abort word (cleared per call)
+constexpr int kHdrCounters = 16;    // [16, 48): per-launch dynamic tile counters
+constexpr int kNumCounters = 32;
+
+struct WsLayout {
+  // schedule
+  size_t header, counts, offsets, padded_offsets, perm, inv_perm, pad_perm, pad_inv, tile_expert;
+  size_t chunk_hist, chunk_base;
+  // forward
+  size_t ring_flags;  // uint32 [2 * tile_capacity]: GEMM1 / GEMM2 tiles done per M tile
+  size_t ring;        // bf16 [ring_slots * minibatch_rows, I]  (MXFP8: e4m3 codes)
+  size_t ring_sf;     // MXFP8: u8 scales [ring_slots * minibatch_rows, I/32]
+  size_t yk;          // bf16 [R, H]: expert outputs (forward), dX parts (backward)
+  // backward
+  size_t dhu;         // bf16 [pad_capacity, 2I]
+  size_t as;          // bf16 [pad_capacity, I]  s * a
+  size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
+  // MXFP8 activation copies
+  size_t xq, xsf;     // x quantised along H: u8 [T, H], [T, H/32]
+  size_t dq, dsf;     // dout quantised along H
+  size_t dhuq, dhusf; // dh|du quantised along I: u8 [pad, 2I], [pad, 2I/32]
+  size_t total;
+  int64_t pad_capacity, tile_capacity, nchunks;
+  int minibatch_rows, ring_slots;
+};
+
+// Host: layout of the workspace (offsets are 256-byte aligned).
+WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, int num_sms);
+int effective_minibatch_rows(const mok_shape& s, const mok_config& c, int num_sms);
+int device_sm_count();
+
+// Host: tensor maps (driver entry point resolved once).
+bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr, const uint64_t* dims,
+               const uint64_t* strides_bytes /* rank-1 */, const uint32_t* box, bool swizzle128);
+
+// Launchers (return a CUDA error code).
+cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, const int32_t* idx,
+                            cudaStream_t st);
+cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* yk,
+                           const float* scores, __nv_bfloat16* out, cudaStream_t st);
+cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_t* ws, float* ds, int n_parts,
+                             cudaStream_t st);
+cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
+                               __nv_bfloat16* xg, cudaStream_t st);
+cudaError_t launch_mxfp8_quantize(const __nv_bfloat16* src, int batch, int rows, int cols, int block_axis,
+                                  uint8_t* q, uint8_t* sf, cudaStream_t st);
+
+}  // namespace mok

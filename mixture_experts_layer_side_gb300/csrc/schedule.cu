@@ -1,0 +1,192 @@
+// Device-side schedule: expert histogram, exclusive scan, stable counting-sort
+// permutation, 128-row padded offsets, tile table and inverse permutations.
+//
+// One schedule table serves forward dispatch/combine and the backward's
+// reverse combine/dispatch ("Cursor Open-Sources Mixture-of-Kittens (MoK)",
+// "Three design decisions that matter", communication-direction paragraph),
+// and it is built on the GPU without any host readback (same section,
+// ring-token-buffer paragraph: the CPU is taken out of the loop).
+//
+// Three kernels, all integer work, so the result is exact and independent
+// of scheduling:
+//   1. sched_count: per chunk of 1024 routed rows, a per-expert histogram.
+//   2. sched_scan : one block; per expert an exclusive scan over chunks (the
+//                   chunk's base position), then the exclusive scans of the
+//                   counts and of the 128-padded counts, the tile table and
+//                   the -1 markers of padding rows.
+//   3. sched_place: per chunk, one warp walks its rows in increasing f,
+//                   32 at a time; __match_any_sync groups equal experts and
+//                   the rank inside the group is the count of lower lanes,
+//                   so positions are assigned in increasing f (stable).
+#include "mok_internal.cuh"
+
+namespace mok {
+
+namespace {
+
+constexpr int kCountThreads = 256;
+
+__global__ void sched_count(const int32_t* __restrict__ idx, int R, int E, int32_t* __restrict__ chunk_hist,
+                            int32_t* __restrict__ hdr) {
+  extern __shared__ int32_t hist[];
+  const int chunk = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int f0 = chunk * kSchedChunk;
+  const int f1 = min(f0 + kSchedChunk, R);
+  bool bad = false;
+  for (int f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+    const int e = idx[f];
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) atomicOr(&hdr[kHdrError], MOK_ERRBIT_BAD_INDEX);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[(size_t)chunk * E + e] = hist[e];
+}
+
+// Exclusive block scan of one value per thread (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total_out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += n;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) *total_out = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) sched_scan(int E, int nchunks, const int32_t* __restrict__ chunk_hist,
+                                                   int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
+                                                   int32_t* __restrict__ offsets, int32_t* __restrict__ poff,
+                                                   int32_t* __restrict__ tile_expert, int32_t* __restrict__ pad_perm,
+                                                   int32_t* __restrict__ hdr) {
+  __shared__ int warp_tot[32];
+  __shared__ int tot0, tot1;
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    // running sum over chunks; loads are independent of the sum, so unroll
+    int c = 0;
+    for (; c + 8 <= nchunks; c += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = chunk_hist[(size_t)(c + u) * E + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        chunk_base[(size_t)(c + u) * E + e] = cnt;
+        cnt += v[u];
+      }
+    }
+    for (; c < nchunks; ++c) {
+      const int v = chunk_hist[(size_t)c * E + e];
+      chunk_base[(size_t)c * E + e] = cnt;
+      cnt += v;
+    }
+  }
+  const int padded = (cnt + kTileRows - 1) / kTileRows * kTileRows;
+  const int off = block_exclusive_scan(e < E ? cnt : 0, warp_tot, &tot0);
+  const int poffe = block_exclusive_scan(e < E ? padded : 0, warp_tot, &tot1);
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = off;
+    poff[e] = poffe;
+    for (int t = poffe / kTileRows; t < (poffe + padded) / kTileRows; ++t) tile_expert[t] = e;
+    for (int r = poffe + cnt; r < poffe + padded; ++r) pad_perm[r] = -1;
+  }
+  if (e == 0) {
+    offsets[E] = tot0;
+    poff[E] = tot1;
+    hdr[kHdrPaddedRows] = tot1;
+    hdr[kHdrTiles] = tot1 / kTileRows;
+  }
+}
+
+// Each warp handles one chunk of kSchedChunk routed rows.
+constexpr int kPlaceWarps = 4;
+
+__global__ void __launch_bounds__(kPlaceWarps * 32)
+    sched_place(const int32_t* __restrict__ idx, int R, int E, int nchunks, const int32_t* __restrict__ chunk_base,
+                const int32_t* __restrict__ offsets, const int32_t* __restrict__ poff, int32_t* __restrict__ perm,
+                int32_t* __restrict__ inv_perm, int32_t* __restrict__ pad_perm, int32_t* __restrict__ pad_inv) {
+  extern __shared__ int32_t cursor_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x * kPlaceWarps + warp;
+  int32_t* cursor = cursor_all + warp * E;
+  if (chunk < nchunks)
+    for (int e = lane; e < E; e += 32) cursor[e] = chunk_base[(size_t)chunk * E + e];
+  __syncwarp();
+  if (chunk >= nchunks) return;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int f0 = chunk * kSchedChunk;
+  for (int it = 0; it < kSchedChunk / 32; ++it) {
+    const int f = f0 + it * 32 + lane;
+    int e = -1;
+    if (f < R) {
+      e = idx[f];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(grp & lt_mask);
+    int pos = 0;
+    if (e >= 0) pos = cursor[e] + rank;
+    __syncwarp();
+    if (e >= 0 && rank == 0) cursor[e] += __popc(grp);
+    __syncwarp();
+    if (f < R) {
+      if (e >= 0) {
+        const int r = offsets[e] + pos;
+        const int prow = poff[e] + pos;
+        perm[r] = f;
+        inv_perm[f] = r;
+        pad_perm[prow] = f;
+        pad_inv[f] = prow;
+      } else {
+        inv_perm[f] = -1;
+        pad_inv[f] = -1;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, const int32_t* idx,
+                            cudaStream_t st) {
+  const int R = s.T * s.k, E = s.E;
+  const int nchunks = (int)L.nchunks;
+  int32_t* hdr = reinterpret_cast<int32_t*>(ws + L.header);
+  auto P = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  cudaError_t err = cudaMemsetAsync(hdr, 0, kHeaderWords * sizeof(int32_t), st);
+  if (err != cudaSuccess) return err;
+  sched_count<<<nchunks, kCountThreads, E * sizeof(int32_t), st>>>(idx, R, E, P(L.chunk_hist), hdr);
+  sched_scan<<<1, 1024, 0, st>>>(E, nchunks, P(L.chunk_hist), P(L.chunk_base), P(L.counts), P(L.offsets),
+                                 P(L.padded_offsets), P(L.tile_expert), P(L.pad_perm), hdr);
+  const int blocks = (nchunks + kPlaceWarps - 1) / kPlaceWarps;
+  const size_t smem = (size_t)kPlaceWarps * E * sizeof(int32_t);
+  sched_place<<<blocks, kPlaceWarps * 32, smem, st>>>(idx, R, E, nchunks, P(L.chunk_base), P(L.offsets),
+                                                      P(L.padded_offsets), P(L.perm), P(L.inv_perm),
+                                                      P(L.pad_perm), P(L.pad_inv));
+  return cudaGetLastError();
+}
+
+}  // namespace mok

@@ -1,0 +1,81 @@
+"""Host-side convenience wrapper around the C ABI (no compute here).
+
+``MoKLayer`` owns the caller-side buffers the C ABI asks for (workspace and
+forward context, allocated once and reused, as the pages' workspace is:
+"Mixture-of-Kittens (MoK)", "Core concepts", Workspace row) and forwards the
+calls of the pages' functional API -- build_schedule, forward, backward --
+to libmok.so.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from .inputs import Shape
+
+PRECISIONS = {"bf16": _lib.MOK_BF16, "mxfp8": _lib.MOK_MXFP8}
+
+
+class MoKLayer:
+    def __init__(self, shape: Shape, precision="bf16", minibatch_rows=0, ring_slots=0, debug_flags=0,
+                 device="cuda"):
+        self.shape = shape
+        self.cshape = _lib.shape_of(shape.T, shape.H, shape.I, shape.E, shape.k)
+        self.cfg = _lib.config(minibatch_rows=minibatch_rows, ring_slots=ring_slots, debug_flags=debug_flags)
+        self.prec = PRECISIONS[precision]
+        self.device = torch.device(device)
+        ws_bytes = _lib.mok_workspace_size(self.cshape, self.cfg, self.prec)
+        ctx_bytes = _lib.mok_ctx_size(self.cshape, self.cfg, self.prec)
+        if ws_bytes == 0 or ctx_bytes == 0:
+            raise _lib.MokError(2, "unsupported shape or config")
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
+        self.ctx = torch.empty(ctx_bytes, dtype=torch.uint8, device=self.device)
+        self.layout = _lib.mok_workspace_layout(self.cshape, self.cfg, self.prec)
+
+    # -- the functional API -------------------------------------------------
+    def build_schedule(self, topk_idx, stream=None):
+        _lib.mok_build_schedule(self.cshape, self.cfg, self.ws, topk_idx, stream)
+
+    def forward(self, x, scores, W1, W3, W2, out=None, stream=None):
+        if out is None:
+            out = torch.empty((self.shape.T, self.shape.H), dtype=torch.bfloat16, device=self.device)
+        _lib.mok_forward(self.cshape, self.cfg, self.prec, self.ws, x, scores, W1, W3, W2, out, self.ctx, stream)
+        return out
+
+    def backward(self, x, scores, W1, W3, W2, dout, grads=None, stream=None):
+        s = self.shape
+        if grads is None:
+            grads = self.alloc_grads()
+        _lib.mok_backward(self.cshape, self.cfg, self.prec, self.ws, self.ctx, x, scores, W1, W3, W2, dout,
+                          grads["dX"], grads["dW1"], grads["dW3"], grads["dW2"], grads["ds"], stream)
+        return grads
+
+    def alloc_grads(self):
+        s, d = self.shape, self.device
+        return dict(dX=torch.empty((s.T, s.H), dtype=torch.bfloat16, device=d),
+                    dW1=torch.empty((s.E, s.H, s.I), dtype=torch.bfloat16, device=d),
+                    dW3=torch.empty((s.E, s.H, s.I), dtype=torch.bfloat16, device=d),
+                    dW2=torch.empty((s.E, s.I, s.H), dtype=torch.bfloat16, device=d),
+                    ds=torch.empty((s.T, s.k), dtype=torch.float32, device=d))
+
+    def check(self, stream=None):
+        """Synchronise and raise if the device recorded an error."""
+        st = _lib.mok_check(self.ws, stream)
+        if st != 0:
+            raise _lib.MokError(st, "device")
+
+    # -- inspection ---------------------------------------------------------
+    def schedule_arrays(self):
+        """Views of the schedule arrays inside the workspace (int32)."""
+        s, L = self.shape, self.layout
+        R, E = s.T * s.k, s.E
+
+        def view(off, n):
+            return self.ws[off:off + 4 * n].view(torch.int32)
+
+        hdr = view(L["header"], 16)
+        return dict(header=hdr, counts=view(L["counts"], E), offsets=view(L["offsets"], E + 1),
+                    padded_offsets=view(L["padded_offsets"], E + 1), perm=view(L["perm"], R),
+                    inv_perm=view(L["inv_perm"], R), pad_perm=view(L["pad_perm"], L["pad_capacity"]),
+                    pad_inv=view(L["pad_inv"], R), tile_expert=view(L["tile_expert"], L["tile_capacity"]))
