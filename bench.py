@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer: one step = schedule + forward + backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dsv3]
+                    [--impl mok|reference]
+
+Default workload: the DeepSeek-V3-shaped layer (T=8192, H=7168, I=2048,
+E=256, top-8, Zipf-skewed routing), BF16, all experts on one GPU -- the
+configuration the tensor-peak target is quoted on.  Inputs are seeded
+synthetic tensors resident in HBM; the expert weights alone (22.5 GB) are far
+larger than L2, so consecutive steps cannot hit in L2.
+
+Prints ONE JSON line (rank 0).  ``value`` is whole-job algorithmic TFLOP/s
+(18*R*H*I FLOPs per step, R = T*k, padding excluded); ``e2e`` is the same
+metric with each step's inputs copied from pinned host memory and its results
+(out, dX, ds) read back inside the timed region.  ``--impl reference`` times
+the float64 CPU oracle (the reference arm of this build) on a bounded sample.
+Under torchrun every rank runs an independent replica (the layer does not
+shard across GPUs); timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd TFLOP/s"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_PHASES = ("fwd_gemm", "bwd_da", "bwd_dx", "bwd_wg13", "bwd_wg2")
+HBM_PHASES = ("fwd_combine", "bwd_dx_combine")
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
+    ap.add_argument("--workload", default="dsv3")
+    ap.add_argument("--minibatch-rows", type=int, default=0)
+    ap.add_argument("--ring-slots", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def flops_per_step(shape):
+    # GEMM FLOPs: forward 6*R*H*I (W1|W3: 4RHI, W2: 2RHI), backward 12*R*H*I
+    return 18.0 * shape.R * shape.H * shape.I
+
+
+def phase_flops(shape):
+    RHI = float(shape.R) * shape.H * shape.I
+    return {"fwd_gemm": 6 * RHI, "bwd_da": 2 * RHI, "bwd_dx": 4 * RHI, "bwd_wg13": 4 * RHI, "bwd_wg2": 2 * RHI}
+
+
+def phase_bytes(shape):
+    # algorithmic bytes of the HBM-bound kernels (bf16 = 2 B, f32 = 4 B)
+    R, T, H = shape.R, shape.T, shape.H
+    return {"fwd_combine": R * H * 2 + R * 4 + T * H * 2, "bwd_dx_combine": R * H * 2 + T * H * 2}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, device_index):
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- traffic
+def recorded_traffic(phase, workload):
+    """DRAM bytes per launch of a kernel from the committed ncu summary, if it
+    was taken on the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    src = os.path.join(ROOT, "mixture_experts_layer_side_gb300", "csrc", "gemm.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    for line in text.splitlines():
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == phase and cells[1] == workload and cells[3] == digest:
+            try:
+                return float(cells[2])
+            except ValueError:
+                return None
+    return None
+
+
+# ---------------------------------------------------------------- oracle
+class OracleSample:
+    """A bounded sample of the workload for the float64 oracle: same H and I,
+    ``tokens`` tokens routed top-``k`` over ``experts`` experts.  Inputs are
+    drawn once; ``run()`` times one forward + backward."""
+
+    def __init__(self, shape, tokens, experts, k, seed):
+        from mixture_experts_layer_side_gb300.inputs import Shape, make_inputs
+        sub = Shape(tokens, shape.H, shape.I, experts, k)
+        inp = make_inputs(sub, "uniform", seed=seed, device="cpu")
+        self.a = {n: (v.double().numpy() if v.is_floating_point() else v.numpy()) for n, v in inp.items()}
+        self.flops = flops_per_step(sub)
+        self.desc = (f"float64 NumPy oracle, forward + backward of a {tokens}-token, {experts}-expert, top-{k} "
+                     f"slice at H={shape.H}, I={shape.I} (R={tokens * k} routed rows); throughput = the "
+                     f"slice's 18*R*H*I FLOPs / its time")
+
+    def run(self):
+        from oracle import moe
+        a = self.a
+        t0 = time.perf_counter()
+        moe.forward(a["x"], a["idx"], a["s"], a["W1"], a["W3"], a["W2"])
+        moe.backward(a["x"], a["idx"], a["s"], a["W1"], a["W3"], a["W2"], a["dout"])
+        return time.perf_counter() - t0
+
+
+def host_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- arms
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from mixture_experts_layer_side_gb300.inputs import WORKLOADS
+    shape, routing, prec = WORKLOADS[args.workload]
+    sample = OracleSample(shape, tokens=64, experts=2, k=2, seed=7)
+    flops, desc = sample.flops, sample.desc
+    for _ in range(args.warmup):
+        sample.run()
+    total = sum(sample.run() for _ in range(args.steps))
+    value = flops * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args, shape, routing, prec),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(args, shape, routing, prec, layer=None):
+    cfg = {"workload": f"{args.workload}: MoE layer T={shape.T} H={shape.H} I={shape.I} E={shape.E} "
+                       f"top-{shape.k}, {routing} routing, {prec}",
+           "T": shape.T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k, "routing": routing,
+           "precision": prec, "global_batch": shape.T, "parallelism": "replicas",
+           "l2": "inputs larger than L2 (expert weights alone exceed 129 MB)"}
+    if layer is not None:
+        cfg["minibatch_rows"] = args.minibatch_rows or "two-wave default"
+        cfg["ring_slots"] = args.ring_slots or 4
+    return cfg
+
+
+def run_mok(args):
+    import torch
+
+    from mixture_experts_layer_side_gb300 import _lib
+    from mixture_experts_layer_side_gb300.inputs import WORKLOADS, load_stats, make_inputs
+    from mixture_experts_layer_side_gb300.layer import MoKLayer
+
+    world, rank, local = dist_setup(args)
+    shape, routing, prec = WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = make_inputs(shape, routing, seed=1000 + rank, device=dev)
+    layer = MoKLayer(shape, precision=prec, minibatch_rows=args.minibatch_rows, ring_slots=args.ring_slots,
+                     device=dev)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    grads = layer.alloc_grads()
+    stream = torch.cuda.current_stream()
+
+    def step(x, idx, s, dout):
+        layer.build_schedule(idx)
+        layer.forward(x, s, inp["W1"], inp["W3"], inp["W2"], out=out)
+        layer.backward(x, s, inp["W1"], inp["W3"], inp["W2"], dout, grads=grads)
+
+    for _ in range(max(args.warmup, 3)):
+        step(inp["x"], inp["idx"], inp["s"], inp["dout"])
+    torch.cuda.synchronize()
+    layer.check()
+
+    # ------------------------------------------------ device-resident timing
+    sampler = ClockSampler(dev.index)
+    barrier(world)
+    torch.cuda.synchronize()
+    _lib.mok_trace_enable(True)
+    launches0 = _lib.mok_launch_count()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first sample before the timed region
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(inp["x"], inp["idx"], inp["s"], inp["dout"])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    launches = _lib.mok_launch_count() - launches0
+    phases = _lib.mok_trace_read()
+    _lib.mok_trace_enable(False)
+    layer.check()
+    ms = max_over_ranks(world, ev0.elapsed_time(ev1) / args.steps)
+    barrier(world)
+
+    fps = flops_per_step(shape)
+    value = world * fps / (ms / 1e3) / 1e12
+
+    # ------------------------------------------------ roofline of the dominant kernel
+    peaks, peaks_src = load_peaks()
+    pf, pb = phase_flops(shape), phase_bytes(shape)
+    per_phase = {n: {"ms": v[0] / max(v[1], 1), "runs": v[1]} for n, v in phases.items() if v[1]}
+    dom = max(GEMM_PHASES, key=lambda n: per_phase.get(n, {"ms": 0})["ms"])
+    dom_ms = per_phase[dom]["ms"]
+    achieved = pf[dom] / (dom_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside a step)",
+                "traffic": recorded_traffic(dom, args.workload)}
+    for n in per_phase:
+        if n in pf:
+            per_phase[n]["tflops"] = pf[n] / (per_phase[n]["ms"] / 1e3) / 1e12
+            per_phase[n]["frac_of_peak"] = per_phase[n]["tflops"] / peak
+        if n in pb:
+            gbs = pb[n] / (per_phase[n]["ms"] / 1e3) / 1e9
+            per_phase[n]["gbs"] = gbs
+            per_phase[n]["frac_of_hbm"] = gbs / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    sched_share = per_phase.get("schedule", {"ms": 0})["ms"] / ms
+
+    # ------------------------------------------------ end to end through the C ABI, host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = inp["x"].cpu().pin_memory()
+        hidx = inp["idx"].cpu().pin_memory()
+        hs = inp["s"].cpu().pin_memory()
+        hd = inp["dout"].cpu().pin_memory()
+        dx_, didx, ds_, dd = (torch.empty_like(inp[n]) for n in ("x", "idx", "s", "dout"))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hdX = torch.empty(grads["dX"].shape, dtype=torch.bfloat16).pin_memory()
+        hds = torch.empty(grads["ds"].shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            dx_.copy_(hx, non_blocking=True)
+            didx.copy_(hidx, non_blocking=True)
+            ds_.copy_(hs, non_blocking=True)
+            dd.copy_(hd, non_blocking=True)
+            step(dx_, didx, ds_, dd)
+            hout.copy_(out, non_blocking=True)
+            hdX.copy_(grads["dX"], non_blocking=True)
+            hds.copy_(grads["ds"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        layer.check()
+        ems = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
+        h2d = sum(t.numel() * t.element_size() for t in (hx, hidx, hs, hd))
+        d2h = sum(t.numel() * t.element_size() for t in (hout, hdX, hds))
+        e2e = {"value": world * fps / (ems / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ------------------------------------------------ CPU baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(shape, tokens=256, experts=4, k=2, seed=11)
+        dt = sample.run()
+        cpu = {"value": sample.flops / dt / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": sample.desc, "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": prec, "data": "synthetic (seeded, resident in HBM)",
+            "config": workload_config(args, shape, routing, prec, layer),
+            "tokens_per_s": world * shape.T / (ms / 1e3),
+            "gpu_launches": launches,
+            "roofline": roofline,
+            "phases": per_phase,
+            "schedule_share": sched_share,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "load": load_stats(inp["idx"], shape.E),
+            "peaks_source": peaks_src,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_mok(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

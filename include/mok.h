@@ -238,6 +238,33 @@ mok_status mok_gather_rows(const mok_shape* shape, const mok_config* cfg, const 
 mok_status mok_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int32_t a_mn_major, const void* B,
                          int32_t b_mn_major, float* C, void* scratch, void* stream);
 
+/*
+ * Phase tracing (a diagnostic for measurement).  While enabled, every call
+ * records a pair of CUDA events on its stream around each of its kernel
+ * phases; mok_trace_read synchronises on them and returns, per phase, the
+ * summed duration in ms and the number of times the phase ran since the
+ * last read, then forgets them.  This is the library's only host-side
+ * global state; enable it from one thread at a time.
+ */
+enum {
+  MOK_PHASE_SCHEDULE = 0,      /* histogram, scan, placement */
+  MOK_PHASE_FWD_GEMM = 1,      /* ring kernel: GEMM1 + SwiGLU, GEMM2 + scatter */
+  MOK_PHASE_FWD_COMBINE = 2,   /* weighted combine */
+  MOK_PHASE_BWD_DA = 3,        /* dA' GEMM + SwiGLU backward + ds partials */
+  MOK_PHASE_BWD_DS = 4,        /* ds reduction */
+  MOK_PHASE_BWD_DX = 5,        /* dX GEMM + scatter */
+  MOK_PHASE_BWD_DX_COMBINE = 6,/* dX combine */
+  MOK_PHASE_BWD_WG13 = 7,      /* dW1 | dW3 grouped GEMM */
+  MOK_PHASE_BWD_WG2 = 8,       /* dW2 grouped GEMM */
+  MOK_PHASE_QUANT = 9,         /* MXFP8 quantisation of activations */
+  MOK_NUM_PHASES = 10
+};
+mok_status mok_trace_enable(int32_t on);
+mok_status mok_trace_read(float* ms /* [MOK_NUM_PHASES] */, int32_t* count /* [MOK_NUM_PHASES] */);
+
+/* Number of kernels the library has launched in this process so far. */
+int64_t mok_launch_count(void);
+
 /* Synchronise `stream`, then return (and clear) the status recorded in the
  * workspace's error word; MOK_OK if none. */
 mok_status mok_check(void* ws, void* stream);

@@ -27,7 +27,11 @@ STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "M
 # every entry point include/mok.h declares
 EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_build_schedule", "mok_forward",
            "mok_backward", "mok_mxfp8_quantize", "mok_gather_rows", "mok_gemm_bf16", "mok_check",
-           "mok_device_sm_count", "mok_status_string", "mok_version"]
+           "mok_device_sm_count", "mok_status_string", "mok_version", "mok_trace_enable", "mok_trace_read",
+           "mok_launch_count"]
+
+PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
+          "bwd_wg2", "quant"]
 
 
 class MokError(RuntimeError):
@@ -79,6 +83,9 @@ def _load():
         "mok_device_sm_count": (i32, []),
         "mok_status_string": (ctypes.c_char_p, [i32]),
         "mok_version": (ctypes.c_char_p, []),
+        "mok_trace_enable": (i32, [i32]),
+        "mok_trace_read": (i32, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),
+        "mok_launch_count": (ctypes.c_int64, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -184,6 +191,22 @@ def mok_gemm_bf16(A, a_mn_major, B, b_mn_major, C, scratch, stream=None):
     K = A.shape[0] if a_mn_major else A.shape[1]
     _ok(LIB.mok_gemm_bf16(M, N, K, _ptr(A), int(a_mn_major), _ptr(B), int(b_mn_major), _ptr(C), _ptr(scratch),
                           _stream(stream)), "mok_gemm_bf16")
+
+
+def mok_trace_enable(on=True):
+    _ok(LIB.mok_trace_enable(1 if on else 0), "mok_trace_enable")
+
+
+def mok_trace_read():
+    """{phase: (summed ms, runs)} since the last read (synchronises)."""
+    ms = (ctypes.c_float * len(PHASES))()
+    cnt = (ctypes.c_int32 * len(PHASES))()
+    _ok(LIB.mok_trace_read(ms, cnt), "mok_trace_read")
+    return {name: (ms[i], cnt[i]) for i, name in enumerate(PHASES)}
+
+
+def mok_launch_count():
+    return LIB.mok_launch_count()
 
 
 def mok_check(ws, stream=None):

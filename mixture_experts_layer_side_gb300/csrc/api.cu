@@ -4,7 +4,9 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "gemm.cuh"
 
@@ -123,6 +125,46 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
 }  // namespace mok
 
 using namespace mok;
+
+namespace {
+
+// ---------------------------------------------------------------- tracing
+std::atomic<int64_t> g_launches{0};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+struct TraceRec {
+  int phase;
+  cudaEvent_t a, b;
+};
+std::vector<TraceRec> g_trace;
+
+// Records an event pair around one phase of a call (when tracing is on) and
+// counts the phase's kernel launches.
+class Phase {
+ public:
+  Phase(int phase, cudaStream_t st, int kernels) : st_(st) {
+    g_launches += kernels;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_trace_on) return;
+    rec_.phase = phase;
+    if (cudaEventCreate(&rec_.a) != cudaSuccess || cudaEventCreate(&rec_.b) != cudaSuccess) return;
+    cudaEventRecord(rec_.a, st_);
+    on_ = true;
+  }
+  ~Phase() {
+    if (!on_) return;
+    cudaEventRecord(rec_.b, st_);
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace.push_back(rec_);
+  }
+
+ private:
+  cudaStream_t st_;
+  TraceRec rec_{};
+  bool on_ = false;
+};
+
+}  // namespace
 
 namespace {
 
@@ -272,6 +314,7 @@ mok_status mok_build_schedule(const mok_shape* shape, const mok_config* cfg, voi
   const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
   // the schedule part of the layout is the same for both precisions
   if (ws_bytes < L.chunk_base + align256(L.nchunks * shape->E * 4)) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  Phase ph(MOK_PHASE_SCHEDULE, static_cast<cudaStream_t>(stream), 3);
   MOK_CUDA(launch_schedule(*shape, L, static_cast<uint8_t*>(ws), topk_idx, static_cast<cudaStream_t>(stream)));
   return MOK_OK;
 }
@@ -319,6 +362,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.g1_tiles = s.I / 128;
     g.m_tiles = (int)L.tile_capacity;
     g.counter = 0;
+    Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
     MOK_CUDA(launch_gemm(GM_FWD_RING, maps, g, gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles)), st));
   } else {
     // minibatch by minibatch in stream order (same ring, no device flags)
@@ -329,6 +373,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     maps.m[3] = m2.m[0];
     const int Mt = M / kTileRows;
     const int nmb = (int)((L.tile_capacity + Mt - 1) / Mt);
+    Phase ph(MOK_PHASE_FWD_GEMM, st, 2 * nmb);
     int counter = 0;
     for (int b = 0; b < nmb; ++b) {
       GemmParams g1 = g;
@@ -348,7 +393,10 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       MOK_CUDA(launch_gemm(GM_FWD2, m2, g2, gemm_grid((long)Mt * g2.n_tiles), st));
     }
   }
-  MOK_CUDA(launch_combine(s, L, w, g.yk, scores, static_cast<__nv_bfloat16*>(out), st));
+  {
+    Phase ph(MOK_PHASE_FWD_COMBINE, st, 1);
+    MOK_CUDA(launch_combine(s, L, w, g.yk, scores, static_cast<__nv_bfloat16*>(out), st));
+  }
   return MOK_OK;
 }
 
@@ -393,7 +441,11 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tile_begin = 0;
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 0;
-    MOK_CUDA(launch_gemm(GM_BWD_DA, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    {
+      Phase ph(MOK_PHASE_BWD_DA, st, 1);
+      MOK_CUDA(launch_gemm(GM_BWD_DA, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    }
+    Phase ph(MOK_PHASE_BWD_DS, st, 1);
     MOK_CUDA(launch_ds_reduce(s, L, w, dscores, q.n_tiles, st));
   }
   // dX parts = [dh|du] [W1|W3]^T scattered to token order, then summed over k
@@ -410,7 +462,11 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tile_begin = 0;
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 1;
-    MOK_CUDA(launch_gemm(GM_BWD_DX, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    {
+      Phase ph(MOK_PHASE_BWD_DX, st, 1);
+      MOK_CUDA(launch_gemm(GM_BWD_DX, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    }
+    Phase ph(MOK_PHASE_BWD_DX_COMBINE, st, 1);
     MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));
   }
   // dW1 | dW3 = gather(x)^T [dh|du], per expert
@@ -427,6 +483,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.counter = 2;
     q.dw0 = static_cast<__nv_bfloat16*>(dW1);
     q.dw1 = static_cast<__nv_bfloat16*>(dW3);
+    Phase ph(MOK_PHASE_BWD_WG13, st, 1);
     MOK_CUDA(launch_gemm(GM_WG13, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
   }
   // dW2 = (s a)^T gather(dout), per expert
@@ -441,6 +498,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tiles = s.I / 128;
     q.counter = 3;
     q.dw0 = static_cast<__nv_bfloat16*>(dW2);
+    Phase ph(MOK_PHASE_BWD_WG2, st, 1);
     MOK_CUDA(launch_gemm(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
   }
   return MOK_OK;
@@ -453,6 +511,7 @@ mok_status mok_mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int3
   if (block_axis != 0 && block_axis != 1) return MOK_ERR_INVALID_ARG;
   if (block_axis == 0 && rows % 32) return MOK_ERR_UNSUPPORTED;
   if (block_axis == 1 && cols % 32) return MOK_ERR_UNSUPPORTED;
+  g_launches += 1;
   MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(src), batch, rows, cols, block_axis, q, scale,
                                  static_cast<cudaStream_t>(stream)));
   return MOK_OK;
@@ -465,6 +524,7 @@ mok_status mok_gather_rows(const mok_shape* shape, const mok_config* cfg, const 
   if (!ws || !x || !xg) return MOK_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
   if (ws_bytes < L.chunk_base) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  g_launches += 1;
   MOK_CUDA(launch_gather_rows(*shape, L, static_cast<const uint8_t*>(ws), static_cast<const __nv_bfloat16*>(x),
                               static_cast<__nv_bfloat16*>(xg), static_cast<cudaStream_t>(stream)));
   return MOK_OK;
@@ -495,9 +555,44 @@ mok_status mok_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int32_t
   g.ld_out = N;
   g.a_mn = a_mn_major ? 1 : 0;
   g.b_mn = b_mn_major ? 1 : 0;
+  g_launches += 1;
   MOK_CUDA(launch_gemm(GM_DENSE, m, g, gemm_grid((long)g.m_tiles * g.n_tiles), st));
   return MOK_OK;
 }
+
+mok_status mok_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = on != 0;
+  return MOK_OK;
+}
+
+mok_status mok_trace_read(float* ms, int32_t* count) {
+  if (!ms || !count) return MOK_ERR_INVALID_ARG;
+  std::vector<TraceRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    recs.swap(g_trace);
+  }
+  for (int i = 0; i < MOK_NUM_PHASES; ++i) {
+    ms[i] = 0.0f;
+    count[i] = 0;
+  }
+  mok_status st = MOK_OK;
+  for (const TraceRec& r : recs) {
+    float t = 0.0f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      st = MOK_ERR_CUDA;
+    if (r.phase >= 0 && r.phase < MOK_NUM_PHASES) {
+      ms[r.phase] += t;
+      count[r.phase] += 1;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  return st;
+}
+
+int64_t mok_launch_count(void) { return g_launches.load(); }
 
 mok_status mok_check(void* ws, void* stream) {
   if (!ws) return MOK_ERR_INVALID_ARG;

@@ -23,7 +23,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|mok_status|size_t|int32_t)\s+(mok_\w+)\s*\(",
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|mok_status|size_t|int32_t|int64_t)\s+(mok_\w+)\s*\(",
                                  text, flags=re.M)))
 
 
