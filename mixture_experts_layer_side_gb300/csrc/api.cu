@@ -345,6 +345,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   g.ring_flags = reinterpret_cast<uint32_t*>(w + L.ring_flags);
   g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
   g.debug_flags = cfg->debug_flags;
+  g.gather_src = static_cast<const __nv_bfloat16*>(x);
 
   TmapSet maps;
   memset(&maps, 0, sizeof(maps));
@@ -435,6 +436,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     if (!map_gather(&m.m[0], dout, s.H, s.T)) return MOK_ERR_CUDA;
     if (!map3d(&m.m[1], W2, s.H, s.I, s.E, bn_i)) return MOK_ERR_CUDA;
     GemmParams q = g;
+    q.gather_src = static_cast<const __nv_bfloat16*>(dout);
     q.nmaps = 2;
     q.bn = bn_i;
     q.n_tiles = s.I / bn_i;
@@ -481,6 +483,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.n_tiles = 2 * s.I / 256;
     q.m_tiles = s.H / 128;
     q.counter = 2;
+    q.gather_src = static_cast<const __nv_bfloat16*>(x);
     q.dw0 = static_cast<__nv_bfloat16*>(dW1);
     q.dw1 = static_cast<__nv_bfloat16*>(dW3);
     Phase ph(MOK_PHASE_BWD_WG13, st, 1);
@@ -497,6 +500,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.n_tiles = s.H / bn_h;
     q.m_tiles = s.I / 128;
     q.counter = 3;
+    q.gather_src = static_cast<const __nv_bfloat16*>(dout);
     q.dw0 = static_cast<__nv_bfloat16*>(dW2);
     Phase ph(MOK_PHASE_BWD_WG2, st, 1);
     MOK_CUDA(launch_gemm(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));

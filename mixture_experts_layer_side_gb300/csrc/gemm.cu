@@ -1,10 +1,15 @@
 // Expert-grouped GEMMs of the MoE layer on sm_103a tensor cores.
 //
 // One persistent, warp-specialised kernel family:
-//   warp 0      TMA producer.  Plain tiles come in with cp.async.bulk.tensor;
-//               the dispatch gather (sorted row -> token) is fused into the
-//               load path with cp.async.bulk.tensor ... tile::gather4, four
-//               token rows per instruction, one instruction per lane.
+//   warp 0      TMA producer for the operands that are plain tiles (weights,
+//               sorted-row activations): cp.async.bulk.tensor.
+//   warps 6..9  gather producers: the dispatch gather (sorted row -> token
+//               row of x or dout) is fused into the load path as 16-byte
+//               cp.async copies written straight into the 128-byte-swizzled
+//               operand layout, completing on the stage's mbarrier
+//               (cp.async.mbarrier.arrive.noinc).  (TMA tile::gather4 moved
+//               a third of the bytes per SM-cycle of these copies at the
+//               same depth, so the gathered operands do not use it.)
 //   warp 1      MMA issuer: tcgen05.mma (BF16 in, FP32 accumulate in TMEM),
 //               128 x N tiles, N = 128 or 256; TMEM holds two accumulators so
 //               the epilogue of one tile overlaps the main loop of the next.
@@ -42,6 +47,7 @@ struct Ctl {
   int q[kQueue];
   uint32_t tmem_base;
   int abort;
+  int po[kMaxExperts + 1];  // padded expert offsets (weight-gradient modes)
 };
 
 // A decoded work item.
@@ -110,7 +116,7 @@ __device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& 
 }
 
 template <int MODE>
-__device__ Item decode(const GemmParams& p, int w) {
+__device__ Item decode(const GemmParams& p, const int* po, int w) {
   Item it;
   if constexpr (MODE == GM_DENSE) {
     it.type = MODE;
@@ -126,8 +132,8 @@ __device__ Item decode(const GemmParams& p, int w) {
     const int r = w % per_e;
     it.m = r / p.n_tiles;
     it.n = r % p.n_tiles;
-    const int a = p.padded_offsets[it.e];
-    const int b = p.padded_offsets[it.e + 1];
+    const int a = po[it.e];
+    const int b = po[it.e + 1];
     it.row0 = a;
     it.k_iters = (b - a) / 64;
   } else {
@@ -152,84 +158,131 @@ __device__ Item decode(const GemmParams& p, int w) {
 
 __device__ __forceinline__ int item_bn(const GemmParams& p, int type) { return type == GM_FWD1 ? 256 : p.bn; }
 
-__device__ __forceinline__ int tok_of(const GemmParams& p, int prow) {
-  const int f = p.pad_perm[prow];
-  return f >= 0 ? f / p.k : p.T;  // row T is outside the tensor: TMA fills zeros
-}
-
 __device__ __forceinline__ int ring_row(const GemmParams& p, int prow) {
   const int mb = prow / p.ring_rows;
   return (mb % p.ring_slots) * p.ring_rows + (prow - mb * p.ring_rows);
 }
 
-// ------------------------------------------------------------------ producer
-// All 32 lanes of warp 0 call this for one K stage; lane 0 has already armed
-// the stage's full barrier with the stage's byte count.
+// ------------------------------------------------------------------ producers
+// Which operand of an item is gathered by token (0 none, 1 A, 2 B).
+__device__ __forceinline__ int gathered_operand(int type) {
+  return (type == GM_FWD1 || type == GM_BWD_DA || type == GM_WG13) ? 1 : (type == GM_WG2 ? 2 : 0);
+}
+
 template <int MODE>
-__device__ __forceinline__ void issue_loads(const TmapSet& mp, const GemmParams& p, const Item& it, int kk,
-                                            uint8_t* a, uint8_t* b, uint64_t* bar, int lane, const int (&tok)[4]) {
+__device__ __forceinline__ constexpr bool mode_gathers() {
+  return MODE == GM_FWD1 || MODE == GM_BWD_DA || MODE == GM_WG13 || MODE == GM_WG2 || MODE == GM_FWD_RING;
+}
+
+// Bytes the TMA producer brings into one stage (gathered operands excluded).
+__device__ __forceinline__ uint32_t tma_stage_bytes(int type, int bn) {
+  const int g = gathered_operand(type);
+  return (g == 1 ? 0u : (uint32_t)kAStage) + (g == 2 ? 0u : (uint32_t)bn * 128u);
+}
+
+// TMA producer (lane 0 of warp 0) for one K stage of the plain operands.
+template <int MODE>
+__device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p, const Item& it, int kk, uint8_t* a,
+                                          uint8_t* b, uint64_t* bar) {
   const int type = it.type;
   if (MODE == GM_DENSE) {
-    if (lane == 0) {
-      if (p.a_mn) {
-        for (int c = 0; c < 2; ++c) tma_load_2d(a + c * 8192, &mp.m[0], bar, it.m * 128 + c * 64, kk * 64);
-      } else {
-        tma_load_2d(a, &mp.m[0], bar, kk * 64, it.m * 128);
-      }
-      if (p.b_mn) {
-        for (int c = 0; c < p.bn / 64; ++c) tma_load_2d(b + c * 8192, &mp.m[1], bar, it.n * p.bn + c * 64, kk * 64);
-      } else {
-        tma_load_2d(b, &mp.m[1], bar, kk * 64, it.n * p.bn);
-      }
+    if (p.a_mn) {
+      for (int c = 0; c < 2; ++c) tma_load_2d(a + c * 8192, &mp.m[0], bar, it.m * 128 + c * 64, kk * 64);
+    } else {
+      tma_load_2d(a, &mp.m[0], bar, kk * 64, it.m * 128);
+    }
+    if (p.b_mn) {
+      for (int c = 0; c < p.bn / 64; ++c) tma_load_2d(b + c * 8192, &mp.m[1], bar, it.n * p.bn + c * 64, kk * 64);
+    } else {
+      tma_load_2d(b, &mp.m[1], bar, kk * 64, it.n * p.bn);
     }
   } else if (type == GM_FWD1) {
-    // A: gathered token rows of x (K-major); B: W1 and W3 column blocks (N-major)
-    tma_gather4(a + lane * 512, &mp.m[0], bar, kk * 64, tok[0], tok[1], tok[2], tok[3]);
-    if (lane == 0) {
-      for (int c = 0; c < 2; ++c) tma_load_3d(b + c * 8192, &mp.m[1], bar, it.n * 128 + c * 64, kk * 64, it.e);
-      for (int c = 0; c < 2; ++c)
-        tma_load_3d(b + (2 + c) * 8192, &mp.m[2], bar, it.n * 128 + c * 64, kk * 64, it.e);
-    }
+    // B: W1 and W3 column blocks (N-major); 128 h columns then 128 u columns
+    for (int c = 0; c < 2; ++c) tma_load_3d(b + c * 8192, &mp.m[1], bar, it.n * 128 + c * 64, kk * 64, it.e);
+    for (int c = 0; c < 2; ++c) tma_load_3d(b + (2 + c) * 8192, &mp.m[2], bar, it.n * 128 + c * 64, kk * 64, it.e);
   } else if (type == GM_FWD2) {
-    if (lane == 0) {
-      const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
-      const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
-      tma_load_2d(a, &mp.m[mslot], bar, kk * 64, ring_row(p, it.row0));
-      for (int c = 0; c < p.bn / 64; ++c)
-        tma_load_3d(b + c * 8192, &mp.m[wmap], bar, it.n * p.bn + c * 64, kk * 64, it.e);
-    }
+    const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
+    const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
+    tma_load_2d(a, &mp.m[mslot], bar, kk * 64, ring_row(p, it.row0));
+    for (int c = 0; c < p.bn / 64; ++c) tma_load_3d(b + c * 8192, &mp.m[wmap], bar, it.n * p.bn + c * 64, kk * 64, it.e);
   } else if (type == GM_BWD_DA) {
-    tma_gather4(a + lane * 512, &mp.m[0], bar, kk * 64, tok[0], tok[1], tok[2], tok[3]);
-    if (lane == 0) tma_load_3d(b, &mp.m[1], bar, kk * 64, it.n * p.bn, it.e);
+    tma_load_3d(b, &mp.m[1], bar, kk * 64, it.n * p.bn, it.e);
   } else if (type == GM_BWD_DX) {
-    if (lane == 0) {
-      tma_load_2d(a, &mp.m[0], bar, kk * 64, it.row0);
-      const int ki = p.I / 64;
-      if (kk < ki)
-        tma_load_3d(b, &mp.m[1], bar, kk * 64, it.n * p.bn, it.e);
-      else
-        tma_load_3d(b, &mp.m[2], bar, (kk - ki) * 64, it.n * p.bn, it.e);
-    }
-  } else if (type == GM_WG13 || type == GM_WG2) {
-    // 64 routed rows of the expert per stage: K dimension, gathered by token
-    const int r0 = it.row0 + kk * 64 + 4 * (lane & 15);
-    const int t0 = tok_of(p, r0), t1 = tok_of(p, r0 + 1), t2 = tok_of(p, r0 + 2), t3 = tok_of(p, r0 + 3);
-    const int c = lane >> 4;
-    if (type == GM_WG13) {
-      // A = x^T (M = H, MN-major), B = [dh|du] (N = 2I, MN-major)
-      tma_gather4(a + c * 8192 + (lane & 15) * 512, &mp.m[0], bar, it.m * 128 + c * 64, t0, t1, t2, t3);
-      if (lane == 0)
-        for (int cc = 0; cc < p.bn / 64; ++cc)
-          tma_load_2d(b + cc * 8192, &mp.m[1], bar, it.n * p.bn + cc * 64, it.row0 + kk * 64);
-    } else {
-      // A = (s a)^T (M = I, MN-major), B = dout (N = H, MN-major, gathered)
-      for (int cc = c; cc < p.bn / 64; cc += 2)
-        tma_gather4(b + cc * 8192 + (lane & 15) * 512, &mp.m[1], bar, it.n * p.bn + cc * 64, t0, t1, t2, t3);
-      if (lane == 0)
-        for (int ca = 0; ca < 2; ++ca)
-          tma_load_2d(a + ca * 8192, &mp.m[0], bar, it.m * 128 + ca * 64, it.row0 + kk * 64);
-    }
+    tma_load_2d(a, &mp.m[0], bar, kk * 64, it.row0);
+    const int ki = p.I / 64;
+    if (kk < ki)
+      tma_load_3d(b, &mp.m[1], bar, kk * 64, it.n * p.bn, it.e);
+    else
+      tma_load_3d(b, &mp.m[2], bar, (kk - ki) * 64, it.n * p.bn, it.e);
+  } else if (type == GM_WG13) {
+    // B = [dh|du] rows of the expert (N = 2I, MN-major)
+    for (int cc = 0; cc < p.bn / 64; ++cc)
+      tma_load_2d(b + cc * 8192, &mp.m[1], bar, it.n * p.bn + cc * 64, it.row0 + kk * 64);
+  } else if (type == GM_WG2) {
+    // A = (s a) rows of the expert (M = I, MN-major)
+    for (int ca = 0; ca < 2; ++ca) tma_load_2d(a + ca * 8192, &mp.m[0], bar, it.m * 128 + ca * 64, it.row0 + kk * 64);
   }
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ int token_or_neg(const GemmParams& p, int prow) {
+  const int f = p.pad_perm[prow];
+  return f >= 0 ? f / p.k : -1;
+}
+
+// Gathered operand of one K stage, by the 128 gather threads (gt = 0..127).
+// K-major (A of GEMM1 / dA'): 128 token rows x 128 bytes; thread gt copies
+//   16-byte chunk (gt & 7) of rows (gt >> 3) + 16 j.  tok[] holds them.
+// M/N-major (A of dW1|dW3, B of dW2): 64 routed rows (the K dimension) x
+//   cpr 16-byte chunks; chunk c = gt + 128 j is row c / cpr, column chunk
+//   c % cpr, stored in 64-column blocks of 8192 bytes.  tok[] holds the
+//   tokens of those rows for this stage.
+// Rows with no token (padding) are zero-filled.  Every thread's copies
+// complete on the stage's full barrier (one no-increment arrival each).
+__device__ __forceinline__ void gather_kmajor(uint8_t* dst, const __nv_bfloat16* src, int ld, int col0, int gt,
+                                              const int (&tok)[16], uint64_t* full) {
+  const int ch = gt & 7;
+  const int sw = (ch ^ ((gt >> 3) & 7)) << 4;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int row = (gt >> 3) + 16 * j;
+    const int t = tok[j];
+    cp_async_16(smem_u32(dst + row * 128 + sw), src + (long)max(t, 0) * ld + col0 + ch * 8, t >= 0 ? 16u : 0u);
+  }
+  cp_async_arrive_noinc(full);
+}
+
+template <int CPR>  // 16-byte chunks per routed row: 16 (128 columns) or 32 (256 columns)
+__device__ __forceinline__ void gather_mnmajor(uint8_t* dst, const __nv_bfloat16* src, int ld, int col0, int gt,
+                                               const int (&tok)[16], uint64_t* full) {
+  constexpr int kRowsPerPass = 128 / CPR;
+  constexpr int kPasses = 64 / kRowsPerPass;
+  const int cc = gt % CPR;
+  const int blk = cc >> 3, ch = cc & 7;
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) {
+    const int krow = gt / CPR + kRowsPerPass * j;
+    const int t = tok[j];
+    cp_async_16(smem_u32(dst + blk * 8192 + krow * 128 + ((ch ^ (krow & 7)) << 4)),
+                src + (long)max(t, 0) * ld + col0 + blk * 64 + ch * 8, t >= 0 ? 16u : 0u);
+  }
+  cp_async_arrive_noinc(full);
+}
+
+// Tokens a gather thread needs for K stage kk of an M/N-major item.
+template <int CPR>
+__device__ __forceinline__ void mn_tokens(const GemmParams& p, const Item& it, int kk, int gt, int (&tok)[16]) {
+  constexpr int kRowsPerPass = 128 / CPR;
+  constexpr int kPasses = 64 / kRowsPerPass;
+#pragma unroll
+  for (int j = 0; j < kPasses; ++j) tok[j] = token_or_neg(p, it.row0 + kk * 64 + gt / CPR + kRowsPerPass * j);
 }
 
 template <int MODE>
@@ -417,10 +470,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   Ctl* ctl = reinterpret_cast<Ctl*>(sB + kStages * kBStage);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WaitCtx wc{&ctl->abort, &p.hdr[kHdrAbort], &p.hdr[kHdrError]};
+  constexpr bool kGather = mode_gathers<MODE>();
+  constexpr bool kWgrad = (MODE == GM_WG13 || MODE == GM_WG2);
+  // consumers of the item queue: MMA warp, 4 epilogue warps, 4 gather warps
+  constexpr uint32_t kQueueConsumers = kGather ? 9u : 5u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&ctl->full[i], 1);
+      // TMA producer's arrive.expect_tx, plus one no-increment arrival per
+      // gather thread when the launch gathers
+      mbar_init(&ctl->full[i], kGather ? 129u : 1u);
       mbar_init(&ctl->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -429,11 +488,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(&ctl->qfull[i], 1);
-      mbar_init(&ctl->qempty[i], 5);
+      mbar_init(&ctl->qempty[i], kQueueConsumers);
     }
     ctl->abort = 0;
     fence_mbar_init();
   }
+  if (kWgrad)
+    for (int e = threadIdx.x; e <= p.E; e += blockDim.x) ctl->po[e] = p.padded_offsets[e];
   if (warp == 0 && lane == 0)
     for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
   if (warp == 1) {
@@ -445,55 +506,106 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const int num_items = count_items<MODE>(p);
+  const int* po = ctl->po;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
-    uint32_t* counter = reinterpret_cast<uint32_t*>(&p.hdr[kHdrCounters + p.counter]);
-    bool ok = true;
-    while (ok) {
-      int w = 0;
-      if (lane == 0) {
-        ok = mbar_wait(&ctl->qempty[qs], qp ^ 1, wc);
-        w = (int)atomicAdd(counter, 1u);
+    // ---------------------------------------------------------------- TMA producer + work fetch
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
+      uint32_t* counter = reinterpret_cast<uint32_t*>(&p.hdr[kHdrCounters + p.counter]);
+      int w = (int)atomicAdd(counter, 1u);
+      bool ok = true;
+      while (ok) {
         if (w >= num_items) w = -1;
+        ok = mbar_wait(&ctl->qempty[qs], qp ^ 1, wc);
         ctl->q[qs] = ok ? w : -1;
         mbar_arrive(&ctl->qfull[qs]);
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      w = __shfl_sync(0xffffffffu, w, 0);
-      if (++qs == kQueue) { qs = 0; qp ^= 1; }
-      if (!ok || w < 0) break;
-      const Item it = decode<MODE>(p, w);
-      int tok[4] = {0, 0, 0, 0};
-      if (it.type == GM_FWD1 || it.type == GM_BWD_DA) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tok[q] = tok_of(p, it.row0 + lane * 4 + q);
-      }
-      if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
-        // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all of
-        // its GEMM1 column tiles are done, then order the async-proxy loads
-        // after the acquire.
-        if (lane == 0) {
+        if (++qs == kQueue) { qs = 0; qp ^= 1; }
+        if (!ok || w < 0) break;
+        // fetch the next item now; its latency overlaps this item's loads
+        const int w_next = (int)atomicAdd(counter, 1u);
+        const Item it = decode<MODE>(p, po, w);
+        if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
+          // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
+          // of its GEMM1 column tiles are published, then order the
+          // async-proxy loads after the acquire
           ok = wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc);
           fence_proxy_async_global();
+          if (!ok) break;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        const uint32_t bytes = tma_stage_bytes(it.type, item_bn(p, it.type));
+        for (int kk = 0; kk < it.k_iters; ++kk) {
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(&ctl->full[stage], bytes);
+          tma_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, &ctl->full[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        w = w_next;
       }
-      const uint32_t bytes = kAStage + item_bn(p, it.type) * 128;
-      for (int kk = 0; kk < it.k_iters; ++kk) {
-        if (lane == 0) {
-          ok = mbar_wait(&ctl->empty[stage], phase ^ 1, wc);
-          if (ok) mbar_arrive_expect_tx(&ctl->full[stage], bytes);
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        issue_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, &ctl->full[stage], lane,
-                          tok);
+    }
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------------- gather producers
+    if (kGather) {
+      const int gt = threadIdx.x - 192;
+      uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
+      while (true) {
+        if (!mbar_wait(&ctl->qfull[qs], qp, wc)) break;
+        const int w = ctl->q[qs];
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
+        if (++qs == kQueue) { qs = 0; qp ^= 1; }
+        if (w < 0) break;
+        const Item it = decode<MODE>(p, po, w);
+        const int g = gathered_operand(it.type);
+        const bool wide = (it.type == GM_WG2 && p.bn == 256);
+        int tok[16], nxt[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tok[j] = nxt[j] = -1;
+        if (it.type == GM_FWD1 || it.type == GM_BWD_DA) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) tok[j] = token_or_neg(p, it.row0 + (gt >> 3) + 16 * j);
+        } else if (it.type == GM_WG13 || (it.type == GM_WG2 && !wide)) {
+          if (it.k_iters > 0) mn_tokens<16>(p, it, 0, gt, tok);
+        } else if (wide) {
+          if (it.k_iters > 0) mn_tokens<32>(p, it, 0, gt, tok);
+        }
+        bool ok = true;
+        for (int kk = 0; kk < it.k_iters; ++kk) {
+          // tokens of the next stage of an M/N-major item, loaded ahead
+          if (g != 0 && (it.type == GM_WG13 || it.type == GM_WG2) && kk + 1 < it.k_iters) {
+            if (wide)
+              mn_tokens<32>(p, it, kk + 1, gt, nxt);
+            else
+              mn_tokens<16>(p, it, kk + 1, gt, nxt);
+          }
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
+          uint64_t* full = &ctl->full[stage];
+          uint8_t* a = sA + stage * kAStage;
+          uint8_t* b = sB + stage * kBStage;
+          if (it.type == GM_FWD1) {
+            gather_kmajor(a, p.gather_src, p.H, kk * 64, gt, tok, full);
+          } else if (it.type == GM_BWD_DA) {
+            gather_kmajor(a, p.gather_src, p.H, kk * 64, gt, tok, full);
+          } else if (it.type == GM_WG13) {
+            gather_mnmajor<16>(a, p.gather_src, p.H, it.m * 128, gt, tok, full);
+          } else if (it.type == GM_WG2) {
+            if (wide)
+              gather_mnmajor<32>(b, p.gather_src, p.H, it.n * p.bn, gt, tok, full);
+            else
+              gather_mnmajor<16>(b, p.gather_src, p.H, it.n * p.bn, gt, tok, full);
+          } else {
+            mbar_arrive(full);  // nothing to gather in this item: keep the phase count
+          }
+          if (it.type == GM_WG13 || it.type == GM_WG2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) tok[j] = nxt[j];
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
       }
+      // let this thread's copies land before the CTA can exit
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -505,7 +617,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE>(p, w);
+      const Item it = decode<MODE>(p, po, w);
       const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
       if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)) break;
       tc_fence_after();
@@ -513,11 +625,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       const bool amn = a_mn_major<MODE>(p, it.type), bmn = b_mn_major<MODE>(p, it.type);
       const uint32_t idesc = idesc_bf16(128, bn, amn ? 1 : 0, bmn ? 1 : 0);
       const uint32_t d = tmem + buf * 256;
+      const bool gathered = gathered_operand(it.type) != 0;
       bool ok = true;
       for (int kk = 0; kk < it.k_iters; ++kk) {
         if (!mbar_wait(&ctl->full[stage], phase, wc)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
+          // the gather threads wrote part of this stage with cp.async: order
+          // those writes before the tensor core's (async-proxy) reads
+          if (gathered) fence_proxy_async_shared();
           const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBStage);
 #pragma unroll
           for (int k16 = 0; k16 < 4; ++k16) {
@@ -536,7 +652,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       ++tcount;
     }
   } else {
-    // ---------------------------------------------------------------- epilogue
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     uint32_t qs = 0, qp = 0, tcount = 0;
@@ -547,7 +663,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE>(p, w);
+      const Item it = decode<MODE>(p, po, w);
       const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();

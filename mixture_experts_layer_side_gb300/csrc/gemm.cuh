@@ -21,7 +21,8 @@ constexpr int kStages = 4;
 constexpr int kAStage = 128 * 128;  // 128 rows x 128 bytes
 constexpr int kBStage = 256 * 128;  // up to 256 rows x 128 bytes
 constexpr int kQueue = 4;           // depth of the work-item queue in smem
-constexpr int kGemmThreads = 192;   // warp 0 TMA producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int kGemmThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-9 gather
+constexpr int kMaxExperts = 1024;
 
 constexpr int kMaxMaps = 6;
 struct TmapSet {
@@ -52,6 +53,7 @@ struct GemmParams {
   __nv_bfloat16* as;       // [pad, I]
   float* dsp;              // [pad, n_tiles]
   const float* scores;     // [R]
+  const __nv_bfloat16* gather_src;  // x (GEMM1, dW1|dW3) or dout (dA', dW2): [T, H]
   __nv_bfloat16* dw0;      // dW1 (WG13) or dW2 (WG2)
   __nv_bfloat16* dw1;      // dW3 (WG13)
   int a_mn, b_mn;          // dense: operand major-ness (1 = M/N-major)

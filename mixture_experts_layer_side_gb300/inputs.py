@@ -48,6 +48,8 @@ class Shape:
 WORKLOADS = {
     "tiny": (Shape(256, 256, 128, 8, 2), "uniform", "bf16"),
     "mid": (Shape(4096, 2048, 768, 64, 8), "uniform", "bf16"),
+    # small profiling case: weights (~300 MB) still exceed L2, device footprint < 1.5 GB
+    "prof": (Shape(2048, 2048, 768, 32, 8), "uniform", "bf16"),
     "dsv3": (Shape(8192, 7168, 2048, 256, 8), "zipf", "bf16"),
     "mid_mxfp8_zipf": (Shape(4096, 2048, 768, 64, 8), "zipf", "mxfp8"),
     "mid_mxfp8_hot": (Shape(4096, 2048, 768, 64, 8), "hot", "mxfp8"),
