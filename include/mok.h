@@ -265,6 +265,51 @@ mok_status mok_trace_read(float* ms /* [MOK_NUM_PHASES] */, int32_t* count /* [M
 /* Number of kernels the library has launched in this process so far. */
 int64_t mok_launch_count(void);
 
+/*
+ * Build the schedule without any device allocation, into caller-owned
+ * buffers.  No counterpart on the pages: this is an addition for callers that
+ * cannot allocate device memory themselves -- code whose device memory is all
+ * owned by another allocator (a pool carved out once at start-up, as
+ * training frameworks do), or code that must not call cudaMalloc because it
+ * synchronises the device and stalls every other stream.  Such callers still
+ * own their inputs and outputs, but the workspace that mok_build_schedule
+ * asks for is one more buffer they cannot create; this entry point needs
+ * none.
+ *
+ * Same computation and same results as mok_build_schedule: bit-identical
+ * arrays.  Its only scratch (the per-chunk expert histograms and their
+ * scans, 2 * ceil(T*k/1024) * E int32) lives in one static device array of
+ * MOK_NOALLOC_SCRATCH_BYTES (1 MiB) built into the library; every GPU that
+ * loads the library holds it until the process exits.
+ *   - Sizes whose scratch exceeds the array (ceil(T*k/1024) * E > 131072)
+ *     return MOK_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads, same device) race and give wrong schedules.
+ *     Serialise them.
+ *   - The function allocates nothing: no cudaMalloc/cudaFree, no library
+ *     routine that allocates.
+ * Outputs (device, int32, caller-owned): the arrays of mok_layout, with the
+ * same lengths; `header` gets [0] error bits (1 = an expert id outside
+ * [0, E)), [1] padded rows used, [2] 128-row tiles used.
+ */
+#define MOK_NOALLOC_SCRATCH_BYTES (1u << 20)
+typedef struct {
+  int32_t* header;         /* [64] */
+  int32_t* counts;         /* [E] */
+  int32_t* offsets;        /* [E+1] */
+  int32_t* padded_offsets; /* [E+1] */
+  int32_t* perm;           /* [R] */
+  int32_t* inv_perm;       /* [R] */
+  int32_t* pad_perm;       /* [pad_capacity] */
+  int32_t* pad_inv;        /* [R] */
+  int32_t* tile_expert;    /* [tile_capacity] */
+} mok_schedule_buffers;
+mok_status mok_build_schedule_noalloc(const mok_shape* shape, const int32_t* topk_idx,
+                                      const mok_schedule_buffers* out, void* stream);
+
 /* Synchronise `stream`, then return (and clear) the status recorded in the
  * workspace's error word; MOK_OK if none. */
 mok_status mok_check(void* ws, void* stream);

@@ -28,7 +28,7 @@ STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_build_schedule", "mok_forward",
            "mok_backward", "mok_mxfp8_quantize", "mok_gather_rows", "mok_gemm_bf16", "mok_check",
            "mok_device_sm_count", "mok_status_string", "mok_version", "mok_trace_enable", "mok_trace_read",
-           "mok_launch_count"]
+           "mok_launch_count", "mok_build_schedule_noalloc"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
           "bwd_wg2", "quant"]
@@ -60,6 +60,11 @@ class MokLayout(ctypes.Structure):
                [("pad_capacity", ctypes.c_int64), ("tile_capacity", ctypes.c_int64)]
 
 
+class MokScheduleBuffers(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("header", "counts", "offsets", "padded_offsets", "perm",
+                                               "inv_perm", "pad_perm", "pad_inv", "tile_expert")]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run mixture_experts_layer_side_gb300.build.build() "
@@ -86,6 +91,7 @@ def _load():
         "mok_trace_enable": (i32, [i32]),
         "mok_trace_read": (i32, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),
         "mok_launch_count": (ctypes.c_int64, []),
+        "mok_build_schedule_noalloc": (i32, [S, P, ctypes.POINTER(MokScheduleBuffers), P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -207,6 +213,13 @@ def mok_trace_read():
 
 def mok_launch_count():
     return LIB.mok_launch_count()
+
+
+def mok_build_schedule_noalloc(shape, topk_idx, buffers, stream=None):
+    """``buffers``: dict of int32 device tensors named as MokScheduleBuffers."""
+    b = MokScheduleBuffers(*[buffers[n].data_ptr() for n, _ in MokScheduleBuffers._fields_])
+    _ok(LIB.mok_build_schedule_noalloc(ctypes.byref(shape), _ptr(topk_idx), ctypes.byref(b), _stream(stream)),
+        "mok_build_schedule_noalloc")
 
 
 def mok_check(ws, stream=None):

@@ -190,3 +190,76 @@ cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, 
 }
 
 }  // namespace mok
+
+// ---------------------------------------------------------------------------
+// Schedule without device allocation: the same three kernels, with their
+// scratch (per-chunk histograms and their scans) in a static device array
+// instead of the caller's workspace.  For callers that cannot allocate
+// device memory (see mok_build_schedule_noalloc in mok.h).
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = MOK_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoallocMaxDevices] = {};
+
+// Device address of the static scratch on the current device, looked up once
+// per device with that device current (host code must not use the symbol
+// itself: on the host it only names a stand-in).
+void* noalloc_scratch_address(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kNoallocMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_noalloc_addr[dev] = ptr;
+  }
+  return g_noalloc_addr[dev];
+}
+
+}  // namespace
+
+extern "C" mok_status mok_build_schedule_noalloc(const mok_shape* shape, const int32_t* topk_idx,
+                                                 const mok_schedule_buffers* out, void* stream) {
+  using namespace mok;
+  if (!shape || !topk_idx || !out) return MOK_ERR_INVALID_ARG;
+  if (!out->header || !out->counts || !out->offsets || !out->padded_offsets || !out->perm || !out->inv_perm ||
+      !out->pad_perm || !out->pad_inv || !out->tile_expert)
+    return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.T < 1 || s.k < 1 || s.E < 1) return MOK_ERR_INVALID_ARG;
+  if (s.E > 1024 || s.k > 32 || (int64_t)s.T * s.k > (1 << 24)) return MOK_ERR_UNSUPPORTED;
+  const int R = s.T * s.k, E = s.E;
+  const int64_t nchunks = (R + kSchedChunk - 1) / kSchedChunk;
+  const size_t need = 2 * (size_t)nchunks * E * sizeof(int32_t);
+  if (need > kNoallocScratchBytes) return MOK_ERR_UNSUPPORTED;  // beyond the static scratch
+  cudaError_t err = cudaSuccess;
+  uint8_t* scratch = static_cast<uint8_t*>(noalloc_scratch_address(&err));
+  if (!scratch) return MOK_ERR_CUDA;
+  int32_t* chunk_hist = reinterpret_cast<int32_t*>(scratch);
+  int32_t* chunk_base = chunk_hist + nchunks * E;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the header starts at zero; the two scratch arrays are fully rewritten
+  if (cudaMemsetAsync(out->header, 0, kHeaderWords * sizeof(int32_t), st) != cudaSuccess) return MOK_ERR_CUDA;
+  sched_count<<<(int)nchunks, kCountThreads, E * sizeof(int32_t), st>>>(topk_idx, R, E, chunk_hist, out->header);
+  sched_scan<<<1, 1024, 0, st>>>(E, (int)nchunks, chunk_hist, chunk_base, out->counts, out->offsets,
+                                 out->padded_offsets, out->tile_expert, out->pad_perm, out->header);
+  const int blocks = (int)((nchunks + kPlaceWarps - 1) / kPlaceWarps);
+  sched_place<<<blocks, kPlaceWarps * 32, (size_t)kPlaceWarps * E * sizeof(int32_t), st>>>(
+      topk_idx, R, E, (int)nchunks, chunk_base, out->offsets, out->padded_offsets, out->perm, out->inv_perm,
+      out->pad_perm, out->pad_inv);
+  return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}
+
