@@ -247,7 +247,7 @@ __device__ __forceinline__ int token_or_neg(const GemmParams& p, int prow) {
 // Rows with no token (padding) are zero-filled.  Every thread's copies
 // complete on the stage's full barrier (one no-increment arrival each).
 __device__ __forceinline__ void gather_kmajor(uint8_t* dst, const __nv_bfloat16* src, int ld, int col0, int gt,
-                                              const int (&tok)[16], uint64_t* full) {
+                                              const int (&tok)[8], uint64_t* full) {
   const int ch = gt & 7;
   const int sw = (ch ^ ((gt >> 3) & 7)) << 4;
 #pragma unroll
@@ -261,7 +261,7 @@ __device__ __forceinline__ void gather_kmajor(uint8_t* dst, const __nv_bfloat16*
 
 template <int CPR>  // 16-byte chunks per routed row: 16 (128 columns) or 32 (256 columns)
 __device__ __forceinline__ void gather_mnmajor(uint8_t* dst, const __nv_bfloat16* src, int ld, int col0, int gt,
-                                               const int (&tok)[16], uint64_t* full) {
+                                               const int (&tok)[64 / (128 / CPR)], uint64_t* full) {
   constexpr int kRowsPerPass = 128 / CPR;
   constexpr int kPasses = 64 / kRowsPerPass;
   const int cc = gt % CPR;
@@ -278,7 +278,8 @@ __device__ __forceinline__ void gather_mnmajor(uint8_t* dst, const __nv_bfloat16
 
 // Tokens a gather thread needs for K stage kk of an M/N-major item.
 template <int CPR>
-__device__ __forceinline__ void mn_tokens(const GemmParams& p, const Item& it, int kk, int gt, int (&tok)[16]) {
+__device__ __forceinline__ void mn_tokens(const GemmParams& p, const Item& it, int kk, int gt,
+                                          int (&tok)[64 / (128 / CPR)]) {
   constexpr int kRowsPerPass = 128 / CPR;
   constexpr int kPasses = 64 / kRowsPerPass;
 #pragma unroll
@@ -417,34 +418,93 @@ __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, 
   p.dsp[prow * p.n_tiles + it.n] = dsum;
 }
 
+// A warp's 32 x 32 bf16 chunk (lane = row, w[] = its 32 values) leaves as
+// coalesced row segments: it is staged in a 2 KB smem buffer (16-byte chunks
+// XOR-swizzled by row to spread banks), read back with 4 lanes per row and
+// stored 8 rows x 64 bytes per instruction.  row_ptr(rr) is the global
+// address of the chunk's row rr; rows with a null address are skipped.
+template <typename RowPtr>
+__device__ __forceinline__ void store_chunk_coalesced(uint8_t* stage, int lane, const uint32_t (&w)[16],
+                                                      RowPtr row_ptr) {
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint4*>(stage + lane * 64 + ((i ^ sw) << 4)) =
+        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  __syncwarp();
+  const int ch = lane & 3;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int rr = 8 * s + (lane >> 2);
+    const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 64 + ((ch ^ ((rr >> 1) & 3)) << 4));
+    __nv_bfloat16* dst = row_ptr(rr);
+    if (dst) *reinterpret_cast<uint4*>(dst + ch * 8) = v;
+  }
+  __syncwarp();
+}
+
 // Weight gradients: tile rows are rows of dW (H rows of dW1/dW3, I rows of
 // dW2), columns are its columns.  An expert with no routed rows has no
-// accumulation and gets exact zeros.
-__device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
-  const int r = it.m * 128 + row;
-  const int bn = p.bn;
-#pragma unroll 1
-  for (int c = 0; c < bn; c += 32) {
-    float v[32];
-    if (it.k_iters > 0) {
-      tmem_ld32(tbase + c, v);
-    } else {
+// accumulation and gets exact zeros.  A weight-gradient item has a short K
+// loop (the expert's rows), so the 64 KB output tile must leave fast:
+// coalesced stores through the warp's staging buffer.
+// 32 columns of accumulator (packed pairs of f32) -> bf16 -> dW rows.
+__device__ __forceinline__ void wgrad_emit32(const GemmParams& p, const Item& it, int r0, int col, int lane,
+                                             uint8_t* stage, const uint32_t (&r)[32]) {
+  uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-    }
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-    const int col = it.n * bn + c;
-    __nv_bfloat16* dst;
-    if (it.type == GM_WG13) {
-      dst = (col < p.I) ? p.dw0 + ((long)it.e * p.H + r) * p.I + col
-                        : p.dw1 + ((long)it.e * p.H + r) * p.I + (col - p.I);
-    } else {
-      dst = p.dw0 + ((long)it.e * p.I + r) * p.H + col;
-    }
-    store32_bf16(dst, w);
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+  __nv_bfloat16* base;
+  long ld;
+  if (it.type == GM_WG13) {
+    base = (col < p.I) ? p.dw0 + ((long)it.e * p.H + r0) * p.I + col
+                       : p.dw1 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
+    ld = p.I;
+  } else {
+    base = p.dw0 + ((long)it.e * p.I + r0) * p.H + col;
+    ld = p.H;
   }
+  store_chunk_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
+}
+
+// TMEM is read 32 columns at a time with the next chunk's load in flight
+// while the current one is converted and stored (two register buffers).
+template <int BN>
+__device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane,
+                                            uint8_t* stage) {
+  const int r0 = it.m * 128 + q * 32;  // first dW row of this warp
+  const int col0 = it.n * BN;
+  uint32_t ra[32], rb[32];
+  if (it.k_iters == 0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ra[i] = 0u;
+#pragma unroll
+    for (int c = 0; c < BN; c += 32) wgrad_emit32(p, it, r0, col0 + c, lane, stage, ra);
+    return;
+  }
+  tmem_ld32_issue(tbase, ra);
+  tmem_wait_ld();
+  tmem_regs_ready(ra);
+#pragma unroll
+  for (int c = 0; c < BN; c += 64) {
+    tmem_ld32_issue(tbase + c + 32, rb);
+    wgrad_emit32(p, it, r0, col0 + c, lane, stage, ra);
+    tmem_wait_ld();
+    tmem_regs_ready(rb);
+    if (c + 64 < BN) tmem_ld32_issue(tbase + c + 64, ra);
+    wgrad_emit32(p, it, r0, col0 + c + 32, lane, stage, rb);
+    if (c + 64 < BN) {
+      tmem_wait_ld();
+      tmem_regs_ready(ra);
+    }
+  }
+}
+
+__device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane, uint8_t* stage) {
+  if (p.bn == 256)
+    epi_wgrad_n<256>(p, it, tbase, q, lane, stage);
+  else
+    epi_wgrad_n<128>(p, it, tbase, q, lane, stage);
 }
 
 __device__ void epi_dense(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
@@ -459,6 +519,53 @@ __device__ void epi_dense(const GemmParams& p, const Item& it, uint32_t tbase, i
   }
 }
 
+// All K stages of one item's M/N-major gathered operand (weight-gradient
+// GEMMs, where K is the expert's routed rows).  Row -> token lookups are
+// dependent loads, so they run kPrefetch stages ahead in a register ring.
+template <int CPR>
+__device__ bool gather_item_mn(const GemmParams& p, const Item& it, uint8_t* op_base, int op_stride, int col0,
+                               Ctl* ctl, uint32_t& stage, uint32_t& phase, int gt, const WaitCtx& wc) {
+  constexpr int kTok = 64 / (128 / CPR);
+  constexpr int kPrefetch = 4;
+  int ring[kPrefetch][kTok];
+#pragma unroll
+  for (int d = 0; d < kPrefetch; ++d)
+    if (d < it.k_iters) mn_tokens<CPR>(p, it, d, gt, ring[d]);
+  for (int kk0 = 0; kk0 < it.k_iters; kk0 += kPrefetch) {
+#pragma unroll
+    for (int u = 0; u < kPrefetch; ++u) {
+      const int kk = kk0 + u;
+      if (kk < it.k_iters) {
+        if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) return false;
+        gather_mnmajor<CPR>(op_base + stage * op_stride, p.gather_src, p.H, col0, gt, ring[u], &ctl->full[stage]);
+        if (kk + kPrefetch < it.k_iters) mn_tokens<CPR>(p, it, kk + kPrefetch, gt, ring[u]);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+    }
+  }
+  return true;
+}
+
+// All K stages of one item whose gathered operand is K-major (GEMM1, dA'):
+// the 128 token rows are fixed for the item.  Items with nothing to gather
+// (GEMM2 inside the ring launch) only keep the stage barriers' phase count.
+__device__ bool gather_item_k(const GemmParams& p, const Item& it, uint8_t* sA, Ctl* ctl, uint32_t& stage,
+                              uint32_t& phase, int gt, const WaitCtx& wc) {
+  const bool gather = gathered_operand(it.type) == 1;
+  int tok[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) tok[j] = gather ? token_or_neg(p, it.row0 + (gt >> 3) + 16 * j) : -1;
+  for (int kk = 0; kk < it.k_iters; ++kk) {
+    if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) return false;
+    if (gather)
+      gather_kmajor(sA + stage * kAStage, p.gather_src, p.H, kk * 64, gt, tok, &ctl->full[stage]);
+    else
+      mbar_arrive(&ctl->full[stage]);
+    if (++stage == kStages) { stage = 0; phase ^= 1; }
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ kernel
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ TmapSet maps,
@@ -468,6 +575,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   uint8_t* sA = base;
   uint8_t* sB = base + kStages * kAStage;
   Ctl* ctl = reinterpret_cast<Ctl*>(sB + kStages * kBStage);
+  // per epilogue warp, one 2 KB output staging buffer (128-byte aligned)
+  uint8_t* sOut = sB + kStages * kBStage + ((sizeof(Ctl) + 127) / 128) * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WaitCtx wc{&ctl->abort, &p.hdr[kHdrAbort], &p.hdr[kHdrError]};
   constexpr bool kGather = mode_gathers<MODE>();
@@ -556,52 +665,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (++qs == kQueue) { qs = 0; qp ^= 1; }
         if (w < 0) break;
         const Item it = decode<MODE>(p, po, w);
-        const int g = gathered_operand(it.type);
-        const bool wide = (it.type == GM_WG2 && p.bn == 256);
-        int tok[16], nxt[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) tok[j] = nxt[j] = -1;
-        if (it.type == GM_FWD1 || it.type == GM_BWD_DA) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) tok[j] = token_or_neg(p, it.row0 + (gt >> 3) + 16 * j);
-        } else if (it.type == GM_WG13 || (it.type == GM_WG2 && !wide)) {
-          if (it.k_iters > 0) mn_tokens<16>(p, it, 0, gt, tok);
-        } else if (wide) {
-          if (it.k_iters > 0) mn_tokens<32>(p, it, 0, gt, tok);
-        }
-        bool ok = true;
-        for (int kk = 0; kk < it.k_iters; ++kk) {
-          // tokens of the next stage of an M/N-major item, loaded ahead
-          if (g != 0 && (it.type == GM_WG13 || it.type == GM_WG2) && kk + 1 < it.k_iters) {
-            if (wide)
-              mn_tokens<32>(p, it, kk + 1, gt, nxt);
-            else
-              mn_tokens<16>(p, it, kk + 1, gt, nxt);
-          }
-          if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
-          uint64_t* full = &ctl->full[stage];
-          uint8_t* a = sA + stage * kAStage;
-          uint8_t* b = sB + stage * kBStage;
-          if (it.type == GM_FWD1) {
-            gather_kmajor(a, p.gather_src, p.H, kk * 64, gt, tok, full);
-          } else if (it.type == GM_BWD_DA) {
-            gather_kmajor(a, p.gather_src, p.H, kk * 64, gt, tok, full);
-          } else if (it.type == GM_WG13) {
-            gather_mnmajor<16>(a, p.gather_src, p.H, it.m * 128, gt, tok, full);
-          } else if (it.type == GM_WG2) {
-            if (wide)
-              gather_mnmajor<32>(b, p.gather_src, p.H, it.n * p.bn, gt, tok, full);
-            else
-              gather_mnmajor<16>(b, p.gather_src, p.H, it.n * p.bn, gt, tok, full);
-          } else {
-            mbar_arrive(full);  // nothing to gather in this item: keep the phase count
-          }
-          if (it.type == GM_WG13 || it.type == GM_WG2) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) tok[j] = nxt[j];
-          }
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
+        bool ok;
+        if (it.type == GM_WG13)
+          ok = gather_item_mn<16>(p, it, sA, kAStage, it.m * 128, ctl, stage, phase, gt, wc);
+        else if (it.type == GM_WG2 && p.bn == 256)
+          ok = gather_item_mn<32>(p, it, sB, kBStage, it.n * p.bn, ctl, stage, phase, gt, wc);
+        else if (it.type == GM_WG2)
+          ok = gather_item_mn<16>(p, it, sB, kBStage, it.n * p.bn, ctl, stage, phase, gt, wc);
+        else
+          ok = gather_item_k(p, it, sA, ctl, stage, phase, gt, wc);
         if (!ok) break;
       }
       // let this thread's copies land before the CTA can exit
@@ -655,6 +727,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // ---------------------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    uint8_t* stage_out = sOut + (warp - 2) * kOutStage;
     uint32_t qs = 0, qp = 0, tcount = 0;
     while (true) {
       if (!mbar_wait(&ctl->qfull[qs], qp, wc)) break;
@@ -691,7 +764,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         case GM_FWD2: epi_scatter(p, it, tbase, row, p.bn); break;
         case GM_BWD_DA: epi_bwd_da(p, it, tbase, row); break;
         case GM_BWD_DX: epi_scatter(p, it, tbase, row, p.bn); break;
-        default: epi_wgrad(p, it, tbase, row); break;
+        default: epi_wgrad(p, it, tbase, q, lane, stage_out); break;
       }
       tc_fence_before();
       __syncwarp();
@@ -733,7 +806,9 @@ cudaError_t launch_mode(const TmapSet& maps, const GemmParams& p, int grid, cuda
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return 1024 + kStages * (kAStage + kBStage) + sizeof(Ctl); }
+size_t gemm_smem_bytes() {
+  return 1024 + kStages * (kAStage + kBStage) + ((sizeof(Ctl) + 127) / 128) * 128 + 4 * kOutStage;
+}
 
 cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
   switch (mode) {

@@ -25,6 +25,7 @@ constexpr int kGemmThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogu
 constexpr int kMaxExperts = 1024;
 
 constexpr int kMaxMaps = 6;
+constexpr int kOutStage = 32 * 32 * 2;  // one epilogue warp's 32 x 32 bf16 output chunk
 struct TmapSet {
   CUtensorMap m[kMaxMaps];
 };
