@@ -39,7 +39,7 @@ METRIC = "MoE layer fwd+bwd TFLOP/s"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_PHASES = ("fwd_gemm", "bwd_da", "bwd_dx", "bwd_wg13", "bwd_wg2")
-HBM_PHASES = ("fwd_combine", "bwd_dx_combine")
+HBM_PHASES = ("fwd_combine", "bwd_dx_combine", "bwd_sort")
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -82,7 +82,9 @@ def phase_flops(shape):
 def phase_bytes(shape):
     # algorithmic bytes of the HBM-bound kernels (bf16 = 2 B, f32 = 4 B)
     R, T, H = shape.R, shape.T, shape.H
-    return {"fwd_combine": R * H * 2 + R * 4 + T * H * 2, "bwd_dx_combine": R * H * 2 + T * H * 2}
+    return {"fwd_combine": R * H * 2 + R * 4 + T * H * 2, "bwd_dx_combine": R * H * 2 + T * H * 2,
+            # token-sorted copy of x or dout: R rows read and written (padding rows excluded)
+            "bwd_sort": 2 * R * H * 2}
 
 
 # ---------------------------------------------------------------- clocks

@@ -89,6 +89,13 @@ typedef struct {
  *                 its consumer's bounded wait runs out and the call records
  *                 MOK_ERR_TIMEOUT -- a host-chosen fault used to test the
  *                 failure path without faulting the GPU.
+ *                 Bit 1 (MOK_DEBUG_SERIAL_RING): run the forward's two GEMMs
+ *                 as one launch pair per minibatch (same ring, stream order)
+ *                 instead of the single persistent ring launch.
+ *                 Bit 2 (MOK_DEBUG_FUSED_WGRAD_GATHER): the weight-gradient
+ *                 GEMMs gather token rows in their load path instead of
+ *                 reading token-sorted copies.  Results are bitwise the same
+ *                 in every mode.
  */
 typedef struct {
   int32_t minibatch_rows;
@@ -99,6 +106,8 @@ typedef struct {
 } mok_config;
 
 #define MOK_DEBUG_SKIP_RING_SIGNAL 1
+#define MOK_DEBUG_SERIAL_RING 2
+#define MOK_DEBUG_FUSED_WGRAD_GATHER 4
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
 typedef struct {
@@ -257,7 +266,8 @@ enum {
   MOK_PHASE_BWD_WG13 = 7,      /* dW1 | dW3 grouped GEMM */
   MOK_PHASE_BWD_WG2 = 8,       /* dW2 grouped GEMM */
   MOK_PHASE_QUANT = 9,         /* MXFP8 quantisation of activations */
-  MOK_NUM_PHASES = 10
+  MOK_PHASE_BWD_SORT = 10,     /* token-sorted copies of x and dout for the weight gradients */
+  MOK_NUM_PHASES = 11
 };
 mok_status mok_trace_enable(int32_t on);
 mok_status mok_trace_read(float* ms /* [MOK_NUM_PHASES] */, int32_t* count /* [MOK_NUM_PHASES] */);

@@ -20,6 +20,7 @@ MOK_BF16 = 0
 MOK_MXFP8 = 1
 MOK_DEBUG_SKIP_RING_SIGNAL = 1
 MOK_DEBUG_SERIAL_RING = 2
+MOK_DEBUG_FUSED_WGRAD_GATHER = 4
 
 STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "MOK_ERR_WORKSPACE_TOO_SMALL",
           4: "MOK_ERR_CUDA", 5: "MOK_ERR_BAD_INDEX", 6: "MOK_ERR_TIMEOUT"}
@@ -31,7 +32,7 @@ EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_bu
            "mok_launch_count", "mok_build_schedule_noalloc"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
-          "bwd_wg2", "quant"]
+          "bwd_wg2", "quant", "bwd_sort"]
 
 
 class MokError(RuntimeError):

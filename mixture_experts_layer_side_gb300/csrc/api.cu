@@ -109,6 +109,16 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   L.dhu = take(P * 2 * I * 2);
   L.as = take(P * I * 2);
   L.dsp = take(P * (I / 128) * 4);
+  L.sorted = take(P * H * 2);
+  {
+    const int64_t t13 = (int64_t)(H / 128) * (2 * I / 256);
+    const int64_t bn_h = (H % 256 == 0) ? 256 : 128;
+    const int64_t t2 = (int64_t)(I / 128) * (H / bn_h);
+    L.wg_tiles = t13 > t2 ? t13 : t2;
+    const int64_t slots = s.E < kSplitSlots ? s.E : kSplitSlots;
+    L.wacc = take((size_t)slots * L.wg_tiles * 128 * 256 * 4);
+    L.wflags = take((size_t)slots * L.wg_tiles * 4 * 4);
+  }
   if (prec == MOK_MXFP8) {
     L.ring_sf = take((size_t)L.ring_slots * M * (I / 32));
     L.xq = take((size_t)s.T * H);
@@ -352,7 +362,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   if (!map_gather(&maps.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
   if (!map3d(&maps.m[1], W1, s.I, s.H, s.E, 64) || !map3d(&maps.m[2], W3, s.I, s.H, s.E, 64)) return MOK_ERR_CUDA;
 
-  const bool serial = (cfg->debug_flags & 2) != 0;
+  const bool serial = (cfg->debug_flags & MOK_DEBUG_SERIAL_RING) != 0;
   if (!serial) {
     // one persistent launch: GEMM1 and GEMM2 interleaved through the ring
     if (!map2d(&maps.m[3], g.ring, s.I, (uint64_t)S * M, 128) || !map3d(&maps.m[4], W2, s.H, s.I, s.E, 64))
@@ -422,6 +432,8 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
 
   GemmParams g;
   base_params(g, s, L, w);
+  g.wacc = reinterpret_cast<float*>(w + L.wacc);
+  g.wflags = reinterpret_cast<uint32_t*>(w + L.wflags);
   g.ctx_hu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(ctx));
   g.dhu = reinterpret_cast<__nv_bfloat16*>(w + L.dhu);
   g.as = reinterpret_cast<__nv_bfloat16*>(w + L.as);
@@ -472,10 +484,16 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));
   }
   // dW1 | dW3 = gather(x)^T [dh|du], per expert
+  const bool sorted = (cfg->debug_flags & MOK_DEBUG_FUSED_WGRAD_GATHER) == 0;
+  __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
   {
     TmapSet m;
     memset(&m, 0, sizeof(m));
-    if (!map_gather(&m.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
+    if (sorted) {
+      Phase ph(MOK_PHASE_BWD_SORT, st, 1);
+      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
+    }
+    if (sorted ? !map2d(&m.m[0], srt, s.H, P, 64) : !map_gather(&m.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
     if (!map2d(&m.m[1], g.dhu, 2 * (uint64_t)s.I, P, 64)) return MOK_ERR_CUDA;
     GemmParams q = g;
     q.nmaps = 2;
@@ -483,6 +501,8 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.n_tiles = 2 * s.I / 256;
     q.m_tiles = s.H / 128;
     q.counter = 2;
+    q.wg_sorted = sorted ? 1 : 0;
+    MOK_CUDA(cudaMemsetAsync(g.wflags, 0, (size_t)(s.E < kSplitSlots ? s.E : kSplitSlots) * L.wg_tiles * 16, st));
     q.gather_src = static_cast<const __nv_bfloat16*>(x);
     q.dw0 = static_cast<__nv_bfloat16*>(dW1);
     q.dw1 = static_cast<__nv_bfloat16*>(dW3);
@@ -493,13 +513,20 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   {
     TmapSet m;
     memset(&m, 0, sizeof(m));
-    if (!map2d(&m.m[0], g.as, s.I, P, 64) || !map_gather(&m.m[1], dout, s.H, s.T)) return MOK_ERR_CUDA;
+    if (sorted) {
+      Phase ph(MOK_PHASE_BWD_SORT, st, 1);
+      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(dout), srt, st));
+    }
+    if (!map2d(&m.m[0], g.as, s.I, P, 64)) return MOK_ERR_CUDA;
+    if (sorted ? !map2d(&m.m[1], srt, s.H, P, 64) : !map_gather(&m.m[1], dout, s.H, s.T)) return MOK_ERR_CUDA;
     GemmParams q = g;
     q.nmaps = 2;
     q.bn = bn_h;
     q.n_tiles = s.H / bn_h;
     q.m_tiles = s.I / 128;
     q.counter = 3;
+    q.wg_sorted = sorted ? 1 : 0;
+    MOK_CUDA(cudaMemsetAsync(g.wflags, 0, (size_t)(s.E < kSplitSlots ? s.E : kSplitSlots) * L.wg_tiles * 16, st));
     q.gather_src = static_cast<const __nv_bfloat16*>(dout);
     q.dw0 = static_cast<__nv_bfloat16*>(dW2);
     Phase ph(MOK_PHASE_BWD_WG2, st, 1);

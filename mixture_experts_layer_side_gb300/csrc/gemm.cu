@@ -48,6 +48,8 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   int po[kMaxExperts + 1];  // padded expert offsets (weight-gradient modes)
+  int item_off[kMaxExperts + 1];  // weight-gradient modes: first item of each expert
+  int slot[kMaxExperts];          // split-K accumulator slot of each expert, or -1
 };
 
 // A decoded work item.
@@ -56,8 +58,9 @@ struct Item {
   int m;        // 128-row tile index (row-tiled modes) or M tile inside the expert (wgrad)
   int n;        // N tile
   int e;        // expert
-  int row0;     // first padded row of the tile (row-tiled) or of the expert (wgrad)
+  int row0;     // first padded row of the tile (row-tiled) or of the K chunk (wgrad)
   int k_iters;  // K iterations of 128 bytes
+  int chunk, nchunk, slot, tile;  // weight-gradient split K (nchunk 1: unsplit)
 };
 
 __device__ __forceinline__ int used_tiles(const GemmParams& p) { return p.hdr[kHdrTiles]; }
@@ -68,7 +71,7 @@ __device__ int count_items(const GemmParams& p) {
   if constexpr (MODE == GM_DENSE) {
     return p.m_tiles * p.n_tiles;
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
-    return p.E * p.m_tiles * p.n_tiles;
+    return 0;  // from the item table in shared memory (see the kernel prologue)
   } else if constexpr (MODE == GM_FWD_RING) {
     return used_tiles(p) * (p.g1_tiles + p.n_tiles);
   } else {
@@ -116,8 +119,13 @@ __device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& 
 }
 
 template <int MODE>
-__device__ Item decode(const GemmParams& p, const int* po, int w) {
+__device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
+  const int* po = ctl->po;
   Item it;
+  it.chunk = 0;
+  it.nchunk = 1;
+  it.slot = -1;
+  it.tile = 0;
   if constexpr (MODE == GM_DENSE) {
     it.type = MODE;
     it.m = w / p.n_tiles;
@@ -126,16 +134,30 @@ __device__ Item decode(const GemmParams& p, const int* po, int w) {
     it.row0 = it.m * kTileRows;
     it.k_iters = p.k_iters;
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
-    const int per_e = p.m_tiles * p.n_tiles;
+    // expert: last e with item_off[e] <= w (every expert has >= 1 item)
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ctl->item_off[mid] <= w) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int local = w - ctl->item_off[e];
+    const int c = local / tiles;  // chunk-major inside the expert
+    const int tile = local - c * tiles;
+    const int k_e = (po[e + 1] - po[e]) / 64;
+    const int nc = (ctl->slot[e] >= 0) ? (k_e + kSplitK - 1) / kSplitK : 1;
+    const int kb = (int)((long)c * k_e / nc), ke = (int)((long)(c + 1) * k_e / nc);
     it.type = MODE;
-    it.e = w / per_e;
-    const int r = w % per_e;
-    it.m = r / p.n_tiles;
-    it.n = r % p.n_tiles;
-    const int a = po[it.e];
-    const int b = po[it.e + 1];
-    it.row0 = a;
-    it.k_iters = (b - a) / 64;
+    it.e = e;
+    it.m = tile / p.n_tiles;
+    it.n = tile % p.n_tiles;
+    it.row0 = po[e] + kb * 64;
+    it.k_iters = ke - kb;
+    it.chunk = c;
+    it.nchunk = nc;
+    it.slot = ctl->slot[e];
+    it.tile = tile;
   } else {
     int type = MODE, m, n;
     if constexpr (MODE == GM_FWD_RING) {
@@ -165,7 +187,10 @@ __device__ __forceinline__ int ring_row(const GemmParams& p, int prow) {
 
 // ------------------------------------------------------------------ producers
 // Which operand of an item is gathered by token (0 none, 1 A, 2 B).
-__device__ __forceinline__ int gathered_operand(int type) {
+// With p.wg_sorted the weight-gradient GEMMs read a token-sorted copy of
+// x / dout (rows in padded schedule order) with plain TMA instead.
+__device__ __forceinline__ int gathered_operand(const GemmParams& p, int type) {
+  if (p.wg_sorted && (type == GM_WG13 || type == GM_WG2)) return 0;
   return (type == GM_FWD1 || type == GM_BWD_DA || type == GM_WG13) ? 1 : (type == GM_WG2 ? 2 : 0);
 }
 
@@ -175,8 +200,8 @@ __device__ __forceinline__ constexpr bool mode_gathers() {
 }
 
 // Bytes the TMA producer brings into one stage (gathered operands excluded).
-__device__ __forceinline__ uint32_t tma_stage_bytes(int type, int bn) {
-  const int g = gathered_operand(type);
+__device__ __forceinline__ uint32_t tma_stage_bytes(const GemmParams& p, int type, int bn) {
+  const int g = gathered_operand(p, type);
   return (g == 1 ? 0u : (uint32_t)kAStage) + (g == 2 ? 0u : (uint32_t)bn * 128u);
 }
 
@@ -218,9 +243,16 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
     // B = [dh|du] rows of the expert (N = 2I, MN-major)
     for (int cc = 0; cc < p.bn / 64; ++cc)
       tma_load_2d(b + cc * 8192, &mp.m[1], bar, it.n * p.bn + cc * 64, it.row0 + kk * 64);
+    // A = token-sorted x rows (M = H, MN-major), when not gathered
+    if (p.wg_sorted)
+      for (int ca = 0; ca < 2; ++ca) tma_load_2d(a + ca * 8192, &mp.m[0], bar, it.m * 128 + ca * 64, it.row0 + kk * 64);
   } else if (type == GM_WG2) {
     // A = (s a) rows of the expert (M = I, MN-major)
     for (int ca = 0; ca < 2; ++ca) tma_load_2d(a + ca * 8192, &mp.m[0], bar, it.m * 128 + ca * 64, it.row0 + kk * 64);
+    // B = token-sorted dout rows (N = H, MN-major), when not gathered
+    if (p.wg_sorted)
+      for (int cc = 0; cc < p.bn / 64; ++cc)
+        tma_load_2d(b + cc * 8192, &mp.m[1], bar, it.n * p.bn + cc * 64, it.row0 + kk * 64);
   }
 }
 
@@ -500,6 +532,74 @@ __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it,
   }
 }
 
+// Chunk c of a split weight-gradient tile.  The tile's f32 accumulator
+// (thread-major: float4 (j, row) at j * 128 + row, j = 4-column group) gets
+// acc = acc + chunk, in chunk order: chunk c waits until chunk c - 1 of the
+// same rows has published (per epilogue warp counter), so the sum order is
+// fixed and the result bitwise reproducible.  The last chunk converts to
+// bf16 and writes dW; the others publish for the next.
+template <int BN>
+__device__ __forceinline__ void epi_wgrad_split_n(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane,
+                                                  uint8_t* stage, const WaitCtx& wc, bool& ok) {
+  const int tiles = p.m_tiles * p.n_tiles;
+  const long tile_id = (long)it.slot * tiles + it.tile;
+  float4* acc = reinterpret_cast<float4*>(p.wacc) + tile_id * (128 * 256 / 4);
+  uint32_t* flag = p.wflags + tile_id * 4 + q;
+  const int row = q * 32 + lane;
+  const int r0 = it.m * 128 + q * 32;
+  const bool first = it.chunk == 0, last = it.chunk == it.nchunk - 1;
+  if (!first) {
+    // every lane acquires the previous chunk's rows itself
+    if (!wait_flag_geq(flag, (uint32_t)it.chunk, wc)) { ok = false; return; }
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    uint32_t r[32];
+    if (it.k_iters > 0) {
+      tmem_ld32_issue(tbase + c, r);
+      tmem_wait_ld();
+      tmem_regs_ready(r);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+    }
+    float v[32];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const long idx = (long)((c >> 2) + g) * 128 + row;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!first) a = acc[idx];
+      v[4 * g] = a.x + __uint_as_float(r[4 * g]);
+      v[4 * g + 1] = a.y + __uint_as_float(r[4 * g + 1]);
+      v[4 * g + 2] = a.z + __uint_as_float(r[4 * g + 2]);
+      v[4 * g + 3] = a.w + __uint_as_float(r[4 * g + 3]);
+      if (!last) acc[idx] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    }
+    if (last) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+      const int col = it.n * BN + c;
+      __nv_bfloat16* base;
+      long ld;
+      if (it.type == GM_WG13) {
+        base = (col < p.I) ? p.dw0 + ((long)it.e * p.H + r0) * p.I + col
+                           : p.dw1 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
+        ld = p.I;
+      } else {
+        base = p.dw0 + ((long)it.e * p.I + r0) * p.H + col;
+        ld = p.H;
+      }
+      store_chunk_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
+    }
+  }
+  if (!last) {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(flag, 1u);
+  }
+}
+
 __device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane, uint8_t* stage) {
   if (p.bn == 256)
     epi_wgrad_n<256>(p, it, tbase, q, lane, stage);
@@ -551,7 +651,7 @@ __device__ bool gather_item_mn(const GemmParams& p, const Item& it, uint8_t* op_
 // (GEMM2 inside the ring launch) only keep the stage barriers' phase count.
 __device__ bool gather_item_k(const GemmParams& p, const Item& it, uint8_t* sA, Ctl* ctl, uint32_t& stage,
                               uint32_t& phase, int gt, const WaitCtx& wc) {
-  const bool gather = gathered_operand(it.type) == 1;
+  const bool gather = gathered_operand(p, it.type) == 1;
   int tok[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) tok[j] = gather ? token_or_neg(p, it.row0 + (gt >> 3) + 16 * j) : -1;
@@ -602,8 +702,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     ctl->abort = 0;
     fence_mbar_init();
   }
-  if (kWgrad)
+  if (kWgrad) {
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) ctl->po[e] = p.padded_offsets[e];
+    __syncthreads();
+    if (warp == 0) {
+      // item table: expert e has tiles x chunks items; an expert with more
+      // than kSplitK K stages takes the next free accumulator slot (if any)
+      // and is split into ceil(stages / kSplitK) chunks
+      const int tiles = p.m_tiles * p.n_tiles;
+      int run_items = 0, run_split = 0;
+      for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        const int k_e = (e < p.E) ? (ctl->po[e + 1] - ctl->po[e]) / 64 : 0;
+        const int want = (e < p.E && k_e > kSplitK) ? 1 : 0;
+        const unsigned wmask = __ballot_sync(0xffffffffu, want);
+        const int slot = run_split + __popc(wmask & ((1u << lane) - 1u));
+        const bool split = want && slot < kSplitSlots;
+        const int items = (e < p.E) ? tiles * (split ? (k_e + kSplitK - 1) / kSplitK : 1) : 0;
+        int incl = items;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += v;
+        }
+        if (e < p.E) {
+          ctl->item_off[e] = run_items + incl - items;
+          ctl->slot[e] = split ? slot : -1;
+        }
+        run_items += __shfl_sync(0xffffffffu, incl, 31);
+        run_split += __popc(wmask);
+      }
+      if (lane == 0) ctl->item_off[p.E] = run_items;
+    }
+  }
   if (warp == 0 && lane == 0)
     for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
   if (warp == 1) {
@@ -614,7 +745,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int num_items = count_items<MODE>(p);
+  const int num_items = kWgrad ? ctl->item_off[p.E] : count_items<MODE>(p);
   const int* po = ctl->po;
 
   if (warp == 0) {
@@ -633,7 +764,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (!ok || w < 0) break;
         // fetch the next item now; its latency overlaps this item's loads
         const int w_next = (int)atomicAdd(counter, 1u);
-        const Item it = decode<MODE>(p, po, w);
+        const Item it = decode<MODE>(p, ctl, w);
         if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
           // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
           // of its GEMM1 column tiles are published, then order the
@@ -642,7 +773,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           fence_proxy_async_global();
           if (!ok) break;
         }
-        const uint32_t bytes = tma_stage_bytes(it.type, item_bn(p, it.type));
+        const uint32_t bytes = tma_stage_bytes(p, it.type, item_bn(p, it.type));
         for (int kk = 0; kk < it.k_iters; ++kk) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&ctl->full[stage], bytes);
@@ -664,9 +795,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
         if (++qs == kQueue) { qs = 0; qp ^= 1; }
         if (w < 0) break;
-        const Item it = decode<MODE>(p, po, w);
+        const Item it = decode<MODE>(p, ctl, w);
         bool ok;
-        if (it.type == GM_WG13)
+        if (gathered_operand(p, it.type) == 0)
+          ok = gather_item_k(p, it, sA, ctl, stage, phase, gt, wc);
+        else if (it.type == GM_WG13)
           ok = gather_item_mn<16>(p, it, sA, kAStage, it.m * 128, ctl, stage, phase, gt, wc);
         else if (it.type == GM_WG2 && p.bn == 256)
           ok = gather_item_mn<32>(p, it, sB, kBStage, it.n * p.bn, ctl, stage, phase, gt, wc);
@@ -689,7 +822,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE>(p, po, w);
+      const Item it = decode<MODE>(p, ctl, w);
       const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
       if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)) break;
       tc_fence_after();
@@ -697,7 +830,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       const bool amn = a_mn_major<MODE>(p, it.type), bmn = b_mn_major<MODE>(p, it.type);
       const uint32_t idesc = idesc_bf16(128, bn, amn ? 1 : 0, bmn ? 1 : 0);
       const uint32_t d = tmem + buf * 256;
-      const bool gathered = gathered_operand(it.type) != 0;
+      const bool gathered = gathered_operand(p, it.type) != 0;
       bool ok = true;
       for (int kk = 0; kk < it.k_iters; ++kk) {
         if (!mbar_wait(&ctl->full[stage], phase, wc)) { ok = false; break; }
@@ -736,7 +869,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE>(p, po, w);
+      const Item it = decode<MODE>(p, ctl, w);
       const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();
@@ -764,8 +897,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         case GM_FWD2: epi_scatter(p, it, tbase, row, p.bn); break;
         case GM_BWD_DA: epi_bwd_da(p, it, tbase, row); break;
         case GM_BWD_DX: epi_scatter(p, it, tbase, row, p.bn); break;
-        default: epi_wgrad(p, it, tbase, q, lane, stage_out); break;
+        default:
+          if (it.nchunk > 1) {
+            if (p.bn == 256)
+              epi_wgrad_split_n<256>(p, it, tbase, q, lane, stage_out, wc, ok);
+            else
+              epi_wgrad_split_n<128>(p, it, tbase, q, lane, stage_out, wc, ok);
+          } else {
+            epi_wgrad(p, it, tbase, q, lane, stage_out);
+          }
+          break;
       }
+      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->tempty[buf]);

@@ -39,6 +39,10 @@ struct WsLayout {
   size_t dhu;         // bf16 [pad_capacity, 2I]
   size_t as;          // bf16 [pad_capacity, I]  s * a
   size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
+  size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x, then dout (weight gradients)
+  size_t wacc;        // f32  weight-gradient split-K accumulators [slots][tiles][128 x 256]
+  size_t wflags;      // u32  their chunk counters [slots][tiles][4]
+  int64_t wg_tiles;   // output tiles per expert of the larger weight-gradient GEMM
   // MXFP8 activation copies
   size_t xq, xsf;     // x quantised along H: u8 [T, H], [T, H/32]
   size_t dq, dsf;     // dout quantised along H
@@ -66,6 +70,9 @@ cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_
                              cudaStream_t st);
 cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
                                __nv_bfloat16* xg, cudaStream_t st);
+cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st);
+cudaError_t launch_quant_rows_tiled(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
+                                    uint8_t* q, uint8_t* sf, cudaStream_t st);
 cudaError_t launch_mxfp8_quantize(const __nv_bfloat16* src, int batch, int rows, int cols, int block_axis,
                                   uint8_t* q, uint8_t* sf, cudaStream_t st);
 

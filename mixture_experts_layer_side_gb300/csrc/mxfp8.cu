@@ -101,7 +101,82 @@ __global__ void quant_colblocks(const __nv_bfloat16* __restrict__ src, int batch
   }
 }
 
+// Offset of scale (mn, kb) inside a 512-byte scale block of 128 rows (or
+// columns) x 4 K-blocks: the layout tcgen05.cp .32x128b.warpx4 replicates
+// into the four TMEM lane quarters, byte (mn % 32) * 16 + (mn / 32) * 4 + kb.
+__device__ __forceinline__ int sf_block_offset(int mn, int kb) { return (mn & 31) * 16 + (mn >> 5) * 4 + kb; }
+
+// Plain scales [batch][K/32][N] (blocks along K = rows) -> tiled
+// [batch][N/128][K/128][512 B] (one block per 128 N x 128 K tile).
+__global__ void tile_scales_kernel(const uint8_t* __restrict__ sf, int batch, int kb_count, int N,
+                                   uint8_t* __restrict__ out) {
+  const int kg_count = kb_count / 4;
+  const long n_words = (long)batch * kg_count * N;  // one 4-byte word per (batch, k group, n)
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n_words; i += (long)gridDim.x * blockDim.x) {
+    const int n = (int)(i % N);
+    const long bg = i / N;
+    const int kg = (int)(bg % kg_count);
+    const long b = bg / kg_count;
+    const uint8_t* src = sf + (b * kb_count + (long)kg * 4) * N + n;
+    const uint32_t w = (uint32_t)src[0] | ((uint32_t)src[N] << 8) | ((uint32_t)src[2L * N] << 16) |
+                       ((uint32_t)src[3L * N] << 24);
+    uint8_t* blk = out + ((b * (N / 128) + n / 128) * kg_count + kg) * 512;
+    *reinterpret_cast<uint32_t*>(blk + sf_block_offset(n & 127, 0)) = w;
+  }
+}
+
+// Quantise bf16 [rows_cap, C] along the rows (blocks of 32 rows) for the rows
+// in use (header word), codes [rows, C] and tiled scales
+// [rows/128][C/128][512 B] (scale of (row block, column) at
+// sf_block_offset(column % 128, (row / 32) % 4)).
+__global__ void quant_rows_tiled_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ rows_used,
+                                        int C, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const int rows = *rows_used;
+  const long n = (long)(rows / 32) * C;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % C);
+    const int rb = (int)(i / C);
+    const long base = (long)rb * 32 * C + c;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      v[r] = __bfloat162float(src[base + (long)r * C]);
+      amax = fmaxf(amax, fabsf(v[r]));
+    }
+    const int X = block_exponent(amax);
+    const float inv = exp2_int(-X);
+#pragma unroll
+    for (int r = 0; r < 32; r += 2) {
+      const uint16_t pr = cvt_e4m3x2(v[r] * inv, v[r + 1] * inv);
+      q[base + (long)r * C] = (uint8_t)(pr & 0xFF);
+      q[base + (long)(r + 1) * C] = (uint8_t)(pr >> 8);
+    }
+    uint8_t* blk = sf + ((long)(rb / 4) * (C / 128) + c / 128) * 512;
+    blk[sf_block_offset(c & 127, rb & 3)] = (uint8_t)(X + 127);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st) {
+  const long words = (long)batch * (kb_count / 4) * N;
+  long grid = (words + 255) / 256;
+  const long cap = (long)device_sm_count() * 32;
+  if (grid > cap) grid = cap;
+  tile_scales_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, kb_count, N, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_tiled(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
+                                    uint8_t* q, uint8_t* sf, cudaStream_t st) {
+  const long n = (rows_cap / 32) * C;
+  long grid = (n + 255) / 256;
+  const long cap = (long)device_sm_count() * 32;
+  if (grid > cap) grid = cap;
+  quant_rows_tiled_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(src, rows_used, C, q, sf);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mxfp8_quantize(const __nv_bfloat16* src, int batch, int rows, int cols, int block_axis,
                                   uint8_t* q, uint8_t* sf, cudaStream_t st) {

@@ -17,6 +17,9 @@ CASES = [
     ("ragged_zipf", (300, 256, 256, 6, 3), "zipf", 2),
     ("hot_empty", (512, 384, 128, 24, 4), "hot", 3),
     ("wide", (200, 512, 384, 5, 2), "uniform", 4),
+    # experts above 1,024 routed rows: weight gradients split into K chunks
+    ("split_2chunk", (3000, 256, 128, 20, 2), "hot", 5),
+    ("split_3chunk", (4096, 256, 256, 20, 2), "hot", 6),
 ]
 
 
@@ -69,12 +72,22 @@ def test_ring_sizes_and_serial_path_are_bitwise_equal(minibatch_rows, ring_slots
         assert torch.equal(g_a[k], g_b[k]), k
 
 
-def test_reruns_are_bitwise_identical():
+@pytest.mark.parametrize("shape,routing", [((512, 256, 256, 24, 4), "hot"), ((4096, 256, 256, 20, 2), "hot")])
+def test_reruns_are_bitwise_identical(shape, routing):
     require_gpu()
-    shape, routing = (512, 256, 256, 24, 4), "hot"
     _, out0, g0 = run_layer(shape, routing, 5)
     for _ in range(3):
         _, out1, g1 = run_layer(shape, routing, 5)
         assert torch.equal(out0, out1)
         for k in g0:
             assert torch.equal(g0[k], g1[k]), k
+
+
+@pytest.mark.parametrize("shape,routing", [((512, 256, 256, 24, 4), "hot"), ((4096, 256, 256, 20, 2), "hot")])
+def test_weight_gradient_gather_paths_are_bitwise_equal(shape, routing):
+    """Token-sorted copies + plain TMA vs gathers fused in the load path."""
+    require_gpu()
+    _, _, g_sorted = run_layer(shape, routing, 8)
+    _, _, g_fused = run_layer(shape, routing, 8, debug_flags=4)
+    for k in ("dW1", "dW3", "dW2"):
+        assert torch.equal(g_sorted[k], g_fused[k]), k
