@@ -110,15 +110,6 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   L.as = take(P * I * 2);
   L.dsp = take(P * (I / 128) * 4);
   L.sorted = take(P * H * 2);
-  {
-    const int64_t t13 = (int64_t)(H / 128) * (2 * I / 256);
-    const int64_t bn_h = (H % 256 == 0) ? 256 : 128;
-    const int64_t t2 = (int64_t)(I / 128) * (H / bn_h);
-    L.wg_tiles = t13 > t2 ? t13 : t2;
-    const int64_t slots = s.E < kSplitSlots ? s.E : kSplitSlots;
-    L.wacc = take((size_t)slots * L.wg_tiles * 128 * 256 * 4);
-    L.wflags = take((size_t)slots * L.wg_tiles * 4 * 4);
-  }
   if (prec == MOK_MXFP8) {
     L.ring_sf = take((size_t)L.ring_slots * M * (I / 32));
     L.xq = take((size_t)s.T * H);
@@ -432,8 +423,6 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
 
   GemmParams g;
   base_params(g, s, L, w);
-  g.wacc = reinterpret_cast<float*>(w + L.wacc);
-  g.wflags = reinterpret_cast<uint32_t*>(w + L.wflags);
   g.ctx_hu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(ctx));
   g.dhu = reinterpret_cast<__nv_bfloat16*>(w + L.dhu);
   g.as = reinterpret_cast<__nv_bfloat16*>(w + L.as);
@@ -502,7 +491,6 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tiles = s.H / 128;
     q.counter = 2;
     q.wg_sorted = sorted ? 1 : 0;
-    MOK_CUDA(cudaMemsetAsync(g.wflags, 0, (size_t)(s.E < kSplitSlots ? s.E : kSplitSlots) * L.wg_tiles * 16, st));
     q.gather_src = static_cast<const __nv_bfloat16*>(x);
     q.dw0 = static_cast<__nv_bfloat16*>(dW1);
     q.dw1 = static_cast<__nv_bfloat16*>(dW3);
@@ -526,7 +514,6 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tiles = s.I / 128;
     q.counter = 3;
     q.wg_sorted = sorted ? 1 : 0;
-    MOK_CUDA(cudaMemsetAsync(g.wflags, 0, (size_t)(s.E < kSplitSlots ? s.E : kSplitSlots) * L.wg_tiles * 16, st));
     q.gather_src = static_cast<const __nv_bfloat16*>(dout);
     q.dw0 = static_cast<__nv_bfloat16*>(dW2);
     Phase ph(MOK_PHASE_BWD_WG2, st, 1);

@@ -48,8 +48,6 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   int po[kMaxExperts + 1];  // padded expert offsets (weight-gradient modes)
-  int item_off[kMaxExperts + 1];  // weight-gradient modes: first item of each expert
-  int slot[kMaxExperts];          // split-K accumulator slot of each expert, or -1
 };
 
 // A decoded work item.
@@ -58,9 +56,8 @@ struct Item {
   int m;        // 128-row tile index (row-tiled modes) or M tile inside the expert (wgrad)
   int n;        // N tile
   int e;        // expert
-  int row0;     // first padded row of the tile (row-tiled) or of the K chunk (wgrad)
+  int row0;     // first padded row of the tile (row-tiled) or of the expert (wgrad)
   int k_iters;  // K iterations of 128 bytes
-  int chunk, nchunk, slot, tile;  // weight-gradient split K (nchunk 1: unsplit)
 };
 
 __device__ __forceinline__ int used_tiles(const GemmParams& p) { return p.hdr[kHdrTiles]; }
@@ -71,7 +68,7 @@ __device__ int count_items(const GemmParams& p) {
   if constexpr (MODE == GM_DENSE) {
     return p.m_tiles * p.n_tiles;
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
-    return 0;  // from the item table in shared memory (see the kernel prologue)
+    return p.E * p.m_tiles * p.n_tiles;
   } else if constexpr (MODE == GM_FWD_RING) {
     return used_tiles(p) * (p.g1_tiles + p.n_tiles);
   } else {
@@ -122,10 +119,6 @@ template <int MODE>
 __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
   const int* po = ctl->po;
   Item it;
-  it.chunk = 0;
-  it.nchunk = 1;
-  it.slot = -1;
-  it.tile = 0;
   if constexpr (MODE == GM_DENSE) {
     it.type = MODE;
     it.m = w / p.n_tiles;
@@ -134,30 +127,14 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.row0 = it.m * kTileRows;
     it.k_iters = p.k_iters;
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
-    // expert: last e with item_off[e] <= w (every expert has >= 1 item)
-    int lo = 0, hi = p.E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ctl->item_off[mid] <= w) lo = mid; else hi = mid - 1;
-    }
-    const int e = lo;
-    const int tiles = p.m_tiles * p.n_tiles;
-    const int local = w - ctl->item_off[e];
-    const int c = local / tiles;  // chunk-major inside the expert
-    const int tile = local - c * tiles;
-    const int k_e = (po[e + 1] - po[e]) / 64;
-    const int nc = (ctl->slot[e] >= 0) ? (k_e + kSplitK - 1) / kSplitK : 1;
-    const int kb = (int)((long)c * k_e / nc), ke = (int)((long)(c + 1) * k_e / nc);
+    const int per_e = p.m_tiles * p.n_tiles;
     it.type = MODE;
-    it.e = e;
-    it.m = tile / p.n_tiles;
-    it.n = tile % p.n_tiles;
-    it.row0 = po[e] + kb * 64;
-    it.k_iters = ke - kb;
-    it.chunk = c;
-    it.nchunk = nc;
-    it.slot = ctl->slot[e];
-    it.tile = tile;
+    it.e = w / per_e;
+    const int r = w - it.e * per_e;
+    it.m = r / p.n_tiles;
+    it.n = r % p.n_tiles;
+    it.row0 = po[it.e];
+    it.k_iters = (po[it.e + 1] - po[it.e]) / 64;
   } else {
     int type = MODE, m, n;
     if constexpr (MODE == GM_FWD_RING) {
@@ -532,74 +509,6 @@ __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it,
   }
 }
 
-// Chunk c of a split weight-gradient tile.  The tile's f32 accumulator
-// (thread-major: float4 (j, row) at j * 128 + row, j = 4-column group) gets
-// acc = acc + chunk, in chunk order: chunk c waits until chunk c - 1 of the
-// same rows has published (per epilogue warp counter), so the sum order is
-// fixed and the result bitwise reproducible.  The last chunk converts to
-// bf16 and writes dW; the others publish for the next.
-template <int BN>
-__device__ __forceinline__ void epi_wgrad_split_n(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane,
-                                                  uint8_t* stage, const WaitCtx& wc, bool& ok) {
-  const int tiles = p.m_tiles * p.n_tiles;
-  const long tile_id = (long)it.slot * tiles + it.tile;
-  float4* acc = reinterpret_cast<float4*>(p.wacc) + tile_id * (128 * 256 / 4);
-  uint32_t* flag = p.wflags + tile_id * 4 + q;
-  const int row = q * 32 + lane;
-  const int r0 = it.m * 128 + q * 32;
-  const bool first = it.chunk == 0, last = it.chunk == it.nchunk - 1;
-  if (!first) {
-    // every lane acquires the previous chunk's rows itself
-    if (!wait_flag_geq(flag, (uint32_t)it.chunk, wc)) { ok = false; return; }
-  }
-#pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
-    uint32_t r[32];
-    if (it.k_iters > 0) {
-      tmem_ld32_issue(tbase + c, r);
-      tmem_wait_ld();
-      tmem_regs_ready(r);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) r[i] = 0u;
-    }
-    float v[32];
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const long idx = (long)((c >> 2) + g) * 128 + row;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (!first) a = acc[idx];
-      v[4 * g] = a.x + __uint_as_float(r[4 * g]);
-      v[4 * g + 1] = a.y + __uint_as_float(r[4 * g + 1]);
-      v[4 * g + 2] = a.z + __uint_as_float(r[4 * g + 2]);
-      v[4 * g + 3] = a.w + __uint_as_float(r[4 * g + 3]);
-      if (!last) acc[idx] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-    }
-    if (last) {
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-      const int col = it.n * BN + c;
-      __nv_bfloat16* base;
-      long ld;
-      if (it.type == GM_WG13) {
-        base = (col < p.I) ? p.dw0 + ((long)it.e * p.H + r0) * p.I + col
-                           : p.dw1 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
-        ld = p.I;
-      } else {
-        base = p.dw0 + ((long)it.e * p.I + r0) * p.H + col;
-        ld = p.H;
-      }
-      store_chunk_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
-    }
-  }
-  if (!last) {
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) red_release_gpu_add(flag, 1u);
-  }
-}
-
 __device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane, uint8_t* stage) {
   if (p.bn == 256)
     epi_wgrad_n<256>(p, it, tbase, q, lane, stage);
@@ -704,36 +613,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
   if (kWgrad) {
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) ctl->po[e] = p.padded_offsets[e];
-    __syncthreads();
-    if (warp == 0) {
-      // item table: expert e has tiles x chunks items; an expert with more
-      // than kSplitK K stages takes the next free accumulator slot (if any)
-      // and is split into ceil(stages / kSplitK) chunks
-      const int tiles = p.m_tiles * p.n_tiles;
-      int run_items = 0, run_split = 0;
-      for (int e0 = 0; e0 < p.E; e0 += 32) {
-        const int e = e0 + lane;
-        const int k_e = (e < p.E) ? (ctl->po[e + 1] - ctl->po[e]) / 64 : 0;
-        const int want = (e < p.E && k_e > kSplitK) ? 1 : 0;
-        const unsigned wmask = __ballot_sync(0xffffffffu, want);
-        const int slot = run_split + __popc(wmask & ((1u << lane) - 1u));
-        const bool split = want && slot < kSplitSlots;
-        const int items = (e < p.E) ? tiles * (split ? (k_e + kSplitK - 1) / kSplitK : 1) : 0;
-        int incl = items;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, d);
-          if (lane >= d) incl += v;
-        }
-        if (e < p.E) {
-          ctl->item_off[e] = run_items + incl - items;
-          ctl->slot[e] = split ? slot : -1;
-        }
-        run_items += __shfl_sync(0xffffffffu, incl, 31);
-        run_split += __popc(wmask);
-      }
-      if (lane == 0) ctl->item_off[p.E] = run_items;
-    }
   }
   if (warp == 0 && lane == 0)
     for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
@@ -745,7 +624,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int num_items = kWgrad ? ctl->item_off[p.E] : count_items<MODE>(p);
+  const int num_items = count_items<MODE>(p);
   const int* po = ctl->po;
 
   if (warp == 0) {
@@ -753,7 +632,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
       uint32_t* counter = reinterpret_cast<uint32_t*>(&p.hdr[kHdrCounters + p.counter]);
+      // Weight-gradient launches keep four tile-counter fetches in flight, so
+      // a run of short items (empty experts, tiny K) does not pay an atomic
+      // round trip each; the values come back in increasing order, so the
+      // CTA still takes its items in fetch order.  Launches with long items
+      // fetch one ahead (holding more would cost tail balance and, in the
+      // ring launch, delay the GEMM2 tiles other CTAs wait on).
       int w = (int)atomicAdd(counter, 1u);
+      int f1 = 0, f2 = 0, f3 = 0;
+      if (kWgrad) {
+        f1 = (int)atomicAdd(counter, 1u);
+        f2 = (int)atomicAdd(counter, 1u);
+        f3 = (int)atomicAdd(counter, 1u);
+      }
       bool ok = true;
       while (ok) {
         if (w >= num_items) w = -1;
@@ -762,8 +653,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         mbar_arrive(&ctl->qfull[qs]);
         if (++qs == kQueue) { qs = 0; qp ^= 1; }
         if (!ok || w < 0) break;
-        // fetch the next item now; its latency overlaps this item's loads
-        const int w_next = (int)atomicAdd(counter, 1u);
+        int w_next;
+        if (kWgrad) {
+          w_next = f1;
+          f1 = f2;
+          f2 = f3;
+          f3 = (int)atomicAdd(counter, 1u);
+        } else {
+          w_next = (int)atomicAdd(counter, 1u);
+        }
         const Item it = decode<MODE>(p, ctl, w);
         if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
           // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
@@ -897,18 +795,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         case GM_FWD2: epi_scatter(p, it, tbase, row, p.bn); break;
         case GM_BWD_DA: epi_bwd_da(p, it, tbase, row); break;
         case GM_BWD_DX: epi_scatter(p, it, tbase, row, p.bn); break;
-        default:
-          if (it.nchunk > 1) {
-            if (p.bn == 256)
-              epi_wgrad_split_n<256>(p, it, tbase, q, lane, stage_out, wc, ok);
-            else
-              epi_wgrad_split_n<128>(p, it, tbase, q, lane, stage_out, wc, ok);
-          } else {
-            epi_wgrad(p, it, tbase, q, lane, stage_out);
-          }
-          break;
+        default: epi_wgrad(p, it, tbase, q, lane, stage_out); break;
       }
-      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->tempty[buf]);

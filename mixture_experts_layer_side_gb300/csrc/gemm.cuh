@@ -23,11 +23,7 @@ constexpr int kBStage = 256 * 128;  // up to 256 rows x 128 bytes
 constexpr int kQueue = 4;           // depth of the work-item queue in smem
 constexpr int kGemmThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-9 gather
 constexpr int kMaxExperts = 1024;
-// Weight-gradient split K: an expert with more than kSplitK K stages (of 64
-// routed rows) is cut into ceil(stages / kSplitK) chunks, at most
-// kSplitSlots such experts per launch (later ones run unsplit).
-constexpr int kSplitK = 16;
-constexpr int kSplitSlots = 32;
+
 
 constexpr int kMaxMaps = 6;
 constexpr int kOutStage = 32 * 32 * 2;  // one epilogue warp's 32 x 32 bf16 output chunk
@@ -66,10 +62,6 @@ struct GemmParams {
   int g1_tiles;            // ring: GEMM1 N tiles per M tile
   int debug_flags;
   int nmaps;               // tensor maps in use (prefetched at start)
-  // weight-gradient split K: f32 accumulator tiles [kSplitSlots][tiles][128x256]
-  // and per-(tile, epilogue warp) chunk counters [kSplitSlots][tiles][4]
-  float* wacc;
-  uint32_t* wflags;
   int wg_sorted;           // weight gradients read token-sorted copies (plain TMA)
   // Ring launch: m_tiles holds the tile capacity; ring_flags[m] counts the
   // epilogue warps (4 per column tile) that published GEMM1 rows of tile m,

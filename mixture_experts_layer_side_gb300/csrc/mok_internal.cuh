@@ -40,9 +40,6 @@ struct WsLayout {
   size_t as;          // bf16 [pad_capacity, I]  s * a
   size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
   size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x, then dout (weight gradients)
-  size_t wacc;        // f32  weight-gradient split-K accumulators [slots][tiles][128 x 256]
-  size_t wflags;      // u32  their chunk counters [slots][tiles][4]
-  int64_t wg_tiles;   // output tiles per expert of the larger weight-gradient GEMM
   // MXFP8 activation copies
   size_t xq, xsf;     // x quantised along H: u8 [T, H], [T, H/32]
   size_t dq, dsf;     // dout quantised along H

@@ -17,9 +17,9 @@ CASES = [
     ("ragged_zipf", (300, 256, 256, 6, 3), "zipf", 2),
     ("hot_empty", (512, 384, 128, 24, 4), "hot", 3),
     ("wide", (200, 512, 384, 5, 2), "uniform", 4),
-    # experts above 1,024 routed rows: weight gradients split into K chunks
-    ("split_2chunk", (3000, 256, 128, 20, 2), "hot", 5),
-    ("split_3chunk", (4096, 256, 256, 20, 2), "hot", 6),
+    # experts above 1,024 routed rows: long weight-gradient K loops
+    ("long_k_a", (3000, 256, 128, 20, 2), "hot", 5),
+    ("long_k_b", (4096, 256, 256, 20, 2), "hot", 6),
 ]
 
 
