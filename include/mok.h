@@ -320,6 +320,24 @@ typedef struct {
 mok_status mok_build_schedule_noalloc(const mok_shape* shape, const int32_t* topk_idx,
                                       const mok_schedule_buffers* out, void* stream);
 
+/*
+ * The block-scaled (MXFP8) tensor-core GEMM the layer's MXFP8 mode is built
+ * on, on one dense problem (a diagnostic of the core: E4M3 operands, one
+ * E8M0 scale per 32 K-elements, f32 accumulation).
+ *   C (device) f32 [M, N] = dequant(A) * dequant(B)
+ *   A: a_mn_major = 0: Aq u8 [M, K] + Asf u8 [M, K/32] (quantised with
+ *      block_axis 1); a_mn_major = 1: Aq u8 [K, M] + Asf u8 [K/32, M]
+ *      (block_axis 0).  B likewise with N: [N, K] + [N, K/32], or
+ *      [K, N] + [K/32, N].
+ *   scratch (device, caller-owned) >= 256 + (a_mn_major ? M*K/32 : 0)
+ *      + (b_mn_major ? N*K/32 : 0) bytes (tile counter, error word, and
+ *      M/N-major scales re-tiled for the GEMM).
+ * M, N, K multiples of 128.
+ */
+mok_status mok_gemm_mxfp8(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, const uint8_t* Asf,
+                          int32_t a_mn_major, const uint8_t* Bq, const uint8_t* Bsf, int32_t b_mn_major, float* C,
+                          void* scratch, size_t scratch_bytes, void* stream);
+
 /* Synchronise `stream`, then return (and clear) the status recorded in the
  * workspace's error word; MOK_OK if none. */
 mok_status mok_check(void* ws, void* stream);

@@ -29,7 +29,7 @@ STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_build_schedule", "mok_forward",
            "mok_backward", "mok_mxfp8_quantize", "mok_gather_rows", "mok_gemm_bf16", "mok_check",
            "mok_device_sm_count", "mok_status_string", "mok_version", "mok_trace_enable", "mok_trace_read",
-           "mok_launch_count", "mok_build_schedule_noalloc"]
+           "mok_launch_count", "mok_build_schedule_noalloc", "mok_gemm_mxfp8"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
           "bwd_wg2", "quant", "bwd_sort"]
@@ -93,6 +93,7 @@ def _load():
         "mok_trace_read": (i32, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),
         "mok_launch_count": (ctypes.c_int64, []),
         "mok_build_schedule_noalloc": (i32, [S, P, ctypes.POINTER(MokScheduleBuffers), P]),
+        "mok_gemm_mxfp8": (i32, [i32, i32, i32, P, P, i32, P, P, i32, P, P, sz, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -198,6 +199,14 @@ def mok_gemm_bf16(A, a_mn_major, B, b_mn_major, C, scratch, stream=None):
     K = A.shape[0] if a_mn_major else A.shape[1]
     _ok(LIB.mok_gemm_bf16(M, N, K, _ptr(A), int(a_mn_major), _ptr(B), int(b_mn_major), _ptr(C), _ptr(scratch),
                           _stream(stream)), "mok_gemm_bf16")
+
+
+def mok_gemm_mxfp8(Aq, Asf, a_mn_major, Bq, Bsf, b_mn_major, C, scratch, stream=None):
+    M, N = C.shape
+    K = Aq.shape[0] if a_mn_major else Aq.shape[1]
+    _ok(LIB.mok_gemm_mxfp8(M, N, K, _ptr(Aq), _ptr(Asf), int(a_mn_major), _ptr(Bq), _ptr(Bsf), int(b_mn_major),
+                           _ptr(C), _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream)),
+        "mok_gemm_mxfp8")
 
 
 def mok_trace_enable(on=True):

@@ -114,10 +114,15 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
     L.ring_sf = take((size_t)L.ring_slots * M * (I / 32));
     L.xq = take((size_t)s.T * H);
     L.xsf = take((size_t)s.T * (H / 32));
-    L.dq = take((size_t)s.T * H);
-    L.dsf = take((size_t)s.T * (H / 32));
+    L.wsf1 = take((size_t)s.E * H * I / 32);
+    L.wsf3 = take((size_t)s.E * H * I / 32);
+    L.wsf2 = take((size_t)s.E * I * H / 32);
     L.dhuq = take(P * 2 * I);
     L.dhusf = take(P * (2 * I / 32));
+    L.wqa = take(P * H);
+    L.wsfa = take(P * H / 32);
+    L.wqb = take(P * 2 * I);
+    L.wsfb = take(P * 2 * I / 32);
   }
   L.total = off;
   return L;
@@ -192,9 +197,30 @@ mok_status check_config(const mok_config* c) {
 }
 
 mok_status check_prec(mok_precision p) {
-  if (p == MOK_BF16) return MOK_OK;
-  if (p == MOK_MXFP8) return MOK_ERR_UNSUPPORTED;
+  if (p == MOK_BF16 || p == MOK_MXFP8) return MOK_OK;
   return MOK_ERR_INVALID_ARG;
+}
+
+const mok_mx* as_mx(const void* p) { return static_cast<const mok_mx*>(p); }
+
+bool mx_ok(const void* p) { return p && as_mx(p)->q && as_mx(p)->scale; }
+
+const CUtensorMapDataType kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+
+// u8 [rows, cols] row-major, box {box_cols, box_rows}, 128-byte swizzle.
+bool map2d_u8(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t str[1] = {cols};
+  const uint32_t box[2] = {box_cols, box_rows};
+  return make_tmap(m, kU8, 2, p, dims, str, box, true);
+}
+
+// u8 [E, rows, cols], box {128, box_rows, 1}, 128-byte swizzle.
+bool map3d_u8(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows, uint64_t E, uint32_t box_rows) {
+  const uint64_t dims[3] = {cols, rows, E};
+  const uint64_t str[2] = {cols, cols * rows};
+  const uint32_t box[3] = {128, box_rows, 1};
+  return make_tmap(m, kU8, 3, p, dims, str, box, true);
 }
 
 #define MOK_TRY(expr)                       \
@@ -258,6 +284,138 @@ mok_status reset_counters(uint8_t* ws, const WsLayout& L, cudaStream_t st) {
   // the abort word and the tile counters (words [3, 48)); the error word,
   // the used-row count and the used-tile count are kept
   MOK_CUDA(cudaMemsetAsync(ws + L.header + kHdrAbort * 4, 0, (kHdrCounters + kNumCounters - kHdrAbort) * 4, st));
+  return MOK_OK;
+}
+
+
+// MXFP8 backward: every GEMM block-scaled along its own K.  Weights come in
+// the orientation the backward contracts over (W1, W3 along I; W2 along H);
+// dout is quantised along H, dh|du along I (in the dA' epilogue), and the
+// weight-gradient operands along the expert's routed rows.
+mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const void* ctx, const void* x,
+                       const float* scores, const mok_mx& q1, const mok_mx& q3, const mok_mx& q2, const void* dout,
+                       void* dX, void* dW1, void* dW3, void* dW2, float* dscores, cudaStream_t st) {
+  const uint64_t P = L.pad_capacity;
+  const int bn_i = (s.I % 256 == 0) ? 256 : 128;
+  const int bn_h = (s.H % 256 == 0) ? 256 : 128;
+  const int32_t* rows_used = reinterpret_cast<const int32_t*>(w + L.header) + kHdrPaddedRows;
+  GemmParams g;
+  base_params(g, s, L, w);
+  g.ctx_hu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(ctx));
+  g.dhu = reinterpret_cast<__nv_bfloat16*>(w + L.dhu);
+  g.as = reinterpret_cast<__nv_bfloat16*>(w + L.as);
+  g.dsp = reinterpret_cast<float*>(w + L.dsp);
+  g.scores = scores;
+  g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
+  {
+    Phase ph(MOK_PHASE_QUANT, st, 1);
+    MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(dout), 1, s.T, s.H, 1, w + L.xq, w + L.xsf, st));
+  }
+  // dA' = gather(dout) W2^T (E4M3), SwiGLU backward, router partials, dh|du quantised along I
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map3d_u8(&m.m[1], q2.q, s.H, s.I, s.E, bn_i)) return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 2;
+    q.bn = bn_i;
+    q.n_tiles = s.I / bn_i;
+    q.m_tiles = 0;
+    q.m_tile_begin = 0;
+    q.m_tile_end = (int)L.tile_capacity;
+    q.counter = 0;
+    q.gq_src = w + L.xq;
+    q.sfa_rows = w + L.xsf;
+    q.sfa_ld = s.H / 32;
+    q.sfb_rows0 = q2.scale;
+    q.sfb_ld = s.H / 32;
+    q.dhu_q = w + L.dhuq;
+    q.dhu_sf = w + L.dhusf;
+    {
+      Phase ph(MOK_PHASE_BWD_DA, st, 1);
+      MOK_CUDA(launch_gemm_mx(GM_BWD_DA, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    }
+    Phase ph(MOK_PHASE_BWD_DS, st, 1);
+    MOK_CUDA(launch_ds_reduce(s, L, w, dscores, q.n_tiles, st));
+  }
+  // dX parts = [dh|du] [W1|W3]^T (E4M3 along I), scattered, then summed over k
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map2d_u8(&m.m[0], w + L.dhuq, 2 * (uint64_t)s.I, P, 128, 128) ||
+        !map3d_u8(&m.m[1], q1.q, s.I, s.H, s.E, bn_h) || !map3d_u8(&m.m[2], q3.q, s.I, s.H, s.E, bn_h))
+      return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 3;
+    q.bn = bn_h;
+    q.n_tiles = s.H / bn_h;
+    q.m_tile_begin = 0;
+    q.m_tile_end = (int)L.tile_capacity;
+    q.counter = 1;
+    q.sfa_rows = w + L.dhusf;
+    q.sfa_ld = 2 * s.I / 32;
+    q.sfb_rows0 = q1.scale;
+    q.sfb_rows1 = q3.scale;
+    q.sfb_ld = s.I / 32;
+    {
+      Phase ph(MOK_PHASE_BWD_DX, st, 1);
+      MOK_CUDA(launch_gemm_mx(GM_BWD_DX, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    }
+    Phase ph(MOK_PHASE_BWD_DX_COMBINE, st, 1);
+    MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));
+  }
+  __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
+  // dW1 | dW3: token-sorted x and dh|du, both quantised along the routed rows
+  {
+    {
+      Phase ph(MOK_PHASE_BWD_SORT, st, 3);
+      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
+      MOK_CUDA(launch_quant_rows_tiled(srt, rows_used, P, s.H, w + L.wqa, w + L.wsfa, st));
+      MOK_CUDA(launch_quant_rows_tiled(g.dhu, rows_used, P, 2 * s.I, w + L.wqb, w + L.wsfb, st));
+    }
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map2d_u8(&m.m[0], w + L.wqa, s.H, P, 128, 128) || !map2d_u8(&m.m[1], w + L.wqb, 2 * (uint64_t)s.I, P, 128, 128))
+      return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 2;
+    q.bn = 256;
+    q.n_tiles = 2 * s.I / 256;
+    q.m_tiles = s.H / 128;
+    q.counter = 2;
+    q.wg_sorted = 1;
+    q.sfa_tiled = w + L.wsfa;
+    q.sfb_tiled0 = w + L.wsfb;
+    q.dw0 = static_cast<__nv_bfloat16*>(dW1);
+    q.dw1 = static_cast<__nv_bfloat16*>(dW3);
+    Phase ph(MOK_PHASE_BWD_WG13, st, 1);
+    MOK_CUDA(launch_gemm_mx(GM_WG13, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
+  }
+  // dW2: s*a and token-sorted dout, both quantised along the routed rows
+  {
+    {
+      Phase ph(MOK_PHASE_BWD_SORT, st, 3);
+      MOK_CUDA(launch_quant_rows_tiled(g.as, rows_used, P, s.I, w + L.wqb, w + L.wsfb, st));
+      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(dout), srt, st));
+      MOK_CUDA(launch_quant_rows_tiled(srt, rows_used, P, s.H, w + L.wqa, w + L.wsfa, st));
+    }
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map2d_u8(&m.m[0], w + L.wqb, s.I, P, 128, 128) || !map2d_u8(&m.m[1], w + L.wqa, s.H, P, 128, 128))
+      return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 2;
+    q.bn = bn_h;
+    q.n_tiles = s.H / bn_h;
+    q.m_tiles = s.I / 128;
+    q.counter = 3;
+    q.wg_sorted = 1;
+    q.sfa_tiled = w + L.wsfb;
+    q.sfb_tiled0 = w + L.wsfa;
+    q.dw0 = static_cast<__nv_bfloat16*>(dW2);
+    Phase ph(MOK_PHASE_BWD_WG2, st, 1);
+    MOK_CUDA(launch_gemm_mx(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
+  }
   return MOK_OK;
 }
 
@@ -337,6 +495,53 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
 
   const int M = L.minibatch_rows, S = L.ring_slots;
   const int bn2 = (s.H % 256 == 0) ? 256 : 128;
+  if (prec == MOK_MXFP8) {
+    if (!mx_ok(W1) || !mx_ok(W3) || !mx_ok(W2)) return MOK_ERR_INVALID_ARG;
+    const mok_mx &q1 = *as_mx(W1), &q3 = *as_mx(W3), &q2 = *as_mx(W2);
+    {
+      // x along H; forward weight scales tiled for the N-major B operands
+      Phase ph(MOK_PHASE_QUANT, st, 4);
+      MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(x), 1, s.T, s.H, 1, w + L.xq, w + L.xsf, st));
+      MOK_CUDA(launch_tile_scales(q1.scale, s.E, s.H / 32, s.I, w + L.wsf1, st));
+      MOK_CUDA(launch_tile_scales(q3.scale, s.E, s.H / 32, s.I, w + L.wsf3, st));
+      MOK_CUDA(launch_tile_scales(q2.scale, s.E, s.I / 32, s.H, w + L.wsf2, st));
+    }
+    GemmParams g;
+    base_params(g, s, L, w);
+    g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
+    g.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);  // E4M3 codes in MXFP8 mode
+    g.ring_sf = w + L.ring_sf;
+    g.ring_rows = M;
+    g.ring_slots = S;
+    g.ring_flags = reinterpret_cast<uint32_t*>(w + L.ring_flags);
+    g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
+    g.debug_flags = cfg->debug_flags;
+    g.gq_src = w + L.xq;
+    g.sfa_rows = w + L.xsf;
+    g.sfa_ld = s.H / 32;
+    g.sfb_tiled0 = w + L.wsf1;
+    g.sfb_tiled1 = w + L.wsf3;
+    g.sfb_tiled2 = w + L.wsf2;
+    TmapSet maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!map3d_u8(&maps.m[1], q1.q, s.I, s.H, s.E, 128) || !map3d_u8(&maps.m[2], q3.q, s.I, s.H, s.E, 128) ||
+        !map2d_u8(&maps.m[3], w + L.ring, s.I, (uint64_t)S * M, 128, 128) ||
+        !map3d_u8(&maps.m[4], q2.q, s.H, s.I, s.E, 128))
+      return MOK_ERR_CUDA;
+    g.nmaps = 5;
+    g.bn = bn2;
+    g.n_tiles = s.H / bn2;
+    g.g1_tiles = s.I / 128;
+    g.m_tiles = (int)L.tile_capacity;
+    g.counter = 0;
+    {
+      Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
+      MOK_CUDA(launch_gemm_mx(GM_FWD_RING, maps, g, gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles)), st));
+    }
+    Phase ph(MOK_PHASE_FWD_COMBINE, st, 1);
+    MOK_CUDA(launch_combine(s, L, w, g.yk, scores, static_cast<__nv_bfloat16*>(out), st));
+    return MOK_OK;
+  }
   GemmParams g;
   base_params(g, s, L, w);
   g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
@@ -421,6 +626,11 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   const int bn_i = (s.I % 256 == 0) ? 256 : 128;
   const int bn_h = (s.H % 256 == 0) ? 256 : 128;
 
+  if (prec == MOK_MXFP8) {
+    if (!mx_ok(W1) || !mx_ok(W3) || !mx_ok(W2)) return MOK_ERR_INVALID_ARG;
+    return backward_mx(s, L, w, ctx, x, scores, *as_mx(W1), *as_mx(W3), *as_mx(W2), dout, dX, dW1, dW3, dW2,
+                       dscores, st);
+  }
   GemmParams g;
   base_params(g, s, L, w);
   g.ctx_hu = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(ctx));
@@ -611,6 +821,56 @@ mok_status mok_trace_read(float* ms, int32_t* count) {
 }
 
 int64_t mok_launch_count(void) { return g_launches.load(); }
+
+mok_status mok_gemm_mxfp8(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, const uint8_t* Asf,
+                          int32_t a_mn_major, const uint8_t* Bq, const uint8_t* Bsf, int32_t b_mn_major, float* C,
+                          void* scratch, size_t scratch_bytes, void* stream) {
+  if (!Aq || !Asf || !Bq || !Bsf || !C || !scratch) return MOK_ERR_INVALID_ARG;
+  if (M < 128 || N < 128 || K < 128 || M % 128 || N % 128 || K % 128) return MOK_ERR_UNSUPPORTED;
+  const size_t need = 256 + (a_mn_major ? (size_t)M * K / 32 : 0) + (b_mn_major ? (size_t)N * K / 32 : 0);
+  if (scratch_bytes < need) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const int bn = (N % 256 == 0) ? 256 : 128;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  uint8_t* sfa_t = sc + 256;
+  uint8_t* sfb_t = sfa_t + (a_mn_major ? (size_t)M * K / 32 : 0);
+  MOK_CUDA(cudaMemsetAsync(sc, 0, kHeaderWords * 4, st));
+  int kernels = 1;
+  if (a_mn_major) {
+    MOK_CUDA(launch_tile_scales(Asf, 1, K / 32, M, sfa_t, st));
+    ++kernels;
+  }
+  if (b_mn_major) {
+    MOK_CUDA(launch_tile_scales(Bsf, 1, K / 32, N, sfb_t, st));
+    ++kernels;
+  }
+  TmapSet m;
+  memset(&m, 0, sizeof(m));
+  bool ok = a_mn_major ? map2d_u8(&m.m[0], Aq, M, K, 128, 128) : map2d_u8(&m.m[0], Aq, K, M, 128, 128);
+  ok = ok && (b_mn_major ? map2d_u8(&m.m[1], Bq, N, K, 128, 128) : map2d_u8(&m.m[1], Bq, K, N, 128, bn));
+  if (!ok) return MOK_ERR_CUDA;
+  GemmParams g;
+  memset(&g, 0, sizeof(g));
+  g.nmaps = 2;
+  g.bn = bn;
+  g.n_tiles = N / bn;
+  g.m_tiles = M / 128;
+  g.k_iters = K / 128;
+  g.hdr = reinterpret_cast<int32_t*>(sc);
+  g.out_f32 = C;
+  g.ld_out = N;
+  g.a_mn = a_mn_major ? 1 : 0;
+  g.b_mn = b_mn_major ? 1 : 0;
+  g.sfa_rows = Asf;
+  g.sfa_ld = K / 32;
+  g.sfb_rows0 = Bsf;
+  g.sfb_ld = K / 32;
+  g.sfa_tiled = sfa_t;
+  g.sfb_tiled0 = sfb_t;
+  g_launches += kernels;
+  MOK_CUDA(launch_gemm_mx(GM_DENSE, m, g, gemm_grid((long)g.m_tiles * g.n_tiles), st));
+  return MOK_OK;
+}
 
 mok_status mok_check(void* ws, void* stream) {
   if (!ws) return MOK_ERR_INVALID_ARG;

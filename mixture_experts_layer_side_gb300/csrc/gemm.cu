@@ -31,6 +31,7 @@
 // the ring token buffer consumed per minibatch (ring-token-buffer paragraph);
 // router gradient fused into the SwiGLU backward (paragraph after the list).
 #include "gemm.cuh"
+#include "mx.cuh"
 #include "tc.cuh"
 
 namespace mok {
@@ -115,8 +116,9 @@ __device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& 
   return emit(GM_FWD2, nb - 1, w, g2);
 }
 
-template <int MODE>
+template <int MODE, bool MX = false>
 __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
+  constexpr int kEl = MX ? 128 : 64;  // K elements per stage (128 bytes)
   const int* po = ctl->po;
   Item it;
   if constexpr (MODE == GM_DENSE) {
@@ -134,7 +136,7 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.m = r / p.n_tiles;
     it.n = r % p.n_tiles;
     it.row0 = po[it.e];
-    it.k_iters = (po[it.e + 1] - po[it.e]) / 64;
+    it.k_iters = (po[it.e + 1] - po[it.e]) / kEl;
   } else {
     int type = MODE, m, n;
     if constexpr (MODE == GM_FWD_RING) {
@@ -148,9 +150,9 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.n = n;
     it.e = p.tile_expert[m];
     it.row0 = m * kTileRows;
-    it.k_iters = (type == GM_FWD1 || type == GM_BWD_DA) ? p.H / 64
-                 : (type == GM_FWD2)                   ? p.I / 64
-                                                       : 2 * p.I / 64;  // GM_BWD_DX
+    it.k_iters = (type == GM_FWD1 || type == GM_BWD_DA) ? p.H / kEl
+                 : (type == GM_FWD2)                   ? p.I / kEl
+                                                       : 2 * p.I / kEl;  // GM_BWD_DX
   }
   return it;
 }
@@ -295,6 +297,145 @@ __device__ __forceinline__ void mn_tokens(const GemmParams& p, const Item& it, i
   for (int j = 0; j < kPasses; ++j) tok[j] = token_or_neg(p, it.row0 + kk * 64 + gt / CPR + kRowsPerPass * j);
 }
 
+// ---------------------------------------------------------------- MXFP8 producers
+// Stage layout in MXFP8 mode: A and B codes fill the same 128-byte rows as
+// bf16 (128 K-elements per stage); an M/N-major operand is one 16 KB
+// 128-column chunk per 128 M/N (128 K-rows x 128 bytes).  Scales of a stage:
+// sfa 512 bytes (128 A rows x 4 K-blocks), sfb 512 bytes per 128 B columns,
+// in the tcgen05.cp .32x128b.warpx4 block layout.
+
+// Bytes the TMA producer brings into one MXFP8 stage.
+template <int MODE>
+__device__ __forceinline__ uint32_t mx_stage_bytes(const GemmParams& p, int type, int bn) {
+  const uint32_t bchunks = (uint32_t)bn / 128;
+  switch (MODE == GM_DENSE ? GM_DENSE : type) {
+    case GM_DENSE: return kAStage + bn * 128 + (p.a_mn ? 512u : 0u) + (p.b_mn ? 512u * bchunks : 0u);
+    case GM_FWD1: return 2u * 16384u + 1024u;
+    case GM_FWD2: return kAStage + bn * 128 + 512u * bchunks;
+    case GM_BWD_DA: return bn * 128;
+    case GM_BWD_DX: return kAStage + bn * 128;
+    case GM_WG13: return kAStage + 2u * 16384u + 512u + 1024u;
+    default: return kAStage + bn * 128 + 512u + 512u * bchunks;  // GM_WG2
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams& p, const Item& it, int kk, uint8_t* a,
+                                             uint8_t* b, uint8_t* sfa, uint8_t* sfb, uint64_t* bar) {
+  const int type = it.type;
+  const int bn = item_bn(p, type);
+  if (MODE == GM_DENSE) {
+    const int kgroups = p.k_iters;
+    if (p.a_mn) {
+      tma_load_2d(a, &mp.m[0], bar, it.m * 128, kk * 128);
+      bulk_load(sfa, p.sfa_tiled + ((long)it.m * kgroups + kk) * 512, 512, bar);
+    } else {
+      tma_load_2d(a, &mp.m[0], bar, kk * 128, it.m * 128);
+    }
+    if (p.b_mn) {
+      for (int c = 0; c < bn / 128; ++c) {
+        tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, kk * 128);
+        bulk_load(sfb + c * 512, p.sfb_tiled0 + ((long)(it.n * (bn / 128) + c) * kgroups + kk) * 512, 512, bar);
+      }
+    } else {
+      tma_load_2d(b, &mp.m[1], bar, kk * 128, it.n * bn);
+    }
+  } else if (type == GM_FWD1) {
+    const int hg = p.H / 128;
+    tma_load_3d(b, &mp.m[1], bar, it.n * 128, kk * 128, it.e);
+    tma_load_3d(b + 16384, &mp.m[2], bar, it.n * 128, kk * 128, it.e);
+    const long blk = ((long)it.e * (p.I / 128) + it.n) * hg + kk;
+    bulk_load(sfb, p.sfb_tiled0 + blk * 512, 512, bar);
+    bulk_load(sfb + 512, p.sfb_tiled1 + blk * 512, 512, bar);
+  } else if (type == GM_FWD2) {
+    const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
+    const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
+    tma_load_2d(a, &mp.m[mslot], bar, kk * 128, ring_row(p, it.row0));
+    for (int c = 0; c < bn / 128; ++c) {
+      tma_load_3d(b + c * 16384, &mp.m[wmap], bar, it.n * bn + c * 128, kk * 128, it.e);
+      const long blk = ((long)it.e * (p.H / 128) + it.n * (bn / 128) + c) * (p.I / 128) + kk;
+      bulk_load(sfb + c * 512, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * 512, 512, bar);
+    }
+  } else if (type == GM_BWD_DA) {
+    tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
+  } else if (type == GM_BWD_DX) {
+    tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
+    const int ki = p.I / 128;
+    if (kk < ki)
+      tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
+    else
+      tma_load_3d(b, &mp.m[2], bar, (kk - ki) * 128, it.n * bn, it.e);
+  } else if (type == GM_WG13 || type == GM_WG2) {
+    // token-sorted operands quantised along the routed rows (K), M/N-major
+    const int cols_a = (type == GM_WG13) ? p.H : p.I;
+    const int cols_b = (type == GM_WG13) ? 2 * p.I : p.H;
+    const int rb = it.row0 / 128 + kk;
+    tma_load_2d(a, &mp.m[0], bar, it.m * 128, it.row0 + kk * 128);
+    bulk_load(sfa, p.sfa_tiled + ((long)rb * (cols_a / 128) + it.m) * 512, 512, bar);
+    for (int c = 0; c < bn / 128; ++c) {
+      tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, it.row0 + kk * 128);
+      bulk_load(sfb + c * 512, p.sfb_tiled0 + ((long)rb * (cols_b / 128) + it.n * (bn / 128) + c) * 512, 512, bar);
+    }
+  }
+}
+
+// Gather threads, one MXFP8 stage: gathered E4M3 rows of A (GEMM1, dA') and
+// the scales of K-major operands, four bytes per row (zero for padding
+// rows), all completing on the stage barrier.
+template <int MODE>
+__device__ __forceinline__ void gather_stage_mx(const GemmParams& p, const Item& it, int kk, uint8_t* a, uint8_t* sfa,
+                                                uint8_t* sfb, int gt, const int (&tok)[8], int tok_row,
+                                                uint64_t* full) {
+  const int type = it.type;
+  const int bn = item_bn(p, type);
+  const bool gather_a = (MODE != GM_DENSE) && (type == GM_FWD1 || type == GM_BWD_DA);
+  if (gather_a) {
+    const int ch = gt & 7;
+    const int sw = (ch ^ ((gt >> 3) & 7)) << 4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int row = (gt >> 3) + 16 * j;
+      const int t = tok[j];
+      cp_async_16(smem_u32(a + row * 128 + sw), p.gq_src + (long)max(t, 0) * p.H + kk * 128 + ch * 16,
+                  t >= 0 ? 16u : 0u);
+    }
+  }
+  // scales of A, row gt of the tile
+  const uint8_t* sa = nullptr;
+  if (MODE == GM_DENSE) {
+    if (!p.a_mn) sa = p.sfa_rows + ((long)it.m * 128 + gt) * p.sfa_ld + kk * 4;
+  } else if (gather_a) {
+    sa = p.sfa_rows + (long)max(tok_row, 0) * p.sfa_ld + kk * 4;
+  } else if (type == GM_FWD2) {
+    // scales of a, written by the GEMM1 epilogue next to the ring codes
+    sa = p.ring_sf + (long)ring_row(p, it.row0 + gt) * (p.I / 32) + kk * 4;
+  } else if (type == GM_BWD_DX) {
+    sa = p.sfa_rows + ((long)it.row0 + gt) * p.sfa_ld + kk * 4;
+  }
+  if (sa) cp_async_4(smem_u32(sfa + mx_sf_offset(gt, 0)), sa, (gather_a && tok_row < 0) ? 0u : 4u);
+  // scales of K-major B, rows gt and gt + 128 of the N tile
+  const uint8_t* sb = nullptr;
+  long brow0 = 0;
+  int kb = kk;
+  if (MODE == GM_DENSE) {
+    if (!p.b_mn) { sb = p.sfb_rows0; brow0 = (long)it.n * bn; }
+  } else if (type == GM_BWD_DA) {
+    sb = p.sfb_rows0;
+    brow0 = (long)it.e * p.I + (long)it.n * bn;
+  } else if (type == GM_BWD_DX) {
+    const int ki = p.I / 128;
+    sb = kk < ki ? p.sfb_rows0 : p.sfb_rows1;
+    kb = kk < ki ? kk : kk - ki;
+    brow0 = (long)it.e * p.H + (long)it.n * bn;
+  }
+  if (sb) {
+    for (int nl = gt; nl < bn; nl += 128)
+      cp_async_4(smem_u32(sfb + (nl >> 7) * 512 + mx_sf_offset(nl & 127, 0)), sb + (brow0 + nl) * p.sfb_ld + kb * 4,
+                 4u);
+  }
+  cp_async_arrive_noinc(full);
+}
+
 template <int MODE>
 __device__ __forceinline__ bool a_mn_major(const GemmParams& p, int type) {
   if (MODE == GM_DENSE) return p.a_mn != 0;
@@ -361,6 +502,42 @@ __device__ void epi_fwd1(const GemmParams& p, const Item& it, uint32_t tbase, in
   }
 }
 
+// MXFP8 GEMM1 epilogue: as epi_fwd1, but a goes to the ring as E4M3 codes
+// with one scale per 32 intermediate columns (the K blocks of GEMM2).
+__device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
+  const long prow = (long)it.row0 + row;
+  const int i0 = it.n * 128;
+  __nv_bfloat16* hrow = p.ctx_hu + prow * 2 * p.I + i0;
+  __nv_bfloat16* urow = hrow + p.I;
+  const long rr = ring_row(p, (int)prow);
+  uint8_t* qrow = reinterpret_cast<uint8_t*>(p.ring) + rr * p.I + i0;
+  uint8_t* srow = p.ring_sf + rr * (p.I / 32) + i0 / 32;
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    float h[32], u[32];
+    tmem_ld32(tbase + c, h);
+    tmem_ld32(tbase + 128 + c, u);
+    uint32_t hw[16], uw[16];
+    float a[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float h0 = bf16_round(h[2 * i]), h1 = bf16_round(h[2 * i + 1]);
+      const float u0 = bf16_round(u[2 * i]), u1 = bf16_round(u[2 * i + 1]);
+      hw[i] = pack_bf16x2(h0, h1);
+      uw[i] = pack_bf16x2(u0, u1);
+      a[2 * i] = h0 * sigmoidf_(h0) * u0;
+      a[2 * i + 1] = h1 * sigmoidf_(h1) * u1;
+    }
+    store32_bf16(hrow + c, hw);
+    store32_bf16(urow + c, uw);
+    uint32_t q[8];
+    srow[c / 32] = mx_quant32(a, q);
+    uint4* d = reinterpret_cast<uint4*>(qrow + c);
+    d[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    d[1] = make_uint4(q[4], q[5], q[6], q[7]);
+  }
+}
+
 // Scatter a tile row to token order: row f of dst (skipped for padding rows;
 // every lane still takes part in the warp-collective TMEM loads).
 __device__ void epi_scatter(const GemmParams& p, const Item& it, uint32_t tbase, int row, int bn) {
@@ -383,6 +560,7 @@ __device__ void epi_scatter(const GemmParams& p, const Item& it, uint32_t tbase,
 //   ds partial = sum_i dA'_i a_i          (router-score gradient)
 //   dA = s dA',  dh = dA u sig(h) (1 + h (1 - sig(h))),  du = dA silu(h)
 //   A_s = s a  (the left operand of dW2)
+template <bool MX>
 __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
   const long prow = (long)it.row0 + row;
   const int f = p.pad_perm[prow];
@@ -423,6 +601,27 @@ __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, 
     store32_bf16(dhrow + c, dhw);
     store32_bf16(durow + c, duw);
     store32_bf16(asrow + c, asw);
+    if constexpr (MX) {
+      // dh|du quantised along I for the dX GEMM (32 columns per scale)
+      const int col = it.n * bn + c;
+      float v[32];
+      uint32_t q[8];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t(&src)[16] = half == 0 ? dhw : duw;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&src[i]));
+          v[2 * i] = f.x;
+          v[2 * i + 1] = f.y;
+        }
+        const long qc = (long)half * p.I + col;
+        p.dhu_sf[prow * (2 * p.I / 32) + qc / 32] = mx_quant32(v, q);
+        uint4* d = reinterpret_cast<uint4*>(p.dhu_q + prow * 2 * p.I + qc);
+        d[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        d[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      }
+    }
   }
   p.dsp[prow * p.n_tiles + it.n] = dsum;
 }
@@ -576,7 +775,7 @@ __device__ bool gather_item_k(const GemmParams& p, const Item& it, uint8_t* sA, 
 }
 
 // ------------------------------------------------------------------ kernel
-template <int MODE>
+template <int MODE, bool MX>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ TmapSet maps,
                                                                 const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -586,9 +785,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   Ctl* ctl = reinterpret_cast<Ctl*>(sB + kStages * kBStage);
   // per epilogue warp, one 2 KB output staging buffer (128-byte aligned)
   uint8_t* sOut = sB + kStages * kBStage + ((sizeof(Ctl) + 127) / 128) * 128;
+  // MXFP8: per stage, the scale blocks of A (512 B) and B (1024 B)
+  uint8_t* sSF = sOut + 4 * kOutStage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WaitCtx wc{&ctl->abort, &p.hdr[kHdrAbort], &p.hdr[kHdrError]};
-  constexpr bool kGather = mode_gathers<MODE>();
+  // MXFP8 launches always use the gather threads (scales of K-major operands)
+  constexpr bool kGather = mode_gathers<MODE>() || MX;
+  // MXFP8 keeps one accumulator (TMEM columns 256.. hold the stage scales)
+  constexpr uint32_t kAccBufs = MX ? 1u : 2u;
   constexpr bool kWgrad = (MODE == GM_WG13 || MODE == GM_WG2);
   // consumers of the item queue: MMA warp, 4 epilogue warps, 4 gather warps
   constexpr uint32_t kQueueConsumers = kGather ? 9u : 5u;
@@ -662,7 +866,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         } else {
           w_next = (int)atomicAdd(counter, 1u);
         }
-        const Item it = decode<MODE>(p, ctl, w);
+        const Item it = decode<MODE, MX>(p, ctl, w);
         if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
           // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
           // of its GEMM1 column tiles are published, then order the
@@ -671,11 +875,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           fence_proxy_async_global();
           if (!ok) break;
         }
-        const uint32_t bytes = tma_stage_bytes(p, it.type, item_bn(p, it.type));
+        const uint32_t bytes = MX ? mx_stage_bytes<MODE>(p, it.type, item_bn(p, it.type))
+                                  : tma_stage_bytes(p, it.type, item_bn(p, it.type));
         for (int kk = 0; kk < it.k_iters; ++kk) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(&ctl->full[stage], bytes);
-          tma_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, &ctl->full[stage]);
+          if constexpr (MX)
+            tma_loads_mx<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, sSF + stage * kSfStage,
+                               sSF + stage * kSfStage + 512, &ctl->full[stage]);
+          else
+            tma_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, &ctl->full[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         w = w_next;
@@ -693,9 +902,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
         if (++qs == kQueue) { qs = 0; qp ^= 1; }
         if (w < 0) break;
-        const Item it = decode<MODE>(p, ctl, w);
-        bool ok;
-        if (gathered_operand(p, it.type) == 0)
+        const Item it = decode<MODE, MX>(p, ctl, w);
+        bool ok = true;
+        if constexpr (MX) {
+          int tok[8];
+          int tok_row = -1;
+          const bool ga = (MODE != GM_DENSE) && (it.type == GM_FWD1 || it.type == GM_BWD_DA);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) tok[j] = ga ? token_or_neg(p, it.row0 + (gt >> 3) + 16 * j) : -1;
+          if (ga) tok_row = token_or_neg(p, it.row0 + gt);
+          if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
+            // this thread reads scales of a that GEMM1 (another CTA) wrote
+            // next to the ring rows: acquire the same completion count the
+            // TMA producer waits for
+            if (!wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc)) break;
+          }
+          const bool copies = (MODE == GM_DENSE) || !(it.type == GM_WG13 || it.type == GM_WG2);
+          for (int kk = 0; kk < it.k_iters; ++kk) {
+            if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
+            if (copies)
+              gather_stage_mx<MODE>(p, it, kk, sA + stage * kAStage, sSF + stage * kSfStage,
+                                    sSF + stage * kSfStage + 512, gt, tok, tok_row, &ctl->full[stage]);
+            else
+              mbar_arrive(&ctl->full[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+        } else if (gathered_operand(p, it.type) == 0)
           ok = gather_item_k(p, it, sA, ctl, stage, phase, gt, wc);
         else if (it.type == GM_WG13)
           ok = gather_item_mn<16>(p, it, sA, kAStage, it.m * 128, ctl, stage, phase, gt, wc);
@@ -720,8 +952,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE>(p, ctl, w);
-      const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
+      const Item it = decode<MODE, MX>(p, ctl, w);
+      const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)) break;
       tc_fence_after();
       const int bn = item_bn(p, it.type);
@@ -736,13 +968,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) {
           // the gather threads wrote part of this stage with cp.async: order
           // those writes before the tensor core's (async-proxy) reads
-          if (gathered) fence_proxy_async_shared();
+          if (gathered || MX) fence_proxy_async_shared();
           const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBStage);
+          if constexpr (MX) {
+            // stage scales into TMEM (columns 256 + 16 * stage): A at +0
+            // (4 columns), B at +4 (4 columns per 128 N)
+            const uint32_t sf_t = tmem + 256 + stage * 16;
+            const uint32_t sfa_s = smem_u32(sSF + stage * kSfStage);
+            tmem_cp_32x128b_warpx4(sf_t, sdesc_plain(sfa_s, 16, 128));
+            for (int c = 0; c < bn / 128; ++c)
+              tmem_cp_32x128b_warpx4(sf_t + 4 + 4 * c, sdesc_plain(sfa_s + 512 + c * 512, 16, 128));
 #pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16) {
-            const uint64_t ad = amn ? sdesc_sw128(a0 + k16 * 2048, 8192, 1024) : sdesc_sw128(a0 + k16 * 32, 16, 1024);
-            const uint64_t bd = bmn ? sdesc_sw128(b0 + k16 * 2048, 8192, 1024) : sdesc_sw128(b0 + k16 * 32, 16, 1024);
-            mma_bf16(d, ad, bd, idesc, (kk | k16) != 0 ? 1u : 0u);
+            for (int k32 = 0; k32 < 4; ++k32) {
+              const uint64_t ad = amn ? sdesc_sw128(a0 + k32 * 4096, 16384, 1024) : sdesc_sw128(a0 + k32 * 32, 16, 1024);
+              const uint64_t bd = bmn ? sdesc_sw128(b0 + k32 * 4096, 16384, 1024) : sdesc_sw128(b0 + k32 * 32, 16, 1024);
+              mma_mxf8(d, ad, bd, idesc_mxf8(128, bn, amn ? 1 : 0, bmn ? 1 : 0, k32, k32), sf_t, sf_t + 4,
+                       (kk | k32) != 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16) {
+              const uint64_t ad = amn ? sdesc_sw128(a0 + k16 * 2048, 8192, 1024) : sdesc_sw128(a0 + k16 * 32, 16, 1024);
+              const uint64_t bd = bmn ? sdesc_sw128(b0 + k16 * 2048, 8192, 1024) : sdesc_sw128(b0 + k16 * 32, 16, 1024);
+              mma_bf16(d, ad, bd, idesc, (kk | k16) != 0 ? 1u : 0u);
+            }
           }
           mma_commit(&ctl->empty[stage]);
         }
@@ -767,8 +1016,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE>(p, ctl, w);
-      const uint32_t buf = tcount & 1, tph = (tcount >> 1) & 1;
+      const Item it = decode<MODE, MX>(p, ctl, w);
+      const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * 256;
@@ -791,9 +1040,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (!ok) break;
       switch (it.type) {
         case GM_DENSE: epi_dense(p, it, tbase, row); break;
-        case GM_FWD1: epi_fwd1(p, it, tbase, row); break;
+        case GM_FWD1:
+          if constexpr (MX) epi_fwd1_mx(p, it, tbase, row); else epi_fwd1(p, it, tbase, row);
+          break;
         case GM_FWD2: epi_scatter(p, it, tbase, row, p.bn); break;
-        case GM_BWD_DA: epi_bwd_da(p, it, tbase, row); break;
+        case GM_BWD_DA: epi_bwd_da<MX>(p, it, tbase, row); break;
         case GM_BWD_DX: epi_scatter(p, it, tbase, row, p.bn); break;
         default: epi_wgrad(p, it, tbase, q, lane, stage_out); break;
       }
@@ -822,35 +1073,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int MODE>
+template <int MODE, bool MX>
 cudaError_t launch_mode(const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
   const size_t smem = gemm_smem_bytes();
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(gemm_kernel<MODE, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured_device = dev;
   }
-  gemm_kernel<MODE><<<grid, kGemmThreads, smem, st>>>(maps, p);
+  gemm_kernel<MODE, MX><<<grid, kGemmThreads, smem, st>>>(maps, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes() {
-  return 1024 + kStages * (kAStage + kBStage) + ((sizeof(Ctl) + 127) / 128) * 128 + 4 * kOutStage;
+  return 1024 + kStages * (kAStage + kBStage) + ((sizeof(Ctl) + 127) / 128) * 128 + 4 * kOutStage +
+         kStages * kSfStage;
 }
 
 cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
   switch (mode) {
-    case GM_DENSE: return launch_mode<GM_DENSE>(maps, p, grid, st);
-    case GM_FWD1: return launch_mode<GM_FWD1>(maps, p, grid, st);
-    case GM_FWD2: return launch_mode<GM_FWD2>(maps, p, grid, st);
-    case GM_BWD_DA: return launch_mode<GM_BWD_DA>(maps, p, grid, st);
-    case GM_BWD_DX: return launch_mode<GM_BWD_DX>(maps, p, grid, st);
-    case GM_WG13: return launch_mode<GM_WG13>(maps, p, grid, st);
-    case GM_WG2: return launch_mode<GM_WG2>(maps, p, grid, st);
-    case GM_FWD_RING: return launch_mode<GM_FWD_RING>(maps, p, grid, st);
+    case GM_DENSE: return launch_mode<GM_DENSE, false>(maps, p, grid, st);
+    case GM_FWD1: return launch_mode<GM_FWD1, false>(maps, p, grid, st);
+    case GM_FWD2: return launch_mode<GM_FWD2, false>(maps, p, grid, st);
+    case GM_BWD_DA: return launch_mode<GM_BWD_DA, false>(maps, p, grid, st);
+    case GM_BWD_DX: return launch_mode<GM_BWD_DX, false>(maps, p, grid, st);
+    case GM_WG13: return launch_mode<GM_WG13, false>(maps, p, grid, st);
+    case GM_WG2: return launch_mode<GM_WG2, false>(maps, p, grid, st);
+    case GM_FWD_RING: return launch_mode<GM_FWD_RING, false>(maps, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// MXFP8 (block-scaled E4M3) launches of the same kernel family.
+cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
+  switch (mode) {
+    case GM_DENSE: return launch_mode<GM_DENSE, true>(maps, p, grid, st);
+    case GM_BWD_DA: return launch_mode<GM_BWD_DA, true>(maps, p, grid, st);
+    case GM_BWD_DX: return launch_mode<GM_BWD_DX, true>(maps, p, grid, st);
+    case GM_WG13: return launch_mode<GM_WG13, true>(maps, p, grid, st);
+    case GM_WG2: return launch_mode<GM_WG2, true>(maps, p, grid, st);
+    case GM_FWD_RING: return launch_mode<GM_FWD_RING, true>(maps, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -27,6 +27,7 @@ constexpr int kMaxExperts = 1024;
 
 constexpr int kMaxMaps = 6;
 constexpr int kOutStage = 32 * 32 * 2;  // one epilogue warp's 32 x 32 bf16 output chunk
+constexpr int kSfStage = 512 + 1024;    // MXFP8 scale blocks of one stage: A (128 rows), B (256)
 struct TmapSet {
   CUtensorMap m[kMaxMaps];
 };
@@ -63,6 +64,24 @@ struct GemmParams {
   int debug_flags;
   int nmaps;               // tensor maps in use (prefetched at start)
   int wg_sorted;           // weight gradients read token-sorted copies (plain TMA)
+  // ---- MXFP8 (E4M3 codes, E8M0 scales per 32 K-elements)
+  // K-major operands: scales [rows][K/32], four bytes per row per stage,
+  // copied by the gather threads; rows of A are gathered by token when A is.
+  const uint8_t* sfa_rows;    // A scales (x, dout, ring or dh|du)
+  long sfa_ld;                // bytes per row of sfa_rows
+  const uint8_t* sfb_rows0;   // B scales (W2 along H; W1 along I)
+  const uint8_t* sfb_rows1;   // B scales, second weight (W3 along I)
+  long sfb_ld;
+  // M/N-major operands: scales pre-tiled into 512-byte blocks
+  // [..][MN/128][K/128] (see mxfp8.cu), loaded by the TMA producer.
+  const uint8_t* sfa_tiled;
+  const uint8_t* sfb_tiled0;
+  const uint8_t* sfb_tiled1;
+  const uint8_t* sfb_tiled2;  // W2 in the ring launch (W1, W3 use tiled0/1)
+  const uint8_t* gq_src;      // gathered E4M3 rows (x or dout codes) [T, H]
+  uint8_t* ring_sf;           // GEMM1 epilogue: scales of a [ring rows][I/32]
+  uint8_t* dhu_q;             // dA' epilogue: dh|du codes [pad, 2I] ...
+  uint8_t* dhu_sf;            // ... and scales [pad, 2I/32]
   // Ring launch: m_tiles holds the tile capacity; ring_flags[m] counts the
   // epilogue warps (4 per column tile) that published GEMM1 rows of tile m,
   // ring_flags[m_tiles + m] counts the GEMM2 column tiles that consumed them.
@@ -70,5 +89,6 @@ struct GemmParams {
 
 size_t gemm_smem_bytes();
 cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
+cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace mok

@@ -40,10 +40,12 @@ struct WsLayout {
   size_t as;          // bf16 [pad_capacity, I]  s * a
   size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
   size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x, then dout (weight gradients)
-  // MXFP8 activation copies
-  size_t xq, xsf;     // x quantised along H: u8 [T, H], [T, H/32]
-  size_t dq, dsf;     // dout quantised along H
+  // MXFP8 operand copies
+  size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
+  size_t wsf1, wsf3, wsf2;  // forward weight scales tiled for the GEMMs
   size_t dhuq, dhusf; // dh|du quantised along I: u8 [pad, 2I], [pad, 2I/32]
+  size_t wqa, wsfa;   // weight gradients: sorted x / dout along rows, [pad, H] + tiled scales
+  size_t wqb, wsfb;   // weight gradients: dh|du / s*a along rows, [pad, 2I] + tiled scales
   size_t total;
   int64_t pad_capacity, tile_capacity, nchunks;
   int minibatch_rows, ring_slots;

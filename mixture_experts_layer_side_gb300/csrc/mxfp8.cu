@@ -11,28 +11,15 @@
 // exact power-of-two scaling, and the conversion is the hardware's
 // round-to-nearest-even, saturate-to-finite cvt.
 #include "mok_internal.cuh"
+#include "mx.cuh"
 
 namespace mok {
 
 namespace {
 
-__device__ __forceinline__ int block_exponent(float amax) {
-  const int ef = (__float_as_int(amax) >> 23) & 0xFF;
-  if (ef == 0) return -127;
-  int x = ef - 127 - 8;
-  return x < -127 ? -127 : (x > 127 ? 127 : x);
-}
-
-__device__ __forceinline__ float exp2_int(int e) {  // 2^e for e in [-126, 127]
-  return __int_as_float((e + 127) << 23);
-}
-
-// Two floats -> two E4M3 codes (lo in the low byte).
-__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
+__device__ __forceinline__ int block_exponent(float amax) { return mx_block_exponent(amax); }
+__device__ __forceinline__ float exp2_int(int e) { return mx_exp2_int(e); }
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) { return mx_cvt_e4m3x2(lo, hi); }
 
 // Blocks along the contiguous axis: one thread per 32-element block.
 __global__ void quant_rowblocks(const __nv_bfloat16* __restrict__ src, long nblocks, uint8_t* __restrict__ q,
@@ -101,10 +88,7 @@ __global__ void quant_colblocks(const __nv_bfloat16* __restrict__ src, int batch
   }
 }
 
-// Offset of scale (mn, kb) inside a 512-byte scale block of 128 rows (or
-// columns) x 4 K-blocks: the layout tcgen05.cp .32x128b.warpx4 replicates
-// into the four TMEM lane quarters, byte (mn % 32) * 16 + (mn / 32) * 4 + kb.
-__device__ __forceinline__ int sf_block_offset(int mn, int kb) { return (mn & 31) * 16 + (mn >> 5) * 4 + kb; }
+__device__ __forceinline__ int sf_block_offset(int mn, int kb) { return mx_sf_offset(mn, kb); }
 
 // Plain scales [batch][K/32][N] (blocks along K = rows) -> tiled
 // [batch][N/128][K/128][512 B] (one block per 128 N x 128 K tile).
