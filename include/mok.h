@@ -72,7 +72,8 @@ typedef struct {
  * pages name a fifth knob without saying what it is, so it is not invented).
  *
  * minibatch_rows  Routed (expert-sorted, padded) rows per minibatch of the
- *                 forward ring; a multiple of 128, or 0 for the default:
+ *                 forward ring, rounded up to a whole number of 128-row
+ *                 tiles (2368 runs as 2432), or 0 for the default:
  *                 the two-wave floor 2*C*128*256/min(2I, H) ([MTP]
  *                 overlap-granularity paragraph, [NOTE] section 2) with C
  *                 the device's SM count, rounded up to a multiple of 128.

@@ -67,7 +67,8 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
 }
 
 int effective_minibatch_rows(const mok_shape& s, const mok_config& c, int num_sms) {
-  if (c.minibatch_rows > 0) return c.minibatch_rows;
+  // a minibatch is a whole number of 128-row tiles (a requested size is rounded up)
+  if (c.minibatch_rows > 0) return (c.minibatch_rows + kTileRows - 1) / kTileRows * kTileRows;
   // two full waves of 128 x 256 output tiles over the narrower grouped GEMM
   const double rows = 2.0 * num_sms * 128.0 * 256.0 / (double)(2 * s.I < s.H ? 2 * s.I : s.H);
   int m = (int)ceil(rows / kTileRows) * kTileRows;
@@ -190,7 +191,7 @@ mok_status check_shape(const mok_shape* s) {
 mok_status check_config(const mok_config* c) {
   if (!c) return MOK_ERR_INVALID_ARG;
   if (c->comm_sms != 0) return MOK_ERR_INVALID_ARG;
-  if (c->minibatch_rows < 0 || c->minibatch_rows % 128) return MOK_ERR_INVALID_ARG;
+  if (c->minibatch_rows < 0) return MOK_ERR_INVALID_ARG;
   if (c->ring_slots < 0 || c->ring_slots == 1) return MOK_ERR_INVALID_ARG;
   if (!(c->capacity_mult == 0.0f || c->capacity_mult >= 1.0f)) return MOK_ERR_INVALID_ARG;
   return MOK_OK;

@@ -52,12 +52,15 @@ def test_host_argument_checks(lib):
     good = lib.shape_of(256, 256, 128, 8, 2)
     cfg = lib.config()
     assert lib.mok_workspace_size(good, cfg) > 0
+    # a minibatch that is not a whole number of tiles is rounded up
+    assert lib.mok_workspace_size(good, lib.config(minibatch_rows=2368, ring_slots=2)) == \
+        lib.mok_workspace_size(good, lib.config(minibatch_rows=2432, ring_slots=2))
     # unsupported sizes
     for bad in (lib.shape_of(256, 100, 128, 8, 2), lib.shape_of(256, 256, 96, 8, 2),
                 lib.shape_of(256, 256, 128, 2000, 2), lib.shape_of(0, 256, 128, 8, 2)):
         assert lib.mok_workspace_size(bad, cfg) == 0
-    # comm_sms must be 0, minibatch a multiple of 128, ring >= 2
-    for badcfg in (lib.config(comm_sms=4), lib.config(minibatch_rows=100), lib.config(ring_slots=1),
+    # comm_sms must be 0, minibatch >= 0, ring >= 2
+    for badcfg in (lib.config(comm_sms=4), lib.config(minibatch_rows=-128), lib.config(ring_slots=1),
                    lib.config(capacity_mult=0.5)):
         assert lib.mok_workspace_size(good, badcfg) == 0
     fake = ctypes.c_void_p(256)
