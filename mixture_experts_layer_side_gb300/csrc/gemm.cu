@@ -49,6 +49,7 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   int po[kMaxExperts + 1];  // padded expert offsets (weight-gradient modes)
+  int order[kMaxExperts];   // weight-gradient modes: experts by descending routed rows
 };
 
 // A decoded work item.
@@ -129,10 +130,17 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.row0 = it.m * kTileRows;
     it.k_iters = p.k_iters;
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
+    // Items are the experts' tiles with experts sorted by descending K
+    // (routed rows); fetches alternate between the two ends of that list, so
+    // a CTA pairs a long-K tile (MMA-bound) with a short or empty one (store-
+    // bound epilogue) and the two overlap through the double-buffered TMEM.
     const int per_e = p.m_tiles * p.n_tiles;
+    const int total = p.E * per_e;
+    const int pos = (w & 1) ? total - 1 - (w >> 1) : (w >> 1);
+    const int rank = pos / per_e;
     it.type = MODE;
-    it.e = w / per_e;
-    const int r = w - it.e * per_e;
+    it.e = ctl->order[rank];
+    const int r = pos - rank * per_e;
     it.m = r / p.n_tiles;
     it.n = r % p.n_tiles;
     it.row0 = po[it.e];
@@ -651,20 +659,48 @@ __device__ __forceinline__ void store_chunk_coalesced(uint8_t* stage, int lane, 
   __syncwarp();
 }
 
+// A warp's 32 x 64 bf16 chunk (lane = row, w[] = its 64 values as bf16
+// pairs) leaves as full 128-byte row segments: staged in a 4 KB smem buffer
+// (16-byte chunks XOR-swizzled by row), read back with 8 lanes per row and
+// stored 4 rows x 128 bytes per instruction -- four whole cache lines each.
+template <typename RowPtr>
+__device__ __forceinline__ void store_chunk64_coalesced(uint8_t* stage, int lane, const uint32_t (&w)[32],
+                                                        RowPtr row_ptr) {
+  const int sw = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<uint4*>(stage + lane * 128 + ((i ^ sw) << 4)) =
+        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  __syncwarp();
+  const int ch = lane & 7;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int rr = 4 * s + (lane >> 3);
+    const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 128 + ((ch ^ (rr & 7)) << 4));
+    __nv_bfloat16* dst = row_ptr(rr);
+    if (dst) *reinterpret_cast<uint4*>(dst + ch * 8) = v;
+  }
+  __syncwarp();
+}
+
 // Weight gradients: tile rows are rows of dW (H rows of dW1/dW3, I rows of
 // dW2), columns are its columns.  An expert with no routed rows has no
 // accumulation and gets exact zeros.  A weight-gradient item has a short K
 // loop (the expert's rows), so the 64 KB output tile must leave fast:
 // coalesced stores through the warp's staging buffer.
-// 32 columns of accumulator (packed pairs of f32) -> bf16 -> dW rows.
-__device__ __forceinline__ void wgrad_emit32(const GemmParams& p, const Item& it, int r0, int col, int lane,
-                                             uint8_t* stage, const uint32_t (&r)[32]) {
-  uint32_t w[16];
+// 64 columns of accumulator (two 32-column TMEM loads) -> bf16 -> dW rows.
+__device__ __forceinline__ void wgrad_emit64(const GemmParams& p, const Item& it, int r0, int col, int lane,
+                                             uint8_t* stage, const uint32_t (&ra)[32], const uint32_t (&rb)[32]) {
+  uint32_t w[32];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+  for (int i = 0; i < 16; ++i) {
+    w[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+    w[16 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+  }
   __nv_bfloat16* base;
   long ld;
   if (it.type == GM_WG13) {
+    // I is a multiple of 128, so a 64-column chunk never straddles dW1 | dW3
     base = (col < p.I) ? p.dw0 + ((long)it.e * p.H + r0) * p.I + col
                        : p.dw1 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
     ld = p.I;
@@ -672,11 +708,10 @@ __device__ __forceinline__ void wgrad_emit32(const GemmParams& p, const Item& it
     base = p.dw0 + ((long)it.e * p.I + r0) * p.H + col;
     ld = p.H;
   }
-  store_chunk_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
+  store_chunk64_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
 }
 
-// TMEM is read 32 columns at a time with the next chunk's load in flight
-// while the current one is converted and stored (two register buffers).
+// 64 columns at a time: two TMEM loads, one wait, then the coalesced store.
 template <int BN>
 __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane,
                                             uint8_t* stage) {
@@ -685,26 +720,19 @@ __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it,
   uint32_t ra[32], rb[32];
   if (it.k_iters == 0) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) ra[i] = 0u;
+    for (int i = 0; i < 32; ++i) ra[i] = rb[i] = 0u;
 #pragma unroll
-    for (int c = 0; c < BN; c += 32) wgrad_emit32(p, it, r0, col0 + c, lane, stage, ra);
+    for (int c = 0; c < BN; c += 64) wgrad_emit64(p, it, r0, col0 + c, lane, stage, ra, rb);
     return;
   }
-  tmem_ld32_issue(tbase, ra);
-  tmem_wait_ld();
-  tmem_regs_ready(ra);
 #pragma unroll
   for (int c = 0; c < BN; c += 64) {
+    tmem_ld32_issue(tbase + c, ra);
     tmem_ld32_issue(tbase + c + 32, rb);
-    wgrad_emit32(p, it, r0, col0 + c, lane, stage, ra);
     tmem_wait_ld();
+    tmem_regs_ready(ra);
     tmem_regs_ready(rb);
-    if (c + 64 < BN) tmem_ld32_issue(tbase + c + 64, ra);
-    wgrad_emit32(p, it, r0, col0 + c + 32, lane, stage, rb);
-    if (c + 64 < BN) {
-      tmem_wait_ld();
-      tmem_regs_ready(ra);
-    }
+    wgrad_emit64(p, it, r0, col0 + c, lane, stage, ra, rb);
   }
 }
 
@@ -817,6 +845,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
   if (kWgrad) {
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) ctl->po[e] = p.padded_offsets[e];
+    __syncthreads();
+    // rank of each expert by descending routed rows (ties by expert id): the
+    // same order in every CTA, a function of the schedule only
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+      const int ke = ctl->po[e + 1] - ctl->po[e];
+      int rank = 0;
+      for (int o = 0; o < p.E; ++o) {
+        const int ko = ctl->po[o + 1] - ctl->po[o];
+        rank += (ko > ke) || (ko == ke && o < e);
+      }
+      ctl->order[rank] = e;
+    }
   }
   if (warp == 0 && lane == 0)
     for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
@@ -953,6 +993,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
       const Item it = decode<MODE, MX>(p, ctl, w);
+      // a weight-gradient tile of an empty expert has no accumulation: it
+      // takes no TMEM buffer (its epilogue writes zeros on its own)
+      if (kWgrad && it.k_iters == 0) continue;
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)) break;
       tc_fence_after();
@@ -1017,6 +1060,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
       const Item it = decode<MODE, MX>(p, ctl, w);
+      if (kWgrad && it.k_iters == 0) {
+        // empty expert: exact zeros, no TMEM buffer involved
+        epi_wgrad(p, it, 0, q, lane, stage_out);
+        continue;
+      }
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();

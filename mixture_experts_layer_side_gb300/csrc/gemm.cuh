@@ -26,7 +26,7 @@ constexpr int kMaxExperts = 1024;
 
 
 constexpr int kMaxMaps = 6;
-constexpr int kOutStage = 32 * 32 * 2;  // one epilogue warp's 32 x 32 bf16 output chunk
+constexpr int kOutStage = 32 * 64 * 2;  // one epilogue warp's 32 x 64 bf16 output chunk
 constexpr int kSfStage = 512 + 1024;    // MXFP8 scale blocks of one stage: A (128 rows), B (256)
 struct TmapSet {
   CUtensorMap m[kMaxMaps];
