@@ -876,18 +876,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
       uint32_t* counter = reinterpret_cast<uint32_t*>(&p.hdr[kHdrCounters + p.counter]);
-      // Weight-gradient launches keep four tile-counter fetches in flight, so
-      // a run of short items (empty experts, tiny K) does not pay an atomic
-      // round trip each; the values come back in increasing order, so the
-      // CTA still takes its items in fetch order.  Launches with long items
-      // fetch one ahead (holding more would cost tail balance and, in the
-      // ring launch, delay the GEMM2 tiles other CTAs wait on).
-      int w = (int)atomicAdd(counter, 1u);
+      // Weight-gradient launches take two consecutive counter values per
+      // fetch -- one item from each end of the descending-K list (see
+      // decode), so every CTA runs a long tile and a short one back to back
+      // -- and keep two such pairs in flight, so a run of short items (empty
+      // experts, tiny K) does not pay an atomic round trip each.  Launches
+      // with long items fetch one ahead (holding more would cost tail balance
+      // and, in the ring launch, delay the GEMM2 tiles other CTAs wait on).
+      int w = (int)atomicAdd(counter, kWgrad ? 2u : 1u);
       int f1 = 0, f2 = 0, f3 = 0;
       if (kWgrad) {
-        f1 = (int)atomicAdd(counter, 1u);
-        f2 = (int)atomicAdd(counter, 1u);
-        f3 = (int)atomicAdd(counter, 1u);
+        f1 = w + 1;
+        f2 = (int)atomicAdd(counter, 2u);
+        f3 = f2 + 1;
       }
       bool ok = true;
       while (ok) {
@@ -902,7 +903,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           w_next = f1;
           f1 = f2;
           f2 = f3;
-          f3 = (int)atomicAdd(counter, 1u);
+          f3 = (f2 & 1) ? (int)atomicAdd(counter, 2u) : f2 + 1;
         } else {
           w_next = (int)atomicAdd(counter, 1u);
         }
