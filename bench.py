@@ -45,7 +45,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
-def parse_args():
+def parse_args_from(argv):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
@@ -56,7 +56,11 @@ def parse_args():
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def parse_args():
+    return parse_args_from(None)
 
 
 def load_peaks():
@@ -193,8 +197,12 @@ def dist_setup(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            # host-only ranks (the CPU tests of this launch logic)
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
@@ -211,9 +219,16 @@ def max_over_ranks(world, value):
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tflops(world, flops_per_rank_step, ms_per_step):
+    """Whole-job throughput: every rank runs the same step on its own replica,
+    and ``ms_per_step`` is the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step / 1e3) / 1e12
 
 
 def run_reference(args):
@@ -310,7 +325,7 @@ def run_mok(args):
     barrier(world)
 
     fps = flops_per_step(shape)
-    value = world * fps / (ms / 1e3) / 1e12
+    value = job_tflops(world, fps, ms)
 
     # ------------------------------------------------ roofline of the dominant kernel
     peaks, peaks_src = load_peaks()
@@ -375,7 +390,7 @@ def run_mok(args):
         ems = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
         h2d = sum(t.numel() * t.element_size() for t in (hx, hidx, hs, hd))
         d2h = sum(t.numel() * t.element_size() for t in (hout, hdX, hds))
-        e2e = {"value": world * fps / (ems / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ems,
+        e2e = {"value": job_tflops(world, fps, ems), "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     # ------------------------------------------------ CPU baseline (rank 0, one GPU only)
