@@ -279,6 +279,7 @@ void base_params(GemmParams& g, const mok_shape& s, const WsLayout& L, uint8_t* 
   g.tile_expert = reinterpret_cast<const int32_t*>(ws + L.tile_expert);
   g.pad_perm = reinterpret_cast<const int32_t*>(ws + L.pad_perm);
   g.padded_offsets = reinterpret_cast<const int32_t*>(ws + L.padded_offsets);
+  g.counts = reinterpret_cast<const int32_t*>(ws + L.counts);
 }
 
 mok_status reset_counters(uint8_t* ws, const WsLayout& L, cudaStream_t st) {

@@ -49,7 +49,10 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   int po[kMaxExperts + 1];  // padded expert offsets (weight-gradient modes)
-  int order[kMaxExperts];   // weight-gradient modes: experts by descending routed rows
+  // weight-gradient modes: experts by descending padded rows, each entry
+  // e | (K iterations << 10); the n_active experts with routed rows first
+  int order[kMaxExperts];
+  int n_active;
 };
 
 // A decoded work item.
@@ -70,7 +73,7 @@ __device__ int count_items(const GemmParams& p) {
   if constexpr (MODE == GM_DENSE) {
     return p.m_tiles * p.n_tiles;
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
-    return p.E * p.m_tiles * p.n_tiles;
+    return 0;  // known only inside the kernel (experts with routed rows)
   } else if constexpr (MODE == GM_FWD_RING) {
     return used_tiles(p) * (p.g1_tiles + p.n_tiles);
   } else {
@@ -130,21 +133,23 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.row0 = it.m * kTileRows;
     it.k_iters = p.k_iters;
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
-    // Items are the experts' tiles with experts sorted by descending K
-    // (routed rows); fetches alternate between the two ends of that list, so
-    // a CTA pairs a long-K tile (MMA-bound) with a short or empty one (store-
+    // Items are the tiles of the experts that have routed rows, experts
+    // sorted by descending K; fetches alternate between the two ends of that
+    // list, so a CTA pairs a long-K tile (MMA-bound) with a short one (store-
     // bound epilogue) and the two overlap through the double-buffered TMEM.
+    // (Empty experts' zero gradients are written outside the item list.)
     const int per_e = p.m_tiles * p.n_tiles;
-    const int total = p.E * per_e;
+    const int total = ctl->n_active * per_e;
     const int pos = (w & 1) ? total - 1 - (w >> 1) : (w >> 1);
     const int rank = pos / per_e;
+    const int oe = ctl->order[rank];
     it.type = MODE;
-    it.e = ctl->order[rank];
+    it.e = oe & 1023;
     const int r = pos - rank * per_e;
     it.m = r / p.n_tiles;
     it.n = r % p.n_tiles;
     it.row0 = po[it.e];
-    it.k_iters = (po[it.e + 1] - po[it.e]) / kEl;
+    it.k_iters = oe >> 10;
   } else {
     int type = MODE, m, n;
     if constexpr (MODE == GM_FWD_RING) {
@@ -718,13 +723,6 @@ __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it,
   const int r0 = it.m * 128 + q * 32;  // first dW row of this warp
   const int col0 = it.n * BN;
   uint32_t ra[32], rb[32];
-  if (it.k_iters == 0) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) ra[i] = rb[i] = 0u;
-#pragma unroll
-    for (int c = 0; c < BN; c += 64) wgrad_emit64(p, it, r0, col0 + c, lane, stage, ra, rb);
-    return;
-  }
 #pragma unroll
   for (int c = 0; c < BN; c += 64) {
     tmem_ld32_issue(tbase + c, ra);
@@ -802,6 +800,30 @@ __device__ bool gather_item_k(const GemmParams& p, const Item& it, uint8_t* sA, 
   return true;
 }
 
+// Weight gradients of the experts without routed rows are exact zeros: the
+// four gather warps of every CTA write them in 32 KB chunks (one 512-byte
+// warp store per step), dealt round-robin over all CTAs' gather warps.  In
+// launches whose operands are TMA-loaded these warps have no other work, so
+// the zero stores overlap the MMA-bound tiles of the item list.
+template <int MODE>
+__device__ void zero_empty_experts(const GemmParams& p, const Ctl* ctl, int gw, int lane) {
+  constexpr long kChunk = 16384;  // bf16 elements per chunk
+  const int n_empty = p.E - ctl->n_active;
+  const long slab = (long)p.H * p.I;  // dW1_e, dW3_e: [H, I]; dW2_e: [I, H]
+  const int per_expert = (MODE == GM_WG13) ? 2 : 1;
+  const long chunks_per_slab = slab / kChunk;  // H and I are multiples of 128
+  const long total = (long)n_empty * per_expert * chunks_per_slab;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (long c = (long)blockIdx.x * 4 + gw; c < total; c += (long)gridDim.x * 4) {
+    const long sl = c / chunks_per_slab;
+    const int e = ctl->order[ctl->n_active + (int)(sl / per_expert)] & 1023;
+    __nv_bfloat16* base = (sl % per_expert) ? p.dw1 : p.dw0;
+    uint4* dst = reinterpret_cast<uint4*>(base + (long)e * slab + (c - sl * chunks_per_slab) * kChunk);
+#pragma unroll 8
+    for (int i = 0; i < (int)(kChunk * 2 / 16 / 32); ++i) __stcs(dst + i * 32 + lane, z);
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <int MODE, bool MX>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ TmapSet maps,
@@ -822,14 +844,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // MXFP8 keeps one accumulator (TMEM columns 256.. hold the stage scales)
   constexpr uint32_t kAccBufs = MX ? 1u : 2u;
   constexpr bool kWgrad = (MODE == GM_WG13 || MODE == GM_WG2);
-  // consumers of the item queue: MMA warp, 4 epilogue warps, 4 gather warps
-  constexpr uint32_t kQueueConsumers = kGather ? 9u : 5u;
+
+  // Weight-gradient launches whose operands are all TMA-loaded (token-sorted
+  // copies) take the gather warps out of the stage pipeline; those warps
+  // write the empty experts' zero gradients instead.
+  const bool gather_in_pipe = kGather && !(kWgrad && (MX || p.wg_sorted));
+  const uint32_t queue_consumers = gather_in_pipe ? 9u : 5u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       // TMA producer's arrive.expect_tx, plus one no-increment arrival per
-      // gather thread when the launch gathers
-      mbar_init(&ctl->full[i], kGather ? 129u : 1u);
+      // gather thread when the gather warps take part
+      mbar_init(&ctl->full[i], gather_in_pipe ? 129u : 1u);
       mbar_init(&ctl->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -838,16 +864,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(&ctl->qfull[i], 1);
-      mbar_init(&ctl->qempty[i], kQueueConsumers);
+      mbar_init(&ctl->qempty[i], queue_consumers);
     }
     ctl->abort = 0;
+    ctl->n_active = 0;
     fence_mbar_init();
   }
   if (kWgrad) {
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) ctl->po[e] = p.padded_offsets[e];
     __syncthreads();
-    // rank of each expert by descending routed rows (ties by expert id): the
-    // same order in every CTA, a function of the schedule only
+    // rank of each expert by descending padded rows (ties by expert id): the
+    // same order in every CTA, a function of the schedule only.  An expert's
+    // K loop covers its routed rows rounded up to one stage (64 rows; MXFP8:
+    // 128, its padding); the rows past the count are zero in both operands.
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
       const int ke = ctl->po[e + 1] - ctl->po[e];
       int rank = 0;
@@ -855,7 +884,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int ko = ctl->po[o + 1] - ctl->po[o];
         rank += (ko > ke) || (ko == ke && o < e);
       }
-      ctl->order[rank] = e;
+      const int kit = MX ? ke / 128 : (p.counts[e] + 63) / 64;
+      ctl->order[rank] = e | (kit << 10);
+      if (ke > 0) atomicAdd(&ctl->n_active, 1);
     }
   }
   if (warp == 0 && lane == 0)
@@ -868,8 +899,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int num_items = count_items<MODE>(p);
-  const int* po = ctl->po;
+  const int num_items = kWgrad ? ctl->n_active * p.m_tiles * p.n_tiles : count_items<MODE>(p);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer + work fetch
@@ -933,7 +963,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
   } else if (warp >= 6) {
     // ---------------------------------------------------------------- gather producers
-    if (kGather) {
+    if (gather_in_pipe) {
       const int gt = threadIdx.x - 192;
       uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
       while (true) {
@@ -983,6 +1013,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       // let this thread's copies land before the CTA can exit
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
+    if (kWgrad) zero_empty_experts<MODE>(p, ctl, warp - 6, lane);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0, qs = 0, qp = 0, tcount = 0;
@@ -994,9 +1025,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
       const Item it = decode<MODE, MX>(p, ctl, w);
-      // a weight-gradient tile of an empty expert has no accumulation: it
-      // takes no TMEM buffer (its epilogue writes zeros on its own)
-      if (kWgrad && it.k_iters == 0) continue;
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)) break;
       tc_fence_after();
@@ -1061,11 +1089,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
       const Item it = decode<MODE, MX>(p, ctl, w);
-      if (kWgrad && it.k_iters == 0) {
-        // empty expert: exact zeros, no TMEM buffer involved
-        epi_wgrad(p, it, 0, q, lane, stage_out);
-        continue;
-      }
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();

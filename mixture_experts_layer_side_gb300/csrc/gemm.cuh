@@ -44,6 +44,7 @@ struct GemmParams {
   const int32_t* tile_expert;
   const int32_t* pad_perm;
   const int32_t* padded_offsets;
+  const int32_t* counts;   // routed rows per expert
   // epilogue operands
   float* out_f32;
   long ld_out;

@@ -40,3 +40,14 @@ def assert_mxfp8_close(got, ref, name):
 def require_gpu():
     if not torch.cuda.is_available():
         pytest.fail("this test needs a CUDA GPU")
+
+
+def poisoned_outputs(layer):
+    """Output and gradient buffers pre-filled with NaN, so that any element a
+    call fails to write shows up in the comparison."""
+    import torch
+    grads = layer.alloc_grads()
+    for t in grads.values():
+        t.fill_(float("nan"))
+    out = torch.full((layer.shape.T, layer.shape.H), float("nan"), dtype=torch.bfloat16, device=layer.device)
+    return out, grads

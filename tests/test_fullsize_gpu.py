@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 import torch
 
-from _helpers import assert_bf16_close, assert_mxfp8_close, require_gpu
+from _helpers import assert_bf16_close, assert_mxfp8_close, require_gpu, poisoned_outputs
 from oracle import moe
 
 pytestmark = pytest.mark.gpu
@@ -40,8 +40,9 @@ def run(shape, prec, inp, wq, minibatch_rows=0):
     layer = MoKLayer(shape, precision=prec, minibatch_rows=minibatch_rows)
     wf, wb = (wq["fwd"], wq["bwd"]) if wq else ((inp["W1"], inp["W3"], inp["W2"]),) * 2
     layer.build_schedule(inp["idx"])
-    out = layer.forward(inp["x"], inp["s"], *wf)
-    grads = layer.backward(inp["x"], inp["s"], *wb, inp["dout"])
+    out, grads = poisoned_outputs(layer)
+    layer.forward(inp["x"], inp["s"], *wf, out=out)
+    layer.backward(inp["x"], inp["s"], *wb, inp["dout"], grads=grads)
     layer.check()
     return out, grads
 
@@ -77,6 +78,13 @@ def sampled_checks(shape, prec, inp, out, grads):
     close(f64(grads["dW1"][e]), dW1[0], f"dW1[{e}]")
     close(f64(grads["dW3"][e]), dW3[0], f"dW3[{e}]")
     close(f64(grads["dW2"][e]), dW2[0], f"dW2[{e}]")
+    # every element written (the buffers started as NaN), and the experts
+    # without routed rows have exact-zero gradients
+    for name, t in [("out", out)] + list(grads.items()):
+        assert not torch.isnan(t).any().item(), name
+    empty = torch.tensor(np.nonzero(counts == 0)[0], device=inp["W1"].device, dtype=torch.long)
+    for k in ("dW1", "dW3", "dW2"):
+        assert torch.count_nonzero(grads[k].index_select(0, empty)).item() == 0, k
 
 
 @pytest.mark.parametrize("workload", ["dsv3", "mid", "mid_mxfp8_hot"])

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from _helpers import assert_bf16_close, np64, require_gpu
+from _helpers import assert_bf16_close, np64, require_gpu, poisoned_outputs
 from oracle import moe
 
 pytestmark = pytest.mark.gpu
@@ -31,8 +31,9 @@ def run_layer(shape, routing, seed, **kw):
     g = {k: v.cuda() for k, v in inp.items()}
     layer = MoKLayer(S, **kw)
     layer.build_schedule(g["idx"])
-    out = layer.forward(g["x"], g["s"], g["W1"], g["W3"], g["W2"])
-    grads = layer.backward(g["x"], g["s"], g["W1"], g["W3"], g["W2"], g["dout"])
+    out, grads = poisoned_outputs(layer)
+    layer.forward(g["x"], g["s"], g["W1"], g["W3"], g["W2"], out=out)
+    layer.backward(g["x"], g["s"], g["W1"], g["W3"], g["W2"], g["dout"], grads=grads)
     layer.check()
     return inp, out, grads
 

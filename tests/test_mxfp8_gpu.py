@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from _helpers import assert_mxfp8_close, np64, require_gpu
+from _helpers import assert_mxfp8_close, np64, require_gpu, poisoned_outputs
 from oracle import moe, mxfp8
 
 pytestmark = pytest.mark.gpu
@@ -85,8 +85,9 @@ def run_mx(shape, routing, seed, **kw):
     layer = MoKLayer(S, precision="mxfp8", **kw)
     wq = layer.quantize_weights(g["W1"], g["W3"], g["W2"])
     layer.build_schedule(g["idx"])
-    out = layer.forward(g["x"], g["s"], *wq["fwd"])
-    grads = layer.backward(g["x"], g["s"], *wq["bwd"], g["dout"])
+    out, grads = poisoned_outputs(layer)
+    layer.forward(g["x"], g["s"], *wq["fwd"], out=out)
+    layer.backward(g["x"], g["s"], *wq["bwd"], g["dout"], grads=grads)
     layer.check()
     return inp, out, grads
 
