@@ -83,6 +83,23 @@ def phase_flops(shape):
     return {"fwd_gemm": 6 * RHI, "bwd_da": 2 * RHI, "bwd_dx": 4 * RHI, "bwd_wg13": 4 * RHI, "bwd_wg2": 2 * RHI}
 
 
+def phase_min_bytes(shape, prec, active_experts):
+    """Compulsory DRAM bytes of each GEMM phase: the weights of the experts
+    with routed rows once, each activation operand once, each output once
+    (MXFP8 operands at 1 + 1/32 bytes per element, bf16 at 2)."""
+    R, T, H, I, E = shape.R, shape.T, shape.H, shape.I, shape.E
+    ob = 1.0 + 1.0 / 32 if prec == "mxfp8" else 2.0
+    w = active_experts * H * I * ob  # one expert weight matrix
+    return {
+        "fwd_gemm": 3 * w + T * H * ob + R * 2 * I * 2 + R * H * 2,           # W1|W3|W2, x; ctx [h|u], y
+        "bwd_da": w + T * H * ob + R * 2 * I * 2 + R * 2 * I * 2 + R * I * 2
+                  + (R * 2 * I * ob if prec == "mxfp8" else 0),               # W2, dout, ctx; dh|du, s*a
+        "bwd_dx": 2 * w + R * 2 * I * ob + R * H * 2,                          # W1|W3, dh|du; dX parts
+        "bwd_wg13": R * H * ob + R * 2 * I * ob + E * 2 * H * I * 2,           # x, dh|du; dW1, dW3
+        "bwd_wg2": R * I * ob + R * H * ob + E * I * H * 2,                    # s*a, dout; dW2
+    }
+
+
 def phase_bytes(shape):
     # algorithmic bytes of the HBM-bound kernels (bf16 = 2 B, f32 = 4 B)
     R, T, H = shape.R, shape.T, shape.H
@@ -351,6 +368,18 @@ def run_mok(args):
             gbs = pb[n] / (per_phase[n]["ms"] / 1e3) / 1e9
             per_phase[n]["gbs"] = gbs
             per_phase[n]["frac_of_hbm"] = gbs / float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # attainable roofline of each GEMM phase: time / max(FLOPs / tensor peak,
+    # compulsory bytes / copy bandwidth), with the binding resource named
+    stats = load_stats(inp["idx"], shape.E)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    mb = phase_min_bytes(shape, prec, shape.E - stats["empty_experts"])
+    for n in GEMM_PHASES:
+        if n in per_phase:
+            t_flop = pf[n] / (peak * 1e12) * 1e3
+            t_byte = mb[n] / (hbm * 1e9) * 1e3
+            floor = max(t_flop, t_byte)
+            per_phase[n].update(min_bytes=mb[n], floor_ms=floor, bound="tensor" if t_flop >= t_byte else "hbm",
+                                attainable_frac=floor / per_phase[n]["ms"])
     sched_share = per_phase.get("schedule", {"ms": 0})["ms"] / ms
 
     # ------------------------------------------------ end to end through the C ABI, host buffers
@@ -419,7 +448,7 @@ def run_mok(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "load": load_stats(inp["idx"], shape.E),
+            "load": stats,
             "peaks_source": peaks_src,
         }
         print(json.dumps(line), flush=True)
