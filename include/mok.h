@@ -95,8 +95,11 @@ typedef struct {
  *                 instead of the single persistent ring launch.
  *                 Bit 2 (MOK_DEBUG_FUSED_WGRAD_GATHER): the weight-gradient
  *                 GEMMs gather token rows in their load path instead of
- *                 reading token-sorted copies.  Results are bitwise the same
- *                 in every mode.
+ *                 reading token-sorted copies.
+ *                 Bit 3 (MOK_DEBUG_SINGLE_CTA_WGRAD): the BF16 weight-gradient
+ *                 GEMMs run one CTA per 128-row tile instead of clusters of
+ *                 two CTAs sharing a 256-row tile (cta_group::2).
+ *                 Results are bitwise the same in every mode.
  */
 typedef struct {
   int32_t minibatch_rows;
@@ -109,6 +112,7 @@ typedef struct {
 #define MOK_DEBUG_SKIP_RING_SIGNAL 1
 #define MOK_DEBUG_SERIAL_RING 2
 #define MOK_DEBUG_FUSED_WGRAD_GATHER 4
+#define MOK_DEBUG_SINGLE_CTA_WGRAD 8
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
 typedef struct {

@@ -39,8 +39,8 @@ namespace mok {
 namespace {
 
 struct Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t qfull[kQueue];
@@ -53,6 +53,7 @@ struct Ctl {
   // e | (K iterations << 10); the n_active experts with routed rows first
   int order[kMaxExperts];
   int n_active;
+  int pair_rank;  // CTA-pair launches: 0 for the leader (issues the MMAs), 1 for the other
 };
 
 // A decoded work item.
@@ -120,7 +121,7 @@ __device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& 
   return emit(GM_FWD2, nb - 1, w, g2);
 }
 
-template <int MODE, bool MX = false>
+template <int MODE, bool MX = false, bool PAIR = false>
 __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
   constexpr int kEl = MX ? 128 : 64;  // K elements per stage (128 bytes)
   const int* po = ctl->po;
@@ -138,7 +139,8 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     // list, so a CTA pairs a long-K tile (MMA-bound) with a short one (store-
     // bound epilogue) and the two overlap through the double-buffered TMEM.
     // (Empty experts' zero gradients are written outside the item list.)
-    const int per_e = p.m_tiles * p.n_tiles;
+    // CTA pairs take the M tiles two at a time: the leader the even one
+    const int per_e = (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;
     const int total = ctl->n_active * per_e;
     const int pos = (w & 1) ? total - 1 - (w >> 1) : (w >> 1);
     const int rank = pos / per_e;
@@ -146,7 +148,7 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.type = MODE;
     it.e = oe & 1023;
     const int r = pos - rank * per_e;
-    it.m = r / p.n_tiles;
+    it.m = PAIR ? 2 * (r / p.n_tiles) + ctl->pair_rank : r / p.n_tiles;
     it.n = r % p.n_tiles;
     it.row0 = po[it.e];
     it.k_iters = oe >> 10;
@@ -246,6 +248,17 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
       for (int cc = 0; cc < p.bn / 64; ++cc)
         tma_load_2d(b + cc * 8192, &mp.m[1], bar, it.n * p.bn + cc * 64, it.row0 + kk * 64);
   }
+}
+
+// CTA-pair weight-gradient stage: this CTA's A tile (its own 128 M rows)
+// and its half of the 256-column B tile, completing on the leader's barrier.
+template <int MODE>
+__device__ __forceinline__ void tma_loads_pair(const TmapSet& mp, const Item& it, int kk, int rank, uint8_t* a,
+                                               uint8_t* b, uint32_t bar) {
+  const int bcol = it.n * 256 + rank * 128;
+  const int krow = it.row0 + kk * 64;
+  for (int c = 0; c < 2; ++c) tma_load_2d_pair(a + c * 8192, &mp.m[0], bar, it.m * 128 + c * 64, krow);
+  for (int c = 0; c < 2; ++c) tma_load_2d_pair(b + c * 8192, &mp.m[1], bar, bcol + c * 64, krow);
 }
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -824,17 +837,26 @@ __device__ void zero_empty_experts(const GemmParams& p, const Ctl* ctl, int gw, 
   }
 }
 
+// At exit, how long a CTA waits for copies still in flight after an abort.
+constexpr uint64_t kDrainNs = 20000000ull;  // 20 ms
+
 // ------------------------------------------------------------------ kernel
-template <int MODE, bool MX>
+template <int MODE, bool MX, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ TmapSet maps,
                                                                 const GemmParams p) {
+  // CTA-pair launches: 6 stages of 16 KB A + 16 KB B (this CTA's half of a
+  // 256-column B tile); otherwise 4 stages of 16 KB A + 32 KB B.  Both fill
+  // the same 192 KB.
+  constexpr int kSt = PAIR ? kPairStages : kStages;
+  constexpr int kBSt = PAIR ? kAStage : kBStage;
+  static_assert(kSt * (kAStage + kBSt) == kStages * (kAStage + kBStage), "stage layouts differ in size");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
-  uint8_t* sB = base + kStages * kAStage;
-  Ctl* ctl = reinterpret_cast<Ctl*>(sB + kStages * kBStage);
-  // per epilogue warp, one 2 KB output staging buffer (128-byte aligned)
-  uint8_t* sOut = sB + kStages * kBStage + ((sizeof(Ctl) + 127) / 128) * 128;
+  uint8_t* sB = base + kSt * kAStage;
+  Ctl* ctl = reinterpret_cast<Ctl*>(sB + kSt * kBSt);
+  // per epilogue warp, one 4 KB output staging buffer (128-byte aligned)
+  uint8_t* sOut = sB + kSt * kBSt + ((sizeof(Ctl) + 127) / 128) * 128;
   // MXFP8: per stage, the scale blocks of A (512 B) and B (1024 B)
   uint8_t* sSF = sOut + 4 * kOutStage;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -849,10 +871,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
   const bool gather_in_pipe = kGather && !(kWgrad && (MX || p.wg_sorted));
-  const uint32_t queue_consumers = gather_in_pipe ? 9u : 5u;
+  // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
+  // by the other CTA's TMA producer and epilogue warps
+  const uint32_t queue_consumers = PAIR ? 10u : gather_in_pipe ? 9u : 5u;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kSt; ++i) {
       // TMA producer's arrive.expect_tx, plus one no-increment arrival per
       // gather thread when the gather warps take part
       mbar_init(&ctl->full[i], gather_in_pipe ? 129u : 1u);
@@ -860,7 +885,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->tfull[i], 1);
-      mbar_init(&ctl->tempty[i], 4);
+      // the epilogue warps that read the accumulator (both CTAs of a pair)
+      mbar_init(&ctl->tempty[i], PAIR ? 8u : 4u);
     }
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(&ctl->qfull[i], 1);
@@ -868,6 +894,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     ctl->abort = 0;
     ctl->n_active = 0;
+    ctl->pair_rank = (int)rank;
+    ctl->tmem_base = 0;  // a 512-column allocation always starts at column 0
     fence_mbar_init();
   }
   if (kWgrad) {
@@ -879,86 +907,148 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // 128, its padding); the rows past the count are zero in both operands.
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
       const int ke = ctl->po[e + 1] - ctl->po[e];
-      int rank = 0;
+      int pos = 0;
       for (int o = 0; o < p.E; ++o) {
         const int ko = ctl->po[o + 1] - ctl->po[o];
-        rank += (ko > ke) || (ko == ke && o < e);
+        pos += (ko > ke) || (ko == ke && o < e);
       }
       const int kit = MX ? ke / 128 : (p.counts[e] + 63) / 64;
-      ctl->order[rank] = e | (kit << 10);
+      ctl->order[pos] = e | (kit << 10);
       if (ke > 0) atomicAdd(&ctl->n_active, 1);
     }
   }
   if (warp == 0 && lane == 0)
     for (int i = 0; i < p.nmaps; ++i) tma_prefetch_desc(&maps.m[i]);
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem_base, 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&ctl->tmem_base, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&ctl->tmem_base, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // CTA pairs: both CTAs' barriers are initialised before either signals
+  // the other's
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int num_items = kWgrad ? ctl->n_active * p.m_tiles * p.n_tiles : count_items<MODE>(p);
+  const int num_items = kWgrad ? ctl->n_active * (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles
+                               : count_items<MODE>(p);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer + work fetch
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
-      uint32_t* counter = reinterpret_cast<uint32_t*>(&p.hdr[kHdrCounters + p.counter]);
-      // Weight-gradient launches take two consecutive counter values per
-      // fetch -- one item from each end of the descending-K list (see
-      // decode), so every CTA runs a long tile and a short one back to back
-      // -- and keep two such pairs in flight, so a run of short items (empty
-      // experts, tiny K) does not pay an atomic round trip each.  Launches
-      // with long items fetch one ahead (holding more would cost tail balance
-      // and, in the ring launch, delay the GEMM2 tiles other CTAs wait on).
-      int w = (int)atomicAdd(counter, kWgrad ? 2u : 1u);
-      int f1 = 0, f2 = 0, f3 = 0;
-      if (kWgrad) {
-        f1 = w + 1;
-        f2 = (int)atomicAdd(counter, 2u);
-        f3 = f2 + 1;
-      }
-      bool ok = true;
-      while (ok) {
-        if (w >= num_items) w = -1;
-        ok = mbar_wait(&ctl->qempty[qs], qp ^ 1, wc);
-        ctl->q[qs] = ok ? w : -1;
-        mbar_arrive(&ctl->qfull[qs]);
-        if (++qs == kQueue) { qs = 0; qp ^= 1; }
-        if (!ok || w < 0) break;
-        int w_next;
-        if (kWgrad) {
-          w_next = f1;
-          f1 = f2;
-          f2 = f3;
-          f3 = (f2 & 1) ? (int)atomicAdd(counter, 2u) : f2 + 1;
-        } else {
-          w_next = (int)atomicAdd(counter, 1u);
-        }
-        const Item it = decode<MODE, MX>(p, ctl, w);
-        if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
-          // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
-          // of its GEMM1 column tiles are published, then order the
-          // async-proxy loads after the acquire
-          ok = wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc);
-          fence_proxy_async_global();
+      uint32_t stage = 0, phase = 0, qs = 0, qp = 0, issued = 0;
+      if (PAIR && rank != 0) {
+        // the other CTA of a pair: take the leader's items from the queue it
+        // fills, load this CTA's operand halves, and complete their bytes on
+        // the leader's stage barrier
+        while (true) {
+          if (!mbar_wait_cluster(&ctl->qfull[qs], qp, wc)) break;
+          const int w = ctl->q[qs];
+          mbar_arrive_cluster(mapa_shared(&ctl->qempty[qs], 0));
+          if (++qs == kQueue) { qs = 0; qp ^= 1; }
+          if (w < 0) break;
+          const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
+          bool ok = true;
+          for (int kk = 0; kk < it.k_iters; ++kk) {
+            if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
+            tma_loads_pair<MODE>(maps, it, kk, 1, sA + stage * kAStage, sB + stage * kBSt,
+                                 mapa_shared(&ctl->full[stage], 0));
+            ++issued;
+            if (++stage == kSt) { stage = 0; phase ^= 1; }
+          }
           if (!ok) break;
         }
-        const uint32_t bytes = MX ? mx_stage_bytes<MODE>(p, it.type, item_bn(p, it.type))
-                                  : tma_stage_bytes(p, it.type, item_bn(p, it.type));
-        for (int kk = 0; kk < it.k_iters; ++kk) {
-          if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(&ctl->full[stage], bytes);
-          if constexpr (MX)
-            tma_loads_mx<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, sSF + stage * kSfStage,
-                               sSF + stage * kSfStage + 512, &ctl->full[stage]);
-          else
-            tma_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBStage, &ctl->full[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        // the leader's MMAs read these stages: wait for their release (which
+        // also means the copies landed) before the CTA may leave
+        const uint64_t t0 = globaltimer();
+        for (uint32_t j = 0; j < kSt; ++j) {
+          const uint64_t spent = globaltimer() - t0;
+          if (spent < kDrainNs) mbar_drain(&ctl->empty[stage], phase ^ 1, kDrainNs - spent);
+          if (++stage == kSt) { stage = 0; phase ^= 1; }
         }
-        w = w_next;
+      } else {
+        uint32_t* counter = reinterpret_cast<uint32_t*>(&p.hdr[kHdrCounters + p.counter]);
+        // Weight-gradient launches take two consecutive counter values per
+        // fetch -- one item from each end of the descending-K list (see
+        // decode), so every CTA runs a long tile and a short one back to
+        // back -- and keep two such pairs in flight, so a run of short items
+        // does not pay an atomic round trip each.  Launches with long items
+        // fetch one ahead (holding more would cost tail balance and, in the
+        // ring launch, delay the GEMM2 tiles other CTAs wait on).
+        int w = (int)atomicAdd(counter, kWgrad ? 2u : 1u);
+        int f1 = 0, f2 = 0, f3 = 0;
+        if (kWgrad) {
+          f1 = w + 1;
+          f2 = (int)atomicAdd(counter, 2u);
+          f3 = f2 + 1;
+        }
+        bool ok = true;
+        while (ok) {
+          if (w >= num_items) w = -1;
+          ok = PAIR ? mbar_wait_cluster(&ctl->qempty[qs], qp ^ 1, wc) : mbar_wait(&ctl->qempty[qs], qp ^ 1, wc);
+          const int wq = ok ? w : -1;
+          ctl->q[qs] = wq;
+          if constexpr (PAIR) {
+            // the same item for the other CTA of the pair
+            st_cluster_u32(mapa_shared(&ctl->q[qs], 1), (uint32_t)wq);
+            mbar_arrive_cluster(mapa_shared(&ctl->qfull[qs], 1));
+          }
+          mbar_arrive(&ctl->qfull[qs]);
+          if (++qs == kQueue) { qs = 0; qp ^= 1; }
+          if (!ok || w < 0) break;
+          int w_next;
+          if (kWgrad) {
+            w_next = f1;
+            f1 = f2;
+            f2 = f3;
+            f3 = (f2 & 1) ? (int)atomicAdd(counter, 2u) : f2 + 1;
+          } else {
+            w_next = (int)atomicAdd(counter, 1u);
+          }
+          const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
+          if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
+            // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
+            // of its GEMM1 column tiles are published, then order the
+            // async-proxy loads after the acquire
+            ok = wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc);
+            fence_proxy_async_global();
+            if (!ok) break;
+          }
+          // CTA pairs: this CTA's 32 KB and the other CTA's 32 KB
+          const uint32_t bytes = PAIR ? 4u * kAStage
+                                 : MX ? mx_stage_bytes<MODE>(p, it.type, item_bn(p, it.type))
+                                      : tma_stage_bytes(p, it.type, item_bn(p, it.type));
+          for (int kk = 0; kk < it.k_iters; ++kk) {
+            if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
+            mbar_arrive_expect_tx(&ctl->full[stage], bytes);
+            if constexpr (PAIR)
+              tma_loads_pair<MODE>(maps, it, kk, 0, sA + stage * kAStage, sB + stage * kBSt,
+                                   mapa_shared(&ctl->full[stage], 0));
+            else if constexpr (MX)
+              tma_loads_mx<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBSt, sSF + stage * kSfStage,
+                                 sSF + stage * kSfStage + 512, &ctl->full[stage]);
+            else
+              tma_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBSt, &ctl->full[stage]);
+            ++issued;
+            if (++stage == kSt) { stage = 0; phase ^= 1; }
+          }
+          w = w_next;
+        }
+        // let the copies in flight land before the CTA may leave (after an
+        // abort the MMA warp may not have waited for them): the last fills
+        // of each stage, newest first
+        const uint64_t t0 = globaltimer();
+        const uint32_t last = issued < (uint32_t)kSt ? issued : (uint32_t)kSt;
+        for (uint32_t j = 1; j <= last; ++j) {
+          const uint32_t f = issued - j;
+          const uint64_t spent = globaltimer() - t0;
+          if (spent < kDrainNs) mbar_drain(&ctl->full[f % kSt], (f / kSt) & 1u, kDrainNs - spent);
+        }
       }
     }
   } else if (warp >= 6) {
@@ -973,7 +1063,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
         if (++qs == kQueue) { qs = 0; qp ^= 1; }
         if (w < 0) break;
-        const Item it = decode<MODE, MX>(p, ctl, w);
+        const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
         bool ok = true;
         if constexpr (MX) {
           int tok[8];
@@ -1016,21 +1106,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     if (kWgrad) zero_empty_experts<MODE>(p, ctl, warp - 6, lane);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
+    // (CTA pairs: the leader issues the pair's MMAs; the other CTA's MMA
+    // warp only takes part in the TMEM allocation)
     uint32_t stage = 0, phase = 0, qs = 0, qp = 0, tcount = 0;
-    while (true) {
+    while (!PAIR || rank == 0) {
       if (!mbar_wait(&ctl->qfull[qs], qp, wc)) break;
       const int w = ctl->q[qs];
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE, MX>(p, ctl, w);
+      const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
-      if (!mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)) break;
+      // (CTA pairs: released by both CTAs' epilogue warps)
+      if (!(PAIR ? mbar_wait_cluster(&ctl->tempty[buf], tph ^ 1, wc) : mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)))
+        break;
       tc_fence_after();
       const int bn = item_bn(p, it.type);
       const bool amn = a_mn_major<MODE>(p, it.type), bmn = b_mn_major<MODE>(p, it.type);
-      const uint32_t idesc = idesc_bf16(128, bn, amn ? 1 : 0, bmn ? 1 : 0);
+      const uint32_t idesc = PAIR ? idesc_bf16(256, 256, amn ? 1 : 0, bmn ? 1 : 0)
+                                  : idesc_bf16(128, bn, amn ? 1 : 0, bmn ? 1 : 0);
       const uint32_t d = tmem + buf * 256;
       const bool gathered = gathered_operand(p, it.type) != 0;
       bool ok = true;
@@ -1041,7 +1136,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           // the gather threads wrote part of this stage with cp.async: order
           // those writes before the tensor core's (async-proxy) reads
           if (gathered || MX) fence_proxy_async_shared();
-          const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBStage);
+          const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBSt);
           if constexpr (MX) {
             // stage scales into TMEM (columns 256 + 16 * stage): A at +0
             // (4 columns), B at +4 (4 columns per 128 N)
@@ -1062,16 +1157,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             for (int k16 = 0; k16 < 4; ++k16) {
               const uint64_t ad = amn ? sdesc_sw128(a0 + k16 * 2048, 8192, 1024) : sdesc_sw128(a0 + k16 * 32, 16, 1024);
               const uint64_t bd = bmn ? sdesc_sw128(b0 + k16 * 2048, 8192, 1024) : sdesc_sw128(b0 + k16 * 32, 16, 1024);
-              mma_bf16(d, ad, bd, idesc, (kk | k16) != 0 ? 1u : 0u);
+              if constexpr (PAIR)
+                mma_bf16_pair(d, ad, bd, idesc, (kk | k16) != 0 ? 1u : 0u);
+              else
+                mma_bf16(d, ad, bd, idesc, (kk | k16) != 0 ? 1u : 0u);
             }
           }
-          mma_commit(&ctl->empty[stage]);
+          // CTA pairs: releases the stage in both CTAs
+          if constexpr (PAIR)
+            mma_commit_pair(&ctl->empty[stage]);
+          else
+            mma_commit(&ctl->empty[stage]);
         }
         __syncwarp();
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == kSt) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(&ctl->tfull[buf]);
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mma_commit_pair(&ctl->tfull[buf]);
+        else
+          mma_commit(&ctl->tfull[buf]);
+      }
       __syncwarp();
       ++tcount;
     }
@@ -1082,13 +1189,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     uint8_t* stage_out = sOut + (warp - 2) * kOutStage;
     uint32_t qs = 0, qp = 0, tcount = 0;
     while (true) {
-      if (!mbar_wait(&ctl->qfull[qs], qp, wc)) break;
+      if (!(PAIR ? mbar_wait_cluster(&ctl->qfull[qs], qp, wc) : mbar_wait(&ctl->qfull[qs], qp, wc))) break;
       const int w = ctl->q[qs];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
+      if (lane == 0) {
+        // CTA pairs: every consumer releases the leader's queue slot
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(&ctl->qempty[qs], 0));
+        else
+          mbar_arrive(&ctl->qempty[qs]);
+      }
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
-      const Item it = decode<MODE, MX>(p, ctl, w);
+      const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();
@@ -1122,7 +1235,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+      if (lane == 0) {
+        // CTA pairs: the leader's MMA warp waits for both CTAs' epilogues
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(&ctl->tempty[buf], 0));
+        else
+          mbar_arrive(&ctl->tempty[buf]);
+      }
       if (MODE == GM_FWD_RING && it.type == GM_FWD1) {
         // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
         // read by TMA): each epilogue warp adds 1, so a tile is complete when
@@ -1141,8 +1260,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   tc_fence_before();
   __syncthreads();
+  // CTA pairs: neither CTA leaves (nor frees TMEM) while the other may
+  // still signal its barriers or run MMAs on its smem and TMEM
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
+  }
 }
 
 template <int MODE, bool MX>
@@ -1153,11 +1280,51 @@ cudaError_t launch_mode(const TmapSet& maps, const GemmParams& p, int grid, cuda
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(gemm_kernel<MODE, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(gemm_kernel<MODE, MX, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_kernel<MODE, MX><<<grid, kGemmThreads, smem, st>>>(maps, p);
+  gemm_kernel<MODE, MX, false><<<grid, kGemmThreads, smem, st>>>(maps, p);
+  return cudaGetLastError();
+}
+
+// Clusters of two CTAs.  The grid is the number of such clusters the device
+// holds at once (each CTA needs a whole SM's shared memory), so the
+// persistent CTAs are all resident.
+template <int MODE>
+cudaError_t launch_pair_mode(const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
+  const size_t smem = gemm_smem_bytes();
+  static int configured_device = -1;
+  static int pair_grid = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(gemm_kernel<MODE, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)(grid & ~1), 1, 1);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel<MODE, false, true>, &cfg);
+    if (e != cudaSuccess) return e;
+    pair_grid = 2 * clusters;
+    configured_device = dev;
+  }
+  const int g = (grid & ~1) < pair_grid ? (grid & ~1) : pair_grid;
+  if (g < 2) return cudaErrorNotSupported;
+  cfg.gridDim = dim3((unsigned)g, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, gemm_kernel<MODE, false, true>, maps, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1191,6 +1358,15 @@ cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, i
     case GM_WG13: return launch_mode<GM_WG13, true>(maps, p, grid, st);
     case GM_WG2: return launch_mode<GM_WG2, true>(maps, p, grid, st);
     case GM_FWD_RING: return launch_mode<GM_FWD_RING, true>(maps, p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
+  if (!p.wg_sorted || p.m_tiles % 2 != 0 || p.bn != 256) return cudaErrorInvalidValue;
+  switch (mode) {
+    case GM_WG13: return launch_pair_mode<GM_WG13>(maps, p, grid, st);
+    case GM_WG2: return launch_pair_mode<GM_WG2>(maps, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

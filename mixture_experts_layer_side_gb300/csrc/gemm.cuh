@@ -18,6 +18,8 @@ enum GemmMode : int {
 };
 
 constexpr int kStages = 4;
+constexpr int kPairStages = 6;      // CTA-pair launches: 16 KB of A + 16 KB of B per stage
+constexpr int kMaxStages = 6;
 constexpr int kAStage = 128 * 128;  // 128 rows x 128 bytes
 constexpr int kBStage = 256 * 128;  // up to 256 rows x 128 bytes
 constexpr int kQueue = 4;           // depth of the work-item queue in smem
@@ -91,5 +93,10 @@ struct GemmParams {
 size_t gemm_smem_bytes();
 cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
+// Weight-gradient GEMMs (GM_WG13 / GM_WG2, BF16, token-sorted operands, an
+// even number of 128-row M tiles, bn = 256) on clusters of two CTAs that
+// share each 256 x 256 tile through one cta_group::2 MMA.  Returns
+// cudaErrorNotSupported when the device cannot hold a cluster of two.
+cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace mok

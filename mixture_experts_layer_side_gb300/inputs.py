@@ -54,6 +54,8 @@ WORKLOADS = {
     "mid_mxfp8_zipf": (Shape(4096, 2048, 768, 64, 8), "zipf", "mxfp8"),
     "mid_mxfp8_hot": (Shape(4096, 2048, 768, 64, 8), "hot", "mxfp8"),
     "kimi": (Shape(16384, 7168, 2048, 384, 8), "uniform", "bf16"),
+    # few experts, long weight-gradient K loops (2,048 routed rows per expert)
+    "long_k": (Shape(16384, 7168, 2048, 16, 2), "uniform", "bf16"),
     "kimi_mxfp8": (Shape(16384, 7168, 2048, 384, 8), "uniform", "mxfp8"),
 }
 

@@ -87,7 +87,7 @@ def sampled_checks(shape, prec, inp, out, grads):
         assert torch.count_nonzero(grads[k].index_select(0, empty)).item() == 0, k
 
 
-@pytest.mark.parametrize("workload", ["dsv3", "mid", "mid_mxfp8_hot"])
+@pytest.mark.parametrize("workload", ["dsv3", "mid", "mid_mxfp8_hot", "long_k"])
 def test_full_size_sampled_parity(workload):
     require_gpu()
     shape, prec, inp, wq = setup(workload)

@@ -20,6 +20,9 @@ CASES = [
     # experts above 1,024 routed rows: long weight-gradient K loops
     ("long_k_a", (3000, 256, 128, 20, 2), "hot", 5),
     ("long_k_b", (4096, 256, 256, 20, 2), "hot", 6),
+    # at least 1,024 routed rows per expert: weight gradients on CTA pairs
+    ("pair_zipf", (4096, 256, 256, 8, 2), "zipf", 7),
+    ("pair_uniform", (8192, 512, 256, 8, 1), "uniform", 8),
 ]
 
 
@@ -92,3 +95,15 @@ def test_weight_gradient_gather_paths_are_bitwise_equal(shape, routing):
     _, _, g_fused = run_layer(shape, routing, 8, debug_flags=4)
     for k in ("dW1", "dW3", "dW2"):
         assert torch.equal(g_sorted[k], g_fused[k]), k
+
+
+@pytest.mark.parametrize("shape,routing", [((4096, 256, 256, 8, 2), "zipf"), ((8192, 512, 512, 6, 1), "uniform"),
+                                           ((8192, 256, 256, 4, 2), "zipf")])
+def test_weight_gradient_cta_pairs_match_single_cta(shape, routing):
+    """BF16 weight gradients on clusters of two CTAs (one cta_group::2 MMA per
+    256 x 256 tile) against one CTA per 128 x 256 tile: bitwise equal."""
+    require_gpu()
+    _, _, g_pair = run_layer(shape, routing, 9)
+    _, _, g_one = run_layer(shape, routing, 9, debug_flags=8)
+    for k in ("dW1", "dW3", "dW2"):
+        assert torch.equal(g_pair[k], g_one[k]), k
