@@ -56,6 +56,8 @@ def parse_args_from(argv):
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # diagnostic: the library's MOK_DEBUG_* bits (alternative launch paths)
+    ap.add_argument("--debug-flags", type=int, default=0)
     return ap.parse_args(argv)
 
 
@@ -282,6 +284,8 @@ def workload_config(args, shape, routing, prec, layer=None):
     if layer is not None:
         cfg["minibatch_rows"] = args.minibatch_rows or "two-wave default"
         cfg["ring_slots"] = args.ring_slots or 4
+        if args.debug_flags:
+            cfg["debug_flags"] = args.debug_flags
     return cfg
 
 
@@ -297,7 +301,7 @@ def run_mok(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = make_inputs(shape, routing, seed=1000 + rank, device=dev)
     layer = MoKLayer(shape, precision=prec, minibatch_rows=args.minibatch_rows, ring_slots=args.ring_slots,
-                     device=dev)
+                     debug_flags=args.debug_flags, device=dev)
     out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
     grads = layer.alloc_grads()
     stream = torch.cuda.current_stream()

@@ -2,6 +2,7 @@
 // launch sequence of each call.  Everything here runs on the host and only
 // enqueues work on the caller's stream.
 #include <math.h>
+#include <limits.h>
 #include <string.h>
 
 #include <atomic>
@@ -268,22 +269,38 @@ int gemm_grid(long items) {
   return (int)(items < sms ? items : sms);
 }
 
-// BF16 weight-gradient GEMM: on clusters of two CTAs (one 256 x 256 tile per
-// pair) when the operands are token-sorted copies, the tile counts allow it
-// and the experts' K loops are long (on average at least 1,024 routed rows
-// per expert: there the pair's halved operand traffic per SM lifts the MMA
-// rate by up to 1.3x; with short K loops the tiles are bound by their dW
-// stores and single CTAs, all SMs resident, are faster), else one CTA per
-// 128 x bn tile.
-cudaError_t launch_wgrad(int mode, const TmapSet& m, const GemmParams& q, int grid, const mok_shape& s,
-                         int debug_flags, cudaStream_t st) {
-  const bool long_k = (int64_t)s.T * s.k >= 1024 * (int64_t)s.E;
-  if (!(debug_flags & MOK_DEBUG_SINGLE_CTA_WGRAD) && long_k && q.wg_sorted && q.m_tiles % 2 == 0 &&
-      q.bn == 256) {
-    const cudaError_t e = launch_gemm_pair(mode, m, q, grid, st);
+// Experts with at least this many padded rows have their BF16 weight
+// gradients computed on CTA pairs (cta_group::2, one 256 x 256 tile per
+// pair): their long K loops are bound by operand delivery, which the pair
+// halves per SM.  Shorter experts' tiles are bound by their dW stores and
+// run on single CTAs, with all SMs resident.
+constexpr int kPairMinRows = 512;
+
+// BF16 weight-gradient GEMM of one mode: the long-K experts on CTA pairs,
+// then the others (and the empty experts' zeros) on single CTAs, when the
+// operands are token-sorted copies and the tile counts allow pairs; else
+// every expert on single CTAs.  Returns the number of launches in *n.
+cudaError_t launch_wgrad(int mode, const TmapSet& m, GemmParams q, int grid, int debug_flags, int light_counter,
+                         int* n, cudaStream_t st) {
+  *n = 0;
+  if (!(debug_flags & MOK_DEBUG_SINGLE_CTA_WGRAD) && q.wg_sorted && q.m_tiles % 2 == 0 && q.bn == 256) {
+    GemmParams qh = q;
+    qh.wg_rows_min = kPairMinRows;
+    qh.wg_rows_max = INT_MAX;
+    const cudaError_t e = launch_gemm_pair(mode, m, qh, grid, st);
+    if (e == cudaSuccess) {
+      q.wg_rows_min = 0;
+      q.wg_rows_max = kPairMinRows;
+      q.counter = light_counter;
+      *n = 2;
+      return launch_gemm(mode, m, q, grid, st);
+    }
     if (e != cudaErrorNotSupported) return e;
     (void)cudaGetLastError();
   }
+  q.wg_rows_min = 0;
+  q.wg_rows_max = INT_MAX;
+  *n = 1;
   return launch_gemm(mode, m, q, grid, st);
 }
 
@@ -299,6 +316,8 @@ void base_params(GemmParams& g, const mok_shape& s, const WsLayout& L, uint8_t* 
   g.pad_perm = reinterpret_cast<const int32_t*>(ws + L.pad_perm);
   g.padded_offsets = reinterpret_cast<const int32_t*>(ws + L.padded_offsets);
   g.counts = reinterpret_cast<const int32_t*>(ws + L.counts);
+  g.wg_rows_min = 0;
+  g.wg_rows_max = INT_MAX;
 }
 
 mok_status reset_counters(uint8_t* ws, const WsLayout& L, cudaStream_t st) {
@@ -407,8 +426,8 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     q.wg_sorted = 1;
     q.sfa_tiled = w + L.wsfa;
     q.sfb_tiled0 = w + L.wsfb;
-    q.dw0 = static_cast<__nv_bfloat16*>(dW1);
-    q.dw1 = static_cast<__nv_bfloat16*>(dW3);
+    q.dW1 = static_cast<__nv_bfloat16*>(dW1);
+    q.dW3 = static_cast<__nv_bfloat16*>(dW3);
     Phase ph(MOK_PHASE_BWD_WG13, st, 1);
     MOK_CUDA(launch_gemm_mx(GM_WG13, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
   }
@@ -433,7 +452,7 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     q.wg_sorted = 1;
     q.sfa_tiled = w + L.wsfb;
     q.sfb_tiled0 = w + L.wsfa;
-    q.dw0 = static_cast<__nv_bfloat16*>(dW2);
+    q.dW2 = static_cast<__nv_bfloat16*>(dW2);
     Phase ph(MOK_PHASE_BWD_WG2, st, 1);
     MOK_CUDA(launch_gemm_mx(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), st));
   }
@@ -723,10 +742,12 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.counter = 2;
     q.wg_sorted = sorted ? 1 : 0;
     q.gather_src = static_cast<const __nv_bfloat16*>(x);
-    q.dw0 = static_cast<__nv_bfloat16*>(dW1);
-    q.dw1 = static_cast<__nv_bfloat16*>(dW3);
-    Phase ph(MOK_PHASE_BWD_WG13, st, 1);
-    MOK_CUDA(launch_wgrad(GM_WG13, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), s, cfg->debug_flags, st));
+    q.dW1 = static_cast<__nv_bfloat16*>(dW1);
+    q.dW3 = static_cast<__nv_bfloat16*>(dW3);
+    Phase ph(MOK_PHASE_BWD_WG13, st, 0);
+    int n = 0;
+    MOK_CUDA(launch_wgrad(GM_WG13, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), cfg->debug_flags, 4, &n, st));
+    g_launches += n;
   }
   // dW2 = (s a)^T gather(dout), per expert
   {
@@ -746,9 +767,11 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.counter = 3;
     q.wg_sorted = sorted ? 1 : 0;
     q.gather_src = static_cast<const __nv_bfloat16*>(dout);
-    q.dw0 = static_cast<__nv_bfloat16*>(dW2);
-    Phase ph(MOK_PHASE_BWD_WG2, st, 1);
-    MOK_CUDA(launch_wgrad(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), s, cfg->debug_flags, st));
+    q.dW2 = static_cast<__nv_bfloat16*>(dW2);
+    Phase ph(MOK_PHASE_BWD_WG2, st, 0);
+    int n = 0;
+    MOK_CUDA(launch_wgrad(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), cfg->debug_flags, 5, &n, st));
+    g_launches += n;
   }
   return MOK_OK;
 }

@@ -50,9 +50,11 @@ struct Ctl {
   int abort;
   int po[kMaxExperts + 1];  // padded expert offsets (weight-gradient modes)
   // weight-gradient modes: experts by descending padded rows, each entry
-  // e | (K iterations << 10); the n_active experts with routed rows first
+  // e | (K iterations << 10); the n_nonempty experts with routed rows first
   int order[kMaxExperts];
-  int n_active;
+  int n_nonempty;
+  int n_skip;  // experts ahead of this launch's row range in that order
+  int n_sel;   // experts in this launch's row range (its items)
   int pair_rank;  // CTA-pair launches: 0 for the leader (issues the MMAs), 1 for the other
 };
 
@@ -141,10 +143,10 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     // (Empty experts' zero gradients are written outside the item list.)
     // CTA pairs take the M tiles two at a time: the leader the even one
     const int per_e = (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles;
-    const int total = ctl->n_active * per_e;
+    const int total = ctl->n_sel * per_e;
     const int pos = (w & 1) ? total - 1 - (w >> 1) : (w >> 1);
     const int rank = pos / per_e;
-    const int oe = ctl->order[rank];
+    const int oe = ctl->order[ctl->n_skip + rank];
     it.type = MODE;
     it.e = oe & 1023;
     const int r = pos - rank * per_e;
@@ -719,11 +721,11 @@ __device__ __forceinline__ void wgrad_emit64(const GemmParams& p, const Item& it
   long ld;
   if (it.type == GM_WG13) {
     // I is a multiple of 128, so a 64-column chunk never straddles dW1 | dW3
-    base = (col < p.I) ? p.dw0 + ((long)it.e * p.H + r0) * p.I + col
-                       : p.dw1 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
+    base = (col < p.I) ? p.dW1 + ((long)it.e * p.H + r0) * p.I + col
+                       : p.dW3 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
     ld = p.I;
   } else {
-    base = p.dw0 + ((long)it.e * p.I + r0) * p.H + col;
+    base = p.dW2 + ((long)it.e * p.I + r0) * p.H + col;
     ld = p.H;
   }
   store_chunk64_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
@@ -821,7 +823,7 @@ __device__ bool gather_item_k(const GemmParams& p, const Item& it, uint8_t* sA, 
 template <int MODE>
 __device__ void zero_empty_experts(const GemmParams& p, const Ctl* ctl, int gw, int lane) {
   constexpr long kChunk = 16384;  // bf16 elements per chunk
-  const int n_empty = p.E - ctl->n_active;
+  const int n_empty = p.E - ctl->n_nonempty;
   const long slab = (long)p.H * p.I;  // dW1_e, dW3_e: [H, I]; dW2_e: [I, H]
   const int per_expert = (MODE == GM_WG13) ? 2 : 1;
   const long chunks_per_slab = slab / kChunk;  // H and I are multiples of 128
@@ -829,8 +831,8 @@ __device__ void zero_empty_experts(const GemmParams& p, const Ctl* ctl, int gw, 
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   for (long c = (long)blockIdx.x * 4 + gw; c < total; c += (long)gridDim.x * 4) {
     const long sl = c / chunks_per_slab;
-    const int e = ctl->order[ctl->n_active + (int)(sl / per_expert)] & 1023;
-    __nv_bfloat16* base = (sl % per_expert) ? p.dw1 : p.dw0;
+    const int e = ctl->order[ctl->n_nonempty + (int)(sl / per_expert)] & 1023;
+    __nv_bfloat16* base = (MODE == GM_WG2) ? p.dW2 : (sl % per_expert) ? p.dW3 : p.dW1;
     uint4* dst = reinterpret_cast<uint4*>(base + (long)e * slab + (c - sl * chunks_per_slab) * kChunk);
 #pragma unroll 8
     for (int i = 0; i < (int)(kChunk * 2 / 16 / 32); ++i) __stcs(dst + i * 32 + lane, z);
@@ -893,7 +895,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       mbar_init(&ctl->qempty[i], queue_consumers);
     }
     ctl->abort = 0;
-    ctl->n_active = 0;
+    ctl->n_nonempty = 0;
+    ctl->n_skip = 0;
+    ctl->n_sel = 0;
     ctl->pair_rank = (int)rank;
     ctl->tmem_base = 0;  // a 512-column allocation always starts at column 0
     fence_mbar_init();
@@ -914,7 +918,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       }
       const int kit = MX ? ke / 128 : (p.counts[e] + 63) / 64;
       ctl->order[pos] = e | (kit << 10);
-      if (ke > 0) atomicAdd(&ctl->n_active, 1);
+      if (ke > 0) atomicAdd(&ctl->n_nonempty, 1);
+      if (ke >= p.wg_rows_max) atomicAdd(&ctl->n_skip, 1);
+      if (ke > 0 && ke >= p.wg_rows_min && ke < p.wg_rows_max) atomicAdd(&ctl->n_sel, 1);
     }
   }
   if (warp == 0 && lane == 0)
@@ -935,7 +941,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int num_items = kWgrad ? ctl->n_active * (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles
+  const int num_items = kWgrad ? ctl->n_sel * (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles
                                : count_items<MODE>(p);
 
   if (warp == 0) {
@@ -1103,7 +1109,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       // let this thread's copies land before the CTA can exit
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
-    if (kWgrad) zero_empty_experts<MODE>(p, ctl, warp - 6, lane);
+    if (kWgrad && p.wg_rows_min == 0) zero_empty_experts<MODE>(p, ctl, warp - 6, lane);
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     // (CTA pairs: the leader issues the pair's MMAs; the other CTA's MMA

@@ -60,8 +60,13 @@ struct GemmParams {
   float* dsp;              // [pad, n_tiles]
   const float* scores;     // [R]
   const __nv_bfloat16* gather_src;  // x (GEMM1, dW1|dW3) or dout (dA', dW2): [T, H]
-  __nv_bfloat16* dw0;      // dW1 (WG13) or dW2 (WG2)
-  __nv_bfloat16* dw1;      // dW3 (WG13)
+  __nv_bfloat16* dW1;      // weight-gradient outputs: dW1, dW3 (GM_WG13)
+  __nv_bfloat16* dW3;
+  __nv_bfloat16* dW2;      // dW2 (GM_WG2)
+  // weight-gradient launches: the experts whose padded rows lie in
+  // [wg_rows_min, wg_rows_max) are this launch's items; the launch with
+  // wg_rows_min = 0 also writes the empty experts' zero gradients
+  int wg_rows_min, wg_rows_max;
   int a_mn, b_mn;          // dense: operand major-ness (1 = M/N-major)
   int g1_tiles;            // ring: GEMM1 N tiles per M tile
   int debug_flags;
