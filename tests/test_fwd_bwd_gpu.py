@@ -23,6 +23,11 @@ CASES = [
     # at least 1,024 routed rows per expert: weight gradients on CTA pairs
     ("pair_zipf", (4096, 256, 256, 8, 2), "zipf", 7),
     ("pair_uniform", (8192, 512, 256, 8, 1), "uniform", 8),
+    # degenerate and limit cases: one token and one expert; the largest
+    # expert count (most experts empty); the largest top-k
+    ("single_token", (1, 128, 128, 1, 1), "uniform", 11),
+    ("max_experts", (512, 128, 128, 1024, 4), "uniform", 12),
+    ("max_topk", (64, 256, 128, 40, 32), "uniform", 13),
 ]
 
 
