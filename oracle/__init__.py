@@ -13,6 +13,7 @@ Modules
 ``moe``        schedule, forward and backward of the routed SwiGLU MoE layer
 ``mxfp8``      E4M3 / E8M0 block quantisation (32-element blocks)
 ``heuristics`` the two-wave minibatch floor
+``router``     top-k softmax router: selection, scores, logit and weight gradients
 
 Parity status (what pins each function, see ``tests/test_oracle.py``):
 
@@ -28,6 +29,11 @@ Parity status (what pins each function, see ``tests/test_oracle.py``):
                              tiny inputs, and identity on pre-quantised data.
 * ``heuristics``          -- the 2,368-token floor printed for the Kimi-2.5
                              shape (golden fixture).
+* ``router``              -- brute-force selection with ties, softmax special
+                             cases, float64 autograd, finite differences, and
+                             the layer's score gradient composed with the
+                             router backward against autograd of the whole
+                             routed network (``tests/test_oracle_router.py``).
 """
 
-from . import heuristics, moe, mxfp8  # noqa: F401
+from . import heuristics, moe, mxfp8, router  # noqa: F401
