@@ -386,6 +386,36 @@ def run_mok(args):
                                 attainable_frac=floor / per_phase[n]["ms"])
     sched_share = per_phase.get("schedule", {"ms": 0})["ms"] / ms
 
+    # ------------------------------------------------ router on either side of the layer (not in the metric)
+    router = None
+    if prec == "bf16":
+        from mixture_experts_layer_side_gb300.layer import MoKRouter
+        rt = MoKRouter(shape, device=dev)
+        g = torch.Generator(device=dev).manual_seed(77)
+        Wr = (0.05 * torch.randn((shape.H, shape.E), generator=g, device=dev)).to(torch.bfloat16)
+        rds = torch.randn((shape.T, shape.k), generator=g, device=dev)
+        ridx, rs = rt.forward(inp["x"], Wr)
+        for _ in range(3):
+            rt.forward(inp["x"], Wr)
+            rt.backward(inp["x"], Wr, ridx, rs, rds)
+        torch.cuda.synchronize()
+        rt.check()
+        _lib.mok_trace_enable(True)
+        for _ in range(args.steps):
+            rt.forward(inp["x"], Wr)
+            rt.backward(inp["x"], Wr, ridx, rs, rds)
+        torch.cuda.synchronize()
+        rph = _lib.mok_trace_read()
+        _lib.mok_trace_enable(False)
+        rt.check()
+        rf = 2.0 * shape.T * shape.H * shape.E
+        router = {}
+        for name, fl in (("router_fwd", rf), ("router_bwd", 2 * rf)):
+            ms_r = rph[name][0] / max(rph[name][1], 1)
+            router[name] = {"ms": ms_r, "tflops": fl / (ms_r / 1e3) / 1e12}
+        router["note"] = "logits GEMM + top-k softmax; logit gradient + dWr and dx GEMMs (outside the layer metric)"
+        del rt
+
     # ------------------------------------------------ end to end through the C ABI, host buffers
     e2e = None
     if not args.no_e2e:
@@ -449,6 +479,7 @@ def run_mok(args):
             "roofline": roofline,
             "phases": per_phase,
             "schedule_share": sched_share,
+            "router": router,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,

@@ -272,7 +272,9 @@ enum {
   MOK_PHASE_BWD_WG2 = 8,       /* dW2 grouped GEMM */
   MOK_PHASE_QUANT = 9,         /* MXFP8 quantisation of activations */
   MOK_PHASE_BWD_SORT = 10,     /* token-sorted copies of x and dout for the weight gradients */
-  MOK_NUM_PHASES = 11
+  MOK_PHASE_ROUTER_FWD = 11,   /* router: logits GEMM, top-k, softmax */
+  MOK_PHASE_ROUTER_BWD = 12,   /* router: logit gradient, dWr and dx GEMMs */
+  MOK_NUM_PHASES = 13
 };
 mok_status mok_trace_enable(int32_t on);
 mok_status mok_trace_read(float* ms /* [MOK_NUM_PHASES] */, int32_t* count /* [MOK_NUM_PHASES] */);
@@ -342,6 +344,41 @@ mok_status mok_build_schedule_noalloc(const mok_shape* shape, const int32_t* top
 mok_status mok_gemm_mxfp8(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, const uint8_t* Asf,
                           int32_t a_mn_major, const uint8_t* Bq, const uint8_t* Bsf, int32_t b_mn_major, float* C,
                           void* scratch, size_t scratch_bytes, void* stream);
+
+/*
+ * Router on either side of the layer.  The pages take the routing as the
+ * schedule's input ("Mixture-of-Kittens (MoK)", "Use the functional API") and
+ * compute the router weight gradients from the score gradient of the SwiGLU
+ * backward ("Cursor Open-Sources Mixture-of-Kittens (MoK)", the paragraph
+ * after "Three design decisions that matter"); these calls supply the plain
+ * top-k softmax router around that path:
+ *
+ *   logits L = x Wr                        (bf16 in, f32 accumulate)
+ *   topk_idx[t] = the k largest L[t] + bias (bias selects only; ties go to the
+ *                 lower expert; columns in descending key order)
+ *   scores[t, j] = softmax over j of L[t, topk_idx[t, j]]   (f32)
+ *
+ * and, from the layer's dscores (mok_backward):
+ *
+ *   dL[t, topk_idx[t, j]] = s_j (ds_j - sum_i s_i ds_i), zero elsewhere
+ *   dWr = x^T dL  (f32 [H, E]),   dx_router = dL Wr^T  (bf16 [T, H], the
+ *   router's share of the input gradient; the caller adds it to dX)
+ *
+ * Layout: x [T, H] bf16, Wr [H, E] bf16, bias [E] f32 or NULL, topk_idx
+ * [T, k] int32, scores and dscores [T, k] f32, logits [T, E] f32 (optional
+ * copy out, NULL to skip).  Requires k <= E <= 1024 and the shape rules of
+ * mok_forward.  `rws` is a caller-owned device workspace of
+ * mok_router_workspace_size bytes (its first word is an error word read by
+ * mok_check; each mok_router_forward clears it, as it starts a router step);
+ * the backward re-reads nothing of the forward but its outputs.
+ * Host errors return before any launch; the calls only enqueue on `stream`.
+ */
+size_t mok_router_workspace_size(const mok_shape* shape); /* 0 for an invalid shape */
+mok_status mok_router_forward(const mok_shape* shape, void* rws, size_t rws_bytes, const void* x, const void* Wr,
+                              const float* bias, int32_t* topk_idx, float* scores, float* logits, void* stream);
+mok_status mok_router_backward(const mok_shape* shape, void* rws, size_t rws_bytes, const void* x, const void* Wr,
+                               const int32_t* topk_idx, const float* scores, const float* dscores, float* dWr,
+                               void* dx_router, void* stream);
 
 /* Synchronise `stream`, then return (and clear) the status recorded in the
  * workspace's error word; MOK_OK if none. */

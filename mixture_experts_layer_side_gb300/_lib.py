@@ -30,10 +30,11 @@ STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_build_schedule", "mok_forward",
            "mok_backward", "mok_mxfp8_quantize", "mok_gather_rows", "mok_gemm_bf16", "mok_check",
            "mok_device_sm_count", "mok_status_string", "mok_version", "mok_trace_enable", "mok_trace_read",
-           "mok_launch_count", "mok_build_schedule_noalloc", "mok_gemm_mxfp8"]
+           "mok_launch_count", "mok_build_schedule_noalloc", "mok_gemm_mxfp8", "mok_router_workspace_size",
+           "mok_router_forward", "mok_router_backward"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
-          "bwd_wg2", "quant", "bwd_sort"]
+          "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd"]
 
 
 class MokError(RuntimeError):
@@ -95,6 +96,9 @@ def _load():
         "mok_launch_count": (ctypes.c_int64, []),
         "mok_build_schedule_noalloc": (i32, [S, P, ctypes.POINTER(MokScheduleBuffers), P]),
         "mok_gemm_mxfp8": (i32, [i32, i32, i32, P, P, i32, P, P, i32, P, P, sz, P]),
+        "mok_router_workspace_size": (sz, [S]),
+        "mok_router_forward": (i32, [S, P, sz, P, P, P, P, P, P, P]),
+        "mok_router_backward": (i32, [S, P, sz, P, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -188,6 +192,22 @@ def mok_mxfp8_quantize(src, block_axis, q, scale, stream=None):
     b, r, c = (src.shape if src.dim() == 3 else (1,) + tuple(src.shape))
     _ok(LIB.mok_mxfp8_quantize(_ptr(src), b, r, c, block_axis, _ptr(q), _ptr(scale), _stream(stream)),
         "mok_mxfp8_quantize")
+
+
+def mok_router_workspace_size(shape):
+    return LIB.mok_router_workspace_size(ctypes.byref(shape))
+
+
+def mok_router_forward(shape, rws, x, Wr, bias, topk_idx, scores, logits=None, stream=None):
+    _ok(LIB.mok_router_forward(ctypes.byref(shape), _ptr(rws), rws.numel() * rws.element_size(), _ptr(x), _ptr(Wr),
+                               _ptr(bias), _ptr(topk_idx), _ptr(scores), _ptr(logits), _stream(stream)),
+        "mok_router_forward")
+
+
+def mok_router_backward(shape, rws, x, Wr, topk_idx, scores, dscores, dWr, dx_router, stream=None):
+    _ok(LIB.mok_router_backward(ctypes.byref(shape), _ptr(rws), rws.numel() * rws.element_size(), _ptr(x), _ptr(Wr),
+                                _ptr(topk_idx), _ptr(scores), _ptr(dscores), _ptr(dWr), _ptr(dx_router),
+                                _stream(stream)), "mok_router_backward")
 
 
 def mok_gather_rows(shape, cfg, ws, x, xg, stream=None):

@@ -916,6 +916,138 @@ mok_status mok_gemm_mxfp8(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, co
   return MOK_OK;
 }
 
+// ------------------------------------------------------------------ router
+namespace {
+
+struct RouterLayout {
+  int Tpad, Epad;
+  size_t header, wpad, logits, dl, dwr, total;
+};
+
+RouterLayout router_layout(const mok_shape& s) {
+  RouterLayout r;
+  r.Tpad = (s.T + 127) / 128 * 128;
+  r.Epad = (s.E + 127) / 128 * 128;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  r.header = take(kHeaderWords * 4);
+  r.wpad = take((size_t)s.H * r.Epad * 2);
+  r.logits = take((size_t)r.Tpad * r.Epad * 4);
+  r.dl = take((size_t)r.Tpad * r.Epad * 2);
+  r.dwr = take((size_t)s.H * r.Epad * 4);
+  r.total = off;
+  return r;
+}
+
+mok_status check_router(const mok_shape* s) {
+  MOK_TRY(check_shape(s));
+  if (s->k > s->E) return MOK_ERR_INVALID_ARG;
+  return MOK_OK;
+}
+
+// N tile of a router GEMM: 128 columns when 256-column tiles would leave SMs
+// idle (the logits and dWr GEMMs have few output tiles: N is the expert
+// count).  A K-major B operand's tensor map box must be this many rows.
+int router_bn(int M, int N) {
+  return (N % 256 == 0 && (long)(M / 128) * (N / 256) >= device_sm_count()) ? 256 : 128;
+}
+
+// One tcgen05 GEMM of the router (GM_DENSE) on the router workspace.
+mok_status router_gemm(uint8_t* rw, const TmapSet& m, int M, int N, int K, int a_mn, int b_mn, float* out_f32,
+                       __nv_bfloat16* out_bf16, long ld_out, long m_valid, int counter, cudaStream_t st) {
+  GemmParams g;
+  memset(&g, 0, sizeof(g));
+  g.nmaps = 2;
+  g.bn = router_bn(M, N);
+  g.n_tiles = N / g.bn;
+  g.m_tiles = M / 128;
+  g.k_iters = K / 64;
+  g.hdr = reinterpret_cast<int32_t*>(rw);
+  g.counter = counter;
+  g.out_f32 = out_f32;
+  g.out_bf16 = out_bf16;
+  g.ld_out = ld_out;
+  g.m_valid = m_valid;
+  g.a_mn = a_mn;
+  g.b_mn = b_mn;
+  MOK_CUDA(launch_gemm(GM_DENSE, m, g, gemm_grid((long)g.m_tiles * g.n_tiles), st));
+  return MOK_OK;
+}
+
+}  // namespace
+
+size_t mok_router_workspace_size(const mok_shape* shape) {
+  if (check_router(shape) != MOK_OK) return 0;
+  return router_layout(*shape).total;
+}
+
+mok_status mok_router_forward(const mok_shape* shape, void* rws, size_t rws_bytes, const void* x, const void* Wr,
+                              const float* bias, int32_t* topk_idx, float* scores, float* logits, void* stream) {
+  MOK_TRY(check_router(shape));
+  if (!rws || !x || !Wr || !topk_idx || !scores) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  const RouterLayout R = router_layout(s);
+  if (rws_bytes < R.total) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* rw = static_cast<uint8_t*>(rws);
+  // a forward starts a router step: the whole header, error word included
+  // (as the layer's schedule call does)
+  MOK_CUDA(cudaMemsetAsync(rw, 0, kHeaderWords * 4, st));
+  __nv_bfloat16* wpad = reinterpret_cast<__nv_bfloat16*>(rw + R.wpad);
+  float* lg = reinterpret_cast<float*>(rw + R.logits);
+  Phase ph(MOK_PHASE_ROUTER_FWD, st, logits ? 4 : 3);
+  MOK_CUDA(launch_router_pad_weights(s.H, s.E, R.Epad, static_cast<const __nv_bfloat16*>(Wr), wpad, st));
+  // logits [Tpad, Epad] = x [T, H] Wr: A K-major (rows past T read as zero), B N-major
+  TmapSet m;
+  memset(&m, 0, sizeof(m));
+  if (!map2d(&m.m[0], x, s.H, s.T, 128) || !map2d(&m.m[1], wpad, R.Epad, s.H, 64)) return MOK_ERR_CUDA;
+  MOK_TRY(router_gemm(rw, m, R.Tpad, R.Epad, s.H, 0, 1, lg, nullptr, R.Epad, 0, 0, st));
+  MOK_CUDA(launch_router_topk(s.T, s.E, R.Epad, s.k, lg, bias, topk_idx, scores, st));
+  if (logits) MOK_CUDA(launch_router_take_cols(s.T, s.E, R.Epad, lg, logits, st));
+  return MOK_OK;
+}
+
+mok_status mok_router_backward(const mok_shape* shape, void* rws, size_t rws_bytes, const void* x, const void* Wr,
+                               const int32_t* topk_idx, const float* scores, const float* dscores, float* dWr,
+                               void* dx_router, void* stream) {
+  MOK_TRY(check_router(shape));
+  if (!rws || !x || !Wr || !topk_idx || !scores || !dscores || !dWr || !dx_router) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  const RouterLayout R = router_layout(s);
+  if (rws_bytes < R.total) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* rw = static_cast<uint8_t*>(rws);
+  MOK_CUDA(cudaMemsetAsync(rw + kHdrAbort * 4, 0, (kHdrCounters + kNumCounters - kHdrAbort) * 4, st));
+  __nv_bfloat16* wpad = reinterpret_cast<__nv_bfloat16*>(rw + R.wpad);
+  __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(rw + R.dl);
+  float* dwr = reinterpret_cast<float*>(rw + R.dwr);
+  Phase ph(MOK_PHASE_ROUTER_BWD, st, 5);
+  MOK_CUDA(launch_router_pad_weights(s.H, s.E, R.Epad, static_cast<const __nv_bfloat16*>(Wr), wpad, st));
+  MOK_CUDA(launch_router_logit_grad(s.T, R.Tpad, s.E, R.Epad, s.k, topk_idx, scores, dscores, dl, st));
+  // dWr [H, Epad] = x^T dL: A = x read M-major (rows past T read as zero), B = dL N-major
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map2d(&m.m[0], x, s.H, s.T, 64) || !map2d(&m.m[1], dl, R.Epad, R.Tpad, 64)) return MOK_ERR_CUDA;
+    MOK_TRY(router_gemm(rw, m, s.H, R.Epad, R.Tpad, 1, 1, dwr, nullptr, R.Epad, 0, 1, st));
+    MOK_CUDA(launch_router_take_cols(s.H, s.E, R.Epad, dwr, dWr, st));
+  }
+  // dx [T, H] = dL Wr^T: A = dL K-major, B = padded Wr K-major; bf16 rows < T
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    const int bn = router_bn(R.Tpad, s.H);
+    if (!map2d(&m.m[0], dl, R.Epad, R.Tpad, 128) || !map2d(&m.m[1], wpad, R.Epad, s.H, bn)) return MOK_ERR_CUDA;
+    MOK_TRY(router_gemm(rw, m, R.Tpad, s.H, R.Epad, 0, 0, nullptr, static_cast<__nv_bfloat16*>(dx_router), s.H,
+                        s.T, 2, st));
+  }
+  return MOK_OK;
+}
+
 mok_status mok_check(void* ws, void* stream) {
   if (!ws) return MOK_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

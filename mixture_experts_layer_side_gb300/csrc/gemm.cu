@@ -757,7 +757,27 @@ __device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, i
 }
 
 __device__ void epi_dense(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
-  float* dst = p.out_f32 + (long)(it.m * 128 + row) * p.ld_out + it.n * p.bn;
+  const long grow = (long)it.m * 128 + row;
+  if (p.out_bf16) {
+    // bf16 output of the first m_valid rows only (the TMEM loads are
+    // warp-wide, so every lane takes part in them)
+    __nv_bfloat16* dst = p.out_bf16 + grow * p.ld_out + it.n * p.bn;
+#pragma unroll 1
+    for (int c = 0; c < p.bn; c += 32) {
+      float v[32];
+      tmem_ld32(tbase + c, v);
+      if (grow < p.m_valid) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        uint4* d = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+    }
+    return;
+  }
+  float* dst = p.out_f32 + grow * p.ld_out + it.n * p.bn;
 #pragma unroll 1
   for (int c = 0; c < p.bn; c += 32) {
     float v[32];

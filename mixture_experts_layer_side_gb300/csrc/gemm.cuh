@@ -50,6 +50,8 @@ struct GemmParams {
   // epilogue operands
   float* out_f32;
   long ld_out;
+  __nv_bfloat16* out_bf16;  // dense: bf16 output instead, of the first m_valid rows
+  long m_valid;
   __nv_bfloat16* ctx_hu;   // [pad, 2I]
   __nv_bfloat16* ring;     // [ring_slots * ring_rows, I]
   int ring_rows, ring_slots;

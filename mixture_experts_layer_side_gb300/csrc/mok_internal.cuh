@@ -70,6 +70,14 @@ cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_
 cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
                                __nv_bfloat16* xg, cudaStream_t st);
 cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st);
+// Router (router.cu)
+cudaError_t launch_router_pad_weights(int H, int E, int Epad, const __nv_bfloat16* w, __nv_bfloat16* wp,
+                                      cudaStream_t st);
+cudaError_t launch_router_topk(int T, int E, int Epad, int k, const float* logits, const float* bias, int32_t* idx,
+                               float* scores, cudaStream_t st);
+cudaError_t launch_router_logit_grad(int T, int Tpad, int E, int Epad, int k, const int32_t* idx, const float* s,
+                                     const float* ds, __nv_bfloat16* dl, cudaStream_t st);
+cudaError_t launch_router_take_cols(int rows, int E, int Epad, const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_quant_rows_tiled(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
                                     uint8_t* q, uint8_t* sf, cudaStream_t st);
 cudaError_t launch_mxfp8_quantize(const __nv_bfloat16* src, int batch, int rows, int cols, int block_axis,

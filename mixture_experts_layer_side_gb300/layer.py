@@ -101,3 +101,38 @@ class MoKLayer:
                     padded_offsets=view(L["padded_offsets"], E + 1), perm=view(L["perm"], R),
                     inv_perm=view(L["inv_perm"], R), pad_perm=view(L["pad_perm"], L["pad_capacity"]),
                     pad_inv=view(L["pad_inv"], R), tile_expert=view(L["tile_expert"], L["tile_capacity"]))
+
+
+class MoKRouter:
+    """Owns the router workspace; forward gives the layer its routing
+    (top-k ids, softmax scores), backward turns the layer's score gradient
+    into router-weight and input gradients (mok_router_forward / _backward)."""
+
+    def __init__(self, shape: Shape, device="cuda"):
+        self.shape = shape
+        self.device = torch.device(device)
+        self.cshape = _lib.shape_of(shape.T, shape.H, shape.I, shape.E, shape.k)
+        n = _lib.mok_router_workspace_size(self.cshape)
+        if n == 0:
+            raise _lib.MokError(1, "mok_router_workspace_size")
+        self.ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+
+    def forward(self, x, Wr, bias=None, with_logits=False, stream=None):
+        s = self.shape
+        idx = torch.empty((s.T, s.k), dtype=torch.int32, device=self.device)
+        scores = torch.empty((s.T, s.k), dtype=torch.float32, device=self.device)
+        logits = torch.empty((s.T, s.E), dtype=torch.float32, device=self.device) if with_logits else None
+        _lib.mok_router_forward(self.cshape, self.ws, x, Wr, bias, idx, scores, logits, stream)
+        return (idx, scores, logits) if with_logits else (idx, scores)
+
+    def backward(self, x, Wr, idx, scores, dscores, stream=None):
+        s = self.shape
+        dWr = torch.empty((s.H, s.E), dtype=torch.float32, device=self.device)
+        dx = torch.empty((s.T, s.H), dtype=torch.bfloat16, device=self.device)
+        _lib.mok_router_backward(self.cshape, self.ws, x, Wr, idx, scores, dscores, dWr, dx, stream)
+        return dWr, dx
+
+    def check(self):
+        st = _lib.mok_check(self.ws)
+        if st != 0:
+            raise _lib.MokError(st, "router device status")

@@ -1,0 +1,124 @@
+"""The top-k softmax router through the C ABI against the float64 router
+oracle: logits, selection (decided on the GPU's own f32 keys, as the kernel
+decides), scores, the logit / weight / input gradients, the router composed
+with the layer, and a full-size DeepSeek-V3-shaped case."""
+
+import numpy as np
+import pytest
+import torch
+
+from _helpers import assert_bf16_close, np64, require_gpu, rel_errors
+from oracle import moe, router
+
+pytestmark = pytest.mark.gpu
+
+
+def make(T, H, E, k, seed, biased):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    Wr = (0.05 * torch.randn((H, E), generator=g)).to(torch.bfloat16)
+    bias = (0.5 * torch.randn(E, generator=g)).float() if biased else None
+    ds = torch.randn((T, k), generator=g).float()
+    return x, Wr, bias, ds
+
+
+def selection_on(logits32, bias, k):
+    """The oracle's selection on the kernel's keys: f32 logit + f32 bias."""
+    key = logits32 if bias is None else (logits32 + bias.numpy().astype(np.float32)[None, :]).astype(np.float32)
+    return router.topk_softmax(key.astype(np.float64), None, k)[0]
+
+
+def run_router(T, H, E, k, seed, biased):
+    from mixture_experts_layer_side_gb300.inputs import Shape
+    from mixture_experts_layer_side_gb300.layer import MoKRouter
+    x, Wr, bias, ds = make(T, H, E, k, seed, biased)
+    r = MoKRouter(Shape(T, H, 128, E, k))
+    xd, Wd, dsd = x.cuda(), Wr.cuda(), ds.cuda()
+    bd = bias.cuda() if bias is not None else None
+    idx, s, logits = r.forward(xd, Wd, bd, with_logits=True)
+    dWr, dx = r.backward(xd, Wd, idx, s, dsd)
+    r.check()
+    return (x, Wr, bias, ds), (idx.cpu().numpy(), s.cpu().numpy(), logits.cpu().numpy(), dWr.cpu().numpy(),
+                                dx.float().cpu().numpy())
+
+
+CASES = [(300, 256, 24, 4, False), (300, 256, 24, 4, True), (1, 128, 5, 1, False), (1000, 512, 256, 8, True),
+         (257, 384, 1024, 32, False), (129, 128, 130, 3, True)]
+
+
+@pytest.mark.parametrize("T,H,E,k,biased", CASES)
+def test_router_matches_oracle(T, H, E, k, biased):
+    require_gpu()
+    (x, Wr, bias, ds), (idx, s, logits, dWr, dx) = run_router(T, H, E, k, T + E + k, biased)
+    L_ref = np64(x) @ np64(Wr)
+    fro = rel_errors(logits, L_ref)[1]
+    assert fro < 1e-5, fro
+    # selection: bit-exact, decided on the kernel's own keys
+    np.testing.assert_array_equal(idx, selection_on(logits, bias, k))
+    # scores: softmax of the chosen logits
+    ch = np.take_along_axis(logits.astype(np.float64), idx.astype(np.int64), axis=1)
+    ez = np.exp(ch - ch.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(s, ez / ez.sum(axis=1, keepdims=True), rtol=2e-6, atol=1e-7)
+    # gradients (dL is rounded to bf16 for the tensor-core GEMMs)
+    _, dWr_ref, dx_ref = router.router_backward(np64(x), np64(Wr), idx, s, np64(ds))
+    assert_bf16_close(dWr, dWr_ref, "dWr")
+    assert_bf16_close(dx, dx_ref, "dx_router")
+
+
+def test_router_reruns_are_bitwise_identical():
+    require_gpu()
+    _, a = run_router(1000, 512, 256, 8, 3, True)
+    for _ in range(2):
+        _, b = run_router(1000, 512, 256, 8, 3, True)
+        for u, v in zip(a, b):
+            np.testing.assert_array_equal(u, v)
+
+
+def test_router_weight_gradient_through_the_layer():
+    """Router forward -> layer forward / backward -> router backward, against
+    the oracle chain (layer score gradient composed with the router
+    backward) on the same routing."""
+    require_gpu()
+    from mixture_experts_layer_side_gb300.inputs import Shape
+    from mixture_experts_layer_side_gb300.layer import MoKLayer, MoKRouter
+    T, H, I, E, k = 384, 256, 128, 12, 3
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    Wr = (0.05 * torch.randn((H, E), generator=g)).to(torch.bfloat16)
+    W1 = (0.02 * torch.randn((E, H, I), generator=g)).to(torch.bfloat16)
+    W3 = (0.02 * torch.randn((E, H, I), generator=g)).to(torch.bfloat16)
+    W2 = (0.02 * torch.randn((E, I, H), generator=g)).to(torch.bfloat16)
+    dout = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    S = Shape(T, H, I, E, k)
+    r, layer = MoKRouter(S), MoKLayer(S)
+    d = {n: t.cuda() for n, t in dict(x=x, Wr=Wr, W1=W1, W3=W3, W2=W2, dout=dout).items()}
+    idx, s = r.forward(d["x"], d["Wr"])
+    layer.build_schedule(idx)
+    layer.forward(d["x"], s, d["W1"], d["W3"], d["W2"])
+    grads = layer.backward(d["x"], s, d["W1"], d["W3"], d["W2"], d["dout"])
+    dWr, _ = r.backward(d["x"], d["Wr"], idx, s, grads["ds"])
+    layer.check()
+    r.check()
+    idx_n, s_n = idx.cpu().numpy(), s.cpu().numpy()
+    _, _, _, _, ds_ref = moe.backward(np64(x), idx_n, s_n, np64(W1), np64(W3), np64(W2), np64(dout))
+    _, dWr_ref, _ = router.router_backward(np64(x), np64(Wr), idx_n, s_n, ds_ref)
+    assert_bf16_close(dWr.cpu().numpy(), dWr_ref, "dWr through the layer")
+
+
+def test_router_full_size_dsv3_shape():
+    """T=8192, H=7168, E=256, top-8 with a selection bias: selection exact on
+    the kernel's keys, logits and scores on every token, dWr in full, dx on
+    sampled rows."""
+    require_gpu()
+    T, H, E, k = 8192, 7168, 256, 8
+    (x, Wr, bias, ds), (idx, s, logits, dWr, dx) = run_router(T, H, E, k, 5, True)
+    rows = np.arange(0, T, 97)
+    L_ref = np64(x[rows]) @ np64(Wr)
+    assert rel_errors(logits[rows], L_ref)[1] < 1e-5
+    np.testing.assert_array_equal(idx, selection_on(logits, bias, k))
+    ch = np.take_along_axis(logits.astype(np.float64), idx.astype(np.int64), axis=1)
+    ez = np.exp(ch - ch.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(s, ez / ez.sum(axis=1, keepdims=True), rtol=2e-6, atol=1e-7)
+    dL = router.logit_grad(idx, s, np64(ds), E)
+    assert_bf16_close(dWr, np64(x).T @ dL, "dWr")
+    assert_bf16_close(dx[rows], dL[rows] @ np64(Wr).T, "dx_router rows")
