@@ -58,6 +58,8 @@ def parse_args_from(argv):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # diagnostic: the library's MOK_DEBUG_* bits (alternative launch paths)
     ap.add_argument("--debug-flags", type=int, default=0)
+    # bounded-memory backward (forward context of ring_slots minibatches, GEMM1 recomputed)
+    ap.add_argument("--replay", action="store_true")
     return ap.parse_args(argv)
 
 
@@ -286,6 +288,8 @@ def workload_config(args, shape, routing, prec, layer=None):
         cfg["ring_slots"] = args.ring_slots or 4
         if args.debug_flags:
             cfg["debug_flags"] = args.debug_flags
+        cfg["replay"] = bool(args.replay)
+        cfg["ctx_bytes"] = int(layer.ctx.numel())
     return cfg
 
 
@@ -301,7 +305,7 @@ def run_mok(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = make_inputs(shape, routing, seed=1000 + rank, device=dev)
     layer = MoKLayer(shape, precision=prec, minibatch_rows=args.minibatch_rows, ring_slots=args.ring_slots,
-                     debug_flags=args.debug_flags, device=dev)
+                     debug_flags=args.debug_flags, replay=args.replay, device=dev)
     out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
     grads = layer.alloc_grads()
     stream = torch.cuda.current_stream()

@@ -100,6 +100,14 @@ typedef struct {
  *                 GEMMs run one CTA per 128-row tile instead of clusters of
  *                 two CTAs sharing a 256-row tile (cta_group::2).
  *                 Results are bitwise the same in every mode.
+ * replay          0: the forward context holds [h|u] of every routed row.
+ *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
+ *                 holds [h|u] of the last ring_slots minibatches only, in
+ *                 ring-slot order (mok_ctx_size shrinks to ring_slots *
+ *                 minibatch_rows rows), and the backward recomputes GEMM1
+ *                 for the earlier minibatches -- the pages' bounded-memory
+ *                 backward ([MTP] ring-token-buffer paragraph; [NOTE] §3).
+ *                 Recomputed values are bitwise those of the forward.
  */
 typedef struct {
   int32_t minibatch_rows;
@@ -107,6 +115,7 @@ typedef struct {
   float capacity_mult;
   int32_t comm_sms;
   int32_t debug_flags;
+  int32_t replay;
 } mok_config;
 
 #define MOK_DEBUG_SKIP_RING_SIGNAL 1
@@ -274,7 +283,8 @@ enum {
   MOK_PHASE_BWD_SORT = 10,     /* token-sorted copies of x and dout for the weight gradients */
   MOK_PHASE_ROUTER_FWD = 11,   /* router: logits GEMM, top-k, softmax */
   MOK_PHASE_ROUTER_BWD = 12,   /* router: logit gradient, dWr and dx GEMMs */
-  MOK_NUM_PHASES = 13
+  MOK_PHASE_BWD_REPLAY = 13,   /* bounded-memory backward: GEMM1 recomputed, context copied back */
+  MOK_NUM_PHASES = 14
 };
 mok_status mok_trace_enable(int32_t on);
 mok_status mok_trace_read(float* ms /* [MOK_NUM_PHASES] */, int32_t* count /* [MOK_NUM_PHASES] */);

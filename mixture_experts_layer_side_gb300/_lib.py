@@ -34,7 +34,7 @@ EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_bu
            "mok_router_forward", "mok_router_backward"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
-          "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd"]
+          "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd", "bwd_replay"]
 
 
 class MokError(RuntimeError):
@@ -50,7 +50,8 @@ class MokShape(ctypes.Structure):
 
 class MokConfig(ctypes.Structure):
     _fields_ = [("minibatch_rows", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
-                ("capacity_mult", ctypes.c_float), ("comm_sms", ctypes.c_int32), ("debug_flags", ctypes.c_int32)]
+                ("capacity_mult", ctypes.c_float), ("comm_sms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
+                ("replay", ctypes.c_int32)]
 
 
 class MokMx(ctypes.Structure):
@@ -135,8 +136,8 @@ def shape_of(T, H, I, E, k):
     return MokShape(T, H, I, E, k)
 
 
-def config(minibatch_rows=0, ring_slots=0, capacity_mult=0.0, comm_sms=0, debug_flags=0):
-    return MokConfig(minibatch_rows, ring_slots, capacity_mult, comm_sms, debug_flags)
+def config(minibatch_rows=0, ring_slots=0, capacity_mult=0.0, comm_sms=0, debug_flags=0, replay=0):
+    return MokConfig(minibatch_rows, ring_slots, capacity_mult, comm_sms, debug_flags, replay)
 
 
 def mx(q, scale):

@@ -5,6 +5,7 @@
 #include <limits.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -195,6 +196,7 @@ mok_status check_config(const mok_config* c) {
   if (c->minibatch_rows < 0) return MOK_ERR_INVALID_ARG;
   if (c->ring_slots < 0 || c->ring_slots == 1) return MOK_ERR_INVALID_ARG;
   if (!(c->capacity_mult == 0.0f || c->capacity_mult >= 1.0f)) return MOK_ERR_INVALID_ARG;
+  if (c->replay != 0 && c->replay != 1) return MOK_ERR_INVALID_ARG;
   return MOK_OK;
 }
 
@@ -482,6 +484,13 @@ size_t mok_ctx_size(const mok_shape* shape, const mok_config* cfg, mok_precision
   if (check_shape(shape) != MOK_OK || check_config(cfg) != MOK_OK) return 0;
   if (prec != MOK_BF16 && prec != MOK_MXFP8) return 0;
   const WsLayout L = ws_layout(*shape, *cfg, prec, device_sm_count());
+  if (cfg->replay) {
+    if (prec != MOK_BF16) return 0;
+    // ring-slot order: slot rows are below min(ring_slots * minibatch_rows,
+    // padded rows)
+    const int64_t rows = std::min<int64_t>((int64_t)L.ring_slots * L.minibatch_rows, L.pad_capacity);
+    return (size_t)rows * 2 * shape->I * 2;
+  }
   return (size_t)L.pad_capacity * 2 * shape->I * 2;
 }
 
@@ -524,6 +533,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   MOK_TRY(check_shape(shape));
   MOK_TRY(check_config(cfg));
   MOK_TRY(check_prec(prec));
+  if (cfg->replay && prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (!ws || !x || !scores || !W1 || !W3 || !W2 || !out || !ctx) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   const WsLayout L = ws_layout(s, *cfg, prec, device_sm_count());
@@ -585,6 +595,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   GemmParams g;
   base_params(g, s, L, w);
   g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
+  g.ctx_ring = cfg->replay;  // bounded context: [h|u] rows in ring-slot order
   g.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);
   g.ring_rows = M;
   g.ring_slots = S;
@@ -654,6 +665,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   MOK_TRY(check_shape(shape));
   MOK_TRY(check_config(cfg));
   MOK_TRY(check_prec(prec));
+  if (cfg->replay && prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (!ws || !ctx || !x || !scores || !W1 || !W3 || !W2 || !dout || !dX || !dW1 || !dW3 || !dW2 || !dscores)
     return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
@@ -679,6 +691,35 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   g.dsp = reinterpret_cast<float*>(w + L.dsp);
   g.scores = scores;
   g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
+
+  if (cfg->replay) {
+    // Bounded-memory backward: [h|u] of the minibatches the forward context
+    // no longer holds is recomputed by GEMM1 straight into the rows of
+    // dh|du, and the last ring_slots minibatches are copied there from the
+    // context; the dA' epilogue reads [h|u] there and overwrites it in place.
+    Phase ph(MOK_PHASE_BWD_REPLAY, st, 2);
+    MOK_CUDA(launch_replay_copy(s, L, w, static_cast<const __nv_bfloat16*>(ctx), g.dhu, st));
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map_gather(&m.m[0], x, s.H, s.T) || !map3d(&m.m[1], W1, s.I, s.H, s.E, 64) ||
+        !map3d(&m.m[2], W3, s.I, s.H, s.E, 64))
+      return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.ctx_hu = g.dhu;
+    q.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);  // a: scratch here
+    q.ring_rows = L.minibatch_rows;
+    q.ring_slots = L.ring_slots;
+    q.gather_src = static_cast<const __nv_bfloat16*>(x);
+    q.nmaps = 3;
+    q.bn = 256;
+    q.n_tiles = s.I / 128;
+    q.m_tile_begin = 0;
+    q.m_tile_end = (int)L.tile_capacity;
+    q.replay_keep = L.ring_slots;
+    q.counter = 6;
+    MOK_CUDA(launch_gemm(GM_FWD1, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    g.ctx_hu = g.dhu;
+  }
 
   // dA' = gather(dout) W2^T, SwiGLU backward + router-score partials
   {

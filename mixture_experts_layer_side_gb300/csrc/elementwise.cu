@@ -8,8 +8,12 @@
 //   ds_reduce   dL/ds[f] = sum over the N tiles of the SwiGLU-backward epilogue's
 //               per-tile partial dot products, in increasing tile order
 //   gather_rows standalone dispatch copy xg[padded row] = x[token]
+//   replay_copy bounded-memory backward: the forward context's last ring
+//               slots of [h|u] back to their routed rows
 // Each thread moves 16-byte vectors; consecutive threads take consecutive
 // vectors of a row, so every warp access is coalesced.
+#include <algorithm>
+
 #include "mok_internal.cuh"
 
 namespace mok {
@@ -102,6 +106,26 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, c
   }
 }
 
+// Bounded-memory backward: the [h|u] rows of the last `slots` minibatches,
+// kept by the forward in ring-slot order, copied to their routed-row places
+// in dh|du (the dA' epilogue then reads and overwrites them in place).
+__global__ void __launch_bounds__(256) replay_copy_kernel(int I, int M, int slots, const int32_t* __restrict__ hdr,
+                                                          const __nv_bfloat16* __restrict__ ctx_ring,
+                                                          __nv_bfloat16* __restrict__ dhu) {
+  const int used = hdr[kHdrPaddedRows];
+  const int nb = (used + M - 1) / M;
+  const long row0 = (long)max(nb - slots, 0) * M;
+  const int vec = 2 * I / 8;
+  const long n = (used - row0) * vec;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const long r = row0 + i / vec;
+    const int c = (int)(i % vec);
+    const long mb = r / M;
+    const long src = (mb % slots) * M + (r - mb * M);
+    reinterpret_cast<uint4*>(dhu + r * 2 * I)[c] = reinterpret_cast<const uint4*>(ctx_ring + src * 2 * I)[c];
+  }
+}
+
 int grid_for(long items, int threads) {
   const int sms = device_sm_count();
   long blocks = (items + threads - 1) / threads;
@@ -112,6 +136,15 @@ int grid_for(long items, int threads) {
 }
 
 }  // namespace
+
+cudaError_t launch_replay_copy(const mok_shape& s, const WsLayout& L, const uint8_t* ws,
+                               const __nv_bfloat16* ctx_ring, __nv_bfloat16* dhu, cudaStream_t st) {
+  const long items = (long)std::min<int64_t>((int64_t)L.ring_slots * L.minibatch_rows, L.pad_capacity) * (2 * s.I / 8);
+  replay_copy_kernel<<<grid_for(items, 256), 256, 0, st>>>(s.I, L.minibatch_rows, L.ring_slots,
+                                                           reinterpret_cast<const int32_t*>(ws + L.header), ctx_ring,
+                                                           dhu);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* yk,
                            const float* scores, __nv_bfloat16* out, cudaStream_t st) {

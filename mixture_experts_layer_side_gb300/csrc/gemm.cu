@@ -80,7 +80,14 @@ __device__ int count_items(const GemmParams& p) {
   } else if constexpr (MODE == GM_FWD_RING) {
     return used_tiles(p) * (p.g1_tiles + p.n_tiles);
   } else {
-    const int end = min(p.m_tile_end, used_tiles(p));
+    int end = min(p.m_tile_end, used_tiles(p));
+    if (p.replay_keep > 0) {
+      // GEMM1 recomputed in the backward: every minibatch but the last
+      // replay_keep, whose [h|u] the bounded forward context still holds
+      const int Mt = p.ring_rows / kTileRows;
+      const int nb = (used_tiles(p) + Mt - 1) / Mt;
+      end = min(end, max(nb - p.replay_keep, 0) * Mt);
+    }
     return max(end - p.m_tile_begin, 0) * p.n_tiles;
   }
 }
@@ -507,7 +514,8 @@ __device__ __forceinline__ float sigmoidf_(float h) { return 1.0f / (1.0f + __ex
 __device__ void epi_fwd1(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
   const long prow = (long)it.row0 + row;
   const int i0 = it.n * 128;
-  __nv_bfloat16* hrow = p.ctx_hu + prow * 2 * p.I + i0;
+  const long crow = p.ctx_ring ? (long)ring_row(p, (int)prow) : prow;
+  __nv_bfloat16* hrow = p.ctx_hu + crow * 2 * p.I + i0;
   __nv_bfloat16* urow = hrow + p.I;
   __nv_bfloat16* arow = p.ring + (long)ring_row(p, (int)prow) * p.I + i0;
 #pragma unroll 1

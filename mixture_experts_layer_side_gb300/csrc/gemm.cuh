@@ -53,6 +53,8 @@ struct GemmParams {
   __nv_bfloat16* out_bf16;  // dense: bf16 output instead, of the first m_valid rows
   long m_valid;
   __nv_bfloat16* ctx_hu;   // [pad, 2I]
+  int ctx_ring;            // GEMM1: [h|u] rows in ring-slot order (bounded-memory forward)
+  int replay_keep;         // GEMM1 launch: stop before the last replay_keep minibatches
   __nv_bfloat16* ring;     // [ring_slots * ring_rows, I]
   int ring_rows, ring_slots;
   uint32_t* ring_flags;    // [2 * tile_capacity]

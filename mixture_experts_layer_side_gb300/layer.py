@@ -19,10 +19,11 @@ PRECISIONS = {"bf16": _lib.MOK_BF16, "mxfp8": _lib.MOK_MXFP8}
 
 class MoKLayer:
     def __init__(self, shape: Shape, precision="bf16", minibatch_rows=0, ring_slots=0, debug_flags=0,
-                 device="cuda"):
+                 replay=False, device="cuda"):
         self.shape = shape
         self.cshape = _lib.shape_of(shape.T, shape.H, shape.I, shape.E, shape.k)
-        self.cfg = _lib.config(minibatch_rows=minibatch_rows, ring_slots=ring_slots, debug_flags=debug_flags)
+        self.cfg = _lib.config(minibatch_rows=minibatch_rows, ring_slots=ring_slots, debug_flags=debug_flags,
+                               replay=int(bool(replay)))
         self.prec = PRECISIONS[precision]
         self.device = torch.device(device)
         ws_bytes = _lib.mok_workspace_size(self.cshape, self.cfg, self.prec)

@@ -94,3 +94,25 @@ def test_workspace_layout_is_consistent(lib):
                              "pad_inv", "tile_expert")]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lib.mok_workspace_size(shape, lib.config()) > lay["tile_expert"]
+
+
+def test_bounded_context_size_and_checks(lib):
+    """replay = 1: the forward context holds ring_slots minibatches of [h|u]
+    (bf16, 2I columns); MXFP8 calls with it are refused on the host."""
+    L = lib.LIB
+    shape = lib.shape_of(4096, 256, 128, 16, 4)
+    plain = lib.config(minibatch_rows=128, ring_slots=2)
+    bounded = lib.config(minibatch_rows=128, ring_slots=2, replay=1)
+    pad = lib.mok_workspace_layout(shape, plain)["pad_capacity"]
+    assert lib.mok_ctx_size(shape, plain) == pad * 2 * 128 * 2
+    assert lib.mok_ctx_size(shape, bounded) == 2 * 128 * 2 * 128 * 2
+    # a ring larger than the padded rows: no more than the padded rows
+    big = lib.config(minibatch_rows=8192, ring_slots=4, replay=1)
+    assert lib.mok_ctx_size(shape, big) == pad * 2 * 128 * 2
+    assert lib.mok_ctx_size(shape, bounded, lib.MOK_MXFP8) == 0
+    assert lib.mok_ctx_size(shape, lib.config(replay=2)) == 0
+    fake = ctypes.c_void_p(256)
+    S, C = ctypes.byref(shape), ctypes.byref(bounded)
+    assert L.mok_forward(S, C, lib.MOK_MXFP8, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, None) == 2
+    assert L.mok_backward(S, C, lib.MOK_MXFP8, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                          fake, fake, fake, None) == 2
