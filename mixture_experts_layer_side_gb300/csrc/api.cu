@@ -369,8 +369,13 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     q.gq_src = w + L.xq;
     q.sfa_rows = w + L.xsf;
     q.sfa_ld = s.H / 32;
-    q.sfb_rows0 = q2.scale;
-    q.sfb_ld = s.H / 32;
+    // W2's scales (along H) tiled for the TMA producer, in the region the
+    // forward uses for its own W2 scales
+    {
+      Phase ph(MOK_PHASE_QUANT, st, 1);
+      MOK_CUDA(launch_tile_scales_rows(q2.scale, s.E, s.I, s.H / 32, w + L.wsf2, st));
+    }
+    q.sfb_tiled0 = w + L.wsf2;
     q.dhu_q = w + L.dhuq;
     q.dhu_sf = w + L.dhusf;
     {
@@ -396,9 +401,14 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     q.counter = 1;
     q.sfa_rows = w + L.dhusf;
     q.sfa_ld = 2 * s.I / 32;
-    q.sfb_rows0 = q1.scale;
-    q.sfb_rows1 = q3.scale;
-    q.sfb_ld = s.I / 32;
+    // W1's and W3's scales (along I) tiled for the TMA producer
+    {
+      Phase ph(MOK_PHASE_QUANT, st, 2);
+      MOK_CUDA(launch_tile_scales_rows(q1.scale, s.E, s.H, s.I / 32, w + L.wsf1, st));
+      MOK_CUDA(launch_tile_scales_rows(q3.scale, s.E, s.H, s.I / 32, w + L.wsf3, st));
+    }
+    q.sfb_tiled0 = w + L.wsf1;
+    q.sfb_tiled1 = w + L.wsf3;
     {
       Phase ph(MOK_PHASE_BWD_DX, st, 1);
       MOK_CUDA(launch_gemm_mx(GM_BWD_DX, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));

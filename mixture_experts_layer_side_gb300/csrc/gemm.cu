@@ -347,8 +347,8 @@ __device__ __forceinline__ uint32_t mx_stage_bytes(const GemmParams& p, int type
     case GM_DENSE: return kAStage + bn * 128 + (p.a_mn ? 512u : 0u) + (p.b_mn ? 512u * bchunks : 0u);
     case GM_FWD1: return 2u * 16384u + 1024u;
     case GM_FWD2: return kAStage + bn * 128 + 512u * bchunks;
-    case GM_BWD_DA: return bn * 128;
-    case GM_BWD_DX: return kAStage + bn * 128;
+    case GM_BWD_DA: return bn * 128 + 512u * bchunks;
+    case GM_BWD_DX: return kAStage + bn * 128 + 512u * bchunks;
     case GM_WG13: return kAStage + 2u * 16384u + 512u + 1024u;
     default: return kAStage + bn * 128 + 512u + 512u * bchunks;  // GM_WG2
   }
@@ -392,14 +392,22 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
       bulk_load(sfb + c * 512, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * 512, 512, bar);
     }
   } else if (type == GM_BWD_DA) {
+    // B = W2 along H (K-major); its scales pre-tiled per 128 rows x 128 K
     tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
+    for (int c = 0; c < bn / 128; ++c) {
+      const long blk = ((long)it.e * (p.I / 128) + it.n * (bn / 128) + c) * (p.H / 128) + kk;
+      bulk_load(sfb + c * 512, p.sfb_tiled0 + blk * 512, 512, bar);
+    }
   } else if (type == GM_BWD_DX) {
+    // B = W1 then W3 along I (K-major); scales pre-tiled likewise
     tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
     const int ki = p.I / 128;
-    if (kk < ki)
-      tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
-    else
-      tma_load_3d(b, &mp.m[2], bar, (kk - ki) * 128, it.n * bn, it.e);
+    const int kb = kk < ki ? kk : kk - ki;
+    tma_load_3d(b, &mp.m[kk < ki ? 1 : 2], bar, kb * 128, it.n * bn, it.e);
+    for (int c = 0; c < bn / 128; ++c) {
+      const long blk = ((long)it.e * (p.H / 128) + it.n * (bn / 128) + c) * ki + kb;
+      bulk_load(sfb + c * 512, (kk < ki ? p.sfb_tiled0 : p.sfb_tiled1) + blk * 512, 512, bar);
+    }
   } else if (type == GM_WG13 || type == GM_WG2) {
     // token-sorted operands quantised along the routed rows (K), M/N-major
     const int cols_a = (type == GM_WG13) ? p.H : p.I;
@@ -448,20 +456,13 @@ __device__ __forceinline__ void gather_stage_mx(const GemmParams& p, const Item&
     sa = p.sfa_rows + ((long)it.row0 + gt) * p.sfa_ld + kk * 4;
   }
   if (sa) cp_async_4(smem_u32(sfa + mx_sf_offset(gt, 0)), sa, (gather_a && tok_row < 0) ? 0u : 4u);
-  // scales of K-major B, rows gt and gt + 128 of the N tile
+  // scales of K-major B, rows gt and gt + 128 of the N tile (dense launches;
+  // the weights' scales of dA' and dX come pre-tiled with the TMA loads)
   const uint8_t* sb = nullptr;
   long brow0 = 0;
-  int kb = kk;
+  const int kb = kk;
   if (MODE == GM_DENSE) {
     if (!p.b_mn) { sb = p.sfb_rows0; brow0 = (long)it.n * bn; }
-  } else if (type == GM_BWD_DA) {
-    sb = p.sfb_rows0;
-    brow0 = (long)it.e * p.I + (long)it.n * bn;
-  } else if (type == GM_BWD_DX) {
-    const int ki = p.I / 128;
-    sb = kk < ki ? p.sfb_rows0 : p.sfb_rows1;
-    kb = kk < ki ? kk : kk - ki;
-    brow0 = (long)it.e * p.H + (long)it.n * bn;
   }
   if (sb) {
     for (int nl = gt; nl < bn; nl += 128)

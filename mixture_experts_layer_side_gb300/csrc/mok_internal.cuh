@@ -70,6 +70,8 @@ cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_
 cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
                                __nv_bfloat16* xg, cudaStream_t st);
 cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st);
+cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_count, uint8_t* out,
+                                    cudaStream_t st);
 cudaError_t launch_replay_copy(const mok_shape& s, const WsLayout& L, const uint8_t* ws,
                                const __nv_bfloat16* ctx_ring, __nv_bfloat16* dhu, cudaStream_t st);
 // Router (router.cu)

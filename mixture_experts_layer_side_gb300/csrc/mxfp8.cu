@@ -109,6 +109,24 @@ __global__ void tile_scales_kernel(const uint8_t* __restrict__ sf, int batch, in
   }
 }
 
+// Plain scales of a K-major operand [batch][N][K/32] (blocks along each
+// row) -> the same tiled [batch][N/128][K/128][512 B] layout: the four
+// scale bytes of (n, 128-wide K group) are contiguous in the source.
+__global__ void tile_scales_rows_kernel(const uint8_t* __restrict__ sf, int batch, int N, int kb_count,
+                                        uint8_t* __restrict__ out) {
+  const int kg_count = kb_count / 4;
+  const long n_words = (long)batch * N * kg_count;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n_words; i += (long)gridDim.x * blockDim.x) {
+    const int kg = (int)(i % kg_count);
+    const long bn = i / kg_count;
+    const int n = (int)(bn % N);
+    const long b = bn / N;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(sf + bn * kb_count + (long)kg * 4);
+    uint8_t* blk = out + ((b * (N / 128) + n / 128) * kg_count + kg) * 512;
+    *reinterpret_cast<uint32_t*>(blk + sf_block_offset(n & 127, 0)) = w;
+  }
+}
+
 // Quantise bf16 [rows_cap, C] along the rows (blocks of 32 rows) for the rows
 // in use (header word), codes [rows, C] and tiled scales
 // [rows/128][C/128][512 B] (scale of (row block, column) at
@@ -149,6 +167,16 @@ cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N
   const long cap = (long)device_sm_count() * 32;
   if (grid > cap) grid = cap;
   tile_scales_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, kb_count, N, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_count, uint8_t* out,
+                                    cudaStream_t st) {
+  const long words = (long)batch * N * (kb_count / 4);
+  long grid = (words + 255) / 256;
+  const long cap = (long)device_sm_count() * 32;
+  if (grid > cap) grid = cap;
+  tile_scales_rows_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, N, kb_count, out);
   return cudaGetLastError();
 }
 
