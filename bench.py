@@ -423,39 +423,66 @@ def run_mok(args):
     # ------------------------------------------------ end to end through the C ABI, host buffers
     e2e = None
     if not args.no_e2e:
-        hx = inp["x"].cpu().pin_memory()
-        hidx = inp["idx"].cpu().pin_memory()
-        hs = inp["s"].cpu().pin_memory()
-        hd = inp["dout"].cpu().pin_memory()
-        dx_, didx, ds_, dd = (torch.empty_like(inp[n]) for n in ("x", "idx", "s", "dout"))
+        # Every step's inputs come from pinned host memory and its results (out,
+        # dX, ds) go back to it.  Two device buffer sets let step i+1's
+        # inputs arrive, and step i-1's results leave, on copy streams while
+        # step i computes -- what a training loop feeding the layer does.
+        host = {n: inp[n].cpu().pin_memory() for n in ("x", "idx", "s", "dout")}
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hdX = torch.empty(grads["dX"].shape, dtype=torch.bfloat16).pin_memory()
         hds = torch.empty(grads["ds"].shape, dtype=torch.float32).pin_memory()
-
-        def e2e_step():
-            dx_.copy_(hx, non_blocking=True)
-            didx.copy_(hidx, non_blocking=True)
-            ds_.copy_(hs, non_blocking=True)
-            dd.copy_(hd, non_blocking=True)
-            step(dx_, didx, ds_, dd)
-            hout.copy_(out, non_blocking=True)
-            hdX.copy_(grads["dX"], non_blocking=True)
-            hds.copy_(grads["ds"], non_blocking=True)
-
+        h2d_st, d2h_st = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        sets = []
         for _ in range(2):
-            e2e_step()
+            b = {n: torch.empty_like(inp[n]) for n in host}
+            b["out"] = torch.empty_like(out)
+            b["grads"] = dict(grads, dX=torch.empty_like(grads["dX"]), ds=torch.empty_like(grads["ds"]))
+            b["loaded"], b["computed"], b["drained"] = (torch.cuda.Event() for _ in range(3))
+            sets.append(b)
+
+        def load(i):
+            b = sets[i % 2]
+            with torch.cuda.stream(h2d_st):
+                h2d_st.wait_event(b["drained"])  # the set's previous results have left
+                for n in host:
+                    b[n].copy_(host[n], non_blocking=True)
+                b["loaded"].record(h2d_st)
+
+        def e2e_steps(n):
+            go = torch.cuda.Event()
+            go.record(stream)
+            h2d_st.wait_event(go)
+            load(0)
+            for i in range(n):
+                b = sets[i % 2]
+                if i + 1 < n:
+                    load(i + 1)
+                stream.wait_event(b["loaded"])
+                layer.build_schedule(b["idx"])
+                layer.forward(b["x"], b["s"], *w_fwd, out=b["out"])
+                layer.backward(b["x"], b["s"], *w_bwd, b["dout"], grads=b["grads"])
+                b["computed"].record(stream)
+                with torch.cuda.stream(d2h_st):
+                    d2h_st.wait_event(b["computed"])
+                    hout.copy_(b["out"], non_blocking=True)
+                    hdX.copy_(b["grads"]["dX"], non_blocking=True)
+                    hds.copy_(b["grads"]["ds"], non_blocking=True)
+                    b["drained"].record(d2h_st)
+            for b in sets:
+                stream.wait_event(b["drained"])
+
+        e2e_steps(2)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_steps(args.steps)
         e1.record(stream)
         torch.cuda.synchronize()
         layer.check()
         ems = max_over_ranks(world, e0.elapsed_time(e1) / args.steps)
-        h2d = sum(t.numel() * t.element_size() for t in (hx, hidx, hs, hd))
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in (hout, hdX, hds))
         e2e = {"value": job_tflops(world, fps, ems), "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
