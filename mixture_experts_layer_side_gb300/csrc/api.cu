@@ -122,6 +122,7 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
     L.wsf2 = take((size_t)s.E * I * H / 32);
     L.dhuq = take(P * 2 * I);
     L.dhusf = take(P * (2 * I / 32));
+    L.sfa_rows_t = take(P * (std::max(H, 2 * I) / 32));
     L.wqa = take(P * H);
     L.wsfa = take(P * H / 32);
     L.wqb = take(P * 2 * I);
@@ -367,14 +368,16 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 0;
     q.gq_src = w + L.xq;
-    q.sfa_rows = w + L.xsf;
-    q.sfa_ld = s.H / 32;
-    // W2's scales (along H) tiled for the TMA producer, in the region the
-    // forward uses for its own W2 scales
+    // dout's scales in padded-row order and W2's scales (along H, in the
+    // region the forward uses for its own W2 scales), tiled for the TMA
+    // producer
     {
-      Phase ph(MOK_PHASE_QUANT, st, 1);
+      Phase ph(MOK_PHASE_QUANT, st, 2);
+      MOK_CUDA(launch_tile_row_scales(w + L.xsf, s.H / 32, reinterpret_cast<const int32_t*>(w + L.pad_perm), s.k,
+                                      rows_used, L.pad_capacity, w + L.sfa_rows_t, st));
       MOK_CUDA(launch_tile_scales_rows(q2.scale, s.E, s.I, s.H / 32, w + L.wsf2, st));
     }
+    q.sfa_tiled = w + L.sfa_rows_t;
     q.sfb_tiled0 = w + L.wsf2;
     q.dhu_q = w + L.dhuq;
     q.dhu_sf = w + L.dhusf;
@@ -399,14 +402,16 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     q.m_tile_begin = 0;
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 1;
-    q.sfa_rows = w + L.dhusf;
-    q.sfa_ld = 2 * s.I / 32;
-    // W1's and W3's scales (along I) tiled for the TMA producer
+    // dh|du's scales (padded rows already) and W1's and W3's scales (along
+    // I), tiled for the TMA producer
     {
-      Phase ph(MOK_PHASE_QUANT, st, 2);
+      Phase ph(MOK_PHASE_QUANT, st, 3);
+      MOK_CUDA(launch_tile_row_scales(w + L.dhusf, 2 * s.I / 32, nullptr, 1, rows_used, L.pad_capacity,
+                                      w + L.sfa_rows_t, st));
       MOK_CUDA(launch_tile_scales_rows(q1.scale, s.E, s.H, s.I / 32, w + L.wsf1, st));
       MOK_CUDA(launch_tile_scales_rows(q3.scale, s.E, s.H, s.I / 32, w + L.wsf3, st));
     }
+    q.sfa_tiled = w + L.sfa_rows_t;
     q.sfb_tiled0 = w + L.wsf1;
     q.sfb_tiled1 = w + L.wsf3;
     {
@@ -566,6 +571,13 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       MOK_CUDA(launch_tile_scales(q3.scale, s.E, s.H / 32, s.I, w + L.wsf3, st));
       MOK_CUDA(launch_tile_scales(q2.scale, s.E, s.I / 32, s.H, w + L.wsf2, st));
     }
+    {
+      // x's scales in padded-row order, tiled for the TMA producer (GEMM1 A)
+      Phase ph(MOK_PHASE_QUANT, st, 1);
+      MOK_CUDA(launch_tile_row_scales(w + L.xsf, s.H / 32, reinterpret_cast<const int32_t*>(w + L.pad_perm), s.k,
+                                      reinterpret_cast<const int32_t*>(w + L.header) + kHdrPaddedRows,
+                                      L.pad_capacity, w + L.sfa_rows_t, st));
+    }
     GemmParams g;
     base_params(g, s, L, w);
     g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
@@ -577,8 +589,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
     g.debug_flags = cfg->debug_flags;
     g.gq_src = w + L.xq;
-    g.sfa_rows = w + L.xsf;
-    g.sfa_ld = s.H / 32;
+    g.sfa_tiled = w + L.sfa_rows_t;
     g.sfb_tiled0 = w + L.wsf1;
     g.sfb_tiled1 = w + L.wsf3;
     g.sfb_tiled2 = w + L.wsf2;

@@ -345,10 +345,10 @@ __device__ __forceinline__ uint32_t mx_stage_bytes(const GemmParams& p, int type
   const uint32_t bchunks = (uint32_t)bn / 128;
   switch (MODE == GM_DENSE ? GM_DENSE : type) {
     case GM_DENSE: return kAStage + bn * 128 + (p.a_mn ? 512u : 0u) + (p.b_mn ? 512u * bchunks : 0u);
-    case GM_FWD1: return 2u * 16384u + 1024u;
+    case GM_FWD1: return 2u * 16384u + 1024u + 512u;
     case GM_FWD2: return kAStage + bn * 128 + 512u * bchunks;
-    case GM_BWD_DA: return bn * 128 + 512u * bchunks;
-    case GM_BWD_DX: return kAStage + bn * 128 + 512u * bchunks;
+    case GM_BWD_DA: return bn * 128 + 512u * bchunks + 512u;
+    case GM_BWD_DX: return kAStage + bn * 128 + 512u * bchunks + 512u;
     case GM_WG13: return kAStage + 2u * 16384u + 512u + 1024u;
     default: return kAStage + bn * 128 + 512u + 512u * bchunks;  // GM_WG2
   }
@@ -382,6 +382,8 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     const long blk = ((long)it.e * (p.I / 128) + it.n) * hg + kk;
     bulk_load(sfb, p.sfb_tiled0 + blk * 512, 512, bar);
     bulk_load(sfb + 512, p.sfb_tiled1 + blk * 512, 512, bar);
+    // A (gathered x rows): its scales pre-tiled in padded-row order
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * hg + kk) * 512, 512, bar);
   } else if (type == GM_FWD2) {
     const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
     const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
@@ -392,8 +394,10 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
       bulk_load(sfb + c * 512, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * 512, 512, bar);
     }
   } else if (type == GM_BWD_DA) {
-    // B = W2 along H (K-major); its scales pre-tiled per 128 rows x 128 K
+    // B = W2 along H (K-major); its scales, and those of the gathered
+    // dout rows, pre-tiled per 128 rows x 128 K
     tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * (p.H / 128) + kk) * 512, 512, bar);
     for (int c = 0; c < bn / 128; ++c) {
       const long blk = ((long)it.e * (p.I / 128) + it.n * (bn / 128) + c) * (p.H / 128) + kk;
       bulk_load(sfb + c * 512, p.sfb_tiled0 + blk * 512, 512, bar);
@@ -401,6 +405,7 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
   } else if (type == GM_BWD_DX) {
     // B = W1 then W3 along I (K-major); scales pre-tiled likewise
     tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * (2 * p.I / 128) + kk) * 512, 512, bar);
     const int ki = p.I / 128;
     const int kb = kk < ki ? kk : kk - ki;
     tma_load_3d(b, &mp.m[kk < ki ? 1 : 2], bar, kb * 128, it.n * bn, it.e);
@@ -443,19 +448,16 @@ __device__ __forceinline__ void gather_stage_mx(const GemmParams& p, const Item&
                   t >= 0 ? 16u : 0u);
     }
   }
-  // scales of A, row gt of the tile
+  // scales of A, row gt of the tile (GEMM1's, dA''s and dX's come pre-tiled
+  // with the TMA loads)
   const uint8_t* sa = nullptr;
   if (MODE == GM_DENSE) {
     if (!p.a_mn) sa = p.sfa_rows + ((long)it.m * 128 + gt) * p.sfa_ld + kk * 4;
-  } else if (gather_a) {
-    sa = p.sfa_rows + (long)max(tok_row, 0) * p.sfa_ld + kk * 4;
   } else if (type == GM_FWD2) {
     // scales of a, written by the GEMM1 epilogue next to the ring codes
     sa = p.ring_sf + (long)ring_row(p, it.row0 + gt) * (p.I / 32) + kk * 4;
-  } else if (type == GM_BWD_DX) {
-    sa = p.sfa_rows + ((long)it.row0 + gt) * p.sfa_ld + kk * 4;
   }
-  if (sa) cp_async_4(smem_u32(sfa + mx_sf_offset(gt, 0)), sa, (gather_a && tok_row < 0) ? 0u : 4u);
+  if (sa) cp_async_4(smem_u32(sfa + mx_sf_offset(gt, 0)), sa, 4u);
   // scales of K-major B, rows gt and gt + 128 of the N tile (dense launches;
   // the weights' scales of dA' and dX come pre-tiled with the TMA loads)
   const uint8_t* sb = nullptr;

@@ -42,6 +42,7 @@ struct WsLayout {
   size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x, then dout (weight gradients)
   // MXFP8 operand copies
   size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
+  size_t sfa_rows_t;  // the A operand's scales in padded-row order, tiled: [pad/128][max(H,2I)/128][512]
   size_t wsf1, wsf3, wsf2;  // forward weight scales tiled for the GEMMs
   size_t dhuq, dhusf; // dh|du quantised along I: u8 [pad, 2I], [pad, 2I/32]
   size_t wqa, wsfa;   // weight gradients: sorted x / dout along rows, [pad, H] + tiled scales
@@ -72,6 +73,8 @@ cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint
 cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st);
 cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_count, uint8_t* out,
                                     cudaStream_t st);
+cudaError_t launch_tile_row_scales(const uint8_t* sf, int kb_count, const int32_t* pad_perm, int k,
+                                   const int32_t* rows_used, long rows_cap, uint8_t* out, cudaStream_t st);
 cudaError_t launch_replay_copy(const mok_shape& s, const WsLayout& L, const uint8_t* ws,
                                const __nv_bfloat16* ctx_ring, __nv_bfloat16* dhu, cudaStream_t st);
 // Router (router.cu)

@@ -127,6 +127,30 @@ __global__ void tile_scales_rows_kernel(const uint8_t* __restrict__ sf, int batc
   }
 }
 
+// Scales of a K-major activation operand, in padded-row order, tiled like
+// the weights': padded row p takes the scales of row src(p) of `sf`
+// [rows][kb_count] (the token of p when `pad_perm` is given, else p itself;
+// a padding row gets scale code 0, its codes being zero), into
+// [used rows / 128][kb_count / 4][512 B] for the rows in use.
+__global__ void tile_row_scales_kernel(const uint8_t* __restrict__ sf, int kb_count,
+                                       const int32_t* __restrict__ pad_perm, int k,
+                                       const int32_t* __restrict__ rows_used, uint8_t* __restrict__ out) {
+  const int kg_count = kb_count / 4;
+  const long n_words = (long)(*rows_used) * kg_count;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n_words; i += (long)gridDim.x * blockDim.x) {
+    const int kg = (int)(i % kg_count);
+    const long p = i / kg_count;
+    long src = p;
+    if (pad_perm) {
+      const int f = pad_perm[p];
+      src = f >= 0 ? f / k : -1;
+    }
+    const uint32_t w = src >= 0 ? *reinterpret_cast<const uint32_t*>(sf + src * kb_count + (long)kg * 4) : 0u;
+    uint8_t* blk = out + ((p / 128) * kg_count + kg) * 512;
+    *reinterpret_cast<uint32_t*>(blk + sf_block_offset((int)(p & 127), 0)) = w;
+  }
+}
+
 // Quantise bf16 [rows_cap, C] along the rows (blocks of 32 rows) for the rows
 // in use (header word), codes [rows, C] and tiled scales
 // [rows/128][C/128][512 B] (scale of (row block, column) at
@@ -177,6 +201,16 @@ cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_
   const long cap = (long)device_sm_count() * 32;
   if (grid > cap) grid = cap;
   tile_scales_rows_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, N, kb_count, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_row_scales(const uint8_t* sf, int kb_count, const int32_t* pad_perm, int k,
+                                   const int32_t* rows_used, long rows_cap, uint8_t* out, cudaStream_t st) {
+  const long words = rows_cap * (kb_count / 4);
+  long grid = (words + 255) / 256;
+  const long cap = (long)device_sm_count() * 32;
+  if (grid > cap) grid = cap;
+  tile_row_scales_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, kb_count, pad_perm, k, rows_used, out);
   return cudaGetLastError();
 }
 
