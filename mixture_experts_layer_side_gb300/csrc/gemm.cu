@@ -493,22 +493,6 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const uint32_t 
   for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float (&v)[32]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 q = s[i];
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
-      const float2 f = __bfloat1622float2(b2);
-      v[8 * i + 2 * j] = f.x;
-      v[8 * i + 2 * j + 1] = f.y;
-    }
-  }
-}
-
 __device__ __forceinline__ float sigmoidf_(float h) { return 1.0f / (1.0f + __expf(-h)); }
 
 // GEMM1: columns [0,128) of the tile are h, [128,256) are u, for
@@ -611,19 +595,42 @@ __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, 
   __nv_bfloat16* durow = dhrow + p.I;
   __nv_bfloat16* asrow = p.as + prow * p.I + it.n * bn;
   float dsum = 0.0f;
+  // h and u of the next 32 columns are in flight while this chunk's TMEM
+  // load and arithmetic run (each row's loads are dependent on nothing but
+  // the address, so their latency need not add to every chunk)
+  uint4 hn[4], un[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    hn[i] = reinterpret_cast<const uint4*>(hrow)[i];
+    un[i] = reinterpret_cast<const uint4*>(urow)[i];
+  }
 #pragma unroll 1
   for (int c = 0; c < bn; c += 32) {
-    float g[32], h[32], u[32];
+    uint32_t hc[16], uc[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      hc[4 * i] = hn[i].x, hc[4 * i + 1] = hn[i].y, hc[4 * i + 2] = hn[i].z, hc[4 * i + 3] = hn[i].w;
+      uc[4 * i] = un[i].x, uc[4 * i + 1] = un[i].y, uc[4 * i + 2] = un[i].z, uc[4 * i + 3] = un[i].w;
+    }
+    if (c + 32 < bn) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        hn[i] = reinterpret_cast<const uint4*>(hrow + c + 32)[i];
+        un[i] = reinterpret_cast<const uint4*>(urow + c + 32)[i];
+      }
+    }
+    float g[32];
     tmem_ld32(tbase + c, g);
-    load32_bf16(hrow + c, h);
-    load32_bf16(urow + c, u);
     uint32_t dhw[16], duw[16], asw[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
+      const float2 h2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hc[i]));
+      const float2 u2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uc[i]));
+      const float hp[2] = {h2.x, h2.y}, up[2] = {u2.x, u2.y};
       float r[2][3];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float hh = h[2 * i + j], uu = u[2 * i + j], gg = g[2 * i + j];
+        const float hh = hp[j], uu = up[j], gg = g[2 * i + j];
         const float sg = sigmoidf_(hh);
         const float sl = hh * sg;
         const float a = sl * uu;
