@@ -701,15 +701,30 @@ __device__ __forceinline__ void store_chunk_coalesced(uint8_t* stage, int lane, 
 // pairs) leaves as full 128-byte row segments: staged in a 4 KB smem buffer
 // (16-byte chunks XOR-swizzled by row), read back with 8 lanes per row and
 // stored 4 rows x 128 bytes per instruction -- four whole cache lines each.
+__device__ __forceinline__ void stage_chunk64(uint8_t* stage, int lane, const uint32_t (&w)[32]);
+template <typename RowPtr>
+__device__ __forceinline__ void flush_chunk64(uint8_t* stage, int lane, RowPtr row_ptr);
+
 template <typename RowPtr>
 __device__ __forceinline__ void store_chunk64_coalesced(uint8_t* stage, int lane, const uint32_t (&w)[32],
                                                         RowPtr row_ptr) {
+  stage_chunk64(stage, lane, w);
+  flush_chunk64(stage, lane, row_ptr);
+}
+
+// The two halves of store_chunk64_coalesced: a lane's row into the staging
+// buffer, then the buffer out as whole row segments.
+__device__ __forceinline__ void stage_chunk64(uint8_t* stage, int lane, const uint32_t (&w)[32]) {
   const int sw = lane & 7;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     *reinterpret_cast<uint4*>(stage + lane * 128 + ((i ^ sw) << 4)) =
         make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
   __syncwarp();
+}
+
+template <typename RowPtr>
+__device__ __forceinline__ void flush_chunk64(uint8_t* stage, int lane, RowPtr row_ptr) {
   const int ch = lane & 7;
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
@@ -727,51 +742,86 @@ __device__ __forceinline__ void store_chunk64_coalesced(uint8_t* stage, int lane
 // loop (the expert's rows), so the 64 KB output tile must leave fast:
 // coalesced stores through the warp's staging buffer.
 // 64 columns of accumulator (two 32-column TMEM loads) -> bf16 -> dW rows.
-__device__ __forceinline__ void wgrad_emit64(const GemmParams& p, const Item& it, int r0, int col, int lane,
-                                             uint8_t* stage, const uint32_t (&ra)[32], const uint32_t (&rb)[32]) {
-  uint32_t w[32];
+// First dW element of rows r0.. at column col of the item's output, and the
+// row pitch.  I is a multiple of 128, so a 64-column chunk never straddles
+// dW1 | dW3.
+__device__ __forceinline__ __nv_bfloat16* wgrad_base(const GemmParams& p, const Item& it, int r0, int col, long& ld) {
+  if (it.type == GM_WG13) {
+    ld = p.I;
+    return (col < p.I) ? p.dW1 + ((long)it.e * p.H + r0) * p.I + col
+                       : p.dW3 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
+  }
+  ld = p.H;
+  return p.dW2 + ((long)it.e * p.I + r0) * p.H + col;
+}
+
+// 64 accumulator columns of this lane's row (two 32-column TMEM loads) as
+// 32 packed bf16 pairs.
+__device__ __forceinline__ void wgrad_load64(uint32_t taddr, uint32_t (&w)[32]) {
+  uint32_t ra[32], rb[32];
+  tmem_ld32_issue(taddr, ra);
+  tmem_ld32_issue(taddr + 32, rb);
+  tmem_wait_ld();
+  tmem_regs_ready(ra);
+  tmem_regs_ready(rb);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     w[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
     w[16 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
   }
-  __nv_bfloat16* base;
-  long ld;
-  if (it.type == GM_WG13) {
-    // I is a multiple of 128, so a 64-column chunk never straddles dW1 | dW3
-    base = (col < p.I) ? p.dW1 + ((long)it.e * p.H + r0) * p.I + col
-                       : p.dW3 + ((long)it.e * p.H + r0) * p.I + (col - p.I);
-    ld = p.I;
-  } else {
-    base = p.dW2 + ((long)it.e * p.I + r0) * p.H + col;
-    ld = p.H;
-  }
-  store_chunk64_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
 }
 
 // 64 columns at a time: two TMEM loads, one wait, then the coalesced store.
-template <int BN>
+// With EARLY the whole accumulator row is read first (the first 64 columns
+// into the staging buffer, the rest in registers as packed bf16), then
+// `release` hands the TMEM buffer back to the MMA warp, then the stores, so
+// the next tile's main loop runs while this tile's rows leave.  That pays
+// where the accumulator is single-buffered (MXFP8) and its 96 extra live
+// registers fit (measured on dW1 | dW3 only); elsewhere each 64 columns are
+// loaded and stored in turn and the caller releases the buffer after.
+template <int BN, bool EARLY, typename Release>
 __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane,
-                                            uint8_t* stage) {
+                                            uint8_t* stage, Release&& release) {
+  constexpr int kGroups = BN / 64;
   const int r0 = it.m * 128 + q * 32;  // first dW row of this warp
   const int col0 = it.n * BN;
-  uint32_t ra[32], rb[32];
+  if constexpr (!EARLY) {
 #pragma unroll
-  for (int c = 0; c < BN; c += 64) {
-    tmem_ld32_issue(tbase + c, ra);
-    tmem_ld32_issue(tbase + c + 32, rb);
-    tmem_wait_ld();
-    tmem_regs_ready(ra);
-    tmem_regs_ready(rb);
-    wgrad_emit64(p, it, r0, col0 + c, lane, stage, ra, rb);
+    for (int g = 0; g < kGroups; ++g) {
+      uint32_t w[32];
+      wgrad_load64(tbase + 64 * g, w);
+      long ld;
+      __nv_bfloat16* base = wgrad_base(p, it, r0, col0 + 64 * g, ld);
+      store_chunk64_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
+    }
+    return;
+  }
+  {
+    uint32_t w0[32];
+    wgrad_load64(tbase, w0);
+    stage_chunk64(stage, lane, w0);
+  }
+  uint32_t w[kGroups - 1][32];
+#pragma unroll
+  for (int g = 1; g < kGroups; ++g) wgrad_load64(tbase + 64 * g, w[g - 1]);
+  release();
+  long ld;
+  __nv_bfloat16* base = wgrad_base(p, it, r0, col0, ld);
+  flush_chunk64(stage, lane, [&](int rr) { return base + rr * ld; });
+#pragma unroll
+  for (int g = 1; g < kGroups; ++g) {
+    base = wgrad_base(p, it, r0, col0 + 64 * g, ld);
+    store_chunk64_coalesced(stage, lane, w[g - 1], [&](int rr) { return base + rr * ld; });
   }
 }
 
-__device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane, uint8_t* stage) {
+template <bool EARLY, typename Release>
+__device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane, uint8_t* stage,
+                          Release&& release) {
   if (p.bn == 256)
-    epi_wgrad_n<256>(p, it, tbase, q, lane, stage);
+    epi_wgrad_n<256, EARLY>(p, it, tbase, q, lane, stage, release);
   else
-    epi_wgrad_n<128>(p, it, tbase, q, lane, stage);
+    epi_wgrad_n<128, EARLY>(p, it, tbase, q, lane, stage, release);
 }
 
 __device__ void epi_dense(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
@@ -1250,6 +1300,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + buf * 256;
+      // hands the accumulator back to the MMA warp, once per tile
+      bool released = false;
+      auto release_acc = [&]() {
+        if (released) return;
+        released = true;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // CTA pairs: the leader's MMA warp waits for both CTAs' epilogues
+          if constexpr (PAIR)
+            mbar_arrive_cluster(mapa_shared(&ctl->tempty[buf], 0));
+          else
+            mbar_arrive(&ctl->tempty[buf]);
+        }
+      };
       if (MODE == GM_FWD_RING && it.type == GM_FWD2 && warp == 2 && lane == 0) {
         // the accumulator is complete, so every load of this tile's ring
         // rows has landed: release the rows for reuse
@@ -1275,17 +1340,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         case GM_FWD2: epi_scatter(p, it, tbase, row, p.bn); break;
         case GM_BWD_DA: epi_bwd_da<MX>(p, it, tbase, row); break;
         case GM_BWD_DX: epi_scatter(p, it, tbase, row, p.bn); break;
-        default: epi_wgrad(p, it, tbase, q, lane, stage_out); break;
+        default: epi_wgrad<MX && MODE == GM_WG13>(p, it, tbase, q, lane, stage_out, release_acc); break;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        // CTA pairs: the leader's MMA warp waits for both CTAs' epilogues
-        if constexpr (PAIR)
-          mbar_arrive_cluster(mapa_shared(&ctl->tempty[buf], 0));
-        else
-          mbar_arrive(&ctl->tempty[buf]);
-      }
+      release_acc();
       if (MODE == GM_FWD_RING && it.type == GM_FWD1) {
         // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
         // read by TMA): each epilogue warp adds 1, so a tile is complete when
