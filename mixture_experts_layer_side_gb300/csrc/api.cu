@@ -257,8 +257,9 @@ bool map3d(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows, uint64_t
   return make_tmap(m, kBF16, 3, p, dims, str, box, true);
 }
 
-// bf16 [rows, cols] row-major read four whole rows at a time (tile::gather4):
-// box {64, 1}.
+// Tensor map of a token-row operand that the gather warps copy with
+// cp.async (bf16 [rows, cols], box {64, 1}): no TMA load reads it; it keeps
+// the map slot of the gathered operand valid for the descriptor prefetch.
 bool map_gather(CUtensorMap* m, const void* p, uint64_t cols, uint64_t rows) {
   const uint64_t dims[2] = {cols, rows};
   const uint64_t str[1] = {cols * 2};

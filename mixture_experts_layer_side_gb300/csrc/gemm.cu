@@ -10,13 +10,19 @@
 //               (cp.async.mbarrier.arrive.noinc).  (TMA tile::gather4 moved
 //               a third of the bytes per SM-cycle of these copies at the
 //               same depth, so the gathered operands do not use it.)
-//   warp 1      MMA issuer: tcgen05.mma (BF16 in, FP32 accumulate in TMEM),
-//               128 x N tiles, N = 128 or 256; TMEM holds two accumulators so
-//               the epilogue of one tile overlaps the main loop of the next.
+//   warp 1      MMA issuer: tcgen05.mma (BF16 kind::f16, or MXFP8
+//               kind::mxf8f6f4.block_scale with the stage scales copied to
+//               TMEM by tcgen05.cp), FP32 accumulate in TMEM, 128 x N tiles,
+//               N = 128 or 256; TMEM holds two accumulators (BF16) so the
+//               epilogue of one tile overlaps the main loop of the next.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, then the fused
 //               per-mode work (SwiGLU, scatter to token order, SwiGLU
 //               backward with the router-score partial sums, weight-gradient
 //               stores).
+// Weight-gradient launches read token-sorted operands with plain TMA (the
+// gather warps write the empty experts' zero gradients instead) and come in
+// two forms: single CTAs, and clusters of two CTAs sharing a 256 x 256 tile
+// through one cta_group::2 MMA (launch_gemm_pair) for long-K experts.
 // Work items (output tiles) are taken from a device counter in increasing
 // order, so a CTA only ever waits on items taken before its own; the
 // numerics of a tile never depend on which CTA computes it (fixed K order,
@@ -670,31 +676,6 @@ __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, 
     }
   }
   p.dsp[prow * p.n_tiles + it.n] = dsum;
-}
-
-// A warp's 32 x 32 bf16 chunk (lane = row, w[] = its 32 values) leaves as
-// coalesced row segments: it is staged in a 2 KB smem buffer (16-byte chunks
-// XOR-swizzled by row to spread banks), read back with 4 lanes per row and
-// stored 8 rows x 64 bytes per instruction.  row_ptr(rr) is the global
-// address of the chunk's row rr; rows with a null address are skipped.
-template <typename RowPtr>
-__device__ __forceinline__ void store_chunk_coalesced(uint8_t* stage, int lane, const uint32_t (&w)[16],
-                                                      RowPtr row_ptr) {
-  const int sw = (lane >> 1) & 3;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    *reinterpret_cast<uint4*>(stage + lane * 64 + ((i ^ sw) << 4)) =
-        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-  __syncwarp();
-  const int ch = lane & 3;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    const int rr = 8 * s + (lane >> 2);
-    const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * 64 + ((ch ^ ((rr >> 1) & 3)) << 4));
-    __nv_bfloat16* dst = row_ptr(rr);
-    if (dst) *reinterpret_cast<uint4*>(dst + ch * 8) = v;
-  }
-  __syncwarp();
 }
 
 // A warp's 32 x 64 bf16 chunk (lane = row, w[] = its 64 values as bf16

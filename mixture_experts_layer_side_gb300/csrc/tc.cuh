@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the sm_103a features the kernels use:
-// mbarriers, TMA tensor copies (tile and tile::gather4), tcgen05 tensor-core
+// mbarriers, TMA tensor copies (tile, CTA-pair tile, bulk), tcgen05 tensor-core
 // MMA with TMEM accumulators, and the global-memory flag operations of the
 // minibatch ring.  Every spin-wait here is bounded: it gives up after
 // kWaitLimitNs of %globaltimer time, records MOK_ERR_TIMEOUT and returns false.
@@ -203,18 +203,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// Four rows (r0..r3) of a 2-D tensor, columns [c0, c0 + box width), into
-// four consecutive smem rows.  The tensor map's box is one row high.  Rows
-// outside the tensor read as zero.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int r0,
-                                            int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 
