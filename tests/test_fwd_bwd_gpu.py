@@ -112,3 +112,46 @@ def test_weight_gradient_cta_pairs_match_single_cta(shape, routing):
     _, _, g_one = run_layer(shape, routing, 9, debug_flags=8)
     for k in ("dW1", "dW3", "dW2"):
         assert torch.equal(g_pair[k], g_one[k]), k
+
+
+def _run_with_idx(shape, idx, seed):
+    from mixture_experts_layer_side_gb300.inputs import Shape, make_inputs
+    from mixture_experts_layer_side_gb300.layer import MoKLayer
+    S = Shape(*shape)
+    inp = make_inputs(S, "uniform", seed=seed, device="cpu")
+    inp["idx"] = idx.to(torch.int32).contiguous()
+    g = {k: v.cuda() for k, v in inp.items()}
+    layer = MoKLayer(S)
+    layer.build_schedule(g["idx"])
+    out, grads = poisoned_outputs(layer)
+    layer.forward(g["x"], g["s"], g["W1"], g["W3"], g["W2"], out=out)
+    layer.backward(g["x"], g["s"], g["W1"], g["W3"], g["W2"], g["dout"], grads=grads)
+    layer.check()
+    ref = oracle_run(inp)
+    assert_bf16_close(np64(out), ref["out"], "out")
+    for k in ("dX", "dW1", "dW3", "dW2", "ds"):
+        assert_bf16_close(np64(grads[k]), ref[k], k)
+    return inp, grads
+
+
+def test_every_token_on_one_expert():
+    """All 2,048 tokens routed to expert 5 of 8 (top-1): one long expert on
+    the CTA-pair weight-gradient path, seven exact-zero experts."""
+    require_gpu()
+    shape = (2048, 256, 128, 8, 1)
+    _, grads = _run_with_idx(shape, torch.full((2048, 1), 5), 51)
+    for e in range(8):
+        if e != 5:
+            for k in ("dW1", "dW3", "dW2"):
+                assert torch.count_nonzero(grads[k][e]).item() == 0
+
+
+def test_duplicate_experts_within_a_token():
+    """Half the tokens pick the same expert twice (legal: the rows are
+    independent routed rows)."""
+    require_gpu()
+    T, E, k = 600, 6, 2
+    g = torch.Generator().manual_seed(52)
+    idx = torch.randint(0, E, (T, k), generator=g)
+    idx[::2, 1] = idx[::2, 0]
+    _run_with_idx((T, 256, 128, E, k), idx, 52)
