@@ -93,12 +93,16 @@ typedef struct {
  *                 Bit 1 (MOK_DEBUG_SERIAL_RING): run the forward's two GEMMs
  *                 as one launch pair per minibatch (same ring, stream order)
  *                 instead of the single persistent ring launch.
- *                 Bit 2 (MOK_DEBUG_FUSED_WGRAD_GATHER): the weight-gradient
- *                 GEMMs gather token rows in their load path instead of
- *                 reading token-sorted copies.
+ *                 Bit 2 (MOK_DEBUG_FUSED_WGRAD_GATHER): the BF16 backward's
+ *                 dA' and weight-gradient GEMMs gather token rows in their
+ *                 load path instead of reading token-sorted copies (dA' then
+ *                 runs one CTA per tile).
  *                 Bit 3 (MOK_DEBUG_SINGLE_CTA_WGRAD): the BF16 weight-gradient
  *                 GEMMs run one CTA per 128-row tile instead of clusters of
  *                 two CTAs sharing a 256-row tile (cta_group::2).
+ *                 Bit 4 (MOK_DEBUG_SINGLE_CTA_ROWS): the BF16 backward's dA'
+ *                 and dX GEMMs run one CTA per 128-row tile instead of
+ *                 clusters of two CTAs sharing two tiles of one expert.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
@@ -122,6 +126,7 @@ typedef struct {
 #define MOK_DEBUG_SERIAL_RING 2
 #define MOK_DEBUG_FUSED_WGRAD_GATHER 4
 #define MOK_DEBUG_SINGLE_CTA_WGRAD 8
+#define MOK_DEBUG_SINGLE_CTA_ROWS 16
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
 typedef struct {

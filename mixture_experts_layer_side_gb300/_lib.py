@@ -22,6 +22,7 @@ MOK_DEBUG_SKIP_RING_SIGNAL = 1
 MOK_DEBUG_SERIAL_RING = 2
 MOK_DEBUG_FUSED_WGRAD_GATHER = 4
 MOK_DEBUG_SINGLE_CTA_WGRAD = 8
+MOK_DEBUG_SINGLE_CTA_ROWS = 16
 
 STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "MOK_ERR_WORKSPACE_TOO_SMALL",
           4: "MOK_ERR_CUDA", 5: "MOK_ERR_BAD_INDEX", 6: "MOK_ERR_TIMEOUT"}

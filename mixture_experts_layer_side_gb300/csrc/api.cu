@@ -113,6 +113,7 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   L.as = take(P * I * 2);
   L.dsp = take(P * (I / 128) * 4);
   L.sorted = take(P * H * 2);
+  L.pair_m0 = take(L.tile_capacity * 4);
   if (prec == MOK_MXFP8) {
     L.ring_sf = take((size_t)L.ring_slots * M * (I / 32));
     L.xq = take((size_t)s.T * H);
@@ -322,6 +323,24 @@ void base_params(GemmParams& g, const mok_shape& s, const WsLayout& L, uint8_t* 
   g.counts = reinterpret_cast<const int32_t*>(ws + L.counts);
   g.wg_rows_min = 0;
   g.wg_rows_max = INT_MAX;
+}
+
+// Whether the BF16 backward's dA' and dX run on CTA pairs.
+bool row_pairs(const mok_config& c) { return (c.debug_flags & MOK_DEBUG_SINGLE_CTA_ROWS) == 0; }
+
+void set_pair_table(GemmParams& g, const WsLayout& L, uint8_t* ws) {
+  g.pair_m0 = reinterpret_cast<const int32_t*>(ws + L.pair_m0);
+}
+
+// A row-tiled launch on CTA pairs, else (no cluster of two on this device)
+// one CTA per tile.
+cudaError_t launch_rows(int mode, bool pairs, const TmapSet& maps, const GemmParams& q, int grid, cudaStream_t st) {
+  if (pairs) {
+    const cudaError_t e = launch_gemm_pair(mode, maps, q, grid, st);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
+  }
+  return launch_gemm(mode, maps, q, grid, st);
 }
 
 mok_status reset_counters(uint8_t* ws, const WsLayout& L, cudaStream_t st) {
@@ -743,14 +762,28 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     g.ctx_hu = g.dhu;
   }
 
-  // dA' = gather(dout) W2^T, SwiGLU backward + router-score partials
+  // Token-sorted copies (rows in padded schedule order, zero padding rows)
+  // feed dA' and dW2 (dout), then dW1|dW3 (x), through one buffer; with
+  // MOK_DEBUG_FUSED_WGRAD_GATHER those GEMMs gather rows in their load path.
+  const bool sorted = (cfg->debug_flags & MOK_DEBUG_FUSED_WGRAD_GATHER) == 0;
+  __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
+  // dA' and dX on CTA pairs: two tiles of one expert per cluster, each CTA
+  // loading a 128-row half of the 256-row weight tile
+  const bool pairs_da = sorted && bn_i == 256 && row_pairs(*cfg);
+  const bool pairs_dx = bn_h == 256 && row_pairs(*cfg);
+  if (sorted) {
+    Phase ph(MOK_PHASE_BWD_SORT, st, 1);
+    MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(dout), srt, st));
+  }
+  // dA' = sorted(dout) W2^T, SwiGLU backward + router-score partials
   {
     TmapSet m;
     memset(&m, 0, sizeof(m));
-    if (!map_gather(&m.m[0], dout, s.H, s.T)) return MOK_ERR_CUDA;
-    if (!map3d(&m.m[1], W2, s.H, s.I, s.E, bn_i)) return MOK_ERR_CUDA;
+    if (sorted ? !map2d(&m.m[0], srt, s.H, P, 128) : !map_gather(&m.m[0], dout, s.H, s.T)) return MOK_ERR_CUDA;
+    if (!map3d(&m.m[1], W2, s.H, s.I, s.E, pairs_da ? 128 : bn_i)) return MOK_ERR_CUDA;
     GemmParams q = g;
     q.gather_src = static_cast<const __nv_bfloat16*>(dout);
+    q.rows_sorted = sorted ? 1 : 0;
     q.nmaps = 2;
     q.bn = bn_i;
     q.n_tiles = s.I / bn_i;
@@ -758,8 +791,10 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 0;
     {
-      Phase ph(MOK_PHASE_BWD_DA, st, 1);
-      MOK_CUDA(launch_gemm(GM_BWD_DA, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+      Phase ph(MOK_PHASE_BWD_DA, st, (pairs_da || pairs_dx) ? 2 : 1);
+      if (pairs_da || pairs_dx) MOK_CUDA(launch_pair_table(L, w, st));
+      if (pairs_da) set_pair_table(q, L, w);
+      MOK_CUDA(launch_rows(GM_BWD_DA, pairs_da, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
     }
     Phase ph(MOK_PHASE_BWD_DS, st, 1);
     MOK_CUDA(launch_ds_reduce(s, L, w, dscores, q.n_tiles, st));
@@ -768,8 +803,9 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   {
     TmapSet m;
     memset(&m, 0, sizeof(m));
-    if (!map2d(&m.m[0], g.dhu, 2 * (uint64_t)s.I, P, 128) || !map3d(&m.m[1], W1, s.I, s.H, s.E, bn_h) ||
-        !map3d(&m.m[2], W3, s.I, s.H, s.E, bn_h))
+    const int box = pairs_dx ? 128 : bn_h;
+    if (!map2d(&m.m[0], g.dhu, 2 * (uint64_t)s.I, P, 128) || !map3d(&m.m[1], W1, s.I, s.H, s.E, box) ||
+        !map3d(&m.m[2], W3, s.I, s.H, s.E, box))
       return MOK_ERR_CUDA;
     GemmParams q = g;
     q.nmaps = 3;
@@ -778,16 +814,35 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tile_begin = 0;
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 1;
+    if (pairs_dx) set_pair_table(q, L, w);
     {
       Phase ph(MOK_PHASE_BWD_DX, st, 1);
-      MOK_CUDA(launch_gemm(GM_BWD_DX, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+      MOK_CUDA(launch_rows(GM_BWD_DX, pairs_dx, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
     }
     Phase ph(MOK_PHASE_BWD_DX_COMBINE, st, 1);
     MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));
   }
-  // dW1 | dW3 = gather(x)^T [dh|du], per expert
-  const bool sorted = (cfg->debug_flags & MOK_DEBUG_FUSED_WGRAD_GATHER) == 0;
-  __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
+  // dW2 = (s a)^T sorted(dout), per expert
+  {
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!map2d(&m.m[0], g.as, s.I, P, 64)) return MOK_ERR_CUDA;
+    if (sorted ? !map2d(&m.m[1], srt, s.H, P, 64) : !map_gather(&m.m[1], dout, s.H, s.T)) return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.nmaps = 2;
+    q.bn = bn_h;
+    q.n_tiles = s.H / bn_h;
+    q.m_tiles = s.I / 128;
+    q.counter = 3;
+    q.wg_sorted = sorted ? 1 : 0;
+    q.gather_src = static_cast<const __nv_bfloat16*>(dout);
+    q.dW2 = static_cast<__nv_bfloat16*>(dW2);
+    Phase ph(MOK_PHASE_BWD_WG2, st, 0);
+    int n = 0;
+    MOK_CUDA(launch_wgrad(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), cfg->debug_flags, 5, &n, st));
+    g_launches += n;
+  }
+  // dW1 | dW3 = sorted(x)^T [dh|du], per expert (x overwrites the sorted dout)
   {
     TmapSet m;
     memset(&m, 0, sizeof(m));
@@ -810,30 +865,6 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     Phase ph(MOK_PHASE_BWD_WG13, st, 0);
     int n = 0;
     MOK_CUDA(launch_wgrad(GM_WG13, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), cfg->debug_flags, 4, &n, st));
-    g_launches += n;
-  }
-  // dW2 = (s a)^T gather(dout), per expert
-  {
-    TmapSet m;
-    memset(&m, 0, sizeof(m));
-    if (sorted) {
-      Phase ph(MOK_PHASE_BWD_SORT, st, 1);
-      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(dout), srt, st));
-    }
-    if (!map2d(&m.m[0], g.as, s.I, P, 64)) return MOK_ERR_CUDA;
-    if (sorted ? !map2d(&m.m[1], srt, s.H, P, 64) : !map_gather(&m.m[1], dout, s.H, s.T)) return MOK_ERR_CUDA;
-    GemmParams q = g;
-    q.nmaps = 2;
-    q.bn = bn_h;
-    q.n_tiles = s.H / bn_h;
-    q.m_tiles = s.I / 128;
-    q.counter = 3;
-    q.wg_sorted = sorted ? 1 : 0;
-    q.gather_src = static_cast<const __nv_bfloat16*>(dout);
-    q.dW2 = static_cast<__nv_bfloat16*>(dW2);
-    Phase ph(MOK_PHASE_BWD_WG2, st, 0);
-    int n = 0;
-    MOK_CUDA(launch_wgrad(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), cfg->debug_flags, 5, &n, st));
     g_launches += n;
   }
   return MOK_OK;

@@ -72,6 +72,7 @@ struct Item {
   int e;        // expert
   int row0;     // first padded row of the tile (row-tiled) or of the expert (wgrad)
   int k_iters;  // K iterations of 128 bytes
+  int idle;     // CTA pairs: the second CTA of a solo pair (loads, stores nothing)
 };
 
 __device__ __forceinline__ int used_tiles(const GemmParams& p) { return p.hdr[kHdrTiles]; }
@@ -97,6 +98,9 @@ __device__ int count_items(const GemmParams& p) {
     return max(end - p.m_tile_begin, 0) * p.n_tiles;
   }
 }
+
+// Work items of a row-tiled launch on CTA pairs: pair tiles x N tiles.
+__device__ __forceinline__ int count_pair_items(const GemmParams& p) { return p.hdr[kHdrPairs] * p.n_tiles; }
 
 // Ring kernel: item w -> (type, tile, n).  Sequence of steps: step 0 is
 // GEMM1 of minibatch 0; step s >= 1 is GEMM1 of minibatch s followed by
@@ -136,11 +140,18 @@ __device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& 
   return emit(GM_FWD2, nb - 1, w, g2);
 }
 
+__device__ __forceinline__ int row_k_iters(const GemmParams& p, int type, int el) {
+  return (type == GM_FWD1 || type == GM_BWD_DA) ? p.H / el
+         : (type == GM_FWD2)                   ? p.I / el
+                                               : 2 * p.I / el;  // GM_BWD_DX
+}
+
 template <int MODE, bool MX = false, bool PAIR = false>
 __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
   constexpr int kEl = MX ? 128 : 64;  // K elements per stage (128 bytes)
   const int* po = ctl->po;
   Item it;
+  it.idle = 0;
   if constexpr (MODE == GM_DENSE) {
     it.type = MODE;
     it.m = w / p.n_tiles;
@@ -167,6 +178,18 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.n = r % p.n_tiles;
     it.row0 = po[it.e];
     it.k_iters = oe >> 10;
+  } else if constexpr (PAIR) {
+    // dA' / dX on CTA pairs: the leader takes the pair's first tile, the
+    // other CTA the second (or, in a solo pair, the first again, idle)
+    const int code = p.pair_m0[w / p.n_tiles];
+    it.idle = (code & 1) && ctl->pair_rank == 1;
+    const int m = (code >> 1) + (it.idle ? 0 : ctl->pair_rank);
+    it.type = MODE;
+    it.m = m;
+    it.n = w % p.n_tiles;
+    it.e = p.tile_expert[m];
+    it.row0 = m * kTileRows;
+    it.k_iters = row_k_iters(p, MODE, kEl);
   } else {
     int type = MODE, m, n;
     if constexpr (MODE == GM_FWD_RING) {
@@ -180,9 +203,7 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.n = n;
     it.e = p.tile_expert[m];
     it.row0 = m * kTileRows;
-    it.k_iters = (type == GM_FWD1 || type == GM_BWD_DA) ? p.H / kEl
-                 : (type == GM_FWD2)                   ? p.I / kEl
-                                                       : 2 * p.I / kEl;  // GM_BWD_DX
+    it.k_iters = row_k_iters(p, type, kEl);
   }
   return it;
 }
@@ -196,10 +217,12 @@ __device__ __forceinline__ int ring_row(const GemmParams& p, int prow) {
 
 // ------------------------------------------------------------------ producers
 // Which operand of an item is gathered by token (0 none, 1 A, 2 B).
-// With p.wg_sorted the weight-gradient GEMMs read a token-sorted copy of
-// x / dout (rows in padded schedule order) with plain TMA instead.
+// With p.wg_sorted the weight-gradient GEMMs, and with p.rows_sorted dA',
+// read a token-sorted copy of x / dout (rows in padded schedule order) with
+// plain TMA instead.
 __device__ __forceinline__ int gathered_operand(const GemmParams& p, int type) {
   if (p.wg_sorted && (type == GM_WG13 || type == GM_WG2)) return 0;
+  if (p.rows_sorted && type == GM_BWD_DA) return 0;
   return (type == GM_FWD1 || type == GM_BWD_DA || type == GM_WG13) ? 1 : (type == GM_WG2 ? 2 : 0);
 }
 
@@ -240,6 +263,7 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
     tma_load_2d(a, &mp.m[mslot], bar, kk * 64, ring_row(p, it.row0));
     for (int c = 0; c < p.bn / 64; ++c) tma_load_3d(b + c * 8192, &mp.m[wmap], bar, it.n * p.bn + c * 64, kk * 64, it.e);
   } else if (type == GM_BWD_DA) {
+    if (p.rows_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 64, it.row0);
     tma_load_3d(b, &mp.m[1], bar, kk * 64, it.n * p.bn, it.e);
   } else if (type == GM_BWD_DX) {
     tma_load_2d(a, &mp.m[0], bar, kk * 64, it.row0);
@@ -265,15 +289,24 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
   }
 }
 
-// CTA-pair weight-gradient stage: this CTA's A tile (its own 128 M rows)
-// and its half of the 256-column B tile, completing on the leader's barrier.
+// CTA-pair stage: this CTA's A tile (its own 128 M rows) and its half of
+// the 256-column B tile, completing on the leader's barrier.
 template <int MODE>
-__device__ __forceinline__ void tma_loads_pair(const TmapSet& mp, const Item& it, int kk, int rank, uint8_t* a,
-                                               uint8_t* b, uint32_t bar) {
+__device__ __forceinline__ void tma_loads_pair(const TmapSet& mp, const GemmParams& p, const Item& it, int kk,
+                                               int rank, uint8_t* a, uint8_t* b, uint32_t bar) {
   const int bcol = it.n * 256 + rank * 128;
-  const int krow = it.row0 + kk * 64;
-  for (int c = 0; c < 2; ++c) tma_load_2d_pair(a + c * 8192, &mp.m[0], bar, it.m * 128 + c * 64, krow);
-  for (int c = 0; c < 2; ++c) tma_load_2d_pair(b + c * 8192, &mp.m[1], bar, bcol + c * 64, krow);
+  if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
+    const int krow = it.row0 + kk * 64;
+    for (int c = 0; c < 2; ++c) tma_load_2d_pair(a + c * 8192, &mp.m[0], bar, it.m * 128 + c * 64, krow);
+    for (int c = 0; c < 2; ++c) tma_load_2d_pair(b + c * 8192, &mp.m[1], bar, bcol + c * 64, krow);
+  } else if (MODE == GM_BWD_DA) {  // A: token-sorted dout rows
+    tma_load_2d_pair(a, &mp.m[0], bar, kk * 64, it.row0);
+    tma_load_3d_pair(b, &mp.m[1], bar, kk * 64, bcol, it.e);
+  } else {  // GM_BWD_DX: K runs over dh (W1) and then du (W3)
+    tma_load_2d_pair(a, &mp.m[0], bar, kk * 64, it.row0);
+    const int ki = p.I / 64;
+    tma_load_3d_pair(b, &mp.m[kk < ki ? 1 : 2], bar, (kk < ki ? kk : kk - ki) * 64, bcol, it.e);
+  }
 }
 
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -840,7 +873,7 @@ __device__ void epi_dense(const GemmParams& p, const Item& it, uint32_t tbase, i
 // All K stages of one item's M/N-major gathered operand (weight-gradient
 // GEMMs, where K is the expert's routed rows).  Row -> token lookups are
 // dependent loads, so they run kPrefetch stages ahead in a register ring.
-template <int CPR>
+template <int CPR, int NST>
 __device__ bool gather_item_mn(const GemmParams& p, const Item& it, uint8_t* op_base, int op_stride, int col0,
                                Ctl* ctl, uint32_t& stage, uint32_t& phase, int gt, const WaitCtx& wc) {
   constexpr int kTok = 64 / (128 / CPR);
@@ -857,7 +890,7 @@ __device__ bool gather_item_mn(const GemmParams& p, const Item& it, uint8_t* op_
         if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) return false;
         gather_mnmajor<CPR>(op_base + stage * op_stride, p.gather_src, p.H, col0, gt, ring[u], &ctl->full[stage]);
         if (kk + kPrefetch < it.k_iters) mn_tokens<CPR>(p, it, kk + kPrefetch, gt, ring[u]);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (++stage == NST) { stage = 0; phase ^= 1; }
       }
     }
   }
@@ -867,6 +900,7 @@ __device__ bool gather_item_mn(const GemmParams& p, const Item& it, uint8_t* op_
 // All K stages of one item whose gathered operand is K-major (GEMM1, dA'):
 // the 128 token rows are fixed for the item.  Items with nothing to gather
 // (GEMM2 inside the ring launch) only keep the stage barriers' phase count.
+template <int NST>
 __device__ bool gather_item_k(const GemmParams& p, const Item& it, uint8_t* sA, Ctl* ctl, uint32_t& stage,
                               uint32_t& phase, int gt, const WaitCtx& wc) {
   const bool gather = gathered_operand(p, it.type) == 1;
@@ -879,7 +913,7 @@ __device__ bool gather_item_k(const GemmParams& p, const Item& it, uint8_t* sA, 
       gather_kmajor(sA + stage * kAStage, p.gather_src, p.H, kk * 64, gt, tok, &ctl->full[stage]);
     else
       mbar_arrive(&ctl->full[stage]);
-    if (++stage == kStages) { stage = 0; phase ^= 1; }
+    if (++stage == NST) { stage = 0; phase ^= 1; }
   }
   return true;
 }
@@ -941,9 +975,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // Weight-gradient launches whose operands are all TMA-loaded (token-sorted
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
-  const bool gather_in_pipe = kGather && !(kWgrad && (MX || p.wg_sorted));
+  const bool gather_in_pipe =
+      kGather && !(kWgrad && (MX || p.wg_sorted)) && !(MODE == GM_BWD_DA && !MX && p.rows_sorted);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
-  // by the other CTA's TMA producer and epilogue warps
+  // by the other CTA's TMA producer and epilogue warps (pair launches have
+  // no gathered operand)
   const uint32_t queue_consumers = PAIR ? 10u : gather_in_pipe ? 9u : 5u;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
 
@@ -1011,6 +1047,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const int num_items = kWgrad ? ctl->n_sel * (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles
+                        : PAIR ? count_pair_items(p)
                                : count_items<MODE>(p);
 
   if (warp == 0) {
@@ -1031,7 +1068,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           bool ok = true;
           for (int kk = 0; kk < it.k_iters; ++kk) {
             if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
-            tma_loads_pair<MODE>(maps, it, kk, 1, sA + stage * kAStage, sB + stage * kBSt,
+            tma_loads_pair<MODE>(maps, p, it, kk, 1, sA + stage * kAStage, sB + stage * kBSt,
                                  mapa_shared(&ctl->full[stage], 0));
             ++issued;
             if (++stage == kSt) { stage = 0; phase ^= 1; }
@@ -1102,7 +1139,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
             mbar_arrive_expect_tx(&ctl->full[stage], bytes);
             if constexpr (PAIR)
-              tma_loads_pair<MODE>(maps, it, kk, 0, sA + stage * kAStage, sB + stage * kBSt,
+              tma_loads_pair<MODE>(maps, p, it, kk, 0, sA + stage * kAStage, sB + stage * kBSt,
                                    mapa_shared(&ctl->full[stage], 0));
             else if constexpr (MX)
               tma_loads_mx<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBSt, sSF + stage * kSfStage,
@@ -1164,15 +1201,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
         } else if (gathered_operand(p, it.type) == 0)
-          ok = gather_item_k(p, it, sA, ctl, stage, phase, gt, wc);
+          ok = gather_item_k<kSt>(p, it, sA, ctl, stage, phase, gt, wc);
         else if (it.type == GM_WG13)
-          ok = gather_item_mn<16>(p, it, sA, kAStage, it.m * 128, ctl, stage, phase, gt, wc);
+          ok = gather_item_mn<16, kSt>(p, it, sA, kAStage, it.m * 128, ctl, stage, phase, gt, wc);
         else if (it.type == GM_WG2 && p.bn == 256)
-          ok = gather_item_mn<32>(p, it, sB, kBStage, it.n * p.bn, ctl, stage, phase, gt, wc);
+          ok = gather_item_mn<32, kSt>(p, it, sB, kBSt, it.n * p.bn, ctl, stage, phase, gt, wc);
         else if (it.type == GM_WG2)
-          ok = gather_item_mn<16>(p, it, sB, kBStage, it.n * p.bn, ctl, stage, phase, gt, wc);
+          ok = gather_item_mn<16, kSt>(p, it, sB, kBSt, it.n * p.bn, ctl, stage, phase, gt, wc);
         else
-          ok = gather_item_k(p, it, sA, ctl, stage, phase, gt, wc);
+          ok = gather_item_k<kSt>(p, it, sA, ctl, stage, phase, gt, wc);
         if (!ok) break;
       }
       // let this thread's copies land before the CTA can exit
@@ -1313,7 +1350,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
       }
       if (!ok) break;
-      switch (it.type) {
+      // (the idle CTA of a solo pair only hands the accumulator back)
+      switch (it.idle ? -1 : it.type) {
+        case -1: break;
         case GM_DENSE: epi_dense(p, it, tbase, row); break;
         case GM_FWD1:
           if constexpr (MX) epi_fwd1_mx(p, it, tbase, row); else epi_fwd1(p, it, tbase, row);
@@ -1445,10 +1484,17 @@ cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, i
 }
 
 cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
-  if (!p.wg_sorted || p.m_tiles % 2 != 0 || p.bn != 256) return cudaErrorInvalidValue;
+  if (p.bn != 256) return cudaErrorInvalidValue;
+  if (mode == GM_WG13 || mode == GM_WG2) {
+    if (!p.wg_sorted || p.m_tiles % 2 != 0) return cudaErrorInvalidValue;
+  } else if (!p.pair_m0 || (mode == GM_BWD_DA && !p.rows_sorted)) {
+    return cudaErrorInvalidValue;
+  }
   switch (mode) {
     case GM_WG13: return launch_pair_mode<GM_WG13>(maps, p, grid, st);
     case GM_WG2: return launch_pair_mode<GM_WG2>(maps, p, grid, st);
+    case GM_BWD_DA: return launch_pair_mode<GM_BWD_DA>(maps, p, grid, st);
+    case GM_BWD_DX: return launch_pair_mode<GM_BWD_DX>(maps, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

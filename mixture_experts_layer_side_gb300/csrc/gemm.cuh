@@ -76,6 +76,9 @@ struct GemmParams {
   int debug_flags;
   int nmaps;               // tensor maps in use (prefetched at start)
   int wg_sorted;           // weight gradients read token-sorted copies (plain TMA)
+  int rows_sorted;         // dA' reads a token-sorted copy of dout (plain TMA)
+  // CTA-pair launches of dA' / dX: the pair table (first M tile * 2 + solo)
+  const int32_t* pair_m0;
   // ---- MXFP8 (E4M3 codes, E8M0 scales per 32 K-elements)
   // K-major operands: scales [rows][K/32], four bytes per row per stage,
   // copied by the gather threads; rows of A are gathered by token when A is.
@@ -102,10 +105,13 @@ struct GemmParams {
 size_t gemm_smem_bytes();
 cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
-// Weight-gradient GEMMs (GM_WG13 / GM_WG2, BF16, token-sorted operands, an
-// even number of 128-row M tiles, bn = 256) on clusters of two CTAs that
-// share each 256 x 256 tile through one cta_group::2 MMA.  Returns
-// cudaErrorNotSupported when the device cannot hold a cluster of two.
+// BF16 launches on clusters of two CTAs that share each 256 x 256 tile
+// through one cta_group::2 MMA: the weight-gradient GEMMs (GM_WG13 / GM_WG2,
+// token-sorted operands, an even number of 128-row M tiles, bn = 256) and
+// the row-tiled backward GEMMs (GM_BWD_DA with token-sorted dout, GM_BWD_DX;
+// bn = 256, the pair table of launch_pair_table, weight maps with 128-row
+// boxes).  Returns cudaErrorNotSupported when the device cannot hold a
+// cluster of two.
 cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace mok

@@ -23,6 +23,7 @@ constexpr int kHdrError = 0;
 constexpr int kHdrPaddedRows = 1;
 constexpr int kHdrTiles = 2;
 constexpr int kHdrAbort = 3;       // launch-wide abort word (cleared per call)
+constexpr int kHdrPairs = 4;       // CTA-pair tiles of the pair table (see launch_pair_table)
 constexpr int kHdrCounters = 16;    // [16, 48): per-launch dynamic tile counters
 constexpr int kNumCounters = 32;
 
@@ -39,7 +40,8 @@ struct WsLayout {
   size_t dhu;         // bf16 [pad_capacity, 2I]
   size_t as;          // bf16 [pad_capacity, I]  s * a
   size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
-  size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x, then dout (weight gradients)
+  size_t sorted;      // bf16 [pad_capacity, H]: token-sorted dout (dA', dW2), then x (dW1|dW3)
+  size_t pair_m0;     // int32 [tile_capacity]: CTA-pair tiles of dA' / dX (first M tile * 2 + solo)
   // MXFP8 operand copies
   size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
   size_t sfa_rows_t;  // the A operand's scales in padded-row order, tiled: [pad/128][max(H,2I)/128][512]
@@ -64,6 +66,7 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
 // Launchers (return a CUDA error code).
 cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, const int32_t* idx,
                             cudaStream_t st);
+cudaError_t launch_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* yk,
                            const float* scores, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_t* ws, float* ds, int n_parts,

@@ -93,12 +93,13 @@ def test_reruns_are_bitwise_identical(shape, routing):
 
 
 @pytest.mark.parametrize("shape,routing", [((512, 256, 256, 24, 4), "hot"), ((4096, 256, 256, 20, 2), "hot")])
-def test_weight_gradient_gather_paths_are_bitwise_equal(shape, routing):
-    """Token-sorted copies + plain TMA vs gathers fused in the load path."""
+def test_backward_gather_paths_are_bitwise_equal(shape, routing):
+    """dA' and the weight gradients: token-sorted copies + plain TMA (dA' on
+    CTA pairs) vs gathers fused in the load path (dA' on single CTAs)."""
     require_gpu()
     _, _, g_sorted = run_layer(shape, routing, 8)
     _, _, g_fused = run_layer(shape, routing, 8, debug_flags=4)
-    for k in ("dW1", "dW3", "dW2"):
+    for k in g_sorted:
         assert torch.equal(g_sorted[k], g_fused[k]), k
 
 
@@ -112,6 +113,27 @@ def test_weight_gradient_cta_pairs_match_single_cta(shape, routing):
     _, _, g_one = run_layer(shape, routing, 9, debug_flags=8)
     for k in ("dW1", "dW3", "dW2"):
         assert torch.equal(g_pair[k], g_one[k]), k
+
+
+@pytest.mark.parametrize("shape,routing,kw", [
+    ((4096, 256, 256, 8, 2), "zipf", {}),
+    # one tile per expert: every pair is a solo pair
+    ((256, 256, 256, 16, 2), "uniform", {}),
+    ((2048, 256, 256, 12, 4), "hot", dict(minibatch_rows=384, ring_slots=3)),
+    # I = 128: dA' on single CTAs (128-column tiles), dX on pairs
+    ((3000, 256, 128, 20, 2), "hot", {}),
+    ((4096, 256, 256, 16, 4), "zipf", dict(replay=True, minibatch_rows=256, ring_slots=2)),
+])
+def test_backward_row_gemm_cta_pairs_match_single_cta(shape, routing, kw):
+    """dA' and dX on clusters of two CTAs (two tiles of one expert per
+    cta_group::2 MMA; a solo tile's second CTA idle) against one CTA per
+    128-row tile: bitwise equal."""
+    require_gpu()
+    _, out_p, g_p = run_layer(shape, routing, 10, **kw)
+    _, out_s, g_s = run_layer(shape, routing, 10, debug_flags=16, **kw)
+    assert torch.equal(out_p, out_s)
+    for k in g_p:
+        assert torch.equal(g_p[k], g_s[k]), k
 
 
 def _run_with_idx(shape, idx, seed):
