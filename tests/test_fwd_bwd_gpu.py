@@ -28,6 +28,8 @@ CASES = [
     ("single_token", (1, 128, 128, 1, 1), "uniform", 11),
     ("max_experts", (512, 128, 128, 1024, 4), "uniform", 12),
     ("max_topk", (64, 256, 128, 40, 32), "uniform", 13),
+    # H >= 4096: dA' on CTA pairs too
+    ("long_h_pairs", (768, 4096, 256, 6, 2), "zipf", 14),
 ]
 
 
@@ -123,6 +125,9 @@ def test_weight_gradient_cta_pairs_match_single_cta(shape, routing):
     # I = 128: dA' on single CTAs (128-column tiles), dX on pairs
     ((3000, 256, 128, 20, 2), "hot", {}),
     ((4096, 256, 256, 16, 4), "zipf", dict(replay=True, minibatch_rows=256, ring_slots=2)),
+    # H >= 4096: dA' on pairs as well
+    ((2048, 4096, 256, 8, 2), "zipf", {}),
+    ((1024, 4096, 256, 24, 4), "hot", {}),
 ])
 def test_backward_row_gemm_cta_pairs_match_single_cta(shape, routing, kw):
     """dA' and dX on clusters of two CTAs (two tiles of one expert per
