@@ -60,6 +60,8 @@ def parse_args_from(argv):
     ap.add_argument("--debug-flags", type=int, default=0)
     # bounded-memory backward (forward context of ring_slots minibatches, GEMM1 recomputed)
     ap.add_argument("--replay", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="schedule + forward as one launch (mok_forward_fused, BF16)")
     return ap.parse_args(argv)
 
 
@@ -84,7 +86,8 @@ def flops_per_step(shape):
 
 def phase_flops(shape):
     RHI = float(shape.R) * shape.H * shape.I
-    return {"fwd_gemm": 6 * RHI, "bwd_da": 2 * RHI, "bwd_dx": 4 * RHI, "bwd_wg13": 4 * RHI, "bwd_wg2": 2 * RHI}
+    return {"fwd_gemm": 6 * RHI, "bwd_da": 2 * RHI, "bwd_dx": 4 * RHI, "bwd_wg13": 4 * RHI, "bwd_wg2": 2 * RHI,
+            "fwd_fused": 6 * RHI}
 
 
 def phase_min_bytes(shape, prec, active_experts):
@@ -289,6 +292,7 @@ def workload_config(args, shape, routing, prec, layer=None):
         if args.debug_flags:
             cfg["debug_flags"] = args.debug_flags
         cfg["replay"] = bool(args.replay)
+        cfg["fused_forward"] = bool(args.fused)
         cfg["ctx_bytes"] = int(layer.ctx.numel())
     return cfg
 
@@ -316,9 +320,18 @@ def run_mok(args):
     else:
         w_fwd = w_bwd = (inp["W1"], inp["W3"], inp["W2"])
 
+    if args.fused and prec != "bf16":
+        raise SystemExit("--fused: the single-launch forward is BF16 only")
+
+    def forward(x, idx, s, o):
+        if args.fused:
+            layer.forward_fused(idx, x, s, *w_fwd, out=o)
+        else:
+            layer.build_schedule(idx)
+            layer.forward(x, s, *w_fwd, out=o)
+
     def step(x, idx, s, dout):
-        layer.build_schedule(idx)
-        layer.forward(x, s, *w_fwd, out=out)
+        forward(x, idx, s, out)
         layer.backward(x, s, *w_bwd, dout, grads=grads)
 
     for _ in range(max(args.warmup, 3)):
@@ -458,8 +471,7 @@ def run_mok(args):
                 if i + 1 < n:
                     load(i + 1)
                 stream.wait_event(b["loaded"])
-                layer.build_schedule(b["idx"])
-                layer.forward(b["x"], b["s"], *w_fwd, out=b["out"])
+                forward(b["x"], b["idx"], b["s"], b["out"])
                 layer.backward(b["x"], b["s"], *w_bwd, b["dout"], grads=b["grads"])
                 b["computed"].record(stream)
                 with torch.cuda.stream(d2h_st):

@@ -204,6 +204,22 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
                        const void* W2, void* out, void* ctx, void* stream);
 
 /*
+ * The schedule and the forward in one persistent launch ([MTP]: the layer
+ * as a single kernel; the ring-token-buffer paragraph).  Same inputs as
+ * mok_build_schedule followed by mok_forward (MOK_BF16 only), same results
+ * bitwise -- the schedule arrays in the workspace (so mok_backward can
+ * follow), out and ctx.  The launch's work items, taken in order from a
+ * device counter, are: a histogram per 1,024 routed rows, the scan, the
+ * placement per 1,024 routed rows, the ring's GEMM1 / GEMM2 tiles, and the
+ * combine per 16 tokens; each waits (bounded) only on items before it.
+ * Clears the workspace error word first; an id outside [0, E) records
+ * MOK_ERR_BAD_INDEX as in mok_build_schedule.
+ */
+mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void* ws, size_t ws_bytes,
+                             const int32_t* topk_idx, const void* x, const float* scores, const void* W1,
+                             const void* W3, const void* W2, void* out, void* ctx, void* stream);
+
+/*
  * Backward ([MoK] "Use the functional API": backward(config, workspace,
  * schedule, fwd_ctx, ...) -> grads).  The router-score gradient is taken in
  * the SwiGLU-backward epilogue ([MTP], the paragraph after "Three design
@@ -285,11 +301,12 @@ enum {
   MOK_PHASE_BWD_WG13 = 7,      /* dW1 | dW3 grouped GEMM */
   MOK_PHASE_BWD_WG2 = 8,       /* dW2 grouped GEMM */
   MOK_PHASE_QUANT = 9,         /* MXFP8 quantisation of activations */
-  MOK_PHASE_BWD_SORT = 10,     /* token-sorted copies of x and dout for the weight gradients */
+  MOK_PHASE_BWD_SORT = 10,     /* token-sorted copies of dout and x (dA', weight gradients) */
   MOK_PHASE_ROUTER_FWD = 11,   /* router: logits GEMM, top-k, softmax */
   MOK_PHASE_ROUTER_BWD = 12,   /* router: logit gradient, dWr and dx GEMMs */
   MOK_PHASE_BWD_REPLAY = 13,   /* bounded-memory backward: GEMM1 recomputed, context copied back */
-  MOK_NUM_PHASES = 14
+  MOK_PHASE_FWD_FUSED = 14,    /* single-launch forward: schedule, GEMMs, combine */
+  MOK_NUM_PHASES = 15
 };
 mok_status mok_trace_enable(int32_t on);
 mok_status mok_trace_read(float* ms /* [MOK_NUM_PHASES] */, int32_t* count /* [MOK_NUM_PHASES] */);

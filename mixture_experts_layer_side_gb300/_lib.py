@@ -29,13 +29,14 @@ STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "M
 
 # every entry point include/mok.h declares
 EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_build_schedule", "mok_forward",
+           "mok_forward_fused",
            "mok_backward", "mok_mxfp8_quantize", "mok_gather_rows", "mok_gemm_bf16", "mok_check",
            "mok_device_sm_count", "mok_status_string", "mok_version", "mok_trace_enable", "mok_trace_read",
            "mok_launch_count", "mok_build_schedule_noalloc", "mok_gemm_mxfp8", "mok_router_workspace_size",
            "mok_router_forward", "mok_router_backward"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
-          "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd", "bwd_replay"]
+          "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd", "bwd_replay", "fwd_fused"]
 
 
 class MokError(RuntimeError):
@@ -85,6 +86,7 @@ def _load():
         "mok_workspace_layout": (i32, [S, C, i32, ctypes.POINTER(MokLayout)]),
         "mok_build_schedule": (i32, [S, C, P, sz, P, P]),
         "mok_forward": (i32, [S, C, i32, P, sz, P, P, P, P, P, P, P, P]),
+        "mok_forward_fused": (i32, [S, C, P, sz, P, P, P, P, P, P, P, P, P]),
         "mok_backward": (i32, [S, C, i32, P, sz, P, P, P, P, P, P, P, P, P, P, P, P, P]),
         "mok_mxfp8_quantize": (i32, [P, i32, i32, i32, i32, P, P, P]),
         "mok_gather_rows": (i32, [S, C, P, sz, P, P, P]),
@@ -182,6 +184,12 @@ def mok_forward(shape, cfg, prec, ws, x, scores, W1, W3, W2, out, ctx, stream=No
     _ok(LIB.mok_forward(ctypes.byref(shape), ctypes.byref(cfg), prec, _ptr(ws), ws.numel() * ws.element_size(),
                         _ptr(x), _ptr(scores), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(out), _ptr(ctx),
                         _stream(stream)), "mok_forward")
+
+
+def mok_forward_fused(shape, cfg, ws, idx, x, scores, W1, W3, W2, out, ctx, stream=None):
+    _ok(LIB.mok_forward_fused(ctypes.byref(shape), ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+                              _ptr(idx), _ptr(x), _ptr(scores), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(out),
+                              _ptr(ctx), _stream(stream)), "mok_forward_fused")
 
 
 def mok_backward(shape, cfg, prec, ws, ctx, x, scores, W1, W3, W2, dout, dX, dW1, dW3, dW2, dscores, stream=None):

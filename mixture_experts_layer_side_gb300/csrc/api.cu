@@ -699,6 +699,65 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   return MOK_OK;
 }
 
+mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void* ws, size_t ws_bytes,
+                             const int32_t* topk_idx, const void* x, const float* scores, const void* W1,
+                             const void* W3, const void* W2, void* out, void* ctx, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  if (!ws || !topk_idx || !x || !scores || !W1 || !W3 || !W2 || !out || !ctx) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  const WsLayout L = ws_layout(s, *cfg, MOK_BF16, device_sm_count());
+  if (ws_bytes < L.total) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  // the whole header (error word, schedule totals, item counters) and the ring flags
+  MOK_CUDA(cudaMemsetAsync(w + L.header, 0, kHeaderWords * 4, st));
+  MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 2 * L.tile_capacity * 4, st));
+  const int M = L.minibatch_rows, S = L.ring_slots;
+  const int bn2 = (s.H % 256 == 0) ? 256 : 128;
+  auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(w + off); };
+  GemmParams g;
+  base_params(g, s, L, w);
+  g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
+  g.ctx_ring = cfg->replay;
+  g.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);
+  g.ring_rows = M;
+  g.ring_slots = S;
+  g.ring_flags = reinterpret_cast<uint32_t*>(w + L.ring_flags);
+  g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
+  g.debug_flags = cfg->debug_flags;
+  g.gather_src = static_cast<const __nv_bfloat16*>(x);
+  g.scores = scores;
+  g.out = static_cast<__nv_bfloat16*>(out);
+  g.topk_idx = topk_idx;
+  g.nchunks = (int)L.nchunks;
+  g.chunk_hist = I32(L.chunk_hist);
+  g.chunk_base = I32(L.chunk_base);
+  g.s_counts = I32(L.counts);
+  g.s_offsets = I32(L.offsets);
+  g.s_poff = I32(L.padded_offsets);
+  g.s_perm = I32(L.perm);
+  g.s_inv_perm = I32(L.inv_perm);
+  g.s_pad_perm = I32(L.pad_perm);
+  g.s_pad_inv = I32(L.pad_inv);
+  g.s_tile_expert = I32(L.tile_expert);
+  TmapSet maps;
+  memset(&maps, 0, sizeof(maps));
+  if (!map_gather(&maps.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
+  if (!map3d(&maps.m[1], W1, s.I, s.H, s.E, 64) || !map3d(&maps.m[2], W3, s.I, s.H, s.E, 64)) return MOK_ERR_CUDA;
+  if (!map2d(&maps.m[3], g.ring, s.I, (uint64_t)S * M, 128) || !map3d(&maps.m[4], W2, s.H, s.I, s.E, 64))
+    return MOK_ERR_CUDA;
+  g.nmaps = 5;
+  g.bn = bn2;
+  g.n_tiles = s.H / bn2;
+  g.g1_tiles = s.I / 128;
+  g.m_tiles = (int)L.tile_capacity;
+  g.counter = 0;
+  Phase ph(MOK_PHASE_FWD_FUSED, st, 1);
+  MOK_CUDA(launch_gemm(GM_FWD_FUSED, maps, g, gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles)), st));
+  return MOK_OK;
+}
+
 mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_precision prec, void* ws,
                         size_t ws_bytes, const void* ctx, const void* x, const float* scores, const void* W1,
                         const void* W3, const void* W2, const void* dout, void* dX, void* dW1, void* dW3,

@@ -36,6 +36,8 @@
 // scatter-in-epilogue (same section, communication-direction paragraph);
 // the ring token buffer consumed per minibatch (ring-token-buffer paragraph);
 // router gradient fused into the SwiGLU backward (paragraph after the list).
+#include <climits>
+
 #include "gemm.cuh"
 #include "mx.cuh"
 #include "tc.cuh"
@@ -62,6 +64,7 @@ struct Ctl {
   int n_skip;  // experts ahead of this launch's row range in that order
   int n_sel;   // experts in this launch's row range (its items)
   int pair_rank;  // CTA-pair launches: 0 for the leader (issues the MMAs), 1 for the other
+  int combine_go;  // single-launch forward: 1 once every GEMM2 row of y is stored, 2 on a wait that gave up
 };
 
 // A decoded work item.
@@ -76,6 +79,22 @@ struct Item {
 };
 
 __device__ __forceinline__ int used_tiles(const GemmParams& p) { return p.hdr[kHdrTiles]; }
+
+// The ring launch, alone or inside the single-launch forward.
+template <int MODE>
+__device__ __forceinline__ constexpr bool is_ring() { return MODE == GM_FWD_RING || MODE == GM_FWD_FUSED; }
+
+// Single-launch forward: items [0, nch) histogram one chunk of routed rows
+// each, item nch scans, items [nch + 1, 2 nch + 1) place one chunk each,
+// then come the ring's items; every item waits only on items before it.
+// A CTA that draws past the last item runs the combine phase (its warps
+// take tokens from a second counter) and stops.
+constexpr int kItemCount = 16, kItemScan = 17, kItemPlace = 18, kItemCombine = 19;
+__device__ __forceinline__ int fused_ring_base(const GemmParams& p) { return 2 * p.nchunks + 1; }
+// (valid once the scan item has published the tile count)
+__device__ __forceinline__ int fused_total(const GemmParams& p) {
+  return fused_ring_base(p) + used_tiles(p) * (p.g1_tiles + p.n_tiles);
+}
 
 // Number of work items of a launch (device-side: depends on the schedule).
 template <int MODE>
@@ -178,6 +197,31 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     it.n = r % p.n_tiles;
     it.row0 = po[it.e];
     it.k_iters = oe >> 10;
+  } else if constexpr (MODE == GM_FWD_FUSED) {
+    const int nch = p.nchunks, a0 = fused_ring_base(p);
+    it.n = 0;
+    it.e = 0;
+    it.row0 = 0;
+    it.k_iters = 0;
+    if (w < a0) {
+      it.type = w < nch ? kItemCount : w == nch ? kItemScan : kItemPlace;
+      it.m = w < nch ? w : w == nch ? 0 : w - nch - 1;
+    } else {
+      const int ring_items = used_tiles(p) * (p.g1_tiles + p.n_tiles);
+      if (w - a0 >= ring_items) {
+        it.type = kItemCombine;
+        it.m = 0;
+      } else {
+        int type, m, n;
+        decode_ring(p, w - a0, type, m, n);
+        it.type = type;
+        it.m = m;
+        it.n = n;
+        it.e = p.tile_expert[m];
+        it.row0 = m * kTileRows;
+        it.k_iters = row_k_iters(p, type, kEl);
+      }
+    }
   } else if constexpr (PAIR) {
     // dA' / dX on CTA pairs: the leader takes the pair's first tile, the
     // other CTA the second (or, in a solo pair, the first again, idle)
@@ -228,7 +272,7 @@ __device__ __forceinline__ int gathered_operand(const GemmParams& p, int type) {
 
 template <int MODE>
 __device__ __forceinline__ constexpr bool mode_gathers() {
-  return MODE == GM_FWD1 || MODE == GM_BWD_DA || MODE == GM_WG13 || MODE == GM_WG2 || MODE == GM_FWD_RING;
+  return MODE == GM_FWD1 || MODE == GM_BWD_DA || MODE == GM_WG13 || MODE == GM_WG2 || is_ring<MODE>();
 }
 
 // Bytes the TMA producer brings into one stage (gathered operands excluded).
@@ -258,8 +302,8 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
     for (int c = 0; c < 2; ++c) tma_load_3d(b + c * 8192, &mp.m[1], bar, it.n * 128 + c * 64, kk * 64, it.e);
     for (int c = 0; c < 2; ++c) tma_load_3d(b + (2 + c) * 8192, &mp.m[2], bar, it.n * 128 + c * 64, kk * 64, it.e);
   } else if (type == GM_FWD2) {
-    const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
-    const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
+    const int mslot = is_ring<MODE>() ? 3 : 0;
+    const int wmap = is_ring<MODE>() ? 4 : 1;
     tma_load_2d(a, &mp.m[mslot], bar, kk * 64, ring_row(p, it.row0));
     for (int c = 0; c < p.bn / 64; ++c) tma_load_3d(b + c * 8192, &mp.m[wmap], bar, it.n * p.bn + c * 64, kk * 64, it.e);
   } else if (type == GM_BWD_DA) {
@@ -942,6 +986,291 @@ __device__ void zero_empty_experts(const GemmParams& p, const Ctl* ctl, int gw, 
   }
 }
 
+
+// ---------------------------------------------------------------- single-launch forward
+// The schedule and combine items of GM_FWD_FUSED.  The four gather warps
+// (128 threads, named barrier 1) run the schedule items; they and the four
+// epilogue warps (256 threads) run the combine items.  Each item publishes
+// its completion with a release add on a header counter, and every item
+// that reads another's output acquires that counter first (bounded waits).
+// The arithmetic is the schedule kernels' and the combine kernel's, so the
+// arrays and the output are bitwise those of the separate launches.
+__device__ __forceinline__ void gather_warps_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t* hdr_word(const GemmParams& p, int i) {
+  return reinterpret_cast<uint32_t*>(&p.hdr[i]);
+}
+
+// Expert histogram of routed-row chunk c (ids outside [0, E) set the error bit).
+__device__ void fused_count(const GemmParams& p, int c, int* hist, int gt) {
+  const int E = p.E, R = p.T * p.k;
+  for (int e = gt; e < E; e += 128) hist[e] = 0;
+  gather_warps_sync();
+  const int f0 = c * kSchedChunk, f1 = min(f0 + kSchedChunk, R);
+  bool bad = false;
+  for (int f = f0 + gt; f < f1; f += 128) {
+    const int e = p.topk_idx[f];
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) atomicOr(&p.hdr[kHdrError], MOK_ERRBIT_BAD_INDEX);
+  gather_warps_sync();
+  for (int e = gt; e < E; e += 128) p.chunk_hist[(size_t)c * E + e] = hist[e];
+  __threadfence();
+  gather_warps_sync();
+  if (gt == 0) red_release_gpu_add(hdr_word(p, kHdrCountDone), 1u);
+}
+
+// Per expert the running base of every chunk, then the exclusive scans of
+// the counts and of the 128-padded counts (thread gt owns the contiguous
+// experts [gt * per, gt * per + per)), the tile table and the padding rows'
+// -1 markers.  tot: 8 ints of shared memory.
+__device__ void fused_scan(const GemmParams& p, int* tot, int gt) {
+  const int E = p.E, nch = p.nchunks, per = (E + 127) / 128;
+  const int lane = gt & 31, wg = gt >> 5;
+  int cnt[8];
+  int tc = 0, tp = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    cnt[i] = 0;
+    const int e = gt * per + i;
+    if (i < per && e < E) {
+      // loads independent of the running sum: eight in flight at a time
+      int run = 0, c = 0;
+      for (; c + 8 <= nch; c += 8) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = p.chunk_hist[(size_t)(c + u) * E + e];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          p.chunk_base[(size_t)(c + u) * E + e] = run;
+          run += v[u];
+        }
+      }
+      for (; c < nch; ++c) {
+        const int v = p.chunk_hist[(size_t)c * E + e];
+        p.chunk_base[(size_t)c * E + e] = run;
+        run += v;
+      }
+      cnt[i] = run;
+      tc += run;
+      tp += (run + kTileRows - 1) / kTileRows * kTileRows;
+    }
+  }
+  int ic = tc, ip = tp;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ic, d), b = __shfl_up_sync(0xffffffffu, ip, d);
+    if (lane >= d) {
+      ic += a;
+      ip += b;
+    }
+  }
+  if (lane == 31) {
+    tot[wg] = ic;
+    tot[4 + wg] = ip;
+  }
+  gather_warps_sync();
+  int bc = ic - tc, bp = ip - tp;
+  for (int v = 0; v < wg; ++v) {
+    bc += tot[v];
+    bp += tot[4 + v];
+  }
+  const int total_c = tot[0] + tot[1] + tot[2] + tot[3];
+  const int total_p = tot[4] + tot[5] + tot[6] + tot[7];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = gt * per + i;
+    if (i < per && e < E) {
+      const int padded = (cnt[i] + kTileRows - 1) / kTileRows * kTileRows;
+      p.s_counts[e] = cnt[i];
+      p.s_offsets[e] = bc;
+      p.s_poff[e] = bp;
+      for (int t = bp / kTileRows; t < (bp + padded) / kTileRows; ++t) p.s_tile_expert[t] = e;
+      for (int r = bp + cnt[i]; r < bp + padded; ++r) p.s_pad_perm[r] = -1;
+      bc += cnt[i];
+      bp += padded;
+    }
+  }
+  if (gt == 0) {
+    p.s_offsets[E] = total_c;
+    p.s_poff[E] = total_p;
+    p.hdr[kHdrPaddedRows] = total_p;
+    p.hdr[kHdrTiles] = total_p / kTileRows;
+  }
+  __threadfence();
+  gather_warps_sync();
+  if (gt == 0) red_release_gpu_add(hdr_word(p, kHdrScanDone), 1u);
+}
+
+// Places chunk c's rows (one warp; cursor: E ints of shared memory): rows of
+// one expert in increasing f, after the chunk's base.
+__device__ void fused_place(const GemmParams& p, int c, int* cursor, int lane) {
+  const int E = p.E, R = p.T * p.k;
+  for (int e = lane; e < E; e += 32) cursor[e] = p.chunk_base[(size_t)c * E + e];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const int f0 = c * kSchedChunk;
+  for (int i = 0; i < kSchedChunk / 32; ++i) {
+    const int f = f0 + i * 32 + lane;
+    int e = -1;
+    if (f < R) {
+      e = p.topk_idx[f];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(grp & lt);
+    int pos = 0;
+    if (e >= 0) pos = cursor[e] + rank;
+    __syncwarp();
+    if (e >= 0 && rank == 0) cursor[e] += __popc(grp);
+    __syncwarp();
+    if (f < R) {
+      if (e >= 0) {
+        const int r = p.s_offsets[e] + pos, prow = p.s_poff[e] + pos;
+        p.s_perm[r] = f;
+        p.s_inv_perm[f] = r;
+        p.s_pad_perm[prow] = f;
+        p.s_pad_inv[f] = prow;
+      } else {
+        p.s_inv_perm[f] = -1;
+        p.s_pad_inv[f] = -1;
+      }
+    }
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) red_release_gpu_add(hdr_word(p, kHdrPlaceDone), 1u);
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4& v, float (&o)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    o[2 * i] = f.x;
+    o[2 * i + 1] = f.y;
+  }
+}
+
+// out[t] = sum_j s[t,j] y[t*k+j] for one token, by one warp: f32,
+// increasing j, one rounding.  A lane takes two 16-byte column chunks at a
+// time and the token's rows eight at a time (16 loads in flight); the
+// token's weights and row validity are L1 hits after the first chunk.
+__device__ void combine_token(const GemmParams& p, int t, int lane) {
+  const int hv = p.H / 8, k = p.k;
+  const long fb = (long)t * k;
+  for (int c0 = lane; c0 < hv; c0 += 64) {
+    const int c1 = c0 + 32;
+    const bool two = c1 < hv;
+    float acc0[8], acc1[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc0[e] = acc1[e] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 v0[8], v1[8];
+      float wgt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        wgt[j] = 0.0f;
+        v0[j] = v1[j] = make_uint4(0, 0, 0, 0);
+        if (j0 + j < k && p.s_pad_inv[fb + j0 + j] >= 0) {
+          const uint4* row = reinterpret_cast<const uint4*>(p.yk + (fb + j0 + j) * p.H);
+          wgt[j] = p.scores[fb + j0 + j];
+          v0[j] = __ldcs(row + c0);
+          if (two) v1[j] = __ldcs(row + c1);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j < k) {
+          float y[8];
+          unpack8_bf16(v0[j], y);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc0[e] = fmaf(wgt[j], y[e], acc0[e]);
+          unpack8_bf16(v1[j], y);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc1[e] = fmaf(wgt[j], y[e], acc1[e]);
+        }
+      }
+    }
+    uint4* orow = reinterpret_cast<uint4*>(p.out + (long)t * p.H);
+    orow[c0] = make_uint4(pack_bf16x2(acc0[0], acc0[1]), pack_bf16x2(acc0[2], acc0[3]),
+                          pack_bf16x2(acc0[4], acc0[5]), pack_bf16x2(acc0[6], acc0[7]));
+    if (two)
+      orow[c1] = make_uint4(pack_bf16x2(acc1[0], acc1[1]), pack_bf16x2(acc1[2], acc1[3]),
+                            pack_bf16x2(acc1[4], acc1[5]), pack_bf16x2(acc1[6], acc1[7]));
+  }
+}
+
+// The combine phase, by each of the four gather warps and four epilogue
+// warps: wait until every GEMM2 epilogue warp has published its rows of y
+// (one thread per CTA polls the global count, the other warps its outcome
+// in shared memory), then take tokens from a device counter until none is
+// left.  False: a bounded wait gave up.
+__device__ bool fused_combine_phase(const GemmParams& p, Ctl* ctl, int warp, int lane, const WaitCtx& wc) {
+  volatile int* go = &ctl->combine_go;
+  int state = 0;
+  if (lane == 0) {
+    if (warp == 6) {
+      state = wait_flag_geq(hdr_word(p, kHdrG2Done), 4u * (uint32_t)(used_tiles(p) * p.n_tiles), wc) ? 1 : 2;
+      __threadfence_block();
+      *go = state;
+    } else {
+      const uint64_t t0 = globaltimer();
+      for (uint32_t it = 1; (state = *go) == 0; ++it) {
+        __nanosleep(128);
+        if ((it & 15u) == 0 && (wait_aborted(wc) || globaltimer() - t0 > kWaitLimitNs)) {
+          state = 2;
+          break;
+        }
+      }
+      __threadfence_block();
+    }
+  }
+  state = __shfl_sync(0xffffffffu, state, 0);
+  __syncwarp();  // the other lanes' loads of y after lane 0's acquire
+  if (state != 1) return false;
+  while (true) {
+    int t = 0;
+    if (lane == 0) t = atomicAdd(reinterpret_cast<int*>(hdr_word(p, kHdrCombineNext)), 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t >= p.T) break;
+    combine_token(p, t, lane);
+  }
+  return true;
+}
+
+// The gather warps' part of a schedule or combine item (false: a bounded
+// wait gave up).
+__device__ bool fused_aux_gather(const GemmParams& p, Ctl* ctl, const Item& it, int gt, const WaitCtx& wc) {
+  const int lane = gt & 31;
+  bool ok = true;
+  if (it.type == kItemCount) {
+    fused_count(p, it.m, ctl->po, gt);
+  } else if (it.type == kItemScan) {
+    // thread 0 acquires the count items' completions and hands the outcome
+    // to all 128 threads through shared memory, so that either all or none
+    // of them enter the scan's barriers
+    volatile int* go = ctl->order + 16;
+    if (gt == 0) *go = wait_flag_geq(hdr_word(p, kHdrCountDone), (uint32_t)p.nchunks, wc) ? 1 : 0;
+    gather_warps_sync();
+    ok = *go != 0;
+    if (ok) fused_scan(p, ctl->order, gt);
+  } else if (it.type == kItemPlace) {
+    // (one warp; the other three go on to the next item)
+    if (gt < 32) {
+      if (lane == 0) ok = wait_flag_geq(hdr_word(p, kHdrScanDone), 1u, wc);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (ok) fused_place(p, it.m, ctl->po, lane);
+    }
+  } else {
+    ok = fused_combine_phase(p, ctl, 6 + (gt >> 5), lane, wc);
+  }
+  return ok;
+}
+
 // At exit, how long a CTA waits for copies still in flight after an abort.
 constexpr uint64_t kDrainNs = 20000000ull;  // 20 ms
 
@@ -1004,6 +1333,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     ctl->n_skip = 0;
     ctl->n_sel = 0;
     ctl->pair_rank = (int)rank;
+    ctl->combine_go = 0;
     ctl->tmem_base = 0;  // a 512-column allocation always starts at column 0
     fence_mbar_init();
   }
@@ -1046,9 +1376,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int num_items = kWgrad ? ctl->n_sel * (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles
-                        : PAIR ? count_pair_items(p)
-                               : count_items<MODE>(p);
+  // (single-launch forward: known once the schedule items are done)
+  int num_items = kWgrad ? ctl->n_sel * (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles
+                  : PAIR ? count_pair_items(p)
+                  : MODE == GM_FWD_FUSED ? INT_MAX
+                                         : count_items<MODE>(p);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer + work fetch
@@ -1100,8 +1432,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           f3 = f2 + 1;
         }
         bool ok = true;
+        bool sched_ready = false, combine_sent = false;
         while (ok) {
-          if (w >= num_items) w = -1;
+          if (MODE == GM_FWD_FUSED && !sched_ready && w >= fused_ring_base(p)) {
+            // the ring's and the combine's items read the whole schedule:
+            // acquire the place items' completions before publishing them
+            sched_ready = true;
+            if (wait_flag_geq(hdr_word(p, kHdrPlaceDone), (uint32_t)p.nchunks, wc))
+              num_items = fused_total(p);
+            else
+              w = -1;
+          }
+          if (MODE == GM_FWD_FUSED && w >= num_items && num_items != INT_MAX && !combine_sent) {
+            // past the last item: this CTA's combine phase, then the end
+            w = num_items;
+            combine_sent = true;
+          } else if (w >= num_items) {
+            w = -1;
+          }
           ok = PAIR ? mbar_wait_cluster(&ctl->qempty[qs], qp ^ 1, wc) : mbar_wait(&ctl->qempty[qs], qp ^ 1, wc);
           const int wq = ok ? w : -1;
           ctl->q[qs] = wq;
@@ -1123,7 +1471,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             w_next = (int)atomicAdd(counter, 1u);
           }
           const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
-          if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
+          if (is_ring<MODE>() && it.type == GM_FWD2) {
             // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
             // of its GEMM1 column tiles are published, then order the
             // async-proxy loads after the acquire
@@ -1163,6 +1511,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
       }
     }
+    // lanes 1-31 skipped the producer loop: the warp reaches the final
+    // barrier converged
+    __syncwarp();
   } else if (warp >= 6) {
     // ---------------------------------------------------------------- gather producers
     if (gather_in_pipe) {
@@ -1177,6 +1528,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (w < 0) break;
         const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
         bool ok = true;
+        if constexpr (MODE == GM_FWD_FUSED) {
+          if (it.type >= kItemCount) {
+            if (!fused_aux_gather(p, ctl, it, gt, wc)) break;
+            continue;
+          }
+        }
         if constexpr (MX) {
           int tok[8];
           int tok_row = -1;
@@ -1229,6 +1586,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
       const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
+      if (MODE == GM_FWD_FUSED && it.type >= kItemCount) continue;  // no MMA
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       // (CTA pairs: released by both CTAs' epilogue warps)
       if (!(PAIR ? mbar_wait_cluster(&ctl->tempty[buf], tph ^ 1, wc) : mbar_wait(&ctl->tempty[buf], tph ^ 1, wc)))
@@ -1314,6 +1672,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (++qs == kQueue) { qs = 0; qp ^= 1; }
       if (w < 0) break;
       const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
+      if (MODE == GM_FWD_FUSED && it.type >= kItemCount) {
+        // schedule items are the gather warps'; combine items are shared
+        if (it.type == kItemCombine && !fused_combine_phase(p, ctl, warp, lane, wc)) break;
+        continue;
+      }
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
       if (!mbar_wait(&ctl->tfull[buf], tph, wc)) break;
       tc_fence_after();
@@ -1333,13 +1696,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_arrive(&ctl->tempty[buf]);
         }
       };
-      if (MODE == GM_FWD_RING && it.type == GM_FWD2 && warp == 2 && lane == 0) {
+      if (is_ring<MODE>() && it.type == GM_FWD2 && warp == 2 && lane == 0) {
         // the accumulator is complete, so every load of this tile's ring
         // rows has landed: release the rows for reuse
         red_release_gpu_add(&p.ring_flags[p.m_tiles + it.m], 1u);
       }
       bool ok = true;
-      if (MODE == GM_FWD_RING && it.type == GM_FWD1) {
+      if (is_ring<MODE>() && it.type == GM_FWD1) {
         // the ring slot rows this tile writes were last read by GEMM2 of the
         // tile ring_slots minibatches back; each warp waits on its own (no
         // CTA-level barrier on a path that a bounded wait can abandon)
@@ -1363,7 +1726,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         default: epi_wgrad<MX && MODE == GM_WG13>(p, it, tbase, q, lane, stage_out, release_acc); break;
       }
       release_acc();
-      if (MODE == GM_FWD_RING && it.type == GM_FWD1) {
+      if (MODE == GM_FWD_FUSED && it.type == GM_FWD2) {
+        // this warp's 32 rows of y are stored: count it for the combine items
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          red_release_gpu_add(hdr_word(p, kHdrG2Done), 1u);
+        }
+      }
+      if (is_ring<MODE>() && it.type == GM_FWD1) {
         // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
         // read by TMA): each epilogue warp adds 1, so a tile is complete when
         // its counter reaches 4 * (GEMM1 column tiles)
@@ -1380,7 +1751,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
 
   tc_fence_before();
-  __syncthreads();
+  // (the non-aligned barrier form, defined for warps that arrive diverged;
+  // the aligned __syncthreads form is not)
+  asm volatile("barrier.sync 0;" ::: "memory");
   // CTA pairs: neither CTA leaves (nor frees TMEM) while the other may
   // still signal its barriers or run MMAs on its smem and TMEM
   if constexpr (PAIR) cluster_sync();
@@ -1466,6 +1839,7 @@ cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int 
     case GM_WG13: return launch_mode<GM_WG13, false>(maps, p, grid, st);
     case GM_WG2: return launch_mode<GM_WG2, false>(maps, p, grid, st);
     case GM_FWD_RING: return launch_mode<GM_FWD_RING, false>(maps, p, grid, st);
+    case GM_FWD_FUSED: return launch_mode<GM_FWD_FUSED, false>(maps, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -14,7 +14,8 @@ enum GemmMode : int {
   GM_BWD_DX = 4,  // dx = [dh|du] * [W1|W3]^T;     epilogue scatter -> dXk[f]
   GM_WG13 = 5,    // [dW1|dW3]_e = gather(x)_e^T * [dh|du]_e
   GM_WG2 = 6,     // dW2_e = (s a)_e^T * gather(dout)_e
-  GM_FWD_RING = 7 // GM_FWD1 and GM_FWD2 interleaved through the minibatch ring in one launch
+  GM_FWD_RING = 7, // GM_FWD1 and GM_FWD2 interleaved through the minibatch ring in one launch
+  GM_FWD_FUSED = 8 // the whole forward in one launch: schedule items, the ring's items, combine items
 };
 
 constexpr int kStages = 4;
@@ -79,6 +80,21 @@ struct GemmParams {
   int rows_sorted;         // dA' reads a token-sorted copy of dout (plain TMA)
   // CTA-pair launches of dA' / dX: the pair table (first M tile * 2 + solo)
   const int32_t* pair_m0;
+  // single-launch forward (GM_FWD_FUSED): the schedule's input and arrays
+  // (written by its schedule items), and the combine's output
+  const int32_t* topk_idx;
+  int nchunks;             // routed-row chunks of kSchedChunk rows
+  int32_t* chunk_hist;     // [nchunks, E]
+  int32_t* chunk_base;     // [nchunks, E]
+  int32_t* s_counts;       // [E]
+  int32_t* s_offsets;      // [E + 1]
+  int32_t* s_poff;         // [E + 1]
+  int32_t* s_perm;         // [R]
+  int32_t* s_inv_perm;     // [R]
+  int32_t* s_pad_perm;     // [pad]
+  int32_t* s_pad_inv;      // [R]
+  int32_t* s_tile_expert;  // [tile_capacity]
+  __nv_bfloat16* out;      // [T, H]
   // ---- MXFP8 (E4M3 codes, E8M0 scales per 32 K-elements)
   // K-major operands: scales [rows][K/32], four bytes per row per stage,
   // copied by the gather threads; rows of A are gathered by token when A is.

@@ -24,6 +24,13 @@ constexpr int kHdrPaddedRows = 1;
 constexpr int kHdrTiles = 2;
 constexpr int kHdrAbort = 3;       // launch-wide abort word (cleared per call)
 constexpr int kHdrPairs = 4;       // CTA-pair tiles of the pair table (see launch_pair_table)
+// single-launch forward: completed schedule items (count, scan, place) and
+// completed GEMM2 epilogue warps
+constexpr int kHdrCountDone = 5;
+constexpr int kHdrScanDone = 6;
+constexpr int kHdrPlaceDone = 7;
+constexpr int kHdrG2Done = 8;
+constexpr int kHdrCombineNext = 9;  // next token of the single-launch forward's combine
 constexpr int kHdrCounters = 16;    // [16, 48): per-launch dynamic tile counters
 constexpr int kNumCounters = 32;
 

@@ -44,6 +44,14 @@ class MoKLayer:
         _lib.mok_forward(self.cshape, self.cfg, self.prec, self.ws, x, scores, W1, W3, W2, out, self.ctx, stream)
         return out
 
+    def forward_fused(self, topk_idx, x, scores, W1, W3, W2, out=None, stream=None):
+        """Schedule and forward in one launch (BF16); backward may follow."""
+        if out is None:
+            out = torch.empty((self.shape.T, self.shape.H), dtype=torch.bfloat16, device=self.device)
+        _lib.mok_forward_fused(self.cshape, self.cfg, self.ws, topk_idx, x, scores, W1, W3, W2, out, self.ctx,
+                               stream)
+        return out
+
     def backward(self, x, scores, W1, W3, W2, dout, grads=None, stream=None):
         s = self.shape
         if grads is None:
