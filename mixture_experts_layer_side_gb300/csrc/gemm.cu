@@ -1156,65 +1156,72 @@ __device__ __forceinline__ void unpack8_bf16(const uint4& v, float (&o)[8]) {
 }
 
 // out[t] = sum_j s[t,j] y[t*k+j] for one token, by one warp: f32,
-// increasing j, one rounding.  A lane takes two 16-byte column chunks at a
-// time and the token's rows eight at a time (16 loads in flight); the
-// token's weights and row validity are L1 hits after the first chunk.
-__device__ void combine_token(const GemmParams& p, int t, int lane) {
+// increasing j, one rounding.  The warp stages four 16-byte column chunks
+// per lane of eight rows at a time in its 16 KB of the (then idle) stage
+// buffers with cp.async, so 32 copies per lane are in flight without
+// holding registers; rows of no expert are zero-filled with weight 0, as
+// in the combine kernel.
+__device__ void combine_token(const GemmParams& p, int t, int lane, uint8_t* buf) {
   const int hv = p.H / 8, k = p.k;
   const long fb = (long)t * k;
-  for (int c0 = lane; c0 < hv; c0 += 64) {
-    const int c1 = c0 + 32;
-    const bool two = c1 < hv;
-    float acc0[8], acc1[8];
+  const uint32_t sb = smem_u32(buf);
+  for (int cb = 0; cb < hv; cb += 128) {
+    float acc[4][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc0[e] = acc1[e] = 0.0f;
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[q][e] = 0.0f;
     for (int j0 = 0; j0 < k; j0 += 8) {
-      uint4 v0[8], v1[8];
       float wgt[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        wgt[j] = 0.0f;
-        v0[j] = v1[j] = make_uint4(0, 0, 0, 0);
-        if (j0 + j < k && p.s_pad_inv[fb + j0 + j] >= 0) {
-          const uint4* row = reinterpret_cast<const uint4*>(p.yk + (fb + j0 + j) * p.H);
-          wgt[j] = p.scores[fb + j0 + j];
-          v0[j] = __ldcs(row + c0);
-          if (two) v1[j] = __ldcs(row + c1);
+        const bool ok = j0 + j < k && p.s_pad_inv[fb + j0 + j] >= 0;
+        wgt[j] = ok ? p.scores[fb + j0 + j] : 0.0f;
+        const __nv_bfloat16* row = p.yk + (fb + min(j0 + j, k - 1)) * p.H;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = cb + lane + 32 * q;
+          const bool in = ok && c < hv;
+          cp_async_16(sb + ((q * 8 + j) * 32 + lane) * 16, row + (in ? c : 0) * 8, in ? 16u : 0u);
         }
       }
+      asm volatile("cp.async.wait_all;" ::: "memory");
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (j0 + j < k) {
-          float y[8];
-          unpack8_bf16(v0[j], y);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc0[e] = fmaf(wgt[j], y[e], acc0[e]);
-          unpack8_bf16(v1[j], y);
+          for (int q = 0; q < 4; ++q) {
+            float y[8];
+            unpack8_bf16(*reinterpret_cast<const uint4*>(buf + ((q * 8 + j) * 32 + lane) * 16), y);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc1[e] = fmaf(wgt[j], y[e], acc1[e]);
+            for (int e = 0; e < 8; ++e) acc[q][e] = fmaf(wgt[j], y[e], acc[q][e]);
+          }
         }
       }
     }
     uint4* orow = reinterpret_cast<uint4*>(p.out + (long)t * p.H);
-    orow[c0] = make_uint4(pack_bf16x2(acc0[0], acc0[1]), pack_bf16x2(acc0[2], acc0[3]),
-                          pack_bf16x2(acc0[4], acc0[5]), pack_bf16x2(acc0[6], acc0[7]));
-    if (two)
-      orow[c1] = make_uint4(pack_bf16x2(acc1[0], acc1[1]), pack_bf16x2(acc1[2], acc1[3]),
-                            pack_bf16x2(acc1[4], acc1[5]), pack_bf16x2(acc1[6], acc1[7]));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = cb + lane + 32 * q;
+      if (c < hv)
+        orow[c] = make_uint4(pack_bf16x2(acc[q][0], acc[q][1]), pack_bf16x2(acc[q][2], acc[q][3]),
+                             pack_bf16x2(acc[q][4], acc[q][5]), pack_bf16x2(acc[q][6], acc[q][7]));
+    }
   }
 }
 
 // The combine phase, by each of the four gather warps and four epilogue
-// warps: wait until every GEMM2 epilogue warp has published its rows of y
-// (one thread per CTA polls the global count, the other warps its outcome
-// in shared memory), then take tokens from a device counter until none is
-// left.  False: a bounded wait gave up.
-__device__ bool fused_combine_phase(const GemmParams& p, Ctl* ctl, int warp, int lane, const WaitCtx& wc) {
+// warps: wait until the epilogue warps of every CTA have published that
+// their rows of y are stored (one thread per CTA polls the global count,
+// the other warps its outcome in shared memory), then take tokens from a
+// device counter until none is left.  False: a bounded wait gave up.
+__device__ bool fused_combine_phase(const GemmParams& p, Ctl* ctl, uint8_t* stages, int warp, int lane,
+                                    const WaitCtx& wc) {
   volatile int* go = &ctl->combine_go;
   int state = 0;
   if (lane == 0) {
     if (warp == 6) {
-      state = wait_flag_geq(hdr_word(p, kHdrG2Done), 4u * (uint32_t)(used_tiles(p) * p.n_tiles), wc) ? 1 : 2;
+      state = wait_flag_geq(hdr_word(p, kHdrG2Done), 4u * gridDim.x, wc) ? 1 : 2;
       __threadfence_block();
       *go = state;
     } else {
@@ -1237,14 +1244,18 @@ __device__ bool fused_combine_phase(const GemmParams& p, Ctl* ctl, int warp, int
     if (lane == 0) t = atomicAdd(reinterpret_cast<int*>(hdr_word(p, kHdrCombineNext)), 1);
     t = __shfl_sync(0xffffffffu, t, 0);
     if (t >= p.T) break;
-    combine_token(p, t, lane);
+    // 16 KB of the stage buffers per warp: gather warps 6-9 slots 0-3,
+    // epilogue warps 2-5 slots 4-7 (every GEMM2 item, hence every MMA
+    // read of those buffers, is complete)
+    combine_token(p, t, lane, stages + (warp >= 6 ? warp - 6 : warp + 2) * 16384);
   }
   return true;
 }
 
 // The gather warps' part of a schedule or combine item (false: a bounded
 // wait gave up).
-__device__ bool fused_aux_gather(const GemmParams& p, Ctl* ctl, const Item& it, int gt, const WaitCtx& wc) {
+__device__ bool fused_aux_gather(const GemmParams& p, Ctl* ctl, uint8_t* stages, const Item& it, int gt,
+                                 const WaitCtx& wc) {
   const int lane = gt & 31;
   bool ok = true;
   if (it.type == kItemCount) {
@@ -1266,7 +1277,7 @@ __device__ bool fused_aux_gather(const GemmParams& p, Ctl* ctl, const Item& it, 
       if (ok) fused_place(p, it.m, ctl->po, lane);
     }
   } else {
-    ok = fused_combine_phase(p, ctl, 6 + (gt >> 5), lane, wc);
+    ok = fused_combine_phase(p, ctl, stages, 6 + (gt >> 5), lane, wc);
   }
   return ok;
 }
@@ -1530,7 +1541,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         bool ok = true;
         if constexpr (MODE == GM_FWD_FUSED) {
           if (it.type >= kItemCount) {
-            if (!fused_aux_gather(p, ctl, it, gt, wc)) break;
+            if (!fused_aux_gather(p, ctl, sA, it, gt, wc)) break;
             continue;
           }
         }
@@ -1673,8 +1684,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (w < 0) break;
       const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
       if (MODE == GM_FWD_FUSED && it.type >= kItemCount) {
-        // schedule items are the gather warps'; combine items are shared
-        if (it.type == kItemCombine && !fused_combine_phase(p, ctl, warp, lane, wc)) break;
+        // schedule items are the gather warps'; the combine phase is shared.
+        // Reaching it, this warp has stored all its rows of y (the phase is
+        // the last item of every CTA): publish that, once per warp.
+        if (it.type == kItemCombine) {
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            red_release_gpu_add(hdr_word(p, kHdrG2Done), 1u);
+          }
+          if (!fused_combine_phase(p, ctl, sA, warp, lane, wc)) break;
+        }
         continue;
       }
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
@@ -1726,14 +1746,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         default: epi_wgrad<MX && MODE == GM_WG13>(p, it, tbase, q, lane, stage_out, release_acc); break;
       }
       release_acc();
-      if (MODE == GM_FWD_FUSED && it.type == GM_FWD2) {
-        // this warp's 32 rows of y are stored: count it for the combine items
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          red_release_gpu_add(hdr_word(p, kHdrG2Done), 1u);
-        }
-      }
       if (is_ring<MODE>() && it.type == GM_FWD1) {
         // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
         // read by TMA): each epilogue warp adds 1, so a tile is complete when
