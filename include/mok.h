@@ -210,8 +210,10 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
  * bitwise -- the schedule arrays in the workspace (so mok_backward can
  * follow), out and ctx.  The launch's work items, taken in order from a
  * device counter, are: a histogram per 1,024 routed rows, the scan, the
- * placement per 1,024 routed rows, the ring's GEMM1 / GEMM2 tiles, and the
- * combine per 16 tokens; each waits (bounded) only on items before it.
+ * placement per 1,024 routed rows and the ring's GEMM1 / GEMM2 tiles; each
+ * waits (bounded) only on items before it.  A CTA that draws past the last
+ * item combines tokens, taken from a second counter, once every GEMM2 row
+ * is stored.
  * Clears the workspace error word first; an id outside [0, E) records
  * MOK_ERR_BAD_INDEX as in mok_build_schedule.
  */

@@ -22,7 +22,10 @@
 // Weight-gradient launches read token-sorted operands with plain TMA (the
 // gather warps write the empty experts' zero gradients instead) and come in
 // two forms: single CTAs, and clusters of two CTAs sharing a 256 x 256 tile
-// through one cta_group::2 MMA (launch_gemm_pair) for long-K experts.
+// through one cta_group::2 MMA (launch_gemm_pair) for long-K experts.  dX,
+// and dA' on token-sorted dout, also run on such clusters, two 128-row
+// tiles of one expert per 256 x 256 tile.  GM_FWD_FUSED adds the
+// schedule's and the combine's work to the forward ring launch.
 // Work items (output tiles) are taken from a device counter in increasing
 // order, so a CTA only ever waits on items taken before its own; the
 // numerics of a tile never depend on which CTA computes it (fixed K order,
@@ -992,9 +995,9 @@ __device__ void zero_empty_experts(const GemmParams& p, const Ctl* ctl, int gw, 
 
 
 // ---------------------------------------------------------------- single-launch forward
-// The schedule and combine items of GM_FWD_FUSED.  The four gather warps
-// (128 threads, named barrier 1) run the schedule items; they and the four
-// epilogue warps (256 threads) run the combine items.  Each item publishes
+// The schedule items and the combine phase of GM_FWD_FUSED.  The four
+// gather warps (128 threads, named barrier 1) run the schedule items; they
+// and the four epilogue warps run the combine phase.  Each item publishes
 // its completion with a release add on a header counter, and every item
 // that reads another's output acquires that counter first (bounded waits).
 // The arithmetic is the schedule kernels' and the combine kernel's, so the
@@ -1256,8 +1259,8 @@ __device__ bool fused_combine_phase(const GemmParams& p, Ctl* ctl, uint8_t* stag
   return true;
 }
 
-// The gather warps' part of a schedule or combine item (false: a bounded
-// wait gave up).
+// The gather warps' part of a schedule item or of the combine phase
+// (false: a bounded wait gave up).
 __device__ bool fused_aux_gather(const GemmParams& p, Ctl* ctl, uint8_t* stages, const Item& it, int gt,
                                  const WaitCtx& wc) {
   const int lane = gt & 31;

@@ -15,7 +15,7 @@ enum GemmMode : int {
   GM_WG13 = 5,    // [dW1|dW3]_e = gather(x)_e^T * [dh|du]_e
   GM_WG2 = 6,     // dW2_e = (s a)_e^T * gather(dout)_e
   GM_FWD_RING = 7, // GM_FWD1 and GM_FWD2 interleaved through the minibatch ring in one launch
-  GM_FWD_FUSED = 8 // the whole forward in one launch: schedule items, the ring's items, combine items
+  GM_FWD_FUSED = 8 // the whole forward in one launch: schedule items, the ring's items, a combine phase
 };
 
 constexpr int kStages = 4;
