@@ -332,11 +332,13 @@ void set_pair_table(GemmParams& g, const WsLayout& L, uint8_t* ws) {
   g.pair_m0 = reinterpret_cast<const int32_t*>(ws + L.pair_m0);
 }
 
-// A row-tiled launch on CTA pairs, else (no cluster of two on this device)
-// one CTA per tile.
-cudaError_t launch_rows(int mode, bool pairs, const TmapSet& maps, const GemmParams& q, int grid, cudaStream_t st) {
+// A row-tiled launch on CTA pairs (pair_maps: weight boxes of 128 rows,
+// each CTA's half of the tile), else -- without pairs, or without clusters
+// of two on the device -- one CTA per tile (maps: boxes of bn rows).
+cudaError_t launch_rows(int mode, bool pairs, const TmapSet& pair_maps, const TmapSet& maps, const GemmParams& q,
+                        int grid, cudaStream_t st) {
   if (pairs) {
-    const cudaError_t e = launch_gemm_pair(mode, maps, q, grid, st);
+    const cudaError_t e = launch_gemm_pair(mode, pair_maps, q, grid, st);
     if (e != cudaErrorNotSupported) return e;
     (void)cudaGetLastError();
   }
@@ -839,10 +841,12 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   }
   // dA' = sorted(dout) W2^T, SwiGLU backward + router-score partials
   {
-    TmapSet m;
+    TmapSet m, mp;
     memset(&m, 0, sizeof(m));
     if (sorted ? !map2d(&m.m[0], srt, s.H, P, 128) : !map_gather(&m.m[0], dout, s.H, s.T)) return MOK_ERR_CUDA;
-    if (!map3d(&m.m[1], W2, s.H, s.I, s.E, pairs_da ? 128 : bn_i)) return MOK_ERR_CUDA;
+    if (!map3d(&m.m[1], W2, s.H, s.I, s.E, bn_i)) return MOK_ERR_CUDA;
+    mp = m;
+    if (pairs_da && !map3d(&mp.m[1], W2, s.H, s.I, s.E, 128)) return MOK_ERR_CUDA;
     GemmParams q = g;
     q.gather_src = static_cast<const __nv_bfloat16*>(dout);
     q.rows_sorted = sorted ? 1 : 0;
@@ -856,18 +860,20 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
       Phase ph(MOK_PHASE_BWD_DA, st, (pairs_da || pairs_dx) ? 2 : 1);
       if (pairs_da || pairs_dx) MOK_CUDA(launch_pair_table(L, w, st));
       if (pairs_da) set_pair_table(q, L, w);
-      MOK_CUDA(launch_rows(GM_BWD_DA, pairs_da, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+      MOK_CUDA(launch_rows(GM_BWD_DA, pairs_da, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
     }
     Phase ph(MOK_PHASE_BWD_DS, st, 1);
     MOK_CUDA(launch_ds_reduce(s, L, w, dscores, q.n_tiles, st));
   }
   // dX parts = [dh|du] [W1|W3]^T scattered to token order, then summed over k
   {
-    TmapSet m;
+    TmapSet m, mp;
     memset(&m, 0, sizeof(m));
-    const int box = pairs_dx ? 128 : bn_h;
-    if (!map2d(&m.m[0], g.dhu, 2 * (uint64_t)s.I, P, 128) || !map3d(&m.m[1], W1, s.I, s.H, s.E, box) ||
-        !map3d(&m.m[2], W3, s.I, s.H, s.E, box))
+    if (!map2d(&m.m[0], g.dhu, 2 * (uint64_t)s.I, P, 128) || !map3d(&m.m[1], W1, s.I, s.H, s.E, bn_h) ||
+        !map3d(&m.m[2], W3, s.I, s.H, s.E, bn_h))
+      return MOK_ERR_CUDA;
+    mp = m;
+    if (pairs_dx && (!map3d(&mp.m[1], W1, s.I, s.H, s.E, 128) || !map3d(&mp.m[2], W3, s.I, s.H, s.E, 128)))
       return MOK_ERR_CUDA;
     GemmParams q = g;
     q.nmaps = 3;
@@ -879,7 +885,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     if (pairs_dx) set_pair_table(q, L, w);
     {
       Phase ph(MOK_PHASE_BWD_DX, st, 1);
-      MOK_CUDA(launch_rows(GM_BWD_DX, pairs_dx, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+      MOK_CUDA(launch_rows(GM_BWD_DX, pairs_dx, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
     }
     Phase ph(MOK_PHASE_BWD_DX_COMBINE, st, 1);
     MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));
