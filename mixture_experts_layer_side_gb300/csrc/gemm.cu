@@ -1218,17 +1218,17 @@ __device__ void combine_token(const GemmParams& p, int t, int lane, uint8_t* buf
 }
 
 // The combine phase, by each of the four gather warps and four epilogue
-// warps: wait until the epilogue warps of every CTA have published that
-// their rows of y are stored (one thread per CTA polls the global count,
-// the other warps its outcome in shared memory), then take tokens from a
-// device counter until none is left.  False: a bounded wait gave up.
+// warps: wait until the epilogue warps of every GEMM2 item have published
+// their rows of y (one thread per CTA polls the global count, the other
+// warps its outcome in shared memory), then take tokens from a device
+// counter until none is left.  False: a bounded wait gave up.
 __device__ bool fused_combine_phase(const GemmParams& p, Ctl* ctl, uint8_t* stages, int warp, int lane,
                                     const WaitCtx& wc) {
   volatile int* go = &ctl->combine_go;
   int state = 0;
   if (lane == 0) {
     if (warp == 6) {
-      state = wait_flag_geq(hdr_word(p, kHdrG2Done), 4u * gridDim.x, wc) ? 1 : 2;
+      state = wait_flag_geq(hdr_word(p, kHdrG2Done), 4u * (uint32_t)(used_tiles(p) * p.n_tiles), wc) ? 1 : 2;
       __threadfence_block();
       *go = state;
     } else {
@@ -1691,17 +1691,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (w < 0) break;
       const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
       if (MODE == GM_FWD_FUSED && it.type >= kItemCount) {
-        // schedule items are the gather warps'; the combine phase is shared.
-        // Reaching it, this warp has stored all its rows of y (the phase is
-        // the last item of every CTA): publish that, once per warp.
-        if (it.type == kItemCombine) {
-          __syncwarp();
-          if (lane == 0) {
-            __threadfence();
-            red_release_gpu_add(hdr_word(p, kHdrG2Done), 1u);
-          }
-          if (!fused_combine_phase(p, ctl, sA, warp, lane, wc)) break;
-        }
+        // schedule items are the gather warps'; the combine phase is shared
+        if (it.type == kItemCombine && !fused_combine_phase(p, ctl, sA, warp, lane, wc)) break;
         continue;
       }
       const uint32_t buf = tcount % kAccBufs, tph = (tcount / kAccBufs) & 1;
@@ -1753,6 +1744,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         default: epi_wgrad<MX && MODE == GM_WG13>(p, it, tbase, q, lane, stage_out, release_acc); break;
       }
       release_acc();
+      if (MODE == GM_FWD_FUSED && it.type == GM_FWD2) {
+        // this warp's 32 rows of y are stored: count them for the combine
+        // phase, which waits on every GEMM2 item (all drawn before it)
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          red_release_gpu_add(hdr_word(p, kHdrG2Done), 1u);
+        }
+      }
       if (is_ring<MODE>() && it.type == GM_FWD1) {
         // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
         // read by TMA): each epilogue warp adds 1, so a tile is complete when

@@ -25,7 +25,7 @@ constexpr int kHdrTiles = 2;
 constexpr int kHdrAbort = 3;       // launch-wide abort word (cleared per call)
 constexpr int kHdrPairs = 4;       // CTA-pair tiles of the pair table (see launch_pair_table)
 // single-launch forward: completed schedule items (count, scan, place) and
-// epilogue warps done with all their GEMM2 rows
+// GEMM2 epilogue warps that stored their rows of y
 constexpr int kHdrCountDone = 5;
 constexpr int kHdrScanDone = 6;
 constexpr int kHdrPlaceDone = 7;
