@@ -25,8 +25,11 @@ Parity status (what pins each function, see ``tests/test_oracle.py``):
                              invariance, empty experts.
 * ``mxfp8``               -- exhaustive nearest-code search over all 256 E4M3
                              codes, exact round trips, power-of-two scales.
-* ``moe`` in MXFP8 mode   -- an independent per-element loop quantiser on
-                             tiny inputs, and identity on pre-quantised data.
+* ``moe`` in MXFP8 mode   -- forward and backward against the layer written
+                             per routed row with an exhaustive-search
+                             quantiser at every quantisation point (per-expert
+                             row blocks for the weight gradients), and
+                             identity on pre-quantised data.
 * ``heuristics``          -- the 2,368-token floor printed for the Kimi-2.5
                              shape (golden fixture).
 * ``router``              -- brute-force selection with ties, softmax special

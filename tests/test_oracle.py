@@ -355,6 +355,101 @@ def test_mxfp8_forward_matches_loop_quantiser():
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
 
 
+def block_search_qdq(a, axis, table):
+    """Quantise-dequantise along ``axis`` in blocks of 32 consecutive elements
+    (a shorter last block stands for a zero-padded one: padding zeros never
+    raise a block's amax).  The block exponent comes from repeated doubling or
+    halving, and each element from an exhaustive search over the finite E4M3
+    codes (nearest value, ties to the even code, saturating at 448).  Shares
+    nothing with ``oracle.mxfp8`` but the format's definition."""
+    codes = np.array(sorted(table), dtype=np.int64)
+    vals = np.array([table[c] for c in codes])
+    a = np.moveaxis(np.array(a, dtype=np.float64), axis, -1).copy()
+    flat = a.reshape(-1, a.shape[-1])
+    for row in flat:
+        for b0 in range(0, row.size, 32):
+            blk = row[b0:b0 + 32]
+            amax = float(np.abs(blk).max())
+            if amax == 0:
+                continue
+            X = 0
+            while 2.0 ** (X + 1) <= amax:
+                X += 1
+            while 2.0 ** X > amax:
+                X -= 1
+            X -= 8
+            v = np.clip(blk / 2.0 ** X, -448.0, 448.0)
+            dist = np.abs(vals[None, :] - v[:, None])
+            tie = dist == dist.min(axis=1, keepdims=True)
+            pick = np.argmin(np.where(tie, codes[None, :] & 1, 2), axis=1)
+            blk[:] = vals[pick] * 2.0 ** X
+    return np.moveaxis(flat.reshape(a.shape), -1, axis)
+
+
+def mxfp8_backward_per_row(x, idx, s, W1, W3, W2, dout, table):
+    """The MXFP8 backward written per routed row, with every quantisation
+    point spelled out (the points the GPU quantises at):
+      forward   x, W1, W3 along H; a and W2 along I;
+      dA'       dout and W2 along H;
+      dX        dh, du and W1, W3 along I;
+      dW        x, dh, du, s*a and dout along the expert's routed rows, in
+                ascending flat-index order, in blocks of 32 per expert."""
+    q = lambda arr, ax: block_search_qdq(arr, ax, table)
+    T, H = x.shape
+    k = idx.shape[1]
+    E, _, I = W1.shape
+    xH, W1H, W3H, W2I = q(x, 1), q(W1, 1), q(W3, 1), q(W2, 1)
+    dOH, W2H, W1I, W3I = q(dout, 1), q(W2, 2), q(W1, 2), q(W3, 2)
+    dX = np.zeros((T, H))
+    ds = np.zeros((T, k))
+    dW1, dW3, dW2 = np.zeros((E, H, I)), np.zeros((E, H, I)), np.zeros((E, I, H))
+    rows_of = {e: [] for e in range(E)}
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            g, up = xH[t] @ W1H[e], xH[t] @ W3H[e]
+            sig = 1.0 / (1.0 + np.exp(-g))
+            act = g * sig * up
+            dAp = dOH[t] @ W2H[e].T
+            ds[t, j] = float(np.dot(dAp, act))
+            dA = s[t, j] * dAp
+            dh = dA * up * sig * (1.0 + g * (1.0 - sig))
+            du = dA * g * sig
+            dX[t] += q(dh[None, :], 1)[0] @ W1I[e].T + q(du[None, :], 1)[0] @ W3I[e].T
+            rows_of[e].append((t, dh, du, s[t, j] * act))
+    for e, rows in rows_of.items():
+        if not rows:
+            continue
+        tt = [r[0] for r in rows]
+        Xe, dOe = q(x[tt], 0), q(dout[tt], 0)
+        dHe, dUe = q(np.array([r[1] for r in rows]), 0), q(np.array([r[2] for r in rows]), 0)
+        Ase = q(np.array([r[3] for r in rows]), 0)
+        for n in range(len(rows)):
+            dW1[e] += np.outer(Xe[n], dHe[n])
+            dW3[e] += np.outer(Xe[n], dUe[n])
+            dW2[e] += np.outer(Ase[n], dOe[n])
+    return dX, dW1, dW3, dW2, ds
+
+
+def test_mxfp8_backward_matches_per_row_quantiser():
+    # Expert 0 takes 36 routed rows (one full 32-row block and a ragged one),
+    # experts 1 and 2 share the rest, so weight-gradient blocks that ran over
+    # an expert's end, or that were taken along the wrong axis, would change
+    # the result.
+    table = e4m3_table()
+    rng = np.random.default_rng(23)
+    T, H, I, E, k = 40, 64, 32, 3, 2
+    x, _, s, W1, W3, W2, dout = rand_layer(rng, T, H, I, E, k)
+    idx = np.zeros((T, k), dtype=np.int64)
+    idx[:36, 0] = 0
+    idx[:36, 1] = rng.integers(1, 3, size=36)
+    idx[36:] = [[1, 2], [2, 1], [2, 1], [1, 2]]
+    got = moe.backward(x, idx, s, W1, W3, W2, dout, quant="mxfp8")
+    ref = mxfp8_backward_per_row(x, idx, s, W1, W3, W2, dout, table)
+    for name, g, r in zip(("dX", "dW1", "dW3", "dW2", "ds"), got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-12, atol=1e-12 * float(np.abs(r).max()), err_msg=name)
+
+
 def test_mxfp8_identity_on_prequantised_inputs():
     # Inputs already on the MXFP8 grid along every axis they are quantised
     # along (powers of two with a common exponent per block): the first GEMM
