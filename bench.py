@@ -14,7 +14,13 @@ Prints ONE JSON line (rank 0).  ``value`` is whole-job algorithmic TFLOP/s
 (18*R*H*I FLOPs per step, R = T*k, padding excluded); ``e2e`` is the same
 metric with each step's inputs copied from pinned host memory and its results
 (out, dX, ds) read back inside the timed region.  ``--impl reference`` times
-the float64 CPU oracle (the reference arm of this build) on a bounded sample.
+the float64 CPU oracle (the reference arm of this build) on a bounded sample,
+the same slice the line's ``cpu_baseline`` leg repeats.  After the headline
+workload the default run also times the two MXFP8 workloads (mid-sized with
+Zipf routing, Kimi-K2-shaped) and the library's dense GEMM core, under
+``secondary`` and ``dense_core``; ``value``, ``config`` and ``dtype`` stay
+the headline's.  Tensor-core fractions are of the measured burst peak (the
+timed region is well under a second); the sustained figure is beside it.
 Under torchrun every rank runs an independent replica (the layer does not
 shard across GPUs); timing is the max over ranks.
 """
@@ -56,6 +62,9 @@ def parse_args_from(argv):
     ap.add_argument("--ring-slots", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # MXFP8 workloads timed after the headline one (default run only)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--secondary-steps", type=int, default=10)
     # diagnostic: the library's MOK_DEBUG_* bits (alternative launch paths)
     ap.add_argument("--debug-flags", type=int, default=0)
     # bounded-memory backward (forward context of ring_slots minibatches, GEMM1 recomputed)
@@ -77,6 +86,20 @@ def load_peaks():
         return p, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def tensor_peaks(peaks, peaks_src, prec):
+    """(peak, sustained peak, note) for the GEMM phases.  ``peak`` is the burst
+    figure: the timed region is well under a second of 10-30 ms steps, not
+    the seconds-long power-capped loop the sustained figure comes from."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    note = f"{peaks_src} bf16 burst (cuBLAS 8192^3); sustained beside it"
+    if prec == "mxfp8":
+        # E4M3 contraction: no measured fp8 peak on this pool; the measured bf16
+        # figures x the nominal dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+        return 2.0 * burst, 2.0 * sus, f"{peaks_src} bf16 burst x 2 (nominal dense fp8 / bf16 ratio)"
+    return burst, sus, note
 
 
 def flops_per_step(shape):
@@ -255,6 +278,12 @@ def job_tflops(world, flops_per_rank_step, ms_per_step):
     return world * flops_per_rank_step / (ms_per_step / 1e3) / 1e12
 
 
+# The one bounded slice of the workload both CPU legs time (the reference arm
+# per step, the cpu_baseline leg repeated for about ten seconds): same H and I,
+# 256 tokens routed top-2 over 4 experts.
+ORACLE_SLICE = dict(tokens=256, experts=4, k=2, seed=11)
+
+
 def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -262,7 +291,7 @@ def run_reference(args):
         return 0
     from mixture_experts_layer_side_gb300.inputs import WORKLOADS
     shape, routing, prec = WORKLOADS[args.workload]
-    sample = OracleSample(shape, tokens=64, experts=2, k=2, seed=7)
+    sample = OracleSample(shape, **ORACLE_SLICE)
     flops, desc = sample.flops, sample.desc
     for _ in range(args.warmup):
         sample.run()
@@ -295,6 +324,115 @@ def workload_config(args, shape, routing, prec, layer=None):
         cfg["fused_forward"] = bool(args.fused)
         cfg["ctx_bytes"] = int(layer.ctx.numel())
     return cfg
+
+
+def secondary_workload(name, steps, dev, peaks, peaks_src):
+    """One more workload timed in the same run (not the headline): its step
+    time, per-phase TFLOP/s and fraction of the tensor peak of its precision,
+    and the clocks seen while it ran."""
+    import torch
+
+    from mixture_experts_layer_side_gb300 import _lib
+    from mixture_experts_layer_side_gb300.inputs import WORKLOADS, load_stats, make_inputs
+    from mixture_experts_layer_side_gb300.layer import MoKLayer
+
+    shape, routing, prec = WORKLOADS[name]
+    inp = make_inputs(shape, routing, seed=2000, device=dev)
+    layer = MoKLayer(shape, precision=prec, device=dev)
+    grads = layer.alloc_grads()
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    if prec == "mxfp8":
+        wq = layer.quantize_weights(inp["W1"], inp["W3"], inp["W2"])
+        w_fwd, w_bwd = wq["fwd"], wq["bwd"]
+    else:
+        w_fwd = w_bwd = (inp["W1"], inp["W3"], inp["W2"])
+
+    def step():
+        layer.build_schedule(inp["idx"])
+        layer.forward(inp["x"], inp["s"], *w_fwd, out=out)
+        layer.backward(inp["x"], inp["s"], *w_bwd, inp["dout"], grads=grads)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    layer.check()
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    _lib.mok_trace_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    phases = _lib.mok_trace_read()
+    _lib.mok_trace_enable(False)
+    layer.check()
+    ms = e0.elapsed_time(e1) / steps
+    peak, peak_sus, note = tensor_peaks(peaks, peaks_src, prec)
+    pf = phase_flops(shape)
+    per = {}
+    for n, (tot, runs) in phases.items():
+        if runs:
+            per[n] = {"ms": tot / runs}
+            if n in pf:
+                tf = pf[n] / (per[n]["ms"] / 1e3) / 1e12
+                per[n].update(tflops=tf, frac_of_peak=tf / peak)
+    fwd_ms = sum(per.get(n, {"ms": 0})["ms"] for n in ("schedule", "quant", "fwd_gemm", "fwd_combine"))
+    stats = load_stats(inp["idx"], shape.E)
+    res = {"workload": f"{name}: T={shape.T} H={shape.H} I={shape.I} E={shape.E} top-{shape.k}, {routing} "
+                       f"routing, {prec}",
+           "dtype": prec, "steps": steps, "ms_per_step": ms, "value": flops_per_step(shape) / (ms / 1e3) / 1e12,
+           "unit": UNIT, "tokens_per_s": shape.T / (ms / 1e3), "peak": peak, "peak_source": note,
+           "frac_of_peak": flops_per_step(shape) / (ms / 1e3) / 1e12 / peak,
+           "phases": per, "clocks": clocks, "load": stats}
+    if "quant" in per:
+        res["note"] = ("the quant phase (activation quantisation, both passes) is summed into the forward's "
+                       f"{fwd_ms:.3f} ms only approximately: it runs in both passes")
+    del layer, inp, grads, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def dense_core_rates(dev, n=8192, reps=20):
+    """The library's tensor-core GEMM on one dense n^3 problem (K-major
+    operands), BF16 and MXFP8: the rate its tile pipeline reaches with no
+    MoE structure around it (context for the per-phase fractions)."""
+    import torch
+
+    from mixture_experts_layer_side_gb300 import _lib
+    g = torch.Generator(device=dev).manual_seed(3)
+    A = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+    B = torch.randn((n, n), generator=g, device=dev).to(torch.bfloat16)
+    C = torch.empty((n, n), dtype=torch.float32, device=dev)
+    scratch = torch.zeros(256 + 2 * n * n // 32, dtype=torch.uint8, device=dev)
+    Aq = torch.empty((n, n), dtype=torch.uint8, device=dev)
+    Bq = torch.empty((n, n), dtype=torch.uint8, device=dev)
+    As = torch.empty((n, n // 32), dtype=torch.uint8, device=dev)
+    Bs = torch.empty((n, n // 32), dtype=torch.uint8, device=dev)
+    _lib.mok_mxfp8_quantize(A, 1, Aq, As)
+    _lib.mok_mxfp8_quantize(B, 1, Bq, Bs)
+    runs = {"bf16": lambda: _lib.mok_gemm_bf16(A, 0, B, 0, C, scratch),
+            "mxfp8": lambda: _lib.mok_gemm_mxfp8(Aq, As, 0, Bq, Bs, 0, C, scratch)}
+    res = {}
+    for name, fn in runs.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"n": n, "ms": ms, "tflops": 2.0 * n ** 3 / (ms / 1e3) / 1e12}
+    del A, B, C, scratch, Aq, Bq, As, Bs
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_mok(args):
@@ -372,14 +510,10 @@ def run_mok(args):
     dom = max(GEMM_PHASES, key=lambda n: per_phase.get(n, {"ms": 0})["ms"])
     dom_ms = per_phase[dom]["ms"]
     achieved = pf[dom] / (dom_ms / 1e3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    peak_note = f"{peaks_src} bf16 sustained (kernel timed inside a step)"
-    if prec == "mxfp8":
-        # E4M3 contraction: the measured bf16 peak x the nominal fp8 / bf16 ratio (4.5 / 2.25)
-        peak *= 2.0
-        peak_note = f"{peaks_src} bf16 sustained x 2 (nominal dense fp8 / bf16 ratio)"
+    peak, peak_sus, peak_note = tensor_peaks(peaks, peaks_src, prec)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": peak_note,
+                "peak_sustained": peak_sus, "frac_of_sustained": achieved / peak_sus,
                 "traffic": recorded_traffic(dom, args.workload)}
     for n in per_phase:
         if n in pf:
@@ -402,6 +536,7 @@ def run_mok(args):
             per_phase[n].update(min_bytes=mb[n], floor_ms=floor, bound="tensor" if t_flop >= t_byte else "hbm",
                                 attainable_frac=floor / per_phase[n]["ms"])
     sched_share = per_phase.get("schedule", {"ms": 0})["ms"] / ms
+    cfg_line = workload_config(args, shape, routing, prec, layer)
 
     # ------------------------------------------------ router on either side of the layer (not in the metric)
     router = None
@@ -497,13 +632,28 @@ def run_mok(args):
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for t in (hout, hdX, hds))
         e2e = {"value": job_tflops(world, fps, ems), "unit": UNIT, "ms_per_step": ems,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "scope": "activations: x, idx, s, dout copied in and out, dX, ds read back every step; the "
+                        "expert weights and their gradients stay resident in HBM (the caller's parameters "
+                        "and gradient buffers), as in a training loop"}
+
+    # ------------------------------------------------ MXFP8 and dense-core context (rank 0, one GPU only)
+    secondary, dense = None, None
+    if rank == 0 and world == 1 and not args.no_secondary and args.workload == "dsv3":
+        # free the headline workload's buffers first (about 60 GB)
+        layer = inp = grads = out = None
+        if not args.no_e2e:
+            sets = host = hout = hdX = hds = None
+        torch.cuda.empty_cache()
+        secondary = [secondary_workload(w, args.secondary_steps, dev, peaks, peaks_src)
+                     for w in ("mid_mxfp8_zipf", "kimi_mxfp8")]
+        dense = dense_core_rates(dev)
 
     # ------------------------------------------------ CPU baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # repeat the slice until about 10 s of CPU work has accumulated (30 s cap)
-        sample = OracleSample(shape, tokens=256, experts=4, k=2, seed=11)
+        sample = OracleSample(shape, **ORACLE_SLICE)
         total, reps = 0.0, 0
         while total < 10.0 and reps < 200:
             total += sample.run()
@@ -516,7 +666,7 @@ def run_mok(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": prec, "data": "synthetic (seeded, resident in HBM)",
-            "config": workload_config(args, shape, routing, prec, layer),
+            "config": cfg_line,
             "tokens_per_s": world * shape.T / (ms / 1e3),
             "gpu_launches": launches,
             "roofline": roofline,
@@ -527,6 +677,8 @@ def run_mok(args):
             "cpu_baseline": cpu,
             "clocks": clocks,
             "load": stats,
+            "secondary": secondary,
+            "dense_core": dense,
             "peaks_source": peaks_src,
         }
         print(json.dumps(line), flush=True)

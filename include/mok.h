@@ -336,12 +336,20 @@ int64_t mok_launch_count(void);
  *     return MOK_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is cached per device and
+ *     context: after a cudaDeviceReset the next call (again the first on a
+ *     new context) looks it up anew.
+ *   - The kernels use the current device's array, so `stream` must belong to
+ *     the current device; a stream of another device returns
+ *     MOK_ERR_INVALID_ARG before anything is enqueued.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads, same device) race and give wrong schedules.
  *     Serialise them.
  *   - The function allocates nothing: no cudaMalloc/cudaFree, no library
  *     routine that allocates.
+ *   - MOK_ERR_CUDA means one of this call's own launches failed (each launch
+ *     is checked on its own; an earlier error pending in the runtime is not
+ *     reported as this call's).
  * Outputs (device, int32, caller-owned): the arrays of mok_layout, with the
  * same lengths; `header` gets [0] error bits (1 = an expert id outside
  * [0, E)), [1] padded rows used, [2] 128-row tiles used.

@@ -238,27 +238,78 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes]
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kNoallocMaxDevices] = {};
+struct NoallocSlot {
+  unsigned long long ctx_id;  // unique id of the context the address belongs to (0: none yet)
+  void* addr;
+};
+NoallocSlot g_noalloc_slot[kNoallocMaxDevices] = {};
 
-// Device address of the static scratch on the current device, looked up once
-// per device with that device current (host code must not use the symbol
-// itself: on the host it only names a stand-in).
-void* noalloc_scratch_address(cudaError_t* err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
+// Unique id of the current context (driver calls reached through the runtime,
+// so the library needs no link to libcuda).  A context made after a
+// cudaDeviceReset gets a new id, so a cached address of the old one is never
+// reused.
+typedef int (*CtxGetCurrentFn)(void**);
+typedef int (*CtxGetIdFn)(void*, unsigned long long*);
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  void* ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx) return false;
+  return get_id(ctx, id) == 0;
+}
+
+// Device address of the static scratch on the current device.  It is looked
+// up with cudaGetSymbolAddress once per device and context, with that device
+// current, and cached; host code must not use the symbol itself, which on
+// the host only names a stand-in.
+void* noalloc_scratch_address(int dev, cudaError_t* err) {
+  *err = cudaSuccess;
   if (dev < 0 || dev >= kNoallocMaxDevices) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  // cudaSetDevice makes (or re-makes, after a reset) the device's primary
+  // context current, so its id can be read
+  *err = cudaSetDevice(dev);
+  if (*err != cudaSuccess) return nullptr;
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) {
+    *err = cudaErrorDeviceUninitialized;
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  NoallocSlot& slot = g_noalloc_slot[dev];
+  if (slot.ctx_id != id || !slot.addr) {
     void* ptr = nullptr;
     *err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (*err != cudaSuccess) return nullptr;
-    g_noalloc_addr[dev] = ptr;
+    slot.addr = ptr;
+    slot.ctx_id = id;
   }
-  return g_noalloc_addr[dev];
+  return slot.addr;
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_on(cudaStream_t st, int grid, int block, size_t smem, void (*kernel)(Params...),
+                      Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace
@@ -277,21 +328,33 @@ extern "C" mok_status mok_build_schedule_noalloc(const mok_shape* shape, const i
   const int64_t nchunks = (R + kSchedChunk - 1) / kSchedChunk;
   const size_t need = 2 * (size_t)nchunks * E * sizeof(int32_t);
   if (need > kNoallocScratchBytes) return MOK_ERR_UNSUPPORTED;  // beyond the static scratch
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOK_ERR_CUDA;
+  if (st) {  // the kernels use the current device's array: the stream must be on that device
+    int sdev = -1;
+    if (cudaStreamGetDevice(st, &sdev) != cudaSuccess) return MOK_ERR_CUDA;
+    if (sdev != dev) return MOK_ERR_INVALID_ARG;
+  }
   cudaError_t err = cudaSuccess;
-  uint8_t* scratch = static_cast<uint8_t*>(noalloc_scratch_address(&err));
+  uint8_t* scratch = static_cast<uint8_t*>(noalloc_scratch_address(dev, &err));
   if (!scratch) return MOK_ERR_CUDA;
   int32_t* chunk_hist = reinterpret_cast<int32_t*>(scratch);
   int32_t* chunk_base = chunk_hist + nchunks * E;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the header starts at zero; the two scratch arrays are fully rewritten
+  // the header starts at zero; the two scratch arrays are fully rewritten.
+  // Each call reports its own launches' status (not an earlier, unrelated
+  // error left in the runtime's last-error slot).
   if (cudaMemsetAsync(out->header, 0, kHeaderWords * sizeof(int32_t), st) != cudaSuccess) return MOK_ERR_CUDA;
-  sched_count<<<(int)nchunks, kCountThreads, E * sizeof(int32_t), st>>>(topk_idx, R, E, chunk_hist, out->header);
-  sched_scan<<<1, 1024, 0, st>>>(E, (int)nchunks, chunk_hist, chunk_base, out->counts, out->offsets,
-                                 out->padded_offsets, out->tile_expert, out->pad_perm, out->header);
+  if (launch_on(st, (int)nchunks, kCountThreads, E * sizeof(int32_t), sched_count, topk_idx, R, E, chunk_hist,
+                out->header) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  if (launch_on(st, 1, 1024, 0, sched_scan, E, (int)nchunks, chunk_hist, chunk_base, out->counts, out->offsets,
+                out->padded_offsets, out->tile_expert, out->pad_perm, out->header) != cudaSuccess)
+    return MOK_ERR_CUDA;
   const int blocks = (int)((nchunks + kPlaceWarps - 1) / kPlaceWarps);
-  sched_place<<<blocks, kPlaceWarps * 32, (size_t)kPlaceWarps * E * sizeof(int32_t), st>>>(
-      topk_idx, R, E, (int)nchunks, chunk_base, out->offsets, out->padded_offsets, out->perm, out->inv_perm,
-      out->pad_perm, out->pad_inv);
-  return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+  if (launch_on(st, blocks, kPlaceWarps * 32, (size_t)kPlaceWarps * E * sizeof(int32_t), sched_place, topk_idx, R,
+                E, (int)nchunks, chunk_base, out->offsets, out->padded_offsets, out->perm, out->inv_perm,
+                out->pad_perm, out->pad_inv) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  return MOK_OK;
 }
-

@@ -3,9 +3,11 @@ bench.py times, on sampled outputs the float64 oracle computes exactly:
 
 * one token: its out, dX and ds rows depend only on that token and its k
   experts, so the oracle runs on that one-token sub-problem;
-* one small expert: its dW1, dW3, dW2 depend only on the tokens routed to it,
-  so the oracle runs on those tokens with k = 1 (same row order, so the same
-  MXFP8 row blocks).
+* the smallest and the largest non-empty expert: an expert's dW1, dW3, dW2
+  depend only on the tokens routed to it, so the oracle runs on those tokens
+  with k = 1 (same row order, so the same MXFP8 row blocks).  The largest
+  expert (8,077 routed rows on the DeepSeek-V3-shaped workload) runs on the
+  long-K CTA-pair weight-gradient path at its full K.
 
 The Kimi-K2-shaped minibatch sweep also checks that every ring size gives
 bitwise the same results (tiles keep their K order at any minibatch size)."""
@@ -64,20 +66,22 @@ def sampled_checks(shape, prec, inp, out, grads):
     close(f64(out[t:t + 1]), ref_out, "out[t]")
     close(f64(grads["dX"][t:t + 1]), dX, "dX[t]")
     close(f64(grads["ds"][t:t + 1]), ds, "ds[t]")
-    # one small non-empty expert: all tokens routed to it, k = 1
+    # the smallest and the largest non-empty expert: all tokens routed to it, k = 1
     counts = np.bincount(idx.reshape(-1), minlength=shape.E)
     nz = np.nonzero(counts)[0]
-    e = int(nz[np.argmin(counts[nz])])
-    rows = np.argwhere(idx == e)  # (t, j), ascending t = ascending flat index
-    toks = torch.tensor(rows[:, 0], device=inp["x"].device)
-    s_e = inp["s"][toks, torch.tensor(rows[:, 1], device=inp["x"].device)].reshape(-1, 1)
-    sel = torch.tensor([e], device=inp["W1"].device)
-    W1, W3, W2 = (f64(inp[n].index_select(0, sel)) for n in ("W1", "W3", "W2"))
-    _, dW1, dW3, dW2, _ = moe.backward(f64(inp["x"].index_select(0, toks)), np.zeros((len(rows), 1), dtype=np.int64),
-                                       f64(s_e), W1, W3, W2, f64(inp["dout"].index_select(0, toks)), quant=quant)
-    close(f64(grads["dW1"][e]), dW1[0], f"dW1[{e}]")
-    close(f64(grads["dW3"][e]), dW3[0], f"dW3[{e}]")
-    close(f64(grads["dW2"][e]), dW2[0], f"dW2[{e}]")
+    for e in sorted({int(nz[np.argmin(counts[nz])]), int(nz[np.argmax(counts[nz])])}):
+        rows = np.argwhere(idx == e)  # (t, j), ascending t = ascending flat index
+        toks = torch.tensor(rows[:, 0], device=inp["x"].device)
+        s_e = inp["s"][toks, torch.tensor(rows[:, 1], device=inp["x"].device)].reshape(-1, 1)
+        sel = torch.tensor([e], device=inp["W1"].device)
+        W1, W3, W2 = (f64(inp[n].index_select(0, sel)) for n in ("W1", "W3", "W2"))
+        _, dW1, dW3, dW2, _ = moe.backward(f64(inp["x"].index_select(0, toks)),
+                                           np.zeros((len(rows), 1), dtype=np.int64), f64(s_e), W1, W3, W2,
+                                           f64(inp["dout"].index_select(0, toks)), quant=quant)
+        close(f64(grads["dW1"][e]), dW1[0], f"dW1[{e}] ({counts[e]} rows)")
+        close(f64(grads["dW3"][e]), dW3[0], f"dW3[{e}] ({counts[e]} rows)")
+        close(f64(grads["dW2"][e]), dW2[0], f"dW2[{e}] ({counts[e]} rows)")
+        del dW1, dW3, dW2
     # every element written (the buffers started as NaN), and the experts
     # without routed rows have exact-zero gradients
     for name, t in [("out", out)] + list(grads.items()):
@@ -87,7 +91,7 @@ def sampled_checks(shape, prec, inp, out, grads):
         assert torch.count_nonzero(grads[k].index_select(0, empty)).item() == 0, k
 
 
-@pytest.mark.parametrize("workload", ["dsv3", "mid", "mid_mxfp8_hot", "long_k"])
+@pytest.mark.parametrize("workload", ["dsv3", "mid", "mid_mxfp8_zipf", "mid_mxfp8_hot", "long_k"])
 def test_full_size_sampled_parity(workload):
     require_gpu()
     shape, prec, inp, wq = setup(workload)

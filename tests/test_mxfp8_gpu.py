@@ -73,6 +73,13 @@ CASES = [
     ("tiny", (256, 256, 128, 8, 2), "uniform", 1),
     ("ragged_zipf", (300, 256, 256, 6, 3), "zipf", 2),
     ("hot_empty", (512, 384, 128, 24, 4), "hot", 3),
+    # degenerate and limit cases: one token and one expert; the largest
+    # expert count (most experts empty); the largest top-k; every token on
+    # one expert (top-1, one long weight-gradient K loop, seven empty experts)
+    ("single_token", (1, 128, 128, 1, 1), "uniform", 11),
+    ("max_experts", (512, 128, 128, 1024, 4), "uniform", 12),
+    ("max_topk", (64, 256, 128, 40, 32), "uniform", 13),
+    ("one_expert", (2048, 256, 128, 8, 1), "all_on_5", 14),
 ]
 
 
@@ -80,7 +87,12 @@ def run_mx(shape, routing, seed, **kw):
     from mixture_experts_layer_side_gb300.inputs import Shape, make_inputs
     from mixture_experts_layer_side_gb300.layer import MoKLayer
     S = Shape(*shape)
-    inp = make_inputs(S, routing, seed=seed, device="cpu")
+    if routing == "all_on_5":
+        inp = make_inputs(S, "uniform", seed=seed, device="cpu")
+        inp["idx"] = torch.full((S.T, S.k), 5, dtype=torch.int32)
+        inp["s"] = torch.ones((S.T, S.k), dtype=torch.float32)
+    else:
+        inp = make_inputs(S, routing, seed=seed, device="cpu")
     g = {k: v.cuda() for k, v in inp.items()}
     layer = MoKLayer(S, precision="mxfp8", **kw)
     wq = layer.quantize_weights(g["W1"], g["W3"], g["W2"])
@@ -103,6 +115,11 @@ def test_mxfp8_layer_matches_quantised_oracle(name, shape, routing, seed):
     assert_mxfp8_close(np64(out), ref_out, "out")
     for k in ref:
         assert_mxfp8_close(np64(grads[k]), ref[k], k)
+    # experts with no routed rows: exact zeros
+    counts = np.bincount(a["idx"].reshape(-1), minlength=shape[3])
+    for e in np.nonzero(counts == 0)[0]:
+        for k in ("dW1", "dW3", "dW2"):
+            assert torch.count_nonzero(grads[k][e]).item() == 0
 
 
 def test_mxfp8_reruns_are_bitwise_identical():
