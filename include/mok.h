@@ -422,6 +422,90 @@ mok_status mok_router_backward(const mok_shape* shape, void* rws, size_t rws_byt
                                const int32_t* topk_idx, const float* scores, const float* dscores, float* dWr,
                                void* dx_router, void* stream);
 
+/* Bytes of workspace mok_build_schedule needs: the schedule's prefix of the
+ * full layout (the source side of expert parallelism needs no more).  0 for
+ * an invalid shape or config. */
+size_t mok_schedule_workspace_size(const mok_shape* shape, const mok_config* cfg);
+
+/*
+ * Expert parallelism (EP): the E experts split over G ranks in contiguous
+ * blocks, each rank holding its own tokens; one exchange of routed rows each
+ * way per pass, all four directions driven by the one schedule ([MTP]
+ * communication-direction paragraph; "Results": the layer at EP 64).  The
+ * exchange itself is the caller's collective (an all-to-all with uneven
+ * splits); these calls are the plan and the source side around it:
+ *
+ *   forward   source: mok_build_schedule (global expert ids), then
+ *             mok_ep_pack_rows -> rows in expert-sorted order, which is
+ *             destination-major; exchange the per-expert counts, plan with
+ *             mok_ep_plan, send send_rows[g] rows to rank g.
+ *             receiver: the ordinary layer calls on its n_recv received rows
+ *             with shape (T = n_recv, k = 1, E = its own experts), routing
+ *             recv_expert, scores 1.0 -> one output row per received row
+ *             (exactly the expert output: a one-term combine with weight 1).
+ *             return the rows; source: mok_ep_combine_rows with the scores.
+ *   backward  source: mok_ep_pack_rows of dout with the scores; receiver:
+ *             mok_backward with those scores -> dX rows, its experts' dW, the
+ *             score gradient per row; return the dX rows and score gradients;
+ *             source: mok_ep_combine_rows with no scores (dX) and
+ *             mok_ep_unsort_scores (dscores).
+ * Received rows are ordered by (source rank, source's sorted order), so each
+ * expert sees its rows in ascending global flat index when token t of rank g
+ * is global token g*T + t: every result is bitwise that of one GPU holding
+ * all tokens and experts.
+ */
+
+/* First expert of rank g (g = G gives E): rank g owns experts
+ * [first(g), first(g+1)), blocks whose sizes differ by at most one.
+ * Requires 1 <= G <= E and 0 <= g <= G; -1 otherwise.  Host only. */
+int32_t mok_ep_first_expert(int32_t E, int32_t G, int32_t g);
+
+/*
+ * The exchange plan of rank `rank` (host only, no device work):
+ *   local_counts  (host) int32 [E]: rows this rank routes to each global
+ *                 expert (the schedule's counts array)
+ *   recv_counts   (host) int32 [G, E_rank]: rows source rank s routes to each
+ *                 of this rank's experts (row s = source s's local_counts
+ *                 over this rank's block)
+ *   send_rows     (host) int64 [G]: rows to send to each rank, in order, from
+ *                 the front of the packed rows
+ *   recv_rows     (host) int64 [G]: rows arriving from each rank, in order
+ *   recv_expert   (host) int32 [recv_capacity] or NULL: local expert id of
+ *                 each received row in arrival order (the receiver's routing)
+ *   n_recv        (host) total received rows
+ * MOK_ERR_UNSUPPORTED if n_recv > recv_capacity (recv_expert given);
+ * MOK_ERR_INVALID_ARG for bad sizes, null pointers or negative counts.
+ */
+mok_status mok_ep_plan(int32_t E, int32_t G, int32_t rank, const int32_t* local_counts, const int32_t* recv_counts,
+                       int64_t* send_rows, int64_t* recv_rows, int32_t* recv_expert, int64_t recv_capacity,
+                       int64_t* n_recv);
+
+/*
+ * Source side of the dispatch (forward) and of the reverse combine
+ * (backward): rows[r] = x[perm[r] / k] (bf16 [T*k, H], device) for every
+ * routed row r of the schedule in `ws`, in its expert-sorted order; rows
+ * past the routed ones (ids outside [0, E)) are not written.  With
+ * row_scores (device f32 [T*k]) also row_scores[r] = scores[perm[r]].
+ * ws needs mok_schedule_workspace_size bytes.
+ */
+mok_status mok_ep_pack_rows(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                            const void* x, const float* scores, void* rows, float* row_scores, void* stream);
+
+/*
+ * Source side of the combine (forward) and reverse dispatch (backward):
+ * out[t] = sum_j w[t,j] * rows[inv_perm[t*k + j]] in f32, increasing j,
+ * rounded once to bf16, with w = scores (device f32 [T, k]) or 1 when scores
+ * is NULL; a row routed nowhere adds nothing.  rows (device bf16 [T*k, H]) in
+ * the schedule's sorted order (the returned expert outputs or dX rows).
+ */
+mok_status mok_ep_combine_rows(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                               const void* rows, const float* scores, void* out, void* stream);
+
+/* out[f] = row_vals[inv_perm[f]] (device f32 [T*k] -> [T, k]), 0 for a row
+ * routed nowhere: the returned per-row score gradients back in token order. */
+mok_status mok_ep_unsort_scores(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                                const float* row_vals, float* out, void* stream);
+
 /* Synchronise `stream`, then return (and clear) the status recorded in the
  * workspace's error word; MOK_OK if none. */
 mok_status mok_check(void* ws, void* stream);

@@ -33,7 +33,8 @@ EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_bu
            "mok_backward", "mok_mxfp8_quantize", "mok_gather_rows", "mok_gemm_bf16", "mok_check",
            "mok_device_sm_count", "mok_status_string", "mok_version", "mok_trace_enable", "mok_trace_read",
            "mok_launch_count", "mok_build_schedule_noalloc", "mok_gemm_mxfp8", "mok_router_workspace_size",
-           "mok_router_forward", "mok_router_backward"]
+           "mok_router_forward", "mok_router_backward", "mok_schedule_workspace_size", "mok_ep_first_expert",
+           "mok_ep_plan", "mok_ep_pack_rows", "mok_ep_combine_rows", "mok_ep_unsort_scores"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
           "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd", "bwd_replay", "fwd_fused"]
@@ -103,6 +104,12 @@ def _load():
         "mok_router_workspace_size": (sz, [S]),
         "mok_router_forward": (i32, [S, P, sz, P, P, P, P, P, P, P]),
         "mok_router_backward": (i32, [S, P, sz, P, P, P, P, P, P, P, P]),
+        "mok_schedule_workspace_size": (sz, [S, C]),
+        "mok_ep_first_expert": (i32, [i32, i32, i32]),
+        "mok_ep_plan": (i32, [i32, i32, i32, P, P, P, P, P, ctypes.c_int64, P]),
+        "mok_ep_pack_rows": (i32, [S, C, P, sz, P, P, P, P, P]),
+        "mok_ep_combine_rows": (i32, [S, C, P, sz, P, P, P, P]),
+        "mok_ep_unsort_scores": (i32, [S, C, P, sz, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -266,3 +273,46 @@ def mok_build_schedule_noalloc(shape, topk_idx, buffers, stream=None):
 def mok_check(ws, stream=None):
     """Synchronise and return the device status recorded in the workspace (int)."""
     return LIB.mok_check(_ptr(ws), _stream(stream))
+
+
+# ---------------------------------------------------------------- expert parallelism
+def mok_schedule_workspace_size(shape, cfg):
+    return LIB.mok_schedule_workspace_size(ctypes.byref(shape), ctypes.byref(cfg))
+
+
+def mok_ep_first_expert(E, G, g):
+    return LIB.mok_ep_first_expert(E, G, g)
+
+
+def mok_ep_plan(E, G, rank, local_counts, recv_counts, recv_capacity=None):
+    """Host-only exchange plan.  ``local_counts``: int32 [E]; ``recv_counts``:
+    int32 [G, E_rank] (array-likes on the host).  Returns (send_rows list,
+    recv_rows list, recv_expert int32 numpy array or None, n_recv)."""
+    import numpy as np
+    lc = np.ascontiguousarray(np.asarray(local_counts, dtype=np.int32))
+    rc = np.ascontiguousarray(np.asarray(recv_counts, dtype=np.int32))
+    send = np.zeros(G, dtype=np.int64)
+    recv = np.zeros(G, dtype=np.int64)
+    n = ctypes.c_int64(0)
+    if recv_capacity is None:
+        recv_capacity = int(rc.sum())
+    experts = np.zeros(max(int(recv_capacity), 1), dtype=np.int32)
+    _ok(LIB.mok_ep_plan(E, G, rank, lc.ctypes.data, rc.ctypes.data, send.ctypes.data, recv.ctypes.data,
+                        experts.ctypes.data, int(recv_capacity), ctypes.byref(n)), "mok_ep_plan")
+    return send.tolist(), recv.tolist(), experts[:n.value], n.value
+
+
+def mok_ep_pack_rows(shape, cfg, ws, x, scores, rows, row_scores=None, stream=None):
+    _ok(LIB.mok_ep_pack_rows(ctypes.byref(shape), ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+                             _ptr(x), _ptr(scores), _ptr(rows), _ptr(row_scores), _stream(stream)),
+        "mok_ep_pack_rows")
+
+
+def mok_ep_combine_rows(shape, cfg, ws, rows, scores, out, stream=None):
+    _ok(LIB.mok_ep_combine_rows(ctypes.byref(shape), ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+                                _ptr(rows), _ptr(scores), _ptr(out), _stream(stream)), "mok_ep_combine_rows")
+
+
+def mok_ep_unsort_scores(shape, cfg, ws, row_vals, out, stream=None):
+    _ok(LIB.mok_ep_unsort_scores(ctypes.byref(shape), ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _ptr(row_vals), _ptr(out), _stream(stream)), "mok_ep_unsort_scores")

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmok.so")
-SOURCES = ["api.cu", "schedule.cu", "elementwise.cu", "gemm.cu", "mxfp8.cu", "router.cu"]
+SOURCES = ["api.cu", "schedule.cu", "elementwise.cu", "gemm.cu", "mxfp8.cu", "router.cu", "ep.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -951,6 +951,51 @@ mok_status mok_mxfp8_quantize(const void* src, int32_t batch, int32_t rows, int3
   return MOK_OK;
 }
 
+size_t mok_schedule_workspace_size(const mok_shape* shape, const mok_config* cfg) {
+  if (check_shape(shape) != MOK_OK || check_config(cfg) != MOK_OK) return 0;
+  const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
+  return L.chunk_base + align256(L.nchunks * shape->E * 4);
+}
+
+mok_status mok_ep_pack_rows(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                            const void* x, const float* scores, void* rows, float* row_scores, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  if (!ws || !x || !rows || (row_scores && !scores)) return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < mok_schedule_workspace_size(shape, cfg)) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
+  g_launches += 1;
+  MOK_CUDA(launch_ep_pack(*shape, L, static_cast<const uint8_t*>(ws), static_cast<const __nv_bfloat16*>(x),
+                          scores, static_cast<__nv_bfloat16*>(rows), row_scores, static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+mok_status mok_ep_combine_rows(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                               const void* rows, const float* scores, void* out, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  if (!ws || !rows || !out) return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < mok_schedule_workspace_size(shape, cfg)) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
+  g_launches += 1;
+  MOK_CUDA(launch_ep_combine(*shape, L, static_cast<const uint8_t*>(ws), static_cast<const __nv_bfloat16*>(rows),
+                             scores, static_cast<__nv_bfloat16*>(out), static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+mok_status mok_ep_unsort_scores(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
+                                const float* row_vals, float* out, void* stream) {
+  MOK_TRY(check_shape(shape));
+  MOK_TRY(check_config(cfg));
+  if (!ws || !row_vals || !out) return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < mok_schedule_workspace_size(shape, cfg)) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const WsLayout L = ws_layout(*shape, *cfg, MOK_BF16, device_sm_count());
+  g_launches += 1;
+  MOK_CUDA(launch_ep_unsort(*shape, L, static_cast<const uint8_t*>(ws), row_vals, out,
+                            static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
 mok_status mok_gather_rows(const mok_shape* shape, const mok_config* cfg, const void* ws, size_t ws_bytes,
                            const void* x, void* xg, void* stream) {
   MOK_TRY(check_shape(shape));

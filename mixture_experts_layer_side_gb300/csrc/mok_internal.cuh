@@ -97,6 +97,13 @@ cudaError_t launch_router_logit_grad(int T, int Tpad, int E, int Epad, int k, co
 cudaError_t launch_router_take_cols(int rows, int E, int Epad, const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_quant_rows_tiled(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
                                     uint8_t* q, uint8_t* sf, cudaStream_t st);
+// Expert parallelism (ep.cu): source-side pack / combine / un-sort around the exchange
+cudaError_t launch_ep_pack(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
+                           const float* scores, __nv_bfloat16* rows, float* s_rows, cudaStream_t st);
+cudaError_t launch_ep_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* rows,
+                              const float* scores, __nv_bfloat16* out, cudaStream_t st);
+cudaError_t launch_ep_unsort(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const float* vals, float* out,
+                             cudaStream_t st);
 cudaError_t launch_mxfp8_quantize(const __nv_bfloat16* src, int batch, int rows, int cols, int block_axis,
                                   uint8_t* q, uint8_t* sf, cudaStream_t st);
 

@@ -17,6 +17,28 @@ from .inputs import Shape
 PRECISIONS = {"bf16": _lib.MOK_BF16, "mxfp8": _lib.MOK_MXFP8}
 
 
+def quantize_weights(W1, W3, W2, stream=None):
+    """Pre-quantise bf16 weights for MXFP8 mode (the pages' ops.mxfp8_quantize
+    step), in both orientations: the forward contracts W1/W3 over H and W2
+    over I (blocks along the rows of each matrix, block_axis 0), the
+    backward contracts W1/W3 over I and W2 over H (block_axis 1).
+    Returns {"fwd": (mx1, mx3, mx2), "bwd": (...)} of descriptors; the
+    code and scale tensors are kept alive on the returned object."""
+    out = {"tensors": []}
+    for orient, axis in (("fwd", 0), ("bwd", 1)):
+        descs = []
+        for W in (W1, W3, W2):
+            E, r, c = W.shape
+            q = torch.empty((E, r, c), dtype=torch.uint8, device=W.device)
+            sf_shape = (E, r // 32, c) if axis == 0 else (E, r, c // 32)
+            sf = torch.empty(sf_shape, dtype=torch.uint8, device=W.device)
+            _lib.mok_mxfp8_quantize(W, axis, q, sf, stream)
+            out["tensors"] += [q, sf]
+            descs.append(_lib.mx(q, sf))
+        out[orient] = tuple(descs)
+    return out
+
+
 class MoKLayer:
     def __init__(self, shape: Shape, precision="bf16", minibatch_rows=0, ring_slots=0, debug_flags=0,
                  replay=False, device="cuda"):
@@ -70,25 +92,7 @@ class MoKLayer:
 
     # -- MXFP8 weights ------------------------------------------------------
     def quantize_weights(self, W1, W3, W2, stream=None):
-        """Pre-quantise bf16 weights for MXFP8 mode (the pages' ops.mxfp8_quantize
-        step), in both orientations: the forward contracts W1/W3 over H and W2
-        over I (blocks along the rows of each matrix, block_axis 0), the
-        backward contracts W1/W3 over I and W2 over H (block_axis 1).
-        Returns {"fwd": (mx1, mx3, mx2), "bwd": (...)} of descriptors; the
-        code and scale tensors are kept alive on the returned object."""
-        out = {"tensors": []}
-        for orient, axis in (("fwd", 0), ("bwd", 1)):
-            descs = []
-            for W in (W1, W3, W2):
-                E, r, c = W.shape
-                q = torch.empty((E, r, c), dtype=torch.uint8, device=W.device)
-                sf_shape = (E, r // 32, c) if axis == 0 else (E, r, c // 32)
-                sf = torch.empty(sf_shape, dtype=torch.uint8, device=W.device)
-                _lib.mok_mxfp8_quantize(W, axis, q, sf, stream)
-                out["tensors"] += [q, sf]
-                descs.append(_lib.mx(q, sf))
-            out[orient] = tuple(descs)
-        return out
+        return quantize_weights(W1, W3, W2, stream)
 
     def check(self, stream=None):
         """Synchronise and raise if the device recorded an error."""
