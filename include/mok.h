@@ -103,6 +103,11 @@ typedef struct {
  *                 Bit 4 (MOK_DEBUG_SINGLE_CTA_ROWS): the BF16 backward's dA'
  *                 and dX GEMMs run one CTA per 128-row tile instead of
  *                 clusters of two CTAs sharing two tiles of one expert.
+ *                 Bit 5 (MOK_DEBUG_SINGLE_CTA_RING): the BF16 forward ring
+ *                 runs one CTA per 128-row tile, gathering token rows of x
+ *                 in its load path, instead of clusters of two CTAs sharing
+ *                 two tiles of one expert and one minibatch, reading a
+ *                 token-sorted copy of x.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
@@ -127,6 +132,7 @@ typedef struct {
 #define MOK_DEBUG_FUSED_WGRAD_GATHER 4
 #define MOK_DEBUG_SINGLE_CTA_WGRAD 8
 #define MOK_DEBUG_SINGLE_CTA_ROWS 16
+#define MOK_DEBUG_SINGLE_CTA_RING 32
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
 typedef struct {
@@ -308,7 +314,8 @@ enum {
   MOK_PHASE_ROUTER_BWD = 12,   /* router: logit gradient, dWr and dx GEMMs */
   MOK_PHASE_BWD_REPLAY = 13,   /* bounded-memory backward: GEMM1 recomputed, context copied back */
   MOK_PHASE_FWD_FUSED = 14,    /* single-launch forward: schedule, GEMMs, combine */
-  MOK_NUM_PHASES = 15
+  MOK_PHASE_FWD_SORT = 15,     /* token-sorted copy of x and the ring's pair table (CTA-pair ring) */
+  MOK_NUM_PHASES = 16
 };
 mok_status mok_trace_enable(int32_t on);
 mok_status mok_trace_read(float* ms /* [MOK_NUM_PHASES] */, int32_t* count /* [MOK_NUM_PHASES] */);

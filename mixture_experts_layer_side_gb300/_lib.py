@@ -23,6 +23,7 @@ MOK_DEBUG_SERIAL_RING = 2
 MOK_DEBUG_FUSED_WGRAD_GATHER = 4
 MOK_DEBUG_SINGLE_CTA_WGRAD = 8
 MOK_DEBUG_SINGLE_CTA_ROWS = 16
+MOK_DEBUG_SINGLE_CTA_RING = 32
 
 STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "MOK_ERR_WORKSPACE_TOO_SMALL",
           4: "MOK_ERR_CUDA", 5: "MOK_ERR_BAD_INDEX", 6: "MOK_ERR_TIMEOUT"}
@@ -37,7 +38,7 @@ EXPORTS = ["mok_workspace_size", "mok_ctx_size", "mok_workspace_layout", "mok_bu
            "mok_ep_plan", "mok_ep_pack_rows", "mok_ep_combine_rows", "mok_ep_unsort_scores"]
 
 PHASES = ["schedule", "fwd_gemm", "fwd_combine", "bwd_da", "bwd_ds", "bwd_dx", "bwd_dx_combine", "bwd_wg13",
-          "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd", "bwd_replay", "fwd_fused"]
+          "bwd_wg2", "quant", "bwd_sort", "router_fwd", "router_bwd", "bwd_replay", "fwd_fused", "fwd_sort"]
 
 
 class MokError(RuntimeError):

@@ -114,6 +114,7 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   L.dsp = take(P * (I / 128) * 4);
   L.sorted = take(P * H * 2);
   L.pair_m0 = take(L.tile_capacity * 4);
+  L.pair_mb = take((L.tile_capacity + 2) * 4);
   if (prec == MOK_MXFP8) {
     L.ring_sf = take((size_t)L.ring_slots * M * (I / 32));
     L.xq = take((size_t)s.T * H);
@@ -663,8 +664,37 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.g1_tiles = s.I / 128;
     g.m_tiles = (int)L.tile_capacity;
     g.counter = 0;
-    Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
-    MOK_CUDA(launch_gemm(GM_FWD_RING, maps, g, gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles)), st));
+    const int grid = gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles));
+    bool launched = false;
+    if (!(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING) && bn2 == 256) {
+      // CTA pairs: GEMM1 reads a token-sorted copy of x with plain TMA (the
+      // backward's sorted buffer, free until the backward), pairs of tiles
+      // from one expert and one minibatch share each 256 x 256 tile
+      __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
+      {
+        Phase ph(MOK_PHASE_FWD_SORT, st, 2);
+        MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
+        MOK_CUDA(launch_ring_pair_table(L, w, st));
+      }
+      TmapSet pm = maps;
+      if (!map2d(&pm.m[0], srt, s.H, (uint64_t)L.pad_capacity, 128)) return MOK_ERR_CUDA;
+      GemmParams gp = g;
+      gp.fwd_sorted = 1;
+      gp.pair_m0 = reinterpret_cast<const int32_t*>(w + L.pair_m0);
+      gp.pair_mb = reinterpret_cast<const int32_t*>(w + L.pair_mb);
+      Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
+      const cudaError_t e = launch_gemm_pair(GM_FWD_RING, pm, gp, grid, st);
+      if (e == cudaSuccess)
+        launched = true;
+      else if (e != cudaErrorNotSupported)
+        return MOK_ERR_CUDA;
+      else
+        (void)cudaGetLastError();  // no cluster of two fits: single CTAs below
+    }
+    if (!launched) {
+      Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
+      MOK_CUDA(launch_gemm(GM_FWD_RING, maps, g, grid, st));
+    }
   } else {
     // minibatch by minibatch in stream order (same ring, no device flags)
     TmapSet m2;

@@ -166,6 +166,38 @@ __device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& 
   return emit(GM_FWD2, nb - 1, w, g2);
 }
 
+// Ring on CTA pairs: the same steps over the ring pair table, N-tile-major
+// over a minibatch's pairs.  Step s (0..nb) holds GEMM1 of minibatch s
+// (s < nb) then GEMM2 of minibatch s - 1 (s >= 1); its first item is
+// g1 * pair_mb[s] + g2 * pair_mb[s - 1], found by bisection.
+__device__ void decode_ring_pair(const GemmParams& p, int w, int& type, int& pidx, int& n) {
+  const int Mt = p.ring_rows / kTileRows;
+  const int nb = (used_tiles(p) + Mt - 1) / Mt;
+  const int g1 = p.g1_tiles, g2 = p.n_tiles;
+  const int32_t* off = p.pair_mb;
+  auto start = [&](int st) { return st == 0 ? 0 : g1 * off[min(st, nb)] + g2 * off[st - 1]; };
+  int lo = 0, hi = nb;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (start(mid) <= w) lo = mid; else hi = mid - 1;
+  }
+  int r = w - start(lo);
+  if (lo < nb) {
+    const int p1 = off[lo + 1] - off[lo];
+    if (r < g1 * p1) {
+      type = GM_FWD1;
+      pidx = off[lo] + r % p1;
+      n = r / p1;
+      return;
+    }
+    r -= g1 * p1;
+  }
+  const int p2 = off[lo] - off[lo - 1];
+  type = GM_FWD2;
+  pidx = off[lo - 1] + r % p2;
+  n = r / p2;
+}
+
 __device__ __forceinline__ int row_k_iters(const GemmParams& p, int type, int el) {
   return (type == GM_FWD1 || type == GM_BWD_DA) ? p.H / el
          : (type == GM_FWD2)                   ? p.I / el
@@ -229,6 +261,19 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
         it.k_iters = row_k_iters(p, type, kEl);
       }
     }
+  } else if constexpr (PAIR && MODE == GM_FWD_RING) {
+    // the ring on CTA pairs: as dA' / dX below, over the ring pair table
+    int type, pidx, n;
+    decode_ring_pair(p, w, type, pidx, n);
+    const int code = p.pair_m0[pidx];
+    it.idle = (code & 1) && ctl->pair_rank == 1;
+    const int m = (code >> 1) + (it.idle ? 0 : ctl->pair_rank);
+    it.type = type;
+    it.m = m;
+    it.n = n;
+    it.e = p.tile_expert[m];
+    it.row0 = m * kTileRows;
+    it.k_iters = row_k_iters(p, type, kEl);
   } else if constexpr (PAIR) {
     // dA' / dX on CTA pairs: the leader takes the pair's first tile, the
     // other CTA the second (or, in a solo pair, the first again, idle)
@@ -273,6 +318,7 @@ __device__ __forceinline__ int ring_row(const GemmParams& p, int prow) {
 // plain TMA instead.
 __device__ __forceinline__ int gathered_operand(const GemmParams& p, int type) {
   if (p.wg_sorted && (type == GM_WG13 || type == GM_WG2)) return 0;
+  if (p.fwd_sorted && type == GM_FWD1) return 0;
   if (p.rows_sorted && type == GM_BWD_DA) return 0;
   return (type == GM_FWD1 || type == GM_BWD_DA || type == GM_WG13) ? 1 : (type == GM_WG2 ? 2 : 0);
 }
@@ -346,7 +392,19 @@ template <int MODE>
 __device__ __forceinline__ void tma_loads_pair(const TmapSet& mp, const GemmParams& p, const Item& it, int kk,
                                                int rank, uint8_t* a, uint8_t* b, uint32_t bar) {
   const int bcol = it.n * 256 + rank * 128;
-  if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
+  if constexpr (MODE == GM_FWD_RING) {
+    if (it.type == GM_FWD1) {
+      // A: token-sorted x rows; B: the leader's half is the W1 column block
+      // (h), the other CTA's the W3 block (u) of intermediate columns n*128..
+      tma_load_2d_pair(a, &mp.m[0], bar, kk * 64, it.row0);
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d_pair(b + c * 8192, &mp.m[rank ? 2 : 1], bar, it.n * 128 + c * 64, kk * 64, it.e);
+    } else {
+      // A: this tile's ring rows; B: this CTA's 128 columns of the W2 block
+      tma_load_2d_pair(a, &mp.m[3], bar, kk * 64, ring_row(p, it.row0));
+      for (int c = 0; c < 2; ++c) tma_load_3d_pair(b + c * 8192, &mp.m[4], bar, bcol + c * 64, kk * 64, it.e);
+    }
+  } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
     const int krow = it.row0 + kk * 64;
     for (int c = 0; c < 2; ++c) tma_load_2d_pair(a + c * 8192, &mp.m[0], bar, it.m * 128 + c * 64, krow);
     for (int c = 0; c < 2; ++c) tma_load_2d_pair(b + c * 8192, &mp.m[1], bar, bcol + c * 64, krow);
@@ -1322,8 +1380,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // Weight-gradient launches whose operands are all TMA-loaded (token-sorted
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
-  const bool gather_in_pipe =
-      kGather && !(kWgrad && (MX || p.wg_sorted)) && !(MODE == GM_BWD_DA && !MX && p.rows_sorted);
+  const bool gather_in_pipe = kGather && !PAIR && !(kWgrad && (MX || p.wg_sorted)) &&
+                              !(MODE == GM_BWD_DA && !MX && p.rows_sorted);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)
@@ -1396,6 +1454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const uint32_t tmem = ctl->tmem_base;
   // (single-launch forward: known once the schedule items are done)
   int num_items = kWgrad ? ctl->n_sel * (PAIR ? p.m_tiles / 2 : p.m_tiles) * p.n_tiles
+                  : (PAIR && MODE == GM_FWD_RING) ? p.hdr[kHdrPairs] * (p.g1_tiles + p.n_tiles)
                   : PAIR ? count_pair_items(p)
                   : MODE == GM_FWD_FUSED ? INT_MAX
                                          : count_items<MODE>(p);
@@ -1416,6 +1475,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           if (w < 0) break;
           const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
           bool ok = true;
+          if (is_ring<MODE>() && it.type == GM_FWD2) {
+            // this CTA loads the ring rows of its own tile: acquire their
+            // GEMM1 completion itself, then order the async-proxy loads after it
+            ok = wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc);
+            fence_proxy_async_global();
+            if (!ok) break;
+          }
           for (int kk = 0; kk < it.k_iters; ++kk) {
             if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
             tma_loads_pair<MODE>(maps, p, it, kk, 1, sA + stage * kAStage, sB + stage * kBSt,
@@ -1714,13 +1780,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_arrive(&ctl->tempty[buf]);
         }
       };
-      if (is_ring<MODE>() && it.type == GM_FWD2 && warp == 2 && lane == 0) {
+      if (is_ring<MODE>() && it.type == GM_FWD2 && !it.idle && warp == 2 && lane == 0) {
         // the accumulator is complete, so every load of this tile's ring
         // rows has landed: release the rows for reuse
         red_release_gpu_add(&p.ring_flags[p.m_tiles + it.m], 1u);
       }
       bool ok = true;
-      if (is_ring<MODE>() && it.type == GM_FWD1) {
+      if (is_ring<MODE>() && it.type == GM_FWD1 && !it.idle) {
         // the ring slot rows this tile writes were last read by GEMM2 of the
         // tile ring_slots minibatches back; each warp waits on its own (no
         // CTA-level barrier on a path that a bounded wait can abandon)
@@ -1753,7 +1819,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           red_release_gpu_add(hdr_word(p, kHdrG2Done), 1u);
         }
       }
-      if (is_ring<MODE>() && it.type == GM_FWD1) {
+      if (is_ring<MODE>() && it.type == GM_FWD1 && !it.idle) {
         // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
         // read by TMA): each epilogue warp adds 1, so a tile is complete when
         // its counter reaches 4 * (GEMM1 column tiles)
@@ -1880,10 +1946,13 @@ cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p,
   if (p.bn != 256) return cudaErrorInvalidValue;
   if (mode == GM_WG13 || mode == GM_WG2) {
     if (!p.wg_sorted || p.m_tiles % 2 != 0) return cudaErrorInvalidValue;
+  } else if (mode == GM_FWD_RING) {
+    if (!p.pair_m0 || !p.pair_mb || !p.fwd_sorted) return cudaErrorInvalidValue;
   } else if (!p.pair_m0 || (mode == GM_BWD_DA && !p.rows_sorted)) {
     return cudaErrorInvalidValue;
   }
   switch (mode) {
+    case GM_FWD_RING: return launch_pair_mode<GM_FWD_RING>(maps, p, grid, st);
     case GM_WG13: return launch_pair_mode<GM_WG13>(maps, p, grid, st);
     case GM_WG2: return launch_pair_mode<GM_WG2>(maps, p, grid, st);
     case GM_BWD_DA: return launch_pair_mode<GM_BWD_DA>(maps, p, grid, st);

@@ -78,8 +78,11 @@ struct GemmParams {
   int nmaps;               // tensor maps in use (prefetched at start)
   int wg_sorted;           // weight gradients read token-sorted copies (plain TMA)
   int rows_sorted;         // dA' reads a token-sorted copy of dout (plain TMA)
-  // CTA-pair launches of dA' / dX: the pair table (first M tile * 2 + solo)
+  // CTA-pair launches of dA' / dX / the forward ring: the pair table (first
+  // M tile * 2 + solo); the ring's pairs of minibatch b are [pair_mb[b], pair_mb[b+1])
   const int32_t* pair_m0;
+  const int32_t* pair_mb;
+  int fwd_sorted;          // GEMM1 reads a token-sorted copy of x (plain TMA) instead of gathering
   // single-launch forward (GM_FWD_FUSED): the schedule's input and arrays
   // (written by its schedule items), and the combine's output
   const int32_t* topk_idx;
@@ -123,11 +126,12 @@ cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int 
 cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 // BF16 launches on clusters of two CTAs that share each 256 x 256 tile
 // through one cta_group::2 MMA: the weight-gradient GEMMs (GM_WG13 / GM_WG2,
-// token-sorted operands, an even number of 128-row M tiles, bn = 256) and
-// the row-tiled backward GEMMs (GM_BWD_DA with token-sorted dout, GM_BWD_DX;
+// token-sorted operands, an even number of 128-row M tiles, bn = 256), the
+// row-tiled backward GEMMs (GM_BWD_DA with token-sorted dout, GM_BWD_DX;
 // bn = 256, the pair table of launch_pair_table, weight maps with 128-row
-// boxes).  Returns cudaErrorNotSupported when the device cannot hold a
-// cluster of two.
+// boxes) and the forward ring (GM_FWD_RING with a token-sorted copy of x,
+// bn = 256, the pair table of launch_ring_pair_table).  Returns
+// cudaErrorNotSupported when the device cannot hold a cluster of two.
 cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace mok

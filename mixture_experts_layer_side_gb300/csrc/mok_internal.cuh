@@ -48,7 +48,8 @@ struct WsLayout {
   size_t as;          // bf16 [pad_capacity, I]  s * a
   size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
   size_t sorted;      // bf16 [pad_capacity, H]: token-sorted dout (dA', dW2), then x (dW1|dW3)
-  size_t pair_m0;     // int32 [tile_capacity]: CTA-pair tiles of dA' / dX (first M tile * 2 + solo)
+  size_t pair_m0;     // int32 [tile_capacity]: CTA-pair tiles of dA' / dX / the ring (first M tile * 2 + solo)
+  size_t pair_mb;     // int32 [tile_capacity + 2]: forward ring, first pair of each minibatch
   // MXFP8 operand copies
   size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
   size_t sfa_rows_t;  // the A operand's scales in padded-row order, tiled: [pad/128][max(H,2I)/128][512]
@@ -74,6 +75,8 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
 cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, const int32_t* idx,
                             cudaStream_t st);
 cudaError_t launch_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
+// the forward ring's pair table: pairs inside one minibatch, per-minibatch offsets in pair_mb
+cudaError_t launch_ring_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* yk,
                            const float* scores, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_t* ws, float* ds, int n_parts,

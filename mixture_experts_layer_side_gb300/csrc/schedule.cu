@@ -168,13 +168,17 @@ __global__ void __launch_bounds__(kPlaceWarps * 32)
   }
 }
 
-// CTA-pair table of the row-tiled backward GEMMs: the tiles of each expert
-// are taken two at a time from its first; a last tile without a partner is
-// a solo pair, whose second CTA loads valid rows but stores nothing.  One
-// block; integer work, exact.
+// CTA-pair table of the row-tiled GEMMs: the tiles of each expert are taken
+// two at a time from its first; a last tile without a partner is a solo
+// pair, whose second CTA loads valid rows but stores nothing.  With seg > 0
+// (the forward ring, seg = tiles per minibatch) a pair never straddles a
+// minibatch either: segments also start at every multiple of seg, and
+// mb_off[b] is the index of minibatch b's first pair (mb_off[nb] = pairs).
+// One block; integer work, exact.
 __global__ void __launch_bounds__(1024) pair_table_kernel(const int32_t* __restrict__ tile_expert,
                                                           const int32_t* __restrict__ poff, int32_t* __restrict__ hdr,
-                                                          int32_t* __restrict__ pair_m0) {
+                                                          int32_t* __restrict__ pair_m0, int seg,
+                                                          int32_t* __restrict__ mb_off) {
   __shared__ int warp_tot[32];
   __shared__ int tot;
   const int U = hdr[kHdrTiles];
@@ -184,14 +188,22 @@ __global__ void __launch_bounds__(1024) pair_table_kernel(const int32_t* __restr
     int head = 0, solo = 0;
     if (m < U) {
       const int e = tile_expert[m];
-      head = ((m - poff[e] / kTileRows) & 1) == 0;
-      solo = head && (m + 1 >= U || tile_expert[m + 1] != e);
+      int start = poff[e] / kTileRows;
+      if (seg > 0) start = max(start, m / seg * seg);
+      head = ((m - start) & 1) == 0;
+      solo = head && (m + 1 >= U || tile_expert[m + 1] != e || (seg > 0 && (m + 1) % seg == 0));
     }
     const int pos = carry + block_exclusive_scan(head, warp_tot, &tot);
-    if (head) pair_m0[pos] = 2 * m + solo;
+    if (head) {
+      pair_m0[pos] = 2 * m + solo;
+      if (seg > 0 && m % seg == 0) mb_off[m / seg] = pos;
+    }
     carry += tot;
   }
-  if (threadIdx.x == 0) hdr[kHdrPairs] = carry;
+  if (threadIdx.x == 0) {
+    hdr[kHdrPairs] = carry;
+    if (seg > 0) mb_off[(U + seg - 1) / seg] = carry;
+  }
 }
 
 }  // namespace
@@ -217,7 +229,15 @@ cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, 
 
 cudaError_t launch_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st) {
   auto P = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
-  pair_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0));
+  pair_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0), 0,
+                                        nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+  auto P = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
+  pair_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0),
+                                        L.minibatch_rows / kTileRows, P(L.pair_mb));
   return cudaGetLastError();
 }
 

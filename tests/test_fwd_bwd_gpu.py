@@ -141,6 +141,29 @@ def test_backward_row_gemm_cta_pairs_match_single_cta(shape, routing, kw):
         assert torch.equal(g_p[k], g_s[k]), k
 
 
+@pytest.mark.parametrize("shape,routing,kw", [
+    ((4096, 256, 256, 8, 2), "zipf", {}),
+    # one tile per expert: every pair is a solo pair
+    ((256, 256, 256, 16, 2), "uniform", {}),
+    # three and five tiles per minibatch: pairs stop at minibatch boundaries
+    ((2048, 256, 256, 12, 4), "hot", dict(minibatch_rows=384, ring_slots=3)),
+    ((1000, 512, 256, 6, 3), "uniform", dict(minibatch_rows=640, ring_slots=2)),
+    ((4096, 256, 256, 16, 4), "zipf", dict(replay=True, minibatch_rows=256, ring_slots=2)),
+    ((1024, 4096, 256, 24, 4), "hot", {}),
+])
+def test_forward_ring_cta_pairs_match_single_cta(shape, routing, kw):
+    """The forward ring on clusters of two CTAs (token-sorted x by plain TMA,
+    two tiles of one expert and one minibatch per cta_group::2 MMA) against
+    one CTA per tile gathering x in its load path: bitwise equal outputs,
+    and the backward from each forward's context bitwise equal too."""
+    require_gpu()
+    _, out_p, g_p = run_layer(shape, routing, 15, **kw)
+    _, out_s, g_s = run_layer(shape, routing, 15, debug_flags=32, **kw)
+    assert torch.equal(out_p, out_s)
+    for k in g_p:
+        assert torch.equal(g_p[k], g_s[k]), k
+
+
 def _run_with_idx(shape, idx, seed):
     from mixture_experts_layer_side_gb300.inputs import Shape, make_inputs
     from mixture_experts_layer_side_gb300.layer import MoKLayer
