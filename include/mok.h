@@ -103,11 +103,18 @@ typedef struct {
  *                 Bit 4 (MOK_DEBUG_SINGLE_CTA_ROWS): the BF16 backward's dA'
  *                 and dX GEMMs run one CTA per 128-row tile instead of
  *                 clusters of two CTAs sharing two tiles of one expert.
- *                 Bit 5 (MOK_DEBUG_SINGLE_CTA_RING): the BF16 forward ring
- *                 runs one CTA per 128-row tile, gathering token rows of x
- *                 in its load path, instead of clusters of two CTAs sharing
- *                 two tiles of one expert and one minibatch, reading a
- *                 token-sorted copy of x.
+ *                 Bits 5 and 7 (MOK_DEBUG_SINGLE_CTA_RING,
+ *                 MOK_DEBUG_PAIR_RING): the BF16 forward ring runs one CTA
+ *                 per 128-row tile, gathering token rows of x in its load
+ *                 path (bit 5), or clusters of two CTAs sharing two tiles of
+ *                 one expert and one minibatch, reading a token-sorted copy
+ *                 of x (bit 7).  By default it takes clusters of two when
+ *                 the experts average at least 1,024 routed rows
+ *                 (T*k >= 1024*E): below that, an expert's odd last tile
+ *                 leaves too many CTAs of a pair idle.
+ *                 Bit 6 (MOK_DEBUG_NO_PREFETCH): the BF16 row-tiled GEMMs
+ *                 (forward ring, dA', dX) do not prefetch their weight tiles
+ *                 into L2 ahead of the shared-memory pipeline.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
@@ -133,6 +140,8 @@ typedef struct {
 #define MOK_DEBUG_SINGLE_CTA_WGRAD 8
 #define MOK_DEBUG_SINGLE_CTA_ROWS 16
 #define MOK_DEBUG_SINGLE_CTA_RING 32
+#define MOK_DEBUG_NO_PREFETCH 64
+#define MOK_DEBUG_PAIR_RING 128
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
 typedef struct {

@@ -666,7 +666,13 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.counter = 0;
     const int grid = gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles));
     bool launched = false;
-    if (!(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING) && bn2 == 256) {
+    // CTA pairs pay for an expert's odd last tile with an idle CTA: take
+    // them when experts average at least 8 tiles (1,024 routed rows), or
+    // when asked to
+    const bool many_rows = (int64_t)s.T * s.k >= (int64_t)1024 * s.E;
+    const bool pairs = (cfg->debug_flags & MOK_DEBUG_PAIR_RING) ||
+                       (many_rows && !(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING));
+    if (pairs && bn2 == 256) {
       // CTA pairs: GEMM1 reads a token-sorted copy of x with plain TMA (the
       // backward's sorted buffer, free until the backward), pairs of tiles
       // from one expert and one minibatch share each 256 x 256 tile

@@ -386,6 +386,38 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
   }
 }
 
+// L2 prefetch of the weight boxes of K stage kk of an item (the operand
+// every tile of an expert re-reads, streamed from DRAM), issued kPrefetchAhead
+// stages before the stage's load so that load finds them in L2.  Weights are
+// read-only in every launch, so a prefetch never sees a stale value.
+constexpr int kPrefetchAhead = 8;
+
+template <int MODE>
+__device__ __forceinline__ void prefetch_weights(const TmapSet& mp, const GemmParams& p, const Item& it, int kk) {
+  const int type = it.type;
+  if (MODE == GM_DENSE) {
+    if (p.a_mn)
+      for (int c = 0; c < 2; ++c) tma_prefetch_l2_2d(&mp.m[0], it.m * 128 + c * 64, kk * 64);
+    else
+      tma_prefetch_l2_2d(&mp.m[0], kk * 64, it.m * 128);
+    if (p.b_mn)
+      for (int c = 0; c < p.bn / 64; ++c) tma_prefetch_l2_2d(&mp.m[1], it.n * p.bn + c * 64, kk * 64);
+    else
+      tma_prefetch_l2_2d(&mp.m[1], kk * 64, it.n * p.bn);
+  } else if (type == GM_FWD1) {
+    for (int c = 0; c < 2; ++c) tma_prefetch_l2_3d(&mp.m[1], it.n * 128 + c * 64, kk * 64, it.e);
+    for (int c = 0; c < 2; ++c) tma_prefetch_l2_3d(&mp.m[2], it.n * 128 + c * 64, kk * 64, it.e);
+  } else if (type == GM_FWD2) {
+    const int wmap = is_ring<MODE>() ? 4 : 1;
+    for (int c = 0; c < p.bn / 64; ++c) tma_prefetch_l2_3d(&mp.m[wmap], it.n * p.bn + c * 64, kk * 64, it.e);
+  } else if (type == GM_BWD_DA) {
+    tma_prefetch_l2_3d(&mp.m[1], kk * 64, it.n * p.bn, it.e);
+  } else if (type == GM_BWD_DX) {
+    const int ki = p.I / 64;
+    tma_prefetch_l2_3d(&mp.m[kk < ki ? 1 : 2], (kk < ki ? kk : kk - ki) * 64, it.n * p.bn, it.e);
+  }
+}
+
 // CTA-pair stage: this CTA's A tile (its own 128 M rows) and its half of
 // the 256-column B tile, completing on the leader's barrier.
 template <int MODE>
@@ -1555,6 +1587,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             w_next = (int)atomicAdd(counter, 1u);
           }
           const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
+          // the item after this one (already fetched): its first stages'
+          // weights are prefetched to L2 during this item's last ones
+          constexpr bool kPf = !MX && !PAIR && !kWgrad && MODE != GM_FWD_FUSED;
+          Item nx;
+          nx.k_iters = 0;
+          if (kPf && w_next < num_items && !(p.debug_flags & MOK_DEBUG_NO_PREFETCH))
+            nx = decode<MODE, MX, PAIR>(p, ctl, w_next);
           if (is_ring<MODE>() && it.type == GM_FWD2) {
             // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
             // of its GEMM1 column tiles are published, then order the
@@ -1567,7 +1606,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           const uint32_t bytes = PAIR ? 4u * kAStage
                                  : MX ? mx_stage_bytes<MODE>(p, it.type, item_bn(p, it.type))
                                       : tma_stage_bytes(p, it.type, item_bn(p, it.type));
+          const bool pf = kPf && !(p.debug_flags & MOK_DEBUG_NO_PREFETCH);
           for (int kk = 0; kk < it.k_iters; ++kk) {
+            if (pf) {
+              const int pk = kk + kPrefetchAhead;
+              if (pk < it.k_iters)
+                prefetch_weights<MODE>(maps, p, it, pk);
+              else if (pk - it.k_iters < nx.k_iters)
+                prefetch_weights<MODE>(maps, p, nx, pk - it.k_iters);
+            }
             if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
             mbar_arrive_expect_tx(&ctl->full[stage], bytes);
             if constexpr (PAIR)
