@@ -112,9 +112,6 @@ typedef struct {
  *                 the experts average at least 1,024 routed rows
  *                 (T*k >= 1024*E): below that, an expert's odd last tile
  *                 leaves too many CTAs of a pair idle.
- *                 Bit 6 (MOK_DEBUG_NO_PREFETCH): the BF16 row-tiled GEMMs
- *                 (forward ring, dA', dX) do not prefetch their weight tiles
- *                 into L2 ahead of the shared-memory pipeline.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
@@ -140,7 +137,6 @@ typedef struct {
 #define MOK_DEBUG_SINGLE_CTA_WGRAD 8
 #define MOK_DEBUG_SINGLE_CTA_ROWS 16
 #define MOK_DEBUG_SINGLE_CTA_RING 32
-#define MOK_DEBUG_NO_PREFETCH 64
 #define MOK_DEBUG_PAIR_RING 128
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
@@ -394,9 +390,9 @@ mok_status mok_build_schedule_noalloc(const mok_shape* shape, const int32_t* top
  *      block_axis 1); a_mn_major = 1: Aq u8 [K, M] + Asf u8 [K/32, M]
  *      (block_axis 0).  B likewise with N: [N, K] + [N, K/32], or
  *      [K, N] + [K/32, N].
- *   scratch (device, caller-owned) >= 256 + (a_mn_major ? M*K/32 : 0)
- *      + (b_mn_major ? N*K/32 : 0) bytes (tile counter, error word, and
- *      M/N-major scales re-tiled for the GEMM).
+ *   scratch (device, caller-owned) >= 256 + M*K/32 + N*K/32 bytes (tile
+ *      counter, error word, and both operands' scales re-tiled for the
+ *      GEMM's bulk loads).
  * M, N, K multiples of 128.
  */
 mok_status mok_gemm_mxfp8(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, const uint8_t* Asf,

@@ -1114,23 +1114,24 @@ mok_status mok_gemm_mxfp8(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, co
                           void* scratch, size_t scratch_bytes, void* stream) {
   if (!Aq || !Asf || !Bq || !Bsf || !C || !scratch) return MOK_ERR_INVALID_ARG;
   if (M < 128 || N < 128 || K < 128 || M % 128 || N % 128 || K % 128) return MOK_ERR_UNSUPPORTED;
-  const size_t need = 256 + (a_mn_major ? (size_t)M * K / 32 : 0) + (b_mn_major ? (size_t)N * K / 32 : 0);
+  const size_t need = 256 + (size_t)M * K / 32 + (size_t)N * K / 32;
   if (scratch_bytes < need) return MOK_ERR_WORKSPACE_TOO_SMALL;
   const int bn = (N % 256 == 0) ? 256 : 128;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   uint8_t* sfa_t = sc + 256;
-  uint8_t* sfb_t = sfa_t + (a_mn_major ? (size_t)M * K / 32 : 0);
+  uint8_t* sfb_t = sfa_t + (size_t)M * K / 32;
   MOK_CUDA(cudaMemsetAsync(sc, 0, kHeaderWords * 4, st));
-  int kernels = 1;
-  if (a_mn_major) {
+  // both operands' scales re-tiled for the TMA thread's bulk loads
+  if (a_mn_major)
     MOK_CUDA(launch_tile_scales(Asf, 1, K / 32, M, sfa_t, st));
-    ++kernels;
-  }
-  if (b_mn_major) {
+  else
+    MOK_CUDA(launch_tile_scales_rows(Asf, 1, M, K / 32, sfa_t, st));
+  if (b_mn_major)
     MOK_CUDA(launch_tile_scales(Bsf, 1, K / 32, N, sfb_t, st));
-    ++kernels;
-  }
+  else
+    MOK_CUDA(launch_tile_scales_rows(Bsf, 1, N, K / 32, sfb_t, st));
+  const int kernels = 3;
   TmapSet m;
   memset(&m, 0, sizeof(m));
   bool ok = a_mn_major ? map2d_u8(&m.m[0], Aq, M, K, 128, 128) : map2d_u8(&m.m[0], Aq, K, M, 128, 128);

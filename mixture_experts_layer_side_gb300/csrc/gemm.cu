@@ -386,38 +386,6 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
   }
 }
 
-// L2 prefetch of the weight boxes of K stage kk of an item (the operand
-// every tile of an expert re-reads, streamed from DRAM), issued kPrefetchAhead
-// stages before the stage's load so that load finds them in L2.  Weights are
-// read-only in every launch, so a prefetch never sees a stale value.
-constexpr int kPrefetchAhead = 8;
-
-template <int MODE>
-__device__ __forceinline__ void prefetch_weights(const TmapSet& mp, const GemmParams& p, const Item& it, int kk) {
-  const int type = it.type;
-  if (MODE == GM_DENSE) {
-    if (p.a_mn)
-      for (int c = 0; c < 2; ++c) tma_prefetch_l2_2d(&mp.m[0], it.m * 128 + c * 64, kk * 64);
-    else
-      tma_prefetch_l2_2d(&mp.m[0], kk * 64, it.m * 128);
-    if (p.b_mn)
-      for (int c = 0; c < p.bn / 64; ++c) tma_prefetch_l2_2d(&mp.m[1], it.n * p.bn + c * 64, kk * 64);
-    else
-      tma_prefetch_l2_2d(&mp.m[1], kk * 64, it.n * p.bn);
-  } else if (type == GM_FWD1) {
-    for (int c = 0; c < 2; ++c) tma_prefetch_l2_3d(&mp.m[1], it.n * 128 + c * 64, kk * 64, it.e);
-    for (int c = 0; c < 2; ++c) tma_prefetch_l2_3d(&mp.m[2], it.n * 128 + c * 64, kk * 64, it.e);
-  } else if (type == GM_FWD2) {
-    const int wmap = is_ring<MODE>() ? 4 : 1;
-    for (int c = 0; c < p.bn / 64; ++c) tma_prefetch_l2_3d(&mp.m[wmap], it.n * p.bn + c * 64, kk * 64, it.e);
-  } else if (type == GM_BWD_DA) {
-    tma_prefetch_l2_3d(&mp.m[1], kk * 64, it.n * p.bn, it.e);
-  } else if (type == GM_BWD_DX) {
-    const int ki = p.I / 64;
-    tma_prefetch_l2_3d(&mp.m[kk < ki ? 1 : 2], (kk < ki ? kk : kk - ki) * 64, it.n * p.bn, it.e);
-  }
-}
-
 // CTA-pair stage: this CTA's A tile (its own 128 M rows) and its half of
 // the 256-column B tile, completing on the leader's barrier.
 template <int MODE>
@@ -524,9 +492,9 @@ template <int MODE>
 __device__ __forceinline__ uint32_t mx_stage_bytes(const GemmParams& p, int type, int bn) {
   const uint32_t bchunks = (uint32_t)bn / 128;
   switch (MODE == GM_DENSE ? GM_DENSE : type) {
-    case GM_DENSE: return kAStage + bn * 128 + (p.a_mn ? 512u : 0u) + (p.b_mn ? 512u * bchunks : 0u);
+    case GM_DENSE: return kAStage + bn * 128 + 512u + 512u * bchunks;
     case GM_FWD1: return 2u * 16384u + 1024u + 512u;
-    case GM_FWD2: return kAStage + bn * 128 + 512u * bchunks;
+    case GM_FWD2: return kAStage + bn * 128 + 512u + 512u * bchunks;
     case GM_BWD_DA: return bn * 128 + 512u * bchunks + 512u;
     case GM_BWD_DX: return kAStage + bn * 128 + 512u * bchunks + 512u;
     case GM_WG13: return kAStage + 2u * 16384u + 512u + 1024u;
@@ -540,21 +508,20 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
   const int type = it.type;
   const int bn = item_bn(p, type);
   if (MODE == GM_DENSE) {
+    // both operands' scales come pre-tiled ([MN/128][K/128][512 B])
     const int kgroups = p.k_iters;
-    if (p.a_mn) {
+    if (p.a_mn)
       tma_load_2d(a, &mp.m[0], bar, it.m * 128, kk * 128);
-      bulk_load(sfa, p.sfa_tiled + ((long)it.m * kgroups + kk) * 512, 512, bar);
-    } else {
+    else
       tma_load_2d(a, &mp.m[0], bar, kk * 128, it.m * 128);
-    }
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * kgroups + kk) * 512, 512, bar);
     if (p.b_mn) {
-      for (int c = 0; c < bn / 128; ++c) {
-        tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, kk * 128);
-        bulk_load(sfb + c * 512, p.sfb_tiled0 + ((long)(it.n * (bn / 128) + c) * kgroups + kk) * 512, 512, bar);
-      }
+      for (int c = 0; c < bn / 128; ++c) tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, kk * 128);
     } else {
       tma_load_2d(b, &mp.m[1], bar, kk * 128, it.n * bn);
     }
+    for (int c = 0; c < bn / 128; ++c)
+      bulk_load(sfb + c * 512, p.sfb_tiled0 + ((long)(it.n * (bn / 128) + c) * kgroups + kk) * 512, 512, bar);
   } else if (type == GM_FWD1) {
     const int hg = p.H / 128;
     tma_load_3d(b, &mp.m[1], bar, it.n * 128, kk * 128, it.e);
@@ -568,6 +535,8 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
     const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
     tma_load_2d(a, &mp.m[mslot], bar, kk * 128, ring_row(p, it.row0));
+    // a's scales, tiled by the GEMM1 epilogue next to the ring codes
+    bulk_load(sfa, p.ring_sf + ((long)(ring_row(p, it.row0) >> 7) * (p.I / 128) + kk) * 512, 512, bar);
     for (int c = 0; c < bn / 128; ++c) {
       tma_load_3d(b + c * 16384, &mp.m[wmap], bar, it.n * bn + c * 128, kk * 128, it.e);
       const long blk = ((long)it.e * (p.H / 128) + it.n * (bn / 128) + c) * (p.I / 128) + kk;
@@ -633,9 +602,6 @@ __device__ __forceinline__ void gather_stage_mx(const GemmParams& p, const Item&
   const uint8_t* sa = nullptr;
   if (MODE == GM_DENSE) {
     if (!p.a_mn) sa = p.sfa_rows + ((long)it.m * 128 + gt) * p.sfa_ld + kk * 4;
-  } else if (type == GM_FWD2) {
-    // scales of a, written by the GEMM1 epilogue next to the ring codes
-    sa = p.ring_sf + (long)ring_row(p, it.row0 + gt) * (p.I / 32) + kk * 4;
   }
   if (sa) cp_async_4(smem_u32(sfa + mx_sf_offset(gt, 0)), sa, 4u);
   // scales of K-major B, rows gt and gt + 128 of the N tile (dense launches;
@@ -714,7 +680,12 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
   __nv_bfloat16* urow = hrow + p.I;
   const long rr = ring_row(p, (int)prow);
   uint8_t* qrow = reinterpret_cast<uint8_t*>(p.ring) + rr * p.I + i0;
-  uint8_t* srow = p.ring_sf + rr * (p.I / 32) + i0 / 32;
+  // the row's four scales of this 128-column group go out as one word, in
+  // the tiled layout GEMM2's TMA thread bulk-loads ([ring rows / 128]
+  // [I / 128][512 B], see mx_sf_offset)
+  uint32_t* sword = reinterpret_cast<uint32_t*>(p.ring_sf + ((rr >> 7) * (p.I / 128) + it.n) * 512 +
+                                                mx_sf_offset((int)(rr & 127), 0));
+  uint32_t scales = 0;
 #pragma unroll 1
   for (int c = 0; c < 128; c += 32) {
     float h[32], u[32];
@@ -734,11 +705,12 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
     store32_bf16(hrow + c, hw);
     store32_bf16(urow + c, uw);
     uint32_t q[8];
-    srow[c / 32] = mx_quant32(a, q);
+    scales |= (uint32_t)mx_quant32(a, q) << (c / 4);  // byte c / 32 of the word
     uint4* d = reinterpret_cast<uint4*>(qrow + c);
     d[0] = make_uint4(q[0], q[1], q[2], q[3]);
     d[1] = make_uint4(q[4], q[5], q[6], q[7]);
   }
+  *sword = scales;
 }
 
 // Scatter a tile row to token order: row f of dst (skipped for padding rows;
@@ -1412,7 +1384,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // Weight-gradient launches whose operands are all TMA-loaded (token-sorted
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
-  const bool gather_in_pipe = kGather && !PAIR && !(kWgrad && (MX || p.wg_sorted)) &&
+  const bool gather_in_pipe = kGather && !PAIR && !(MODE == GM_DENSE && MX) && !(kWgrad && (MX || p.wg_sorted)) &&
                               !(MODE == GM_BWD_DA && !MX && p.rows_sorted);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
@@ -1587,13 +1559,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             w_next = (int)atomicAdd(counter, 1u);
           }
           const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
-          // the item after this one (already fetched): its first stages'
-          // weights are prefetched to L2 during this item's last ones
-          constexpr bool kPf = !MX && !PAIR && !kWgrad && MODE != GM_FWD_FUSED;
-          Item nx;
-          nx.k_iters = 0;
-          if (kPf && w_next < num_items && !(p.debug_flags & MOK_DEBUG_NO_PREFETCH))
-            nx = decode<MODE, MX, PAIR>(p, ctl, w_next);
           if (is_ring<MODE>() && it.type == GM_FWD2) {
             // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
             // of its GEMM1 column tiles are published, then order the
@@ -1606,15 +1571,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           const uint32_t bytes = PAIR ? 4u * kAStage
                                  : MX ? mx_stage_bytes<MODE>(p, it.type, item_bn(p, it.type))
                                       : tma_stage_bytes(p, it.type, item_bn(p, it.type));
-          const bool pf = kPf && !(p.debug_flags & MOK_DEBUG_NO_PREFETCH);
           for (int kk = 0; kk < it.k_iters; ++kk) {
-            if (pf) {
-              const int pk = kk + kPrefetchAhead;
-              if (pk < it.k_iters)
-                prefetch_weights<MODE>(maps, p, it, pk);
-              else if (pk - it.k_iters < nx.k_iters)
-                prefetch_weights<MODE>(maps, p, nx, pk - it.k_iters);
-            }
             if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
             mbar_arrive_expect_tx(&ctl->full[stage], bytes);
             if constexpr (PAIR)
@@ -1672,12 +1629,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 #pragma unroll
           for (int j = 0; j < 8; ++j) tok[j] = ga ? token_or_neg(p, it.row0 + (gt >> 3) + 16 * j) : -1;
           if (ga) tok_row = token_or_neg(p, it.row0 + gt);
-          if (MODE == GM_FWD_RING && it.type == GM_FWD2) {
-            // this thread reads scales of a that GEMM1 (another CTA) wrote
-            // next to the ring rows: acquire the same completion count the
-            // TMA producer waits for
-            if (!wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc)) break;
-          }
           const bool copies = (MODE == GM_DENSE) || !(it.type == GM_WG13 || it.type == GM_WG2);
           for (int kk = 0; kk < it.k_iters; ++kk) {
             if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }

@@ -113,7 +113,7 @@ struct GemmParams {
   const uint8_t* sfb_tiled1;
   const uint8_t* sfb_tiled2;  // W2 in the ring launch (W1, W3 use tiled0/1)
   const uint8_t* gq_src;      // gathered E4M3 rows (x or dout codes) [T, H]
-  uint8_t* ring_sf;           // GEMM1 epilogue: scales of a [ring rows][I/32]
+  uint8_t* ring_sf;           // GEMM1 epilogue: scales of a, tiled [ring rows/128][I/128][512 B]
   uint8_t* dhu_q;             // dA' epilogue: dh|du codes [pad, 2I] ...
   uint8_t* dhu_sf;            // ... and scales [pad, 2I/32]
   // Ring launch: m_tiles holds the tile capacity; ring_flags[m] counts the

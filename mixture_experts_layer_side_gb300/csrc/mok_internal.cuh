@@ -41,7 +41,7 @@ struct WsLayout {
   // forward
   size_t ring_flags;  // uint32 [2 * tile_capacity]: GEMM1 / GEMM2 tiles done per M tile
   size_t ring;        // bf16 [ring_slots * minibatch_rows, I]  (MXFP8: e4m3 codes)
-  size_t ring_sf;     // MXFP8: u8 scales [ring_slots * minibatch_rows, I/32]
+  size_t ring_sf;     // MXFP8: u8 scales of the ring rows, tiled [ring rows/128][I/128][512 B]
   size_t yk;          // bf16 [R, H]: expert outputs (forward), dX parts (backward)
   // backward
   size_t dhu;         // bf16 [pad_capacity, 2I]

@@ -57,6 +57,10 @@ WORKLOADS = {
     # few experts, long weight-gradient K loops (2,048 routed rows per expert)
     "long_k": (Shape(16384, 7168, 2048, 16, 2), "uniform", "bf16"),
     "kimi_mxfp8": (Shape(16384, 7168, 2048, 384, 8), "uniform", "mxfp8"),
+    # small multi-pass ncu cases with the DeepSeek-V3 H and I (weights 1.4 GB,
+    # larger than L2; device footprint about 4 GB)
+    "prof_wide": (Shape(2048, 7168, 2048, 16, 4), "zipf", "bf16"),
+    "prof_wide_mx": (Shape(2048, 7168, 2048, 16, 4), "zipf", "mxfp8"),
 }
 
 ZIPF_S = 1.2

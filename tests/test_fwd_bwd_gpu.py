@@ -83,19 +83,6 @@ def test_ring_sizes_and_serial_path_are_bitwise_equal(minibatch_rows, ring_slots
         assert torch.equal(g_a[k], g_b[k]), k
 
 
-@pytest.mark.parametrize("shape,routing,flags", [((4096, 256, 256, 8, 2), "zipf", 0), ((1024, 4096, 256, 24, 4), "hot", 0),
-                                                 ((8192, 256, 256, 4, 2), "uniform", 0)])
-def test_weight_prefetch_changes_nothing(shape, routing, flags):
-    """The L2 prefetch of weight tiles ahead of the smem pipeline (forward
-    ring, dA', dX) against no prefetch: bitwise equal."""
-    require_gpu()
-    _, out_a, g_a = run_layer(shape, routing, 16, debug_flags=flags)
-    _, out_b, g_b = run_layer(shape, routing, 16, debug_flags=flags | 64)
-    assert torch.equal(out_a, out_b)
-    for k in g_a:
-        assert torch.equal(g_a[k], g_b[k]), k
-
-
 @pytest.mark.parametrize("shape,routing", [((512, 256, 256, 24, 4), "hot"), ((4096, 256, 256, 20, 2), "hot")])
 def test_reruns_are_bitwise_identical(shape, routing):
     require_gpu()
