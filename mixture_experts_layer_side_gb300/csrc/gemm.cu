@@ -671,11 +671,72 @@ __device__ void epi_fwd1(const GemmParams& p, const Item& it, uint32_t tbase, in
   }
 }
 
+// 64 accumulator columns of this lane's row (two 32-column TMEM loads, one
+// wait) as 32 packed bf16 pairs (round to nearest even, low half first).
+__device__ __forceinline__ void acc_load64_bf16(uint32_t taddr, uint32_t (&w)[32]) {
+  uint32_t ra[32], rb[32];
+  tmem_ld32_issue(taddr, ra);
+  tmem_ld32_issue(taddr + 32, rb);
+  tmem_wait_ld();
+  tmem_regs_ready(ra);
+  tmem_regs_ready(rb);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    w[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+    w[16 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+  }
+}
+
+// A lane's 32 packed words parked in (and read back from) its own 128-byte
+// row of the warp's staging buffer, 16-byte chunks XOR-swizzled by lane.
+__device__ __forceinline__ void park64(uint8_t* stage, int lane, const uint32_t (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<uint4*>(stage + lane * 128 + ((i ^ (lane & 7)) << 4)) =
+        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+__device__ __forceinline__ uint4 unpark16(const uint8_t* stage, int lane, int i) {
+  return *reinterpret_cast<const uint4*>(stage + lane * 128 + ((i ^ (lane & 7)) << 4));
+}
+
+// 32 accumulator columns as 16 packed bf16 pairs (half the registers of
+// acc_load64_bf16 in flight).
+__device__ __forceinline__ void acc_load32_bf16(uint32_t taddr, uint32_t* w16) {
+  uint32_t r[32];
+  tmem_ld32_issue(taddr, r);
+  tmem_wait_ld();
+  tmem_regs_ready(r);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w16[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 // MXFP8 GEMM1 epilogue: as epi_fwd1, but a goes to the ring as E4M3 codes
-// with one scale per 32 intermediate columns (the K blocks of GEMM2).
-__device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
+// with one scale per 32 intermediate columns (the K blocks of GEMM2).  The
+// MXFP8 accumulator is single-buffered (TMEM also holds the stage scales),
+// so the row's h and u are first read as the bf16 values the backward keeps
+// (128 registers), the accumulator is handed back (`release`), and only then
+// is a formed, quantised and stored: the same values, with the next tile's
+// main loop already running.
+template <typename Release>
+__device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase, int row, int lane, uint8_t* stage,
+                            Release&& release) {
   const long prow = (long)it.row0 + row;
   const int i0 = it.n * 128;
+  // h columns 0..63 parked in the staging buffer, the rest in registers
+  uint32_t hw1[32], uw[2][32];
+  {
+    uint32_t hw0[32];
+    acc_load64_bf16(tbase, hw0);
+    park64(stage, lane, hw0);
+  }
+  acc_load64_bf16(tbase + 64, hw1);
+  acc_load64_bf16(tbase + 128, uw[0]);
+  acc_load64_bf16(tbase + 192, uw[1]);
+  release();
   __nv_bfloat16* hrow = p.ctx_hu + prow * 2 * p.I + i0;
   __nv_bfloat16* urow = hrow + p.I;
   const long rr = ring_row(p, (int)prow);
@@ -686,31 +747,105 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
   uint32_t* sword = reinterpret_cast<uint32_t*>(p.ring_sf + ((rr >> 7) * (p.I / 128) + it.n) * 512 +
                                                 mx_sf_offset((int)(rr & 127), 0));
   uint32_t scales = 0;
-#pragma unroll 1
-  for (int c = 0; c < 128; c += 32) {
-    float h[32], u[32];
-    tmem_ld32(tbase + c, h);
-    tmem_ld32(tbase + 128 + c, u);
-    uint32_t hw[16], uw[16];
-    float a[32];
+  // columns 64..127 first, so their registers are free before the parked
+  // columns 0..63 are read back
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float h0 = bf16_round(h[2 * i]), h1 = bf16_round(h[2 * i + 1]);
-      const float u0 = bf16_round(u[2 * i]), u1 = bf16_round(u[2 * i + 1]);
-      hw[i] = pack_bf16x2(h0, h1);
-      uw[i] = pack_bf16x2(u0, u1);
-      a[2 * i] = h0 * sigmoidf_(h0) * u0;
-      a[2 * i + 1] = h1 * sigmoidf_(h1) * u1;
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = (cc + 2) & 3;
+    const int o = (c & 1) * 16;  // 32 columns = 16 packed words
+    uint32_t h[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (c < 2) {
+        const uint4 v = unpark16(stage, lane, (c & 1) * 4 + i);
+        h[4 * i] = v.x; h[4 * i + 1] = v.y; h[4 * i + 2] = v.z; h[4 * i + 3] = v.w;
+      } else {
+        h[4 * i] = hw1[o + 4 * i]; h[4 * i + 1] = hw1[o + 4 * i + 1];
+        h[4 * i + 2] = hw1[o + 4 * i + 2]; h[4 * i + 3] = hw1[o + 4 * i + 3];
+      }
     }
-    store32_bf16(hrow + c, hw);
-    store32_bf16(urow + c, uw);
+    const uint32_t* u = &uw[c >> 1][o];
+    uint4* dh = reinterpret_cast<uint4*>(hrow + c * 32);
+    uint4* du = reinterpret_cast<uint4*>(urow + c * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      dh[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+      du[i] = make_uint4(u[4 * i], u[4 * i + 1], u[4 * i + 2], u[4 * i + 3]);
+    }
+    // a = silu(h) u of the 32-column block, quantised as mx_quant32 does:
+    // its amax first, then a formed again (the same values) as it is converted
+    auto act = [&](int e) {
+      const uint32_t hv = h[e >> 1], uv = u[e >> 1];
+      const float hh = (e & 1) ? bf16_hi(hv) : bf16_lo(hv);
+      const float uu = (e & 1) ? bf16_hi(uv) : bf16_lo(uv);
+      return hh * sigmoidf_(hh) * uu;
+    };
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(act(e)));
+    const int X = mx_block_exponent(amax);
+    const float inv = mx_exp2_int(-X);
     uint32_t q[8];
-    scales |= (uint32_t)mx_quant32(a, q) << (c / 4);  // byte c / 32 of the word
-    uint4* d = reinterpret_cast<uint4*>(qrow + c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint16_t lo = mx_cvt_e4m3x2(act(4 * i) * inv, act(4 * i + 1) * inv);
+      const uint16_t hi = mx_cvt_e4m3x2(act(4 * i + 2) * inv, act(4 * i + 3) * inv);
+      q[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    scales |= (uint32_t)(X + 127) << (8 * c);
+    uint4* d = reinterpret_cast<uint4*>(qrow + c * 32);
     d[0] = make_uint4(q[0], q[1], q[2], q[3]);
     d[1] = make_uint4(q[4], q[5], q[6], q[7]);
   }
   *sword = scales;
+}
+
+// MXFP8 scatter (single-buffered accumulator): the whole row is read as
+// packed bf16 first (columns 0..63 parked in the staging buffer), the
+// accumulator handed back, then the row stored.
+template <int BN, typename Release>
+__device__ void epi_scatter_mx_n(const GemmParams& p, const Item& it, uint32_t tbase, int row, int lane,
+                                 uint8_t* stage, Release&& release) {
+  constexpr int bn = BN;
+  const int prow = it.row0 + row;
+  const int f = p.pad_perm[prow];
+  uint32_t w[3][32];
+  {
+    uint32_t w0[32];
+    acc_load64_bf16(tbase, w0);
+    park64(stage, lane, w0);
+  }
+#pragma unroll
+  for (int g = 1; g < 4; ++g) {
+    if (g * 64 < bn) {
+      acc_load32_bf16(tbase + 64 * g, &w[g - 1][0]);
+      acc_load32_bf16(tbase + 64 * g + 32, &w[g - 1][16]);
+    }
+  }
+  release();
+  if (f < 0) return;
+  __nv_bfloat16* dst = p.yk + (long)f * p.H + it.n * bn;
+  uint4* d0 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d0[i] = unpark16(stage, lane, i);
+#pragma unroll
+  for (int g = 1; g < 4; ++g) {
+    if (g * 64 < bn) {
+      uint4* d = reinterpret_cast<uint4*>(dst + 64 * g);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        d[i] = make_uint4(w[g - 1][4 * i], w[g - 1][4 * i + 1], w[g - 1][4 * i + 2], w[g - 1][4 * i + 3]);
+    }
+  }
+}
+
+template <typename Release>
+__device__ void epi_scatter_mx(const GemmParams& p, const Item& it, uint32_t tbase, int row, int bn, int lane,
+                               uint8_t* stage, Release&& release) {
+  if (bn == 256)
+    epi_scatter_mx_n<256>(p, it, tbase, row, lane, stage, release);
+  else
+    epi_scatter_mx_n<128>(p, it, tbase, row, lane, stage, release);
 }
 
 // Scatter a tile row to token order: row f of dst (skipped for padding rows;
@@ -882,22 +1017,6 @@ __device__ __forceinline__ __nv_bfloat16* wgrad_base(const GemmParams& p, const 
   return p.dW2 + ((long)it.e * p.I + r0) * p.H + col;
 }
 
-// 64 accumulator columns of this lane's row (two 32-column TMEM loads) as
-// 32 packed bf16 pairs.
-__device__ __forceinline__ void wgrad_load64(uint32_t taddr, uint32_t (&w)[32]) {
-  uint32_t ra[32], rb[32];
-  tmem_ld32_issue(taddr, ra);
-  tmem_ld32_issue(taddr + 32, rb);
-  tmem_wait_ld();
-  tmem_regs_ready(ra);
-  tmem_regs_ready(rb);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    w[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
-    w[16 + i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
-  }
-}
-
 // 64 columns at a time: two TMEM loads, one wait, then the coalesced store.
 // With EARLY the whole accumulator row is read first (the first 64 columns
 // into the staging buffer, the rest in registers as packed bf16), then
@@ -916,7 +1035,7 @@ __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it,
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
       uint32_t w[32];
-      wgrad_load64(tbase + 64 * g, w);
+      acc_load64_bf16(tbase + 64 * g, w);
       long ld;
       __nv_bfloat16* base = wgrad_base(p, it, r0, col0 + 64 * g, ld);
       store_chunk64_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
@@ -925,12 +1044,12 @@ __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it,
   }
   {
     uint32_t w0[32];
-    wgrad_load64(tbase, w0);
+    acc_load64_bf16(tbase, w0);
     stage_chunk64(stage, lane, w0);
   }
   uint32_t w[kGroups - 1][32];
 #pragma unroll
-  for (int g = 1; g < kGroups; ++g) wgrad_load64(tbase + 64 * g, w[g - 1]);
+  for (int g = 1; g < kGroups; ++g) acc_load64_bf16(tbase + 64 * g, w[g - 1]);
   release();
   long ld;
   __nv_bfloat16* base = wgrad_base(p, it, r0, col0, ld);
@@ -1800,11 +1919,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         case -1: break;
         case GM_DENSE: epi_dense(p, it, tbase, row); break;
         case GM_FWD1:
-          if constexpr (MX) epi_fwd1_mx(p, it, tbase, row); else epi_fwd1(p, it, tbase, row);
+          if constexpr (MX) epi_fwd1_mx(p, it, tbase, row, lane, stage_out, release_acc);
+          else epi_fwd1(p, it, tbase, row);
           break;
-        case GM_FWD2: epi_scatter(p, it, tbase, row, p.bn); break;
+        case GM_FWD2:
+        case GM_BWD_DX:
+          if constexpr (MX) epi_scatter_mx(p, it, tbase, row, p.bn, lane, stage_out, release_acc);
+          else epi_scatter(p, it, tbase, row, p.bn);
+          break;
         case GM_BWD_DA: epi_bwd_da<MX>(p, it, tbase, row); break;
-        case GM_BWD_DX: epi_scatter(p, it, tbase, row, p.bn); break;
         default: epi_wgrad<MX && MODE == GM_WG13>(p, it, tbase, q, lane, stage_out, release_acc); break;
       }
       release_acc();
