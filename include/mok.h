@@ -112,6 +112,9 @@ typedef struct {
  *                 the experts average at least 1,024 routed rows
  *                 (T*k >= 1024*E): below that, an expert's odd last tile
  *                 leaves too many CTAs of a pair idle.
+ *                 Bit 6 (MOK_DEBUG_SORTED_X_RING): the single-CTA BF16 ring
+ *                 reads a token-sorted copy of x with plain TMA instead of
+ *                 gathering token rows.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
@@ -137,6 +140,7 @@ typedef struct {
 #define MOK_DEBUG_SINGLE_CTA_WGRAD 8
 #define MOK_DEBUG_SINGLE_CTA_ROWS 16
 #define MOK_DEBUG_SINGLE_CTA_RING 32
+#define MOK_DEBUG_SORTED_X_RING 64
 #define MOK_DEBUG_PAIR_RING 128
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */

@@ -697,6 +697,21 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       else
         (void)cudaGetLastError();  // no cluster of two fits: single CTAs below
     }
+    if (!launched && (cfg->debug_flags & MOK_DEBUG_SORTED_X_RING)) {
+      // single CTAs reading the token-sorted copy of x with plain TMA
+      __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
+      {
+        Phase ph(MOK_PHASE_FWD_SORT, st, 1);
+        MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
+      }
+      TmapSet sm = maps;
+      if (!map2d(&sm.m[0], srt, s.H, (uint64_t)L.pad_capacity, 128)) return MOK_ERR_CUDA;
+      GemmParams gs = g;
+      gs.fwd_sorted = 1;
+      Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
+      MOK_CUDA(launch_gemm(GM_FWD_RING, sm, gs, grid, st));
+      launched = true;
+    }
     if (!launched) {
       Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
       MOK_CUDA(launch_gemm(GM_FWD_RING, maps, g, grid, st));

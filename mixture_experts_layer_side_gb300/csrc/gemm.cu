@@ -351,6 +351,8 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
       tma_load_2d(b, &mp.m[1], bar, kk * 64, it.n * p.bn);
     }
   } else if (type == GM_FWD1) {
+    // A: the token-sorted copy of x, when GEMM1 does not gather
+    if (p.fwd_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 64, it.row0);
     // B: W1 and W3 column blocks (N-major); 128 h columns then 128 u columns
     for (int c = 0; c < 2; ++c) tma_load_3d(b + c * 8192, &mp.m[1], bar, it.n * 128 + c * 64, kk * 64, it.e);
     for (int c = 0; c < 2; ++c) tma_load_3d(b + (2 + c) * 8192, &mp.m[2], bar, it.n * 128 + c * 64, kk * 64, it.e);
@@ -1504,7 +1506,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
   const bool gather_in_pipe = kGather && !PAIR && !(MODE == GM_DENSE && MX) && !(kWgrad && (MX || p.wg_sorted)) &&
-                              !(MODE == GM_BWD_DA && !MX && p.rows_sorted);
+                              !(MODE == GM_BWD_DA && !MX && p.rows_sorted) &&
+                              !(MODE == GM_FWD_RING && !MX && p.fwd_sorted);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)

@@ -153,15 +153,17 @@ def test_backward_row_gemm_cta_pairs_match_single_cta(shape, routing, kw):
 ])
 def test_forward_ring_cta_pairs_match_single_cta(shape, routing, kw):
     """The forward ring on clusters of two CTAs (token-sorted x by plain TMA,
-    two tiles of one expert and one minibatch per cta_group::2 MMA) against
-    one CTA per tile gathering x in its load path: bitwise equal outputs,
-    and the backward from each forward's context bitwise equal too."""
+    two tiles of one expert and one minibatch per cta_group::2 MMA) and on
+    single CTAs reading the sorted copy by TMA, against one CTA per tile
+    gathering x in its load path: bitwise equal outputs, and the backward
+    from each forward's context bitwise equal too."""
     require_gpu()
     _, out_p, g_p = run_layer(shape, routing, 15, debug_flags=128, **kw)
     _, out_s, g_s = run_layer(shape, routing, 15, debug_flags=32, **kw)
-    assert torch.equal(out_p, out_s)
+    _, out_t, g_t = run_layer(shape, routing, 15, debug_flags=32 | 64, **kw)
+    assert torch.equal(out_p, out_s) and torch.equal(out_t, out_s)
     for k in g_p:
-        assert torch.equal(g_p[k], g_s[k]), k
+        assert torch.equal(g_p[k], g_s[k]) and torch.equal(g_t[k], g_s[k]), k
 
 
 def _run_with_idx(shape, idx, seed):
