@@ -105,16 +105,16 @@ typedef struct {
  *                 clusters of two CTAs sharing two tiles of one expert.
  *                 Bits 5 and 7 (MOK_DEBUG_SINGLE_CTA_RING,
  *                 MOK_DEBUG_PAIR_RING): the BF16 forward ring runs one CTA
- *                 per 128-row tile, gathering token rows of x in its load
- *                 path (bit 5), or clusters of two CTAs sharing two tiles of
- *                 one expert and one minibatch, reading a token-sorted copy
- *                 of x (bit 7).  By default it takes clusters of two when
+ *                 per 128-row tile (bit 5), or clusters of two CTAs sharing
+ *                 two tiles of one expert and one minibatch (bit 7); both
+ *                 read a token-sorted copy of x with plain TMA.  By default it takes clusters of two when
  *                 the experts average at least 1,024 routed rows
  *                 (T*k >= 1024*E): below that, an expert's odd last tile
  *                 leaves too many CTAs of a pair idle.
- *                 Bit 6 (MOK_DEBUG_SORTED_X_RING): the single-CTA BF16 ring
- *                 reads a token-sorted copy of x with plain TMA instead of
- *                 gathering token rows.
+ *                 Bit 6 (MOK_DEBUG_GATHER_X_RING): the single-CTA BF16 ring
+ *                 gathers token rows of x in its load path instead of
+ *                 reading the token-sorted copy of x (which the backward's
+ *                 dW1|dW3 then sorts itself) with plain TMA.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
@@ -140,7 +140,7 @@ typedef struct {
 #define MOK_DEBUG_SINGLE_CTA_WGRAD 8
 #define MOK_DEBUG_SINGLE_CTA_ROWS 16
 #define MOK_DEBUG_SINGLE_CTA_RING 32
-#define MOK_DEBUG_SORTED_X_RING 64
+#define MOK_DEBUG_GATHER_X_RING 64
 #define MOK_DEBUG_PAIR_RING 128
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */

@@ -24,7 +24,7 @@ MOK_DEBUG_FUSED_WGRAD_GATHER = 4
 MOK_DEBUG_SINGLE_CTA_WGRAD = 8
 MOK_DEBUG_SINGLE_CTA_ROWS = 16
 MOK_DEBUG_SINGLE_CTA_RING = 32
-MOK_DEBUG_SORTED_X_RING = 64
+MOK_DEBUG_GATHER_X_RING = 64
 MOK_DEBUG_PAIR_RING = 128
 
 STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "MOK_ERR_WORKSPACE_TOO_SMALL",

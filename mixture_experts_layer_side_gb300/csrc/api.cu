@@ -113,6 +113,7 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   L.as = take(P * I * 2);
   L.dsp = take(P * (I / 128) * 4);
   L.sorted = take(P * H * 2);
+  L.sorted2 = prec == MOK_BF16 ? take(P * H * 2) : 0;
   L.pair_m0 = take(L.tile_capacity * 4);
   L.pair_mb = take((L.tile_capacity + 2) * 4);
   if (prec == MOK_MXFP8) {
@@ -584,6 +585,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   const int M = L.minibatch_rows, S = L.ring_slots;
   const int bn2 = (s.H % 256 == 0) ? 256 : 128;
   if (prec == MOK_MXFP8) {
+    MOK_CUDA(cudaMemsetAsync(reinterpret_cast<int32_t*>(w + L.header) + kHdrSortedX, 0, 4, st));
     if (!mx_ok(W1) || !mx_ok(W3) || !mx_ok(W2)) return MOK_ERR_INVALID_ARG;
     const mok_mx &q1 = *as_mx(W1), &q3 = *as_mx(W3), &q2 = *as_mx(W2);
     {
@@ -638,6 +640,9 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   }
   GemmParams g;
   base_params(g, s, L, w);
+  // set again below once the token-sorted copy of x is made
+  int32_t* sorted_x_flag = reinterpret_cast<int32_t*>(w + L.header) + kHdrSortedX;
+  MOK_CUDA(cudaMemsetAsync(sorted_x_flag, 0, 4, st));
   g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
   g.ctx_ring = cfg->replay;  // bounded context: [h|u] rows in ring-slot order
   g.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);
@@ -680,6 +685,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       {
         Phase ph(MOK_PHASE_FWD_SORT, st, 2);
         MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
+        MOK_CUDA(cudaMemsetAsync(sorted_x_flag, 1, 1, st));
         MOK_CUDA(launch_ring_pair_table(L, w, st));
       }
       TmapSet pm = maps;
@@ -697,12 +703,14 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       else
         (void)cudaGetLastError();  // no cluster of two fits: single CTAs below
     }
-    if (!launched && (cfg->debug_flags & MOK_DEBUG_SORTED_X_RING)) {
-      // single CTAs reading the token-sorted copy of x with plain TMA
+    if (!launched && !(cfg->debug_flags & MOK_DEBUG_GATHER_X_RING)) {
+      // single CTAs reading the token-sorted copy of x with plain TMA (the
+      // backward's dW1|dW3 reads the same copy)
       __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
       {
         Phase ph(MOK_PHASE_FWD_SORT, st, 1);
         MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
+        MOK_CUDA(cudaMemsetAsync(sorted_x_flag, 1, 1, st));
       }
       TmapSet sm = maps;
       if (!map2d(&sm.m[0], srt, s.H, (uint64_t)L.pad_capacity, 128)) return MOK_ERR_CUDA;
@@ -878,7 +886,8 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   // feed dA' and dW2 (dout), then dW1|dW3 (x), through one buffer; with
   // MOK_DEBUG_FUSED_WGRAD_GATHER those GEMMs gather rows in their load path.
   const bool sorted = (cfg->debug_flags & MOK_DEBUG_FUSED_WGRAD_GATHER) == 0;
-  __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
+  __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted2);    // dout
+  __nv_bfloat16* srt_x = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);   // x
   // dA' and dX on CTA pairs: two tiles of one expert per cluster, each CTA
   // loading a 128-row half of the 256-row weight tile.  dA' only for long K
   // (H): with short main loops it is bound by its SwiGLU-backward epilogue,
@@ -961,15 +970,17 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     MOK_CUDA(launch_wgrad(GM_WG2, m, q, gemm_grid((long)s.E * q.m_tiles * q.n_tiles), cfg->debug_flags, 5, &n, st));
     g_launches += n;
   }
-  // dW1 | dW3 = sorted(x)^T [dh|du], per expert (x overwrites the sorted dout)
+  // dW1 | dW3 = sorted(x)^T [dh|du], per expert; the sort of x does
+  // nothing when the forward left its sorted copy in place
   {
     TmapSet m;
     memset(&m, 0, sizeof(m));
     if (sorted) {
       Phase ph(MOK_PHASE_BWD_SORT, st, 1);
-      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
+      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt_x, st,
+                                  reinterpret_cast<const int32_t*>(w + L.header) + kHdrSortedX));
     }
-    if (sorted ? !map2d(&m.m[0], srt, s.H, P, 64) : !map_gather(&m.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
+    if (sorted ? !map2d(&m.m[0], srt_x, s.H, P, 64) : !map_gather(&m.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
     if (!map2d(&m.m[1], g.dhu, 2 * (uint64_t)s.I, P, 64)) return MOK_ERR_CUDA;
     GemmParams q = g;
     q.nmaps = 2;

@@ -92,7 +92,9 @@ __global__ void ds_reduce_kernel(int R, int nparts, const int32_t* __restrict__ 
 __global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, const int32_t* __restrict__ hdr,
                                                           const int32_t* __restrict__ pad_perm,
                                                           const __nv_bfloat16* __restrict__ x,
-                                                          __nv_bfloat16* __restrict__ xg) {
+                                                          __nv_bfloat16* __restrict__ xg,
+                                                          const int32_t* __restrict__ skip) {
+  if (skip && *skip) return;  // the copy is already there
   const int rows = hdr[kHdrPaddedRows];
   const int hv = H / 8;
   const long n = (long)rows * hv;
@@ -173,11 +175,11 @@ cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_
 }
 
 cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
-                               __nv_bfloat16* xg, cudaStream_t st) {
+                               __nv_bfloat16* xg, cudaStream_t st, const int32_t* skip) {
   const long items = L.pad_capacity * (s.H / 8);
   gather_rows_kernel<<<grid_for(items, 256), 256, 0, st>>>(
       s.T, s.H, s.k, reinterpret_cast<const int32_t*>(ws + L.header),
-      reinterpret_cast<const int32_t*>(ws + L.pad_perm), x, xg);
+      reinterpret_cast<const int32_t*>(ws + L.pad_perm), x, xg, skip);
   return cudaGetLastError();
 }
 

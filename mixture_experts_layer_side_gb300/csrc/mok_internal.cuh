@@ -31,6 +31,10 @@ constexpr int kHdrScanDone = 6;
 constexpr int kHdrPlaceDone = 7;
 constexpr int kHdrG2Done = 8;
 constexpr int kHdrCombineNext = 9;  // next token of the single-launch forward's combine
+// nonzero while the sorted buffer holds the token-sorted x of the last
+// BF16 forward on this schedule (its backward then skips sorting x again);
+// cleared by every schedule build and by forwards that do not sort x
+constexpr int kHdrSortedX = 10;
 constexpr int kHdrCounters = 16;    // [16, 48): per-launch dynamic tile counters
 constexpr int kNumCounters = 32;
 
@@ -47,7 +51,9 @@ struct WsLayout {
   size_t dhu;         // bf16 [pad_capacity, 2I]
   size_t as;          // bf16 [pad_capacity, I]  s * a
   size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
-  size_t sorted;      // bf16 [pad_capacity, H]: token-sorted dout (dA', dW2), then x (dW1|dW3)
+  size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x (the forward ring reads it; then dW1|dW3),
+                      // in MXFP8 also dout (dW2)
+  size_t sorted2;     // bf16 [pad_capacity, H]: BF16 token-sorted dout (dA', dW2)
   size_t pair_m0;     // int32 [tile_capacity]: CTA-pair tiles of dA' / dX / the ring (first M tile * 2 + solo)
   size_t pair_mb;     // int32 [tile_capacity + 2]: forward ring, first pair of each minibatch
   // MXFP8 operand copies
@@ -81,8 +87,9 @@ cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t*
                            const float* scores, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_t* ws, float* ds, int n_parts,
                              cudaStream_t st);
+// skip (device, optional): the launch does nothing while *skip != 0
 cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
-                               __nv_bfloat16* xg, cudaStream_t st);
+                               __nv_bfloat16* xg, cudaStream_t st, const int32_t* skip = nullptr);
 cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st);
 cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_count, uint8_t* out,
                                     cudaStream_t st);

@@ -153,10 +153,11 @@ def test_backward_row_gemm_cta_pairs_match_single_cta(shape, routing, kw):
 ])
 def test_forward_ring_cta_pairs_match_single_cta(shape, routing, kw):
     """The forward ring on clusters of two CTAs (token-sorted x by plain TMA,
-    two tiles of one expert and one minibatch per cta_group::2 MMA) and on
-    single CTAs reading the sorted copy by TMA, against one CTA per tile
-    gathering x in its load path: bitwise equal outputs, and the backward
-    from each forward's context bitwise equal too."""
+    two tiles of one expert and one minibatch per cta_group::2 MMA), on
+    single CTAs reading the sorted copy by TMA (whose backward reuses that
+    copy for dW1|dW3), and on single CTAs gathering x in their load path:
+    bitwise equal outputs, and the backward from each forward bitwise equal
+    too."""
     require_gpu()
     _, out_p, g_p = run_layer(shape, routing, 15, debug_flags=128, **kw)
     _, out_s, g_s = run_layer(shape, routing, 15, debug_flags=32, **kw)
