@@ -96,7 +96,8 @@ typedef struct {
  *                 Bit 2 (MOK_DEBUG_FUSED_WGRAD_GATHER): the BF16 backward's
  *                 dA' and weight-gradient GEMMs gather token rows in their
  *                 load path instead of reading token-sorted copies (dA' then
- *                 runs one CTA per tile).
+ *                 runs one CTA per tile); the MXFP8 dA' gathers dout's E4M3
+ *                 rows instead of reading their token-sorted copy.
  *                 Bit 3 (MOK_DEBUG_SINGLE_CTA_WGRAD): the BF16 weight-gradient
  *                 GEMMs run one CTA per 128-row tile instead of clusters of
  *                 two CTAs sharing a 256-row tile (cta_group::2).
@@ -111,10 +112,11 @@ typedef struct {
  *                 the experts average at least 1,024 routed rows
  *                 (T*k >= 1024*E): below that, an expert's odd last tile
  *                 leaves too many CTAs of a pair idle.
- *                 Bit 6 (MOK_DEBUG_GATHER_X_RING): the single-CTA BF16 ring
- *                 gathers token rows of x in its load path instead of
- *                 reading the token-sorted copy of x (which the backward's
- *                 dW1|dW3 then sorts itself) with plain TMA.
+ *                 Bit 6 (MOK_DEBUG_GATHER_X_RING): the single-CTA ring
+ *                 gathers token rows of x (MXFP8: of x's E4M3 codes) in its
+ *                 load path instead of reading a token-sorted copy with
+ *                 plain TMA (in BF16 the backward's dW1|dW3 then sorts x
+ *                 itself).
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it

@@ -120,6 +120,7 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
     L.ring_sf = take((size_t)L.ring_slots * M * (I / 32));
     L.xq = take((size_t)s.T * H);
     L.xsf = take((size_t)s.T * (H / 32));
+    L.xq_sorted = take(P * H);
     L.wsf1 = take((size_t)s.E * H * I / 32);
     L.wsf3 = take((size_t)s.E * H * I / 32);
     L.wsf2 = take((size_t)s.E * I * H / 32);
@@ -361,7 +362,10 @@ mok_status reset_counters(uint8_t* ws, const WsLayout& L, cudaStream_t st) {
 // weight-gradient operands along the expert's routed rows.
 mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const void* ctx, const void* x,
                        const float* scores, const mok_mx& q1, const mok_mx& q3, const mok_mx& q2, const void* dout,
-                       void* dX, void* dW1, void* dW3, void* dW2, float* dscores, cudaStream_t st) {
+                       void* dX, void* dW1, void* dW3, void* dW2, float* dscores, int debug_flags, cudaStream_t st) {
+  // dA' reads dout's codes in padded-row order by plain TMA, unless asked to
+  // gather them in its load path
+  const bool sorted_codes = !(debug_flags & MOK_DEBUG_FUSED_WGRAD_GATHER);
   const uint64_t P = L.pad_capacity;
   const int bn_i = (s.I % 256 == 0) ? 256 : 128;
   const int bn_h = (s.H % 256 == 0) ? 256 : 128;
@@ -383,11 +387,15 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     TmapSet m;
     memset(&m, 0, sizeof(m));
     if (!map3d_u8(&m.m[1], q2.q, s.H, s.I, s.E, bn_i)) return MOK_ERR_CUDA;
+    if (!(sorted_codes ? map2d_u8(&m.m[0], w + L.xq_sorted, s.H, P, 128, 128)
+                       : map2d_u8(&m.m[0], w + L.xq, s.H, s.T, 128, 128)))
+      return MOK_ERR_CUDA;
     GemmParams q = g;
     q.nmaps = 2;
     q.bn = bn_i;
     q.n_tiles = s.I / bn_i;
     q.m_tiles = 0;
+    q.rows_sorted = sorted_codes ? 1 : 0;
     q.m_tile_begin = 0;
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 0;
@@ -396,10 +404,11 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     // region the forward uses for its own W2 scales), tiled for the TMA
     // producer
     {
-      Phase ph(MOK_PHASE_QUANT, st, 2);
+      Phase ph(MOK_PHASE_QUANT, st, sorted_codes ? 3 : 2);
       MOK_CUDA(launch_tile_row_scales(w + L.xsf, s.H / 32, reinterpret_cast<const int32_t*>(w + L.pad_perm), s.k,
                                       rows_used, L.pad_capacity, w + L.sfa_rows_t, st));
       MOK_CUDA(launch_tile_scales_rows(q2.scale, s.E, s.I, s.H / 32, w + L.wsf2, st));
+      if (sorted_codes) MOK_CUDA(launch_gather_code_rows(s, L, w, w + L.xq, w + L.xq_sorted, st));
     }
     q.sfa_tiled = w + L.sfa_rows_t;
     q.sfb_tiled0 = w + L.wsf2;
@@ -596,12 +605,15 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       MOK_CUDA(launch_tile_scales(q3.scale, s.E, s.H / 32, s.I, w + L.wsf3, st));
       MOK_CUDA(launch_tile_scales(q2.scale, s.E, s.I / 32, s.H, w + L.wsf2, st));
     }
+    const bool sorted_codes = !(cfg->debug_flags & MOK_DEBUG_GATHER_X_RING);
     {
-      // x's scales in padded-row order, tiled for the TMA producer (GEMM1 A)
-      Phase ph(MOK_PHASE_QUANT, st, 1);
+      // x's scales in padded-row order, tiled for the TMA producer (GEMM1 A),
+      // and x's codes in padded-row order (GEMM1's A by plain TMA)
+      Phase ph(MOK_PHASE_QUANT, st, sorted_codes ? 2 : 1);
       MOK_CUDA(launch_tile_row_scales(w + L.xsf, s.H / 32, reinterpret_cast<const int32_t*>(w + L.pad_perm), s.k,
                                       reinterpret_cast<const int32_t*>(w + L.header) + kHdrPaddedRows,
                                       L.pad_capacity, w + L.sfa_rows_t, st));
+      if (sorted_codes) MOK_CUDA(launch_gather_code_rows(s, L, w, w + L.xq, w + L.xq_sorted, st));
     }
     GemmParams g;
     base_params(g, s, L, w);
@@ -624,6 +636,12 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
         !map2d_u8(&maps.m[3], w + L.ring, s.I, (uint64_t)S * M, 128, 128) ||
         !map3d_u8(&maps.m[4], q2.q, s.H, s.I, s.E, 128))
       return MOK_ERR_CUDA;
+    if (sorted_codes) {
+      if (!map2d_u8(&maps.m[0], w + L.xq_sorted, s.H, (uint64_t)L.pad_capacity, 128, 128)) return MOK_ERR_CUDA;
+      g.fwd_sorted = 1;
+    } else if (!map2d_u8(&maps.m[0], w + L.xq, s.H, s.T, 128, 128)) {  // a valid map for the prefetch
+      return MOK_ERR_CUDA;
+    }
     g.nmaps = 5;
     g.bn = bn2;
     g.n_tiles = s.H / bn2;
@@ -842,7 +860,7 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   if (prec == MOK_MXFP8) {
     if (!mx_ok(W1) || !mx_ok(W3) || !mx_ok(W2)) return MOK_ERR_INVALID_ARG;
     return backward_mx(s, L, w, ctx, x, scores, *as_mx(W1), *as_mx(W3), *as_mx(W2), dout, dX, dW1, dW3, dW2,
-                       dscores, st);
+                       dscores, cfg->debug_flags, st);
   }
   GemmParams g;
   base_params(g, s, L, w);

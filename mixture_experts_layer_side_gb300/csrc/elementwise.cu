@@ -108,6 +108,25 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int T, int H, int k, c
   }
 }
 
+// Token-sorted copy of E4M3 code rows (MXFP8 x or dout quantised along H):
+// dst[padded row] = codes[token] (zeros for padding rows), 16 bytes a thread.
+__global__ void __launch_bounds__(256) gather_code_rows_kernel(int H, int k, const int32_t* __restrict__ hdr,
+                                                               const int32_t* __restrict__ pad_perm,
+                                                               const uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ dst) {
+  const int rows = hdr[kHdrPaddedRows];
+  const int hv = H / 16;
+  const long n = (long)rows * hv;
+  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const int p = (int)(i / hv);
+    const int c = (int)(i - (long)p * hv);
+    const int f = pad_perm[p];
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (f >= 0) v = __ldg(reinterpret_cast<const uint4*>(codes + (long)(f / k) * H) + c);
+    __stcs(reinterpret_cast<uint4*>(dst + (long)p * H) + c, v);
+  }
+}
+
 // Bounded-memory backward: the [h|u] rows of the last `slots` minibatches,
 // kept by the forward in ring-slot order, copied to their routed-row places
 // in dh|du (the dA' epilogue then reads and overwrites them in place).
@@ -180,6 +199,15 @@ cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint
   gather_rows_kernel<<<grid_for(items, 256), 256, 0, st>>>(
       s.T, s.H, s.k, reinterpret_cast<const int32_t*>(ws + L.header),
       reinterpret_cast<const int32_t*>(ws + L.pad_perm), x, xg, skip);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_code_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const uint8_t* codes,
+                                    uint8_t* dst, cudaStream_t st) {
+  const long items = L.pad_capacity * (s.H / 16);
+  gather_code_rows_kernel<<<grid_for(items, 256), 256, 0, st>>>(
+      s.H, s.k, reinterpret_cast<const int32_t*>(ws + L.header), reinterpret_cast<const int32_t*>(ws + L.pad_perm),
+      codes, dst);
   return cudaGetLastError();
 }
 

@@ -495,9 +495,9 @@ __device__ __forceinline__ uint32_t mx_stage_bytes(const GemmParams& p, int type
   const uint32_t bchunks = (uint32_t)bn / 128;
   switch (MODE == GM_DENSE ? GM_DENSE : type) {
     case GM_DENSE: return kAStage + bn * 128 + 512u + 512u * bchunks;
-    case GM_FWD1: return 2u * 16384u + 1024u + 512u;
+    case GM_FWD1: return 2u * 16384u + 1024u + 512u + (p.fwd_sorted ? (uint32_t)kAStage : 0u);
     case GM_FWD2: return kAStage + bn * 128 + 512u + 512u * bchunks;
-    case GM_BWD_DA: return bn * 128 + 512u * bchunks + 512u;
+    case GM_BWD_DA: return bn * 128 + 512u * bchunks + 512u + (p.rows_sorted ? (uint32_t)kAStage : 0u);
     case GM_BWD_DX: return kAStage + bn * 128 + 512u * bchunks + 512u;
     case GM_WG13: return kAStage + 2u * 16384u + 512u + 1024u;
     default: return kAStage + bn * 128 + 512u + 512u * bchunks;  // GM_WG2
@@ -526,6 +526,8 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
       bulk_load(sfb + c * 512, p.sfb_tiled0 + ((long)(it.n * (bn / 128) + c) * kgroups + kk) * 512, 512, bar);
   } else if (type == GM_FWD1) {
     const int hg = p.H / 128;
+    // A: x's codes in padded-row order, when GEMM1 does not gather them
+    if (p.fwd_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
     tma_load_3d(b, &mp.m[1], bar, it.n * 128, kk * 128, it.e);
     tma_load_3d(b + 16384, &mp.m[2], bar, it.n * 128, kk * 128, it.e);
     const long blk = ((long)it.e * (p.I / 128) + it.n) * hg + kk;
@@ -545,8 +547,10 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
       bulk_load(sfb + c * 512, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * 512, 512, bar);
     }
   } else if (type == GM_BWD_DA) {
-    // B = W2 along H (K-major); its scales, and those of the gathered
-    // dout rows, pre-tiled per 128 rows x 128 K
+    // A: dout's codes in padded-row order, when dA' does not gather them;
+    // B = W2 along H (K-major); its scales, and those of the dout rows,
+    // pre-tiled per 128 rows x 128 K
+    if (p.rows_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
     tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
     bulk_load(sfa, p.sfa_tiled + ((long)it.m * (p.H / 128) + kk) * 512, 512, bar);
     for (int c = 0; c < bn / 128; ++c) {
@@ -1506,8 +1510,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
   const bool gather_in_pipe = kGather && !PAIR && !(MODE == GM_DENSE && MX) && !(kWgrad && (MX || p.wg_sorted)) &&
-                              !(MODE == GM_BWD_DA && !MX && p.rows_sorted) &&
-                              !(MODE == GM_FWD_RING && !MX && p.fwd_sorted);
+                              !(MODE == GM_BWD_DA && p.rows_sorted) && !(MODE == GM_FWD_RING && p.fwd_sorted);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)

@@ -58,6 +58,7 @@ struct WsLayout {
   size_t pair_mb;     // int32 [tile_capacity + 2]: forward ring, first pair of each minibatch
   // MXFP8 operand copies
   size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
+  size_t xq_sorted;   // those codes in padded-row order (GEMM1 / dA' A operand): u8 [pad_capacity, H]
   size_t sfa_rows_t;  // the A operand's scales in padded-row order, tiled: [pad/128][max(H,2I)/128][512]
   size_t wsf1, wsf3, wsf2;  // forward weight scales tiled for the GEMMs
   size_t dhuq, dhusf; // dh|du quantised along I: u8 [pad, 2I], [pad, 2I/32]
@@ -87,6 +88,9 @@ cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t*
                            const float* scores, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_t* ws, float* ds, int n_parts,
                              cudaStream_t st);
+// MXFP8: token-sorted copy of E4M3 code rows [T, H] -> [pad_capacity, H]
+cudaError_t launch_gather_code_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const uint8_t* codes,
+                                    uint8_t* dst, cudaStream_t st);
 // skip (device, optional): the launch does nothing while *skip != 0
 cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
                                __nv_bfloat16* xg, cudaStream_t st, const int32_t* skip = nullptr);

@@ -122,6 +122,19 @@ def test_mxfp8_layer_matches_quantised_oracle(name, shape, routing, seed):
             assert torch.count_nonzero(grads[k][e]).item() == 0
 
 
+@pytest.mark.parametrize("shape,routing", [((512, 256, 256, 24, 4), "hot"), ((1000, 512, 256, 6, 3), "zipf")])
+def test_mxfp8_sorted_and_gathered_code_rows_are_bitwise_equal(shape, routing):
+    """GEMM1 and dA' reading x's / dout's E4M3 rows from token-sorted copies
+    by plain TMA (default) against gathering them in the load path
+    (MOK_DEBUG_GATHER_X_RING | MOK_DEBUG_FUSED_WGRAD_GATHER)."""
+    require_gpu()
+    _, out_s, g_s = run_mx(shape, routing, 7)
+    _, out_g, g_g = run_mx(shape, routing, 7, debug_flags=64 | 4)
+    assert torch.equal(out_s, out_g)
+    for k in g_s:
+        assert torch.equal(g_s[k], g_g[k]), k
+
+
 def test_mxfp8_reruns_are_bitwise_identical():
     require_gpu()
     shape, routing = (512, 256, 256, 24, 4), "hot"
