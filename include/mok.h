@@ -119,13 +119,17 @@ typedef struct {
  *                 itself).
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
- *                 1 (BF16 only; MXFP8 calls return MOK_ERR_UNSUPPORTED): it
- *                 holds [h|u] of the last ring_slots minibatches only, in
- *                 ring-slot order (mok_ctx_size shrinks to ring_slots *
- *                 minibatch_rows rows), and the backward recomputes GEMM1
- *                 for the earlier minibatches -- the pages' bounded-memory
- *                 backward ([MTP] ring-token-buffer paragraph; [NOTE] §3).
- *                 Recomputed values are bitwise those of the forward.
+ *                 1: it holds [h|u] of the last ring_slots minibatches
+ *                 only, in ring-slot order (mok_ctx_size shrinks to
+ *                 ring_slots * minibatch_rows rows), and the backward
+ *                 recomputes GEMM1 for the earlier minibatches -- the pages'
+ *                 bounded-memory backward ([MTP] ring-token-buffer
+ *                 paragraph; [NOTE] §3).  Recomputed values are bitwise
+ *                 those of the forward.  In MXFP8 mode the recomputation
+ *                 needs the forward's weight orientation too: mok_backward's
+ *                 W1 and W3 then each point to TWO consecutive mok_mx, the
+ *                 backward orientation (along I) followed by the forward
+ *                 one (along H).
  */
 typedef struct {
   int32_t minibatch_rows;

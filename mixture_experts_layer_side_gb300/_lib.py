@@ -137,6 +137,8 @@ def _ptr(t):
         return None
     if isinstance(t, MokMx):
         return ctypes.cast(ctypes.pointer(t), ctypes.c_void_p)
+    if isinstance(t, ctypes.Array):  # consecutive mok_mx descriptors
+        return ctypes.cast(t, ctypes.c_void_p)
     return ctypes.c_void_p(t.data_ptr())
 
 

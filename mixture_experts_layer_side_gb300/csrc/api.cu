@@ -360,11 +360,13 @@ mok_status reset_counters(uint8_t* ws, const WsLayout& L, cudaStream_t st) {
 // the orientation the backward contracts over (W1, W3 along I; W2 along H);
 // dout is quantised along H, dh|du along I (in the dA' epilogue), and the
 // weight-gradient operands along the expert's routed rows.
-mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const void* ctx, const void* x,
-                       const float* scores, const mok_mx& q1, const mok_mx& q3, const mok_mx& q2, const void* dout,
-                       void* dX, void* dW1, void* dW3, void* dW2, float* dscores, int debug_flags, cudaStream_t st) {
+mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const mok_config& cfg, const void* ctx,
+                       const void* x, const float* scores, const mok_mx& q1, const mok_mx& q3, const mok_mx& q2,
+                       const mok_mx* f1, const mok_mx* f3, const void* dout, void* dX, void* dW1, void* dW3,
+                       void* dW2, float* dscores, cudaStream_t st) {
   // dA' reads dout's codes in padded-row order by plain TMA, unless asked to
   // gather them in its load path
+  const int debug_flags = cfg.debug_flags;
   const bool sorted_codes = !(debug_flags & MOK_DEBUG_FUSED_WGRAD_GATHER);
   const uint64_t P = L.pad_capacity;
   const int bn_i = (s.I % 256 == 0) ? 256 : 128;
@@ -378,6 +380,52 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
   g.dsp = reinterpret_cast<float*>(w + L.dsp);
   g.scores = scores;
   g.yk = reinterpret_cast<__nv_bfloat16*>(w + L.yk);
+  if (cfg.replay) {
+    // Bounded-memory backward, as in BF16: the context's last ring_slots
+    // minibatches of [h|u] go back to their rows of dh|du, and GEMM1 is
+    // recomputed for the earlier ones straight into those rows -- with the
+    // forward's operands (x quantised along H, W1 / W3 along H) and tiles,
+    // so the values are the forward's bit for bit.
+    const bool srt = !(debug_flags & MOK_DEBUG_GATHER_X_RING);
+    {
+      Phase ph(MOK_PHASE_BWD_REPLAY, st, srt ? 6 : 5);
+      MOK_CUDA(launch_replay_copy(s, L, w, static_cast<const __nv_bfloat16*>(ctx), g.dhu, st));
+      MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(x), 1, s.T, s.H, 1, w + L.xq, w + L.xsf, st));
+      MOK_CUDA(launch_tile_scales(f1->scale, s.E, s.H / 32, s.I, w + L.wsf1, st));
+      MOK_CUDA(launch_tile_scales(f3->scale, s.E, s.H / 32, s.I, w + L.wsf3, st));
+      MOK_CUDA(launch_tile_row_scales(w + L.xsf, s.H / 32, reinterpret_cast<const int32_t*>(w + L.pad_perm), s.k,
+                                      rows_used, L.pad_capacity, w + L.sfa_rows_t, st));
+      if (srt) MOK_CUDA(launch_gather_code_rows(s, L, w, w + L.xq, w + L.xq_sorted, st));
+    }
+    TmapSet m;
+    memset(&m, 0, sizeof(m));
+    if (!(srt ? map2d_u8(&m.m[0], w + L.xq_sorted, s.H, P, 128, 128) : map2d_u8(&m.m[0], w + L.xq, s.H, s.T, 128, 128)) ||
+        !map3d_u8(&m.m[1], f1->q, s.I, s.H, s.E, 128) || !map3d_u8(&m.m[2], f3->q, s.I, s.H, s.E, 128))
+      return MOK_ERR_CUDA;
+    GemmParams q = g;
+    q.ctx_hu = g.dhu;
+    q.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);  // a and its scales: scratch here
+    q.ring_sf = w + L.ring_sf;
+    q.ring_rows = L.minibatch_rows;
+    q.ring_slots = L.ring_slots;
+    q.gq_src = w + L.xq;
+    q.fwd_sorted = srt ? 1 : 0;
+    q.sfa_tiled = w + L.sfa_rows_t;
+    q.sfb_tiled0 = w + L.wsf1;
+    q.sfb_tiled1 = w + L.wsf3;
+    q.nmaps = 3;
+    q.bn = 256;
+    q.n_tiles = s.I / 128;
+    q.m_tile_begin = 0;
+    q.m_tile_end = (int)L.tile_capacity;
+    q.replay_keep = L.ring_slots;
+    q.counter = 6;
+    {
+      Phase ph(MOK_PHASE_BWD_REPLAY, st, 1);
+      MOK_CUDA(launch_gemm_mx(GM_FWD1, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+    }
+    g.ctx_hu = g.dhu;
+  }
   {
     Phase ph(MOK_PHASE_QUANT, st, 1);
     MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(dout), 1, s.T, s.H, 1, w + L.xq, w + L.xsf, st));
@@ -533,7 +581,6 @@ size_t mok_ctx_size(const mok_shape* shape, const mok_config* cfg, mok_precision
   if (prec != MOK_BF16 && prec != MOK_MXFP8) return 0;
   const WsLayout L = ws_layout(*shape, *cfg, prec, device_sm_count());
   if (cfg->replay) {
-    if (prec != MOK_BF16) return 0;
     // ring-slot order: slot rows are below min(ring_slots * minibatch_rows,
     // padded rows)
     const int64_t rows = std::min<int64_t>((int64_t)L.ring_slots * L.minibatch_rows, L.pad_capacity);
@@ -581,7 +628,6 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   MOK_TRY(check_shape(shape));
   MOK_TRY(check_config(cfg));
   MOK_TRY(check_prec(prec));
-  if (cfg->replay && prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (!ws || !x || !scores || !W1 || !W3 || !W2 || !out || !ctx) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   const WsLayout L = ws_layout(s, *cfg, prec, device_sm_count());
@@ -618,6 +664,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     GemmParams g;
     base_params(g, s, L, w);
     g.ctx_hu = static_cast<__nv_bfloat16*>(ctx);
+    g.ctx_ring = cfg->replay;  // bounded context: [h|u] rows in ring-slot order
     g.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring);  // E4M3 codes in MXFP8 mode
     g.ring_sf = w + L.ring_sf;
     g.ring_rows = M;
@@ -844,12 +891,24 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   MOK_TRY(check_shape(shape));
   MOK_TRY(check_config(cfg));
   MOK_TRY(check_prec(prec));
-  if (cfg->replay && prec != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (!ws || !ctx || !x || !scores || !W1 || !W3 || !W2 || !dout || !dX || !dW1 || !dW3 || !dW2 || !dscores)
     return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   const WsLayout L = ws_layout(s, *cfg, prec, device_sm_count());
   if (ws_bytes < L.total) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  // MXFP8 descriptors are checked before anything touches the device; with
+  // replay, W1 and W3 each point to two descriptors: the backward's
+  // orientation (along I) and the forward's (along H, for the replayed GEMM1)
+  const mok_mx* f1 = nullptr;
+  const mok_mx* f3 = nullptr;
+  if (prec == MOK_MXFP8) {
+    if (!mx_ok(W1) || !mx_ok(W3) || !mx_ok(W2)) return MOK_ERR_INVALID_ARG;
+    if (cfg->replay) {
+      f1 = as_mx(W1) + 1;
+      f3 = as_mx(W3) + 1;
+      if (!mx_ok(f1) || !mx_ok(f3)) return MOK_ERR_INVALID_ARG;
+    }
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   MOK_TRY(reset_counters(w, L, st));
@@ -858,9 +917,8 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
   const int bn_h = (s.H % 256 == 0) ? 256 : 128;
 
   if (prec == MOK_MXFP8) {
-    if (!mx_ok(W1) || !mx_ok(W3) || !mx_ok(W2)) return MOK_ERR_INVALID_ARG;
-    return backward_mx(s, L, w, ctx, x, scores, *as_mx(W1), *as_mx(W3), *as_mx(W2), dout, dX, dW1, dW3, dW2,
-                       dscores, cfg->debug_flags, st);
+    return backward_mx(s, L, w, *cfg, ctx, x, scores, *as_mx(W1), *as_mx(W3), *as_mx(W2), f1, f3, dout, dX, dW1,
+                       dW3, dW2, dscores, st);
   }
   GemmParams g;
   base_params(g, s, L, w);

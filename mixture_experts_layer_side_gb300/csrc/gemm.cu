@@ -732,6 +732,7 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
                             Release&& release) {
   const long prow = (long)it.row0 + row;
   const int i0 = it.n * 128;
+  const long crow = p.ctx_ring ? (long)ring_row(p, (int)prow) : prow;
   // h columns 0..63 parked in the staging buffer, the rest in registers
   uint32_t hw1[32], uw[2][32];
   {
@@ -743,7 +744,7 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
   acc_load64_bf16(tbase + 128, uw[0]);
   acc_load64_bf16(tbase + 192, uw[1]);
   release();
-  __nv_bfloat16* hrow = p.ctx_hu + prow * 2 * p.I + i0;
+  __nv_bfloat16* hrow = p.ctx_hu + crow * 2 * p.I + i0;
   __nv_bfloat16* urow = hrow + p.I;
   const long rr = ring_row(p, (int)prow);
   uint8_t* qrow = reinterpret_cast<uint8_t*>(p.ring) + rr * p.I + i0;
@@ -1510,7 +1511,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
   const bool gather_in_pipe = kGather && !PAIR && !(MODE == GM_DENSE && MX) && !(kWgrad && (MX || p.wg_sorted)) &&
-                              !(MODE == GM_BWD_DA && p.rows_sorted) && !(MODE == GM_FWD_RING && p.fwd_sorted);
+                              !(MODE == GM_BWD_DA && p.rows_sorted) &&
+                              !((MODE == GM_FWD_RING || MODE == GM_FWD1) && p.fwd_sorted);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)
@@ -2060,6 +2062,7 @@ cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int 
 cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st) {
   switch (mode) {
     case GM_DENSE: return launch_mode<GM_DENSE, true>(maps, p, grid, st);
+    case GM_FWD1: return launch_mode<GM_FWD1, true>(maps, p, grid, st);
     case GM_BWD_DA: return launch_mode<GM_BWD_DA, true>(maps, p, grid, st);
     case GM_BWD_DX: return launch_mode<GM_BWD_DX, true>(maps, p, grid, st);
     case GM_WG13: return launch_mode<GM_WG13, true>(maps, p, grid, st);

@@ -22,8 +22,11 @@ def quantize_weights(W1, W3, W2, stream=None):
     step), in both orientations: the forward contracts W1/W3 over H and W2
     over I (blocks along the rows of each matrix, block_axis 0), the
     backward contracts W1/W3 over I and W2 over H (block_axis 1).
-    Returns {"fwd": (mx1, mx3, mx2), "bwd": (...)} of descriptors; the
-    code and scale tensors are kept alive on the returned object."""
+    Returns {"fwd": (mx1, mx3, mx2), "bwd": (...), "bwd_replay": (...)} of
+    descriptors; "bwd_replay" is what the bounded-memory backward (replay)
+    takes: W1 and W3 as two descriptors each, the backward orientation then
+    the forward one (its replayed GEMM1 contracts over H).  The code and
+    scale tensors are kept alive on the returned object."""
     out = {"tensors": []}
     for orient, axis in (("fwd", 0), ("bwd", 1)):
         descs = []
@@ -36,6 +39,8 @@ def quantize_weights(W1, W3, W2, stream=None):
             out["tensors"] += [q, sf]
             descs.append(_lib.mx(q, sf))
         out[orient] = tuple(descs)
+    pair = _lib.MokMx * 2
+    out["bwd_replay"] = (pair(out["bwd"][0], out["fwd"][0]), pair(out["bwd"][1], out["fwd"][1]), out["bwd"][2])
     return out
 
 

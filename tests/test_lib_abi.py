@@ -107,7 +107,8 @@ def test_workspace_layout_is_consistent(lib):
 
 def test_bounded_context_size_and_checks(lib):
     """replay = 1: the forward context holds ring_slots minibatches of [h|u]
-    (bf16, 2I columns); MXFP8 calls with it are refused on the host."""
+    (bf16, 2I columns) in both precisions; an MXFP8 backward with it needs
+    W1 and W3 in both orientations and is refused on the host without."""
     L = lib.LIB
     shape = lib.shape_of(4096, 256, 128, 16, 4)
     plain = lib.config(minibatch_rows=128, ring_slots=2)
@@ -118,10 +119,14 @@ def test_bounded_context_size_and_checks(lib):
     # a ring larger than the padded rows: no more than the padded rows
     big = lib.config(minibatch_rows=8192, ring_slots=4, replay=1)
     assert lib.mok_ctx_size(shape, big) == pad * 2 * 128 * 2
-    assert lib.mok_ctx_size(shape, bounded, lib.MOK_MXFP8) == 0
+    assert lib.mok_ctx_size(shape, bounded, lib.MOK_MXFP8) == 2 * 128 * 2 * 128 * 2
     assert lib.mok_ctx_size(shape, lib.config(replay=2)) == 0
     fake = ctypes.c_void_p(256)
     S, C = ctypes.byref(shape), ctypes.byref(bounded)
-    assert L.mok_forward(S, C, lib.MOK_MXFP8, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, None) == 2
-    assert L.mok_backward(S, C, lib.MOK_MXFP8, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, fake,
-                          fake, fake, fake, None) == 2
+    # the second (forward-orientation) descriptor of W1 / W3 missing: refused
+    # before anything is enqueued
+    pair = (lib.MokMx * 2)(lib.MokMx(256, 256), lib.MokMx(0, 0))
+    one = lib.MokMx(256, 256)
+    P = lambda t: ctypes.cast(t, ctypes.c_void_p)
+    assert L.mok_backward(S, C, lib.MOK_MXFP8, fake, 1 << 30, fake, fake, fake, P(pair), P(pair),
+                          P(ctypes.pointer(one)), fake, fake, fake, fake, fake, fake, None) == 1

@@ -72,3 +72,38 @@ def test_replay_full_size_dsv3():
     assert torch.equal(out_a, out_b)
     for k in g_a:
         assert torch.equal(g_a[k], g_b[k]), k
+
+
+def run_mx(shape, routing, seed, inp=None, **kw):
+    from mixture_experts_layer_side_gb300.inputs import make_inputs
+    from mixture_experts_layer_side_gb300.layer import MoKLayer
+    if inp is None:
+        inp = {k: v.cuda() for k, v in make_inputs(shape, routing, seed=seed, device="cpu").items()}
+    layer = MoKLayer(shape, precision="mxfp8", **kw)
+    wq = layer.quantize_weights(inp["W1"], inp["W3"], inp["W2"])
+    layer.build_schedule(inp["idx"])
+    out, grads = poisoned_outputs(layer)
+    layer.forward(inp["x"], inp["s"], *wq["fwd"], out=out)
+    wb = wq["bwd_replay"] if kw.get("replay") else wq["bwd"]
+    layer.backward(inp["x"], inp["s"], *wb, inp["dout"], grads=grads)
+    layer.check()
+    return inp, out, grads, layer.ctx.numel()
+
+
+@pytest.mark.parametrize("shape,routing,mb,slots,flags", [
+    ((4096, 256, 128, 16, 4), "zipf", 128, 2, 0), ((4096, 256, 256, 16, 4), "zipf", 256, 3, 0),
+    ((512, 384, 128, 24, 4), "hot", 256, 3, 0), ((3000, 256, 128, 20, 2), "hot", 128, 2, 64 | 4)])
+def test_mxfp8_replay_is_bitwise_equal_to_the_saved_context(shape, routing, mb, slots, flags):
+    """MXFP8 bounded-memory backward: GEMM1 recomputed from x quantised along
+    H and the forward orientation of W1 / W3 gives the forward's [h|u] bit
+    for bit, so every output and gradient equals the saved context's."""
+    require_gpu()
+    from mixture_experts_layer_side_gb300.inputs import Shape
+    S = Shape(*shape)
+    kw = dict(minibatch_rows=mb, ring_slots=slots, debug_flags=flags)
+    inp, out_a, g_a, ctx_a = run_mx(S, routing, 33, **kw)
+    _, out_b, g_b, ctx_b = run_mx(S, routing, 33, inp=inp, replay=True, **kw)
+    assert ctx_b < ctx_a
+    assert torch.equal(out_a, out_b)
+    for k in g_a:
+        assert torch.equal(g_a[k], g_b[k]), k
