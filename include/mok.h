@@ -249,7 +249,9 @@ mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void
  * decisions that matter": router gradients fused into the SwiGLU backward).
  *
  *   ctx      (device) the forward's context, same routing and inputs
- *   x, scores, W1, W3, W2   as for mok_forward, except that in MXFP8 mode
+ *   x, scores, W1, W3, W2   as for mok_forward (the same x: a BF16 backward
+ *            reuses the token-sorted copy of x its forward left in the
+ *            workspace), except that in MXFP8 mode
  *            the weights are passed in the orientation the backward GEMMs
  *            contract over: W1, W3 quantised along I (block_axis 1), W2
  *            quantised along H (block_axis 1).

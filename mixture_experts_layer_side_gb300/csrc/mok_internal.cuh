@@ -33,10 +33,13 @@ constexpr int kHdrG2Done = 8;
 constexpr int kHdrCombineNext = 9;  // next token of the single-launch forward's combine
 // nonzero while the sorted buffer holds the token-sorted x of the last
 // BF16 forward on this schedule (its backward then skips sorting x again);
-// cleared by every schedule build and by forwards that do not sort x
-constexpr int kHdrSortedX = 10;
+// cleared by every schedule build and by forwards that do not sort x.  Past
+// the words each call's counter reset clears ([kHdrAbort, kHdrCounters +
+// kNumCounters)), so it lives from the forward to the backward.
+constexpr int kHdrSortedX = 56;
 constexpr int kHdrCounters = 16;    // [16, 48): per-launch dynamic tile counters
 constexpr int kNumCounters = 32;
+static_assert(kHdrSortedX >= kHdrCounters + kNumCounters && kHdrSortedX < kHeaderWords, "flag outside the reset words");
 
 struct WsLayout {
   // schedule
