@@ -45,7 +45,7 @@ METRIC = "MoE layer fwd+bwd TFLOP/s"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_PHASES = ("fwd_gemm", "bwd_da", "bwd_dx", "bwd_wg13", "bwd_wg2")
-HBM_PHASES = ("fwd_combine", "bwd_dx_combine", "bwd_sort")
+HBM_PHASES = ("fwd_combine", "bwd_dx_combine", "fwd_sort", "bwd_sort")
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -131,11 +131,22 @@ def phase_min_bytes(shape, prec, active_experts):
 
 
 def phase_bytes(shape):
-    # algorithmic bytes of the HBM-bound kernels (bf16 = 2 B, f32 = 4 B)
+    # algorithmic bytes per run of the HBM-bound kernels (bf16 = 2 B, f32 = 4 B)
     R, T, H = shape.R, shape.T, shape.H
     return {"fwd_combine": R * H * 2 + R * 4 + T * H * 2, "bwd_dx_combine": R * H * 2 + T * H * 2,
-            # token-sorted copy of x or dout: R rows read and written (padding rows excluded)
-            "bwd_sort": 2 * R * H * 2}
+            # token-sorted copy of x: R rows read and written (padding rows excluded)
+            "fwd_sort": 2 * R * H * 2}
+
+
+def sort_copies_per_step(args, prec):
+    """Token-sorted copies the BF16 backward really makes per step: dout
+    always; x only when the forward left no sorted copy of x (the fused
+    forward, the gathered ring).  The launch for x runs either way and
+    returns at once when the copy is there."""
+    if prec != "bf16":
+        return None
+    forward_sorts_x = not args.fused and not (args.debug_flags & 64)
+    return 1 if forward_sorts_x else 2
 
 
 # ---------------------------------------------------------------- clocks
@@ -515,6 +526,11 @@ def run_mok(args):
                 "frac": achieved / peak, "peak_source": peak_note,
                 "peak_sustained": peak_sus, "frac_of_sustained": achieved / peak_sus,
                 "traffic": recorded_traffic(dom, args.workload)}
+    copies = sort_copies_per_step(args, prec)
+    if copies is not None and "bwd_sort" in per_phase:
+        # bytes of the copies made, over the time of every launch of the phase
+        pb["bwd_sort"] = copies * 2 * shape.R * shape.H * 2 * args.steps / per_phase["bwd_sort"]["runs"]
+        per_phase["bwd_sort"]["copies_per_step"] = copies
     for n in per_phase:
         if n in pf:
             per_phase[n]["tflops"] = pf[n] / (per_phase[n]["ms"] / 1e3) / 1e12
