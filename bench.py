@@ -145,7 +145,12 @@ def sort_copies_per_step(args, prec):
     returns at once when the copy is there."""
     if prec != "bf16":
         return None
-    forward_sorts_x = not args.fused and not (args.debug_flags & 64)
+    f = args.debug_flags
+    # a gathered ring (bit 6) runs only where the ring is one single-CTA
+    # launch (bit 5, or replay); the serial two-launch debug path (bit 1)
+    # gathers too
+    gathered = bool(f & 64) and (bool(f & 32) or args.replay)
+    forward_sorts_x = not args.fused and not gathered and not (f & 2)
     return 1 if forward_sorts_x else 2
 
 

@@ -104,14 +104,14 @@ typedef struct {
  *                 Bit 4 (MOK_DEBUG_SINGLE_CTA_ROWS): the BF16 backward's dA'
  *                 and dX GEMMs run one CTA per 128-row tile instead of
  *                 clusters of two CTAs sharing two tiles of one expert.
- *                 Bits 5 and 7 (MOK_DEBUG_SINGLE_CTA_RING,
- *                 MOK_DEBUG_PAIR_RING): the BF16 forward ring runs one CTA
- *                 per 128-row tile (bit 5), or clusters of two CTAs sharing
- *                 two tiles of one expert and one minibatch (bit 7); both
- *                 read a token-sorted copy of x with plain TMA.  By default it takes clusters of two when
- *                 the experts average at least 1,024 routed rows
- *                 (T*k >= 1024*E): below that, an expert's odd last tile
- *                 leaves too many CTAs of a pair idle.
+ *                 Bit 5 (MOK_DEBUG_SINGLE_CTA_RING): the BF16 forward ring
+ *                 runs every tile on one CTA, in one launch.  By default it
+ *                 runs in two launches: each expert's first 2*floor(t/2)
+ *                 tiles on clusters of two CTAs (two tiles of one expert per
+ *                 256 x 256 tile, an even number of tiles per minibatch, so
+ *                 no CTA of a pair idles), then the experts' odd last tiles
+ *                 on single CTAs; with replay = 1 it keeps the one launch.
+ *                 Both forms read a token-sorted copy of x with plain TMA.
  *                 Bit 6 (MOK_DEBUG_GATHER_X_RING): the single-CTA ring
  *                 gathers token rows of x (MXFP8: of x's E4M3 codes) in its
  *                 load path instead of reading a token-sorted copy with
@@ -147,7 +147,6 @@ typedef struct {
 #define MOK_DEBUG_SINGLE_CTA_ROWS 16
 #define MOK_DEBUG_SINGLE_CTA_RING 32
 #define MOK_DEBUG_GATHER_X_RING 64
-#define MOK_DEBUG_PAIR_RING 128
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
 typedef struct {

@@ -25,7 +25,6 @@ MOK_DEBUG_SINGLE_CTA_WGRAD = 8
 MOK_DEBUG_SINGLE_CTA_ROWS = 16
 MOK_DEBUG_SINGLE_CTA_RING = 32
 MOK_DEBUG_GATHER_X_RING = 64
-MOK_DEBUG_PAIR_RING = 128
 
 STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "MOK_ERR_WORKSPACE_TOO_SMALL",
           4: "MOK_ERR_CUDA", 5: "MOK_ERR_BAD_INDEX", 6: "MOK_ERR_TIMEOUT"}

@@ -326,6 +326,7 @@ void base_params(GemmParams& g, const mok_shape& s, const WsLayout& L, uint8_t* 
   g.counts = reinterpret_cast<const int32_t*>(ws + L.counts);
   g.wg_rows_min = 0;
   g.wg_rows_max = INT_MAX;
+  g.ring_count_word = kHdrTiles;  // a ring launch walks every tile unless given a list
 }
 
 // Whether the BF16 backward's dA' and dX run on CTA pairs.
@@ -736,37 +737,49 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.counter = 0;
     const int grid = gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles));
     bool launched = false;
-    // CTA pairs pay for an expert's odd last tile with an idle CTA: take
-    // them when experts average at least 8 tiles (1,024 routed rows), or
-    // when asked to
-    const bool many_rows = (int64_t)s.T * s.k >= (int64_t)1024 * s.E;
-    const bool pairs = (cfg->debug_flags & MOK_DEBUG_PAIR_RING) ||
-                       (many_rows && !(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING));
-    if (pairs && bn2 == 256) {
-      // CTA pairs: GEMM1 reads a token-sorted copy of x with plain TMA (the
-      // backward's sorted buffer, free until the backward), pairs of tiles
-      // from one expert and one minibatch share each 256 x 256 tile
+    // The ring in two launches (unless single CTAs are asked for, or the
+    // context must keep the minibatches in one order for replay): each
+    // expert's first 2 * floor(t / 2) tiles on CTA pairs, two tiles of one
+    // expert per 256 x 256 tile, never a solo pair (an even number of tiles
+    // per minibatch); the experts' odd last tiles on single CTAs.  Both read
+    // the token-sorted copy of x with plain TMA.
+    const int Mt_pair = (M / kTileRows) & ~1;
+    if (!(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING) && !cfg->replay && bn2 == 256 && Mt_pair >= 2) {
       __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
       {
         Phase ph(MOK_PHASE_FWD_SORT, st, 2);
         MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
         MOK_CUDA(cudaMemsetAsync(sorted_x_flag, 1, 1, st));
-        MOK_CUDA(launch_ring_pair_table(L, w, st));
+        MOK_CUDA(launch_split_table(L, w, st));
       }
-      TmapSet pm = maps;
-      if (!map2d(&pm.m[0], srt, s.H, (uint64_t)L.pad_capacity, 128)) return MOK_ERR_CUDA;
+      TmapSet sm = maps;
+      if (!map2d(&sm.m[0], srt, s.H, (uint64_t)L.pad_capacity, 128)) return MOK_ERR_CUDA;
       GemmParams gp = g;
       gp.fwd_sorted = 1;
       gp.pair_m0 = reinterpret_cast<const int32_t*>(w + L.pair_m0);
-      gp.pair_mb = reinterpret_cast<const int32_t*>(w + L.pair_mb);
-      Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
-      const cudaError_t e = launch_gemm_pair(GM_FWD_RING, pm, gp, grid, st);
-      if (e == cudaSuccess)
+      gp.ring_count_word = kHdrPairs;
+      gp.ring_rows = Mt_pair * kTileRows;
+      Phase ph(MOK_PHASE_FWD_GEMM, st, 2);
+      const cudaError_t e = launch_gemm_pair(GM_FWD_RING, sm, gp, grid, st);
+      if (e == cudaSuccess) {
+        // the odd last tiles: a fresh ring walk (flags and tile counter)
+        MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 2 * L.tile_capacity * 4, st));
+        GemmParams gs = g;
+        gs.fwd_sorted = 1;
+        gs.ring_list = reinterpret_cast<const int32_t*>(w + L.pair_mb);
+        gs.ring_count_word = kHdrSingles;
+        gs.counter = 7;
+        MOK_CUDA(launch_gemm(GM_FWD_RING, sm, gs, grid, st));
         launched = true;
-      else if (e != cudaErrorNotSupported)
+      } else if (e != cudaErrorNotSupported) {
         return MOK_ERR_CUDA;
-      else
-        (void)cudaGetLastError();  // no cluster of two fits: single CTAs below
+      } else {
+        (void)cudaGetLastError();  // no cluster of two fits: all tiles on single CTAs below
+        GemmParams ga = g;
+        ga.fwd_sorted = 1;
+        MOK_CUDA(launch_gemm(GM_FWD_RING, sm, ga, grid, st));
+        launched = true;
+      }
     }
     if (!launched && !(cfg->debug_flags & MOK_DEBUG_GATHER_X_RING)) {
       // single CTAs reading the token-sorted copy of x with plain TMA (the

@@ -79,6 +79,7 @@ struct Item {
   int row0;     // first padded row of the tile (row-tiled) or of the expert (wgrad)
   int k_iters;  // K iterations of 128 bytes
   int idle;     // CTA pairs: the second CTA of a solo pair (loads, stores nothing)
+  int rp;       // ring launches: the tile's position in the launch's walk (ring rows, flags)
 };
 
 __device__ __forceinline__ int used_tiles(const GemmParams& p) { return p.hdr[kHdrTiles]; }
@@ -107,7 +108,7 @@ __device__ int count_items(const GemmParams& p) {
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
     return 0;  // known only inside the kernel (experts with routed rows)
   } else if constexpr (MODE == GM_FWD_RING) {
-    return used_tiles(p) * (p.g1_tiles + p.n_tiles);
+    return p.hdr[p.ring_count_word] * (p.g1_tiles + p.n_tiles);
   } else {
     int end = min(p.m_tile_end, used_tiles(p));
     if (p.replay_keep > 0) {
@@ -130,9 +131,9 @@ __device__ __forceinline__ int count_pair_items(const GemmParams& p) { return p.
 // Inside a step the items run N-tile-major over the minibatch's M tiles,
 // so the M tiles of one expert, which share a weight slice, run together
 // (1.8% faster on the DeepSeek-V3-shaped forward than M-tile-major).
-__device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& n) {
-  const int Mt = p.ring_rows / kTileRows;
-  const int tiles = used_tiles(p);
+// Generic form: `tiles` units (tiles, or pairs of tiles), Mt units per
+// minibatch.
+__device__ void decode_ring_n(const GemmParams& p, int w, int tiles, int Mt, int& type, int& m, int& n) {
   const int nb = (tiles + Mt - 1) / Mt;
   const int g1 = p.g1_tiles, g2 = p.n_tiles;
   auto mt_of = [&](int b) { return min(Mt, tiles - b * Mt); };
@@ -166,36 +167,8 @@ __device__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& 
   return emit(GM_FWD2, nb - 1, w, g2);
 }
 
-// Ring on CTA pairs: the same steps over the ring pair table, N-tile-major
-// over a minibatch's pairs.  Step s (0..nb) holds GEMM1 of minibatch s
-// (s < nb) then GEMM2 of minibatch s - 1 (s >= 1); its first item is
-// g1 * pair_mb[s] + g2 * pair_mb[s - 1], found by bisection.
-__device__ void decode_ring_pair(const GemmParams& p, int w, int& type, int& pidx, int& n) {
-  const int Mt = p.ring_rows / kTileRows;
-  const int nb = (used_tiles(p) + Mt - 1) / Mt;
-  const int g1 = p.g1_tiles, g2 = p.n_tiles;
-  const int32_t* off = p.pair_mb;
-  auto start = [&](int st) { return st == 0 ? 0 : g1 * off[min(st, nb)] + g2 * off[st - 1]; };
-  int lo = 0, hi = nb;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (start(mid) <= w) lo = mid; else hi = mid - 1;
-  }
-  int r = w - start(lo);
-  if (lo < nb) {
-    const int p1 = off[lo + 1] - off[lo];
-    if (r < g1 * p1) {
-      type = GM_FWD1;
-      pidx = off[lo] + r % p1;
-      n = r / p1;
-      return;
-    }
-    r -= g1 * p1;
-  }
-  const int p2 = off[lo] - off[lo - 1];
-  type = GM_FWD2;
-  pidx = off[lo - 1] + r % p2;
-  n = r / p2;
+__device__ __forceinline__ void decode_ring(const GemmParams& p, int w, int& type, int& m, int& n) {
+  decode_ring_n(p, w, used_tiles(p), p.ring_rows / kTileRows, type, m, n);
 }
 
 __device__ __forceinline__ int row_k_iters(const GemmParams& p, int type, int el) {
@@ -210,6 +183,7 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
   const int* po = ctl->po;
   Item it;
   it.idle = 0;
+  it.rp = 0;
   if constexpr (MODE == GM_DENSE) {
     it.type = MODE;
     it.m = w / p.n_tiles;
@@ -255,6 +229,7 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
         decode_ring(p, w - a0, type, m, n);
         it.type = type;
         it.m = m;
+        it.rp = m;
         it.n = n;
         it.e = p.tile_expert[m];
         it.row0 = m * kTileRows;
@@ -262,14 +237,19 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
       }
     }
   } else if constexpr (PAIR && MODE == GM_FWD_RING) {
-    // the ring on CTA pairs: as dA' / dX below, over the ring pair table
-    int type, pidx, n;
-    decode_ring_pair(p, w, type, pidx, n);
-    const int code = p.pair_m0[pidx];
+    // the ring on CTA pairs: its units are the pairs of the split table (two
+    // tiles of one expert, never solo), ring_rows / 256 of them per
+    // minibatch; the leader takes the pair's first tile, the other CTA the
+    // second, and pair u's tiles sit at walk positions 2u and 2u + 1
+    int type, u, n;
+    decode_ring_n(p, w, p.hdr[kHdrPairs], p.ring_rows / (2 * kTileRows), type, u, n);
+    const int code = p.pair_m0[u];
     it.idle = (code & 1) && ctl->pair_rank == 1;
-    const int m = (code >> 1) + (it.idle ? 0 : ctl->pair_rank);
+    const int r = it.idle ? 0 : ctl->pair_rank;
+    const int m = (code >> 1) + r;
     it.type = type;
     it.m = m;
+    it.rp = 2 * u + r;
     it.n = n;
     it.e = p.tile_expert[m];
     it.row0 = m * kTileRows;
@@ -282,20 +262,25 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     const int m = (code >> 1) + (it.idle ? 0 : ctl->pair_rank);
     it.type = MODE;
     it.m = m;
+    it.rp = m;
     it.n = w % p.n_tiles;
     it.e = p.tile_expert[m];
     it.row0 = m * kTileRows;
     it.k_iters = row_k_iters(p, MODE, kEl);
   } else {
-    int type = MODE, m, n;
+    int type = MODE, m, n, rp;
     if constexpr (MODE == GM_FWD_RING) {
-      decode_ring(p, w, type, m, n);
+      // walk position -> tile: the position itself, or the tile a list holds there
+      decode_ring_n(p, w, p.hdr[p.ring_count_word], p.ring_rows / kTileRows, type, rp, n);
+      m = p.ring_list ? p.ring_list[rp] : rp;
     } else {
       m = p.m_tile_begin + w / p.n_tiles;
       n = w % p.n_tiles;
+      rp = m;
     }
     it.type = type;
     it.m = m;
+    it.rp = rp;
     it.n = n;
     it.e = p.tile_expert[m];
     it.row0 = m * kTileRows;
@@ -359,7 +344,7 @@ __device__ __forceinline__ void tma_loads(const TmapSet& mp, const GemmParams& p
   } else if (type == GM_FWD2) {
     const int mslot = is_ring<MODE>() ? 3 : 0;
     const int wmap = is_ring<MODE>() ? 4 : 1;
-    tma_load_2d(a, &mp.m[mslot], bar, kk * 64, ring_row(p, it.row0));
+    tma_load_2d(a, &mp.m[mslot], bar, kk * 64, ring_row(p, it.rp * kTileRows));
     for (int c = 0; c < p.bn / 64; ++c) tma_load_3d(b + c * 8192, &mp.m[wmap], bar, it.n * p.bn + c * 64, kk * 64, it.e);
   } else if (type == GM_BWD_DA) {
     if (p.rows_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 64, it.row0);
@@ -403,7 +388,7 @@ __device__ __forceinline__ void tma_loads_pair(const TmapSet& mp, const GemmPara
         tma_load_3d_pair(b + c * 8192, &mp.m[rank ? 2 : 1], bar, it.n * 128 + c * 64, kk * 64, it.e);
     } else {
       // A: this tile's ring rows; B: this CTA's 128 columns of the W2 block
-      tma_load_2d_pair(a, &mp.m[3], bar, kk * 64, ring_row(p, it.row0));
+      tma_load_2d_pair(a, &mp.m[3], bar, kk * 64, ring_row(p, it.rp * kTileRows));
       for (int c = 0; c < 2; ++c) tma_load_3d_pair(b + c * 8192, &mp.m[4], bar, bcol + c * 64, kk * 64, it.e);
     }
   } else if constexpr (MODE == GM_WG13 || MODE == GM_WG2) {
@@ -538,9 +523,9 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
   } else if (type == GM_FWD2) {
     const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
     const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
-    tma_load_2d(a, &mp.m[mslot], bar, kk * 128, ring_row(p, it.row0));
+    tma_load_2d(a, &mp.m[mslot], bar, kk * 128, ring_row(p, it.rp * kTileRows));
     // a's scales, tiled by the GEMM1 epilogue next to the ring codes
-    bulk_load(sfa, p.ring_sf + ((long)(ring_row(p, it.row0) >> 7) * (p.I / 128) + kk) * 512, 512, bar);
+    bulk_load(sfa, p.ring_sf + ((long)(ring_row(p, it.rp * kTileRows) >> 7) * (p.I / 128) + kk) * 512, 512, bar);
     for (int c = 0; c < bn / 128; ++c) {
       tma_load_3d(b + c * 16384, &mp.m[wmap], bar, it.n * bn + c * 128, kk * 128, it.e);
       const long blk = ((long)it.e * (p.H / 128) + it.n * (bn / 128) + c) * (p.I / 128) + kk;
@@ -656,7 +641,7 @@ __device__ void epi_fwd1(const GemmParams& p, const Item& it, uint32_t tbase, in
   const long crow = p.ctx_ring ? (long)ring_row(p, (int)prow) : prow;
   __nv_bfloat16* hrow = p.ctx_hu + crow * 2 * p.I + i0;
   __nv_bfloat16* urow = hrow + p.I;
-  __nv_bfloat16* arow = p.ring + (long)ring_row(p, (int)prow) * p.I + i0;
+  __nv_bfloat16* arow = p.ring + (long)ring_row(p, it.rp * kTileRows + row) * p.I + i0;
 #pragma unroll 1
   for (int c = 0; c < 128; c += 32) {
     float h[32], u[32];
@@ -746,7 +731,7 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
   release();
   __nv_bfloat16* hrow = p.ctx_hu + crow * 2 * p.I + i0;
   __nv_bfloat16* urow = hrow + p.I;
-  const long rr = ring_row(p, (int)prow);
+  const long rr = ring_row(p, it.rp * kTileRows + row);
   uint8_t* qrow = reinterpret_cast<uint8_t*>(p.ring) + rr * p.I + i0;
   // the row's four scales of this 128-column group go out as one word, in
   // the tiled layout GEMM2's TMA thread bulk-loads ([ring rows / 128]
@@ -1609,7 +1594,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           if (is_ring<MODE>() && it.type == GM_FWD2) {
             // this CTA loads the ring rows of its own tile: acquire their
             // GEMM1 completion itself, then order the async-proxy loads after it
-            ok = wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc);
+            ok = wait_flag_geq(&p.ring_flags[it.rp], 4u * (uint32_t)p.g1_tiles, wc);
             fence_proxy_async_global();
             if (!ok) break;
           }
@@ -1690,7 +1675,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
             // of its GEMM1 column tiles are published, then order the
             // async-proxy loads after the acquire
-            ok = wait_flag_geq(&p.ring_flags[it.m], 4u * (uint32_t)p.g1_tiles, wc);
+            ok = wait_flag_geq(&p.ring_flags[it.rp], 4u * (uint32_t)p.g1_tiles, wc);
             fence_proxy_async_global();
             if (!ok) break;
           }
@@ -1908,14 +1893,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (is_ring<MODE>() && it.type == GM_FWD2 && !it.idle && warp == 2 && lane == 0) {
         // the accumulator is complete, so every load of this tile's ring
         // rows has landed: release the rows for reuse
-        red_release_gpu_add(&p.ring_flags[p.m_tiles + it.m], 1u);
+        red_release_gpu_add(&p.ring_flags[p.m_tiles + it.rp], 1u);
       }
       bool ok = true;
       if (is_ring<MODE>() && it.type == GM_FWD1 && !it.idle) {
         // the ring slot rows this tile writes were last read by GEMM2 of the
         // tile ring_slots minibatches back; each warp waits on its own (no
         // CTA-level barrier on a path that a bounded wait can abandon)
-        const int back = it.m - p.ring_slots * (p.ring_rows / kTileRows);
+        const int back = it.rp - p.ring_slots * (p.ring_rows / kTileRows);
         if (back >= 0) {
           if (lane == 0) ok = wait_flag_geq(&p.ring_flags[p.m_tiles + back], (uint32_t)p.n_tiles, wc);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -1957,7 +1942,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) {
           const bool skip = (p.debug_flags & MOK_DEBUG_SKIP_RING_SIGNAL) && it.m == 0 && it.n == 0 && warp == 2;
           __threadfence();
-          if (!skip) red_release_gpu_add(&p.ring_flags[it.m], 1u);
+          if (!skip) red_release_gpu_add(&p.ring_flags[it.rp], 1u);
         }
       }
       ++tcount;
@@ -2077,7 +2062,8 @@ cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p,
   if (mode == GM_WG13 || mode == GM_WG2) {
     if (!p.wg_sorted || p.m_tiles % 2 != 0) return cudaErrorInvalidValue;
   } else if (mode == GM_FWD_RING) {
-    if (!p.pair_m0 || !p.pair_mb || !p.fwd_sorted) return cudaErrorInvalidValue;
+    if (!p.pair_m0 || !p.fwd_sorted || p.ring_count_word != kHdrPairs || (p.ring_rows / kTileRows) % 2)
+      return cudaErrorInvalidValue;
   } else if (!p.pair_m0 || (mode == GM_BWD_DA && !p.rows_sorted)) {
     return cudaErrorInvalidValue;
   }

@@ -79,9 +79,14 @@ struct GemmParams {
   int wg_sorted;           // weight gradients read token-sorted copies (plain TMA)
   int rows_sorted;         // dA' reads a token-sorted copy of dout (plain TMA)
   // CTA-pair launches of dA' / dX / the forward ring: the pair table (first
-  // M tile * 2 + solo); the ring's pairs of minibatch b are [pair_mb[b], pair_mb[b+1])
+  // M tile * 2 + solo)
   const int32_t* pair_m0;
-  const int32_t* pair_mb;
+  // ring launches: the units they walk, counted by header word
+  // ring_count_word -- all tiles (kHdrTiles, ring_list null), the tiles of
+  // ring_list (kHdrSingles), or the pairs of pair_m0 (kHdrPairs, CTA pairs);
+  // a tile's ring rows and flags follow its position in that walk
+  const int32_t* ring_list;
+  int ring_count_word;
   int fwd_sorted;          // GEMM1 reads a token-sorted copy of x (plain TMA) instead of gathering
   // single-launch forward (GM_FWD_FUSED): the schedule's input and arrays
   // (written by its schedule items), and the combine's output
@@ -130,8 +135,9 @@ cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, i
 // row-tiled backward GEMMs (GM_BWD_DA with token-sorted dout, GM_BWD_DX;
 // bn = 256, the pair table of launch_pair_table, weight maps with 128-row
 // boxes) and the forward ring (GM_FWD_RING with a token-sorted copy of x,
-// bn = 256, the pair table of launch_ring_pair_table).  Returns
-// cudaErrorNotSupported when the device cannot hold a cluster of two.
+// bn = 256, over the pairs of launch_split_table, an even number of tiles per
+// minibatch).  Returns cudaErrorNotSupported when the device cannot hold a
+// cluster of two.
 cudaError_t launch_gemm_pair(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 
 }  // namespace mok

@@ -23,7 +23,8 @@ constexpr int kHdrError = 0;
 constexpr int kHdrPaddedRows = 1;
 constexpr int kHdrTiles = 2;
 constexpr int kHdrAbort = 3;       // launch-wide abort word (cleared per call)
-constexpr int kHdrPairs = 4;       // CTA-pair tiles of the pair table (see launch_pair_table)
+constexpr int kHdrPairs = 4;       // CTA-pair tiles of the pair table (see launch_pair_table, launch_split_table)
+constexpr int kHdrSingles = 11;    // single tiles of the forward ring's split (see launch_split_table)
 // single-launch forward: completed schedule items (count, scan, place) and
 // GEMM2 epilogue warps that stored their rows of y
 constexpr int kHdrCountDone = 5;
@@ -58,7 +59,7 @@ struct WsLayout {
                       // in MXFP8 also dout (dW2)
   size_t sorted2;     // bf16 [pad_capacity, H]: BF16 token-sorted dout (dA', dW2)
   size_t pair_m0;     // int32 [tile_capacity]: CTA-pair tiles of dA' / dX / the ring (first M tile * 2 + solo)
-  size_t pair_mb;     // int32 [tile_capacity + 2]: forward ring, first pair of each minibatch
+  size_t pair_mb;     // int32 [tile_capacity + 2]: forward ring, the list of single (odd last) tiles
   // MXFP8 operand copies
   size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
   size_t xq_sorted;   // those codes in padded-row order (GEMM1 / dA' A operand): u8 [pad_capacity, H]
@@ -85,8 +86,9 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
 cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, const int32_t* idx,
                             cudaStream_t st);
 cudaError_t launch_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
-// the forward ring's pair table: pairs inside one minibatch, per-minibatch offsets in pair_mb
-cudaError_t launch_ring_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
+// the forward ring's split: pairs of an expert's tiles (pair_m0, header word
+// kHdrPairs) and the odd last tiles (pair_mb as the single-tile list, word kHdrSingles)
+cudaError_t launch_split_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* yk,
                            const float* scores, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_t* ws, float* ds, int n_parts,

@@ -168,17 +168,13 @@ __global__ void __launch_bounds__(kPlaceWarps * 32)
   }
 }
 
-// CTA-pair table of the row-tiled GEMMs: the tiles of each expert are taken
-// two at a time from its first; a last tile without a partner is a solo
-// pair, whose second CTA loads valid rows but stores nothing.  With seg > 0
-// (the forward ring, seg = tiles per minibatch) a pair never straddles a
-// minibatch either: segments also start at every multiple of seg, and
-// mb_off[b] is the index of minibatch b's first pair (mb_off[nb] = pairs).
-// One block; integer work, exact.
+// CTA-pair table of the row-tiled backward GEMMs: the tiles of each expert
+// are taken two at a time from its first; a last tile without a partner is
+// a solo pair, whose second CTA loads valid rows but stores nothing.  One
+// block; integer work, exact.
 __global__ void __launch_bounds__(1024) pair_table_kernel(const int32_t* __restrict__ tile_expert,
                                                           const int32_t* __restrict__ poff, int32_t* __restrict__ hdr,
-                                                          int32_t* __restrict__ pair_m0, int seg,
-                                                          int32_t* __restrict__ mb_off) {
+                                                          int32_t* __restrict__ pair_m0) {
   __shared__ int warp_tot[32];
   __shared__ int tot;
   const int U = hdr[kHdrTiles];
@@ -188,21 +184,51 @@ __global__ void __launch_bounds__(1024) pair_table_kernel(const int32_t* __restr
     int head = 0, solo = 0;
     if (m < U) {
       const int e = tile_expert[m];
-      int start = poff[e] / kTileRows;
-      if (seg > 0) start = max(start, m / seg * seg);
-      head = ((m - start) & 1) == 0;
-      solo = head && (m + 1 >= U || tile_expert[m + 1] != e || (seg > 0 && (m + 1) % seg == 0));
+      head = ((m - poff[e] / kTileRows) & 1) == 0;
+      solo = head && (m + 1 >= U || tile_expert[m + 1] != e);
     }
     const int pos = carry + block_exclusive_scan(head, warp_tot, &tot);
-    if (head) {
-      pair_m0[pos] = 2 * m + solo;
-      if (seg > 0 && m % seg == 0) mb_off[m / seg] = pos;
-    }
+    if (head) pair_m0[pos] = 2 * m + solo;
     carry += tot;
   }
+  if (threadIdx.x == 0) hdr[kHdrPairs] = carry;
+}
+
+// Split of the row tiles for CTA pairs with no idle CTA: each expert's
+// first 2 * floor(t / 2) tiles (t = its padded tiles) are taken two at a
+// time as pairs, pair_m0[j] = 2 * (first tile of pair j); an odd last tile
+// goes to the list of single tiles, single_list[q] = tile.  Both lists are
+// in increasing tile order.  One block; integer work, exact.
+__global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __restrict__ tile_expert,
+                                                           const int32_t* __restrict__ poff, int32_t* __restrict__ hdr,
+                                                           int32_t* __restrict__ pair_m0,
+                                                           int32_t* __restrict__ single_list) {
+  __shared__ int warp_tot[32];
+  __shared__ int tot;
+  const int U = hdr[kHdrTiles];
+  int carry_p = 0, carry_s = 0;
+  for (int base = 0; base < U; base += 1024) {
+    const int m = base + threadIdx.x;
+    int head = 0, single = 0;
+    if (m < U) {
+      const int e = tile_expert[m];
+      const int first = poff[e] / kTileRows;
+      const int t = (poff[e + 1] - poff[e]) / kTileRows;
+      const int j = m - first;
+      head = (j < (t & ~1)) && !(j & 1);
+      single = (t & 1) && j == t - 1;
+    }
+    const int pp = carry_p + block_exclusive_scan(head, warp_tot, &tot);
+    const int np = tot;
+    const int ps = carry_s + block_exclusive_scan(single, warp_tot, &tot);
+    if (head) pair_m0[pp] = 2 * m;
+    if (single) single_list[ps] = m;
+    carry_p += np;
+    carry_s += tot;
+  }
   if (threadIdx.x == 0) {
-    hdr[kHdrPairs] = carry;
-    if (seg > 0) mb_off[(U + seg - 1) / seg] = carry;
+    hdr[kHdrPairs] = carry_p;
+    hdr[kHdrSingles] = carry_s;
   }
 }
 
@@ -229,15 +255,14 @@ cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, 
 
 cudaError_t launch_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st) {
   auto P = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
-  pair_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0), 0,
-                                        nullptr);
+  pair_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0));
   return cudaGetLastError();
 }
 
-cudaError_t launch_ring_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+cudaError_t launch_split_table(const WsLayout& L, uint8_t* ws, cudaStream_t st) {
   auto P = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
-  pair_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0),
-                                        L.minibatch_rows / kTileRows, P(L.pair_mb));
+  split_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0),
+                                         P(L.pair_mb));
   return cudaGetLastError();
 }
 

@@ -152,14 +152,14 @@ def test_backward_row_gemm_cta_pairs_match_single_cta(shape, routing, kw):
     ((1024, 4096, 256, 24, 4), "hot", {}),
 ])
 def test_forward_ring_cta_pairs_match_single_cta(shape, routing, kw):
-    """The forward ring on clusters of two CTAs (token-sorted x by plain TMA,
-    two tiles of one expert and one minibatch per cta_group::2 MMA), on
-    single CTAs reading the sorted copy by TMA (whose backward reuses that
-    copy for dW1|dW3), and on single CTAs gathering x in their load path:
-    bitwise equal outputs, and the backward from each forward bitwise equal
-    too."""
+    """The forward ring split in two launches (each expert's tiles two at a
+    time on clusters of two CTAs, one cta_group::2 MMA per pair; the odd last
+    tiles on single CTAs; token-sorted x by plain TMA), all tiles on single
+    CTAs reading the sorted copy, and all on single CTAs gathering x in
+    their load path: bitwise equal outputs, and the backward from each
+    forward (which reuses the sorted x when there is one) bitwise equal."""
     require_gpu()
-    _, out_p, g_p = run_layer(shape, routing, 15, debug_flags=128, **kw)
+    _, out_p, g_p = run_layer(shape, routing, 15, **kw)
     _, out_s, g_s = run_layer(shape, routing, 15, debug_flags=32, **kw)
     _, out_t, g_t = run_layer(shape, routing, 15, debug_flags=32 | 64, **kw)
     assert torch.equal(out_p, out_s) and torch.equal(out_t, out_s)
