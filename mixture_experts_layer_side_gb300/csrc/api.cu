@@ -738,11 +738,12 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     const int grid = gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles));
     bool launched = false;
     // The ring in two launches (unless single CTAs are asked for, or the
-    // context must keep the minibatches in one order for replay): each
-    // expert's first 2 * floor(t / 2) tiles on CTA pairs, two tiles of one
-    // expert per 256 x 256 tile, never a solo pair (an even number of tiles
-    // per minibatch); the experts' odd last tiles on single CTAs.  Both read
-    // the token-sorted copy of x with plain TMA.
+    // context must keep the minibatches in one order for replay): the
+    // experts with an even number of tiles, or five and more, on CTA pairs
+    // (two tiles of one expert per 256 x 256 tile, an even number of tiles
+    // per minibatch), those of one or three tiles on single CTAs; every
+    // expert in one launch, so its weights stream once.  Both read the
+    // token-sorted copy of x with plain TMA.
     const int Mt_pair = (M / kTileRows) & ~1;
     if (!(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING) && !cfg->replay && bn2 == 256 && Mt_pair >= 2) {
       __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);

@@ -238,9 +238,10 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
     }
   } else if constexpr (PAIR && MODE == GM_FWD_RING) {
     // the ring on CTA pairs: its units are the pairs of the split table (two
-    // tiles of one expert, never solo), ring_rows / 256 of them per
-    // minibatch; the leader takes the pair's first tile, the other CTA the
-    // second, and pair u's tiles sit at walk positions 2u and 2u + 1
+    // tiles of one expert, or an expert's odd last tile as a solo pair),
+    // ring_rows / 256 of them per minibatch; the leader takes the unit's
+    // first tile, the other CTA the second (idle in a solo pair), and unit
+    // u's tiles sit at walk positions 2u and 2u + 1
     int type, u, n;
     decode_ring_n(p, w, p.hdr[kHdrPairs], p.ring_rows / (2 * kTileRows), type, u, n);
     const int code = p.pair_m0[u];

@@ -194,11 +194,14 @@ __global__ void __launch_bounds__(1024) pair_table_kernel(const int32_t* __restr
   if (threadIdx.x == 0) hdr[kHdrPairs] = carry;
 }
 
-// Split of the row tiles for CTA pairs with no idle CTA: each expert's
-// first 2 * floor(t / 2) tiles (t = its padded tiles) are taken two at a
-// time as pairs, pair_m0[j] = 2 * (first tile of pair j); an odd last tile
-// goes to the list of single tiles, single_list[q] = tile.  Both lists are
-// in increasing tile order.  One block; integer work, exact.
+// Split of the forward ring's tiles between a CTA-pair launch and a
+// single-CTA launch, every expert wholly in one of them (its weights then
+// stream from DRAM in one launch only).  An expert with t padded tiles goes
+// to the pairs when t is even, or odd and at least 5 (its last tile is then
+// a solo pair, an idle CTA for one tile in t + 1); experts of 1 or 3 tiles
+// run on single CTAs, where a solo would cost more than the pair saves.
+// pair_m0[j] = 2 * (first tile of unit j) + solo, single_list[q] = tile,
+// both in increasing tile order.  One block; integer work, exact.
 __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __restrict__ tile_expert,
                                                            const int32_t* __restrict__ poff, int32_t* __restrict__ hdr,
                                                            int32_t* __restrict__ pair_m0,
@@ -209,19 +212,21 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
   int carry_p = 0, carry_s = 0;
   for (int base = 0; base < U; base += 1024) {
     const int m = base + threadIdx.x;
-    int head = 0, single = 0;
+    int head = 0, solo = 0, single = 0;
     if (m < U) {
       const int e = tile_expert[m];
       const int first = poff[e] / kTileRows;
       const int t = (poff[e + 1] - poff[e]) / kTileRows;
       const int j = m - first;
-      head = (j < (t & ~1)) && !(j & 1);
-      single = (t & 1) && j == t - 1;
+      const bool paired = t >= 2 && (!(t & 1) || t >= 5);
+      head = paired && !(j & 1);
+      solo = head && j == t - 1;
+      single = !paired;
     }
     const int pp = carry_p + block_exclusive_scan(head, warp_tot, &tot);
     const int np = tot;
     const int ps = carry_s + block_exclusive_scan(single, warp_tot, &tot);
-    if (head) pair_m0[pp] = 2 * m;
+    if (head) pair_m0[pp] = 2 * m + solo;
     if (single) single_list[ps] = m;
     carry_p += np;
     carry_s += tot;
