@@ -339,10 +339,20 @@ void set_pair_table(GemmParams& g, const WsLayout& L, uint8_t* ws) {
 // A row-tiled launch on CTA pairs (pair_maps: weight boxes of 128 rows,
 // each CTA's half of the tile), else -- without pairs, or without clusters
 // of two on the device -- one CTA per tile (maps: boxes of bn rows).
+// With pairs the split table of launch_split_table decides: its pair units
+// run on CTA pairs, then its single-tile list on single CTAs (tile counter
+// `single_counter`), every expert wholly in one of the two launches.
 cudaError_t launch_rows(int mode, bool pairs, const TmapSet& pair_maps, const TmapSet& maps, const GemmParams& q,
-                        int grid, cudaStream_t st) {
+                        int grid, const WsLayout& L, uint8_t* ws, int single_counter, cudaStream_t st) {
   if (pairs) {
     const cudaError_t e = launch_gemm_pair(mode, pair_maps, q, grid, st);
+    if (e == cudaSuccess) {
+      GemmParams qs = q;
+      qs.ring_list = reinterpret_cast<const int32_t*>(ws + L.pair_mb);
+      qs.ring_count_word = kHdrSingles;
+      qs.counter = single_counter;
+      return launch_gemm(mode, maps, qs, grid, st);
+    }
     if (e != cudaErrorNotSupported) return e;
     (void)cudaGetLastError();
   }
@@ -1007,10 +1017,10 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 0;
     {
-      Phase ph(MOK_PHASE_BWD_DA, st, (pairs_da || pairs_dx) ? 2 : 1);
-      if (pairs_da || pairs_dx) MOK_CUDA(launch_pair_table(L, w, st));
+      Phase ph(MOK_PHASE_BWD_DA, st, 1 + (pairs_da || pairs_dx ? 1 : 0) + (pairs_da ? 1 : 0));
+      if (pairs_da || pairs_dx) MOK_CUDA(launch_split_table(L, w, st));
       if (pairs_da) set_pair_table(q, L, w);
-      MOK_CUDA(launch_rows(GM_BWD_DA, pairs_da, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+      MOK_CUDA(launch_rows(GM_BWD_DA, pairs_da, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), L, w, 8, st));
     }
     Phase ph(MOK_PHASE_BWD_DS, st, 1);
     MOK_CUDA(launch_ds_reduce(s, L, w, dscores, q.n_tiles, st));
@@ -1034,8 +1044,8 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.counter = 1;
     if (pairs_dx) set_pair_table(q, L, w);
     {
-      Phase ph(MOK_PHASE_BWD_DX, st, 1);
-      MOK_CUDA(launch_rows(GM_BWD_DX, pairs_dx, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
+      Phase ph(MOK_PHASE_BWD_DX, st, pairs_dx ? 2 : 1);
+      MOK_CUDA(launch_rows(GM_BWD_DX, pairs_dx, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), L, w, 9, st));
     }
     Phase ph(MOK_PHASE_BWD_DX_COMBINE, st, 1);
     MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));

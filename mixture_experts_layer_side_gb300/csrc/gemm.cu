@@ -110,6 +110,8 @@ __device__ int count_items(const GemmParams& p) {
   } else if constexpr (MODE == GM_FWD_RING) {
     return p.hdr[p.ring_count_word] * (p.g1_tiles + p.n_tiles);
   } else {
+    // a launch over a tile list (the single tiles of a split)
+    if (p.ring_list) return p.hdr[p.ring_count_word] * p.n_tiles;
     int end = min(p.m_tile_end, used_tiles(p));
     if (p.replay_keep > 0) {
       // GEMM1 recomputed in the backward: every minibatch but the last
@@ -275,7 +277,7 @@ __device__ Item decode(const GemmParams& p, const Ctl* ctl, int w) {
       decode_ring_n(p, w, p.hdr[p.ring_count_word], p.ring_rows / kTileRows, type, rp, n);
       m = p.ring_list ? p.ring_list[rp] : rp;
     } else {
-      m = p.m_tile_begin + w / p.n_tiles;
+      m = p.ring_list ? p.ring_list[w / p.n_tiles] : p.m_tile_begin + w / p.n_tiles;
       n = w % p.n_tiles;
       rp = m;
     }

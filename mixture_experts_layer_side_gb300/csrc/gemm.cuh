@@ -133,7 +133,7 @@ cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, i
 // through one cta_group::2 MMA: the weight-gradient GEMMs (GM_WG13 / GM_WG2,
 // token-sorted operands, an even number of 128-row M tiles, bn = 256), the
 // row-tiled backward GEMMs (GM_BWD_DA with token-sorted dout, GM_BWD_DX;
-// bn = 256, the pair table of launch_pair_table, weight maps with 128-row
+// bn = 256, the pair units of launch_split_table, weight maps with 128-row
 // boxes) and the forward ring (GM_FWD_RING with a token-sorted copy of x,
 // bn = 256, over the pairs of launch_split_table, an even number of tiles per
 // minibatch).  Returns cudaErrorNotSupported when the device cannot hold a

@@ -23,8 +23,8 @@ constexpr int kHdrError = 0;
 constexpr int kHdrPaddedRows = 1;
 constexpr int kHdrTiles = 2;
 constexpr int kHdrAbort = 3;       // launch-wide abort word (cleared per call)
-constexpr int kHdrPairs = 4;       // CTA-pair tiles of the pair table (see launch_pair_table, launch_split_table)
-constexpr int kHdrSingles = 11;    // single tiles of the forward ring's split (see launch_split_table)
+constexpr int kHdrPairs = 4;       // CTA-pair units of the split table (see launch_split_table)
+constexpr int kHdrSingles = 11;    // single tiles of the split table (see launch_split_table)
 // single-launch forward: completed schedule items (count, scan, place) and
 // GEMM2 epilogue warps that stored their rows of y
 constexpr int kHdrCountDone = 5;
@@ -58,8 +58,8 @@ struct WsLayout {
   size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x (the forward ring reads it; then dW1|dW3),
                       // in MXFP8 also dout (dW2)
   size_t sorted2;     // bf16 [pad_capacity, H]: BF16 token-sorted dout (dA', dW2)
-  size_t pair_m0;     // int32 [tile_capacity]: CTA-pair tiles of dA' / dX / the ring (first M tile * 2 + solo)
-  size_t pair_mb;     // int32 [tile_capacity + 2]: forward ring, the list of single (odd last) tiles
+  size_t pair_m0;     // int32 [tile_capacity]: CTA-pair units of dA' / dX / the ring (first M tile * 2 + solo)
+  size_t pair_mb;     // int32 [tile_capacity + 2]: the list of tiles those launches run on single CTAs
   // MXFP8 operand copies
   size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
   size_t xq_sorted;   // those codes in padded-row order (GEMM1 / dA' A operand): u8 [pad_capacity, H]
@@ -85,9 +85,8 @@ bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ptr
 // Launchers (return a CUDA error code).
 cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, const int32_t* idx,
                             cudaStream_t st);
-cudaError_t launch_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
-// the forward ring's split: pairs of an expert's tiles (pair_m0, header word
-// kHdrPairs) and the odd last tiles (pair_mb as the single-tile list, word kHdrSingles)
+// the row tiles' split (forward ring, dA', dX): CTA-pair units (pair_m0,
+// header word kHdrPairs) and single tiles (pair_mb as the list, word kHdrSingles)
 cudaError_t launch_split_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
 cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* yk,
                            const float* scores, __nv_bfloat16* out, cudaStream_t st);

@@ -168,34 +168,8 @@ __global__ void __launch_bounds__(kPlaceWarps * 32)
   }
 }
 
-// CTA-pair table of the row-tiled backward GEMMs: the tiles of each expert
-// are taken two at a time from its first; a last tile without a partner is
-// a solo pair, whose second CTA loads valid rows but stores nothing.  One
-// block; integer work, exact.
-__global__ void __launch_bounds__(1024) pair_table_kernel(const int32_t* __restrict__ tile_expert,
-                                                          const int32_t* __restrict__ poff, int32_t* __restrict__ hdr,
-                                                          int32_t* __restrict__ pair_m0) {
-  __shared__ int warp_tot[32];
-  __shared__ int tot;
-  const int U = hdr[kHdrTiles];
-  int carry = 0;
-  for (int base = 0; base < U; base += 1024) {
-    const int m = base + threadIdx.x;
-    int head = 0, solo = 0;
-    if (m < U) {
-      const int e = tile_expert[m];
-      head = ((m - poff[e] / kTileRows) & 1) == 0;
-      solo = head && (m + 1 >= U || tile_expert[m + 1] != e);
-    }
-    const int pos = carry + block_exclusive_scan(head, warp_tot, &tot);
-    if (head) pair_m0[pos] = 2 * m + solo;
-    carry += tot;
-  }
-  if (threadIdx.x == 0) hdr[kHdrPairs] = carry;
-}
-
-// Split of the forward ring's tiles between a CTA-pair launch and a
-// single-CTA launch, every expert wholly in one of them (its weights then
+// Split of the row tiles (forward ring, dA', dX) between a CTA-pair launch
+// and a single-CTA launch, every expert wholly in one of them (its weights then
 // stream from DRAM in one launch only).  An expert with t padded tiles goes
 // to the pairs when t is even, or odd and at least 5 (its last tile is then
 // a solo pair, an idle CTA for one tile in t + 1); experts of 1 or 3 tiles
@@ -255,12 +229,6 @@ cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, 
   sched_place<<<blocks, kPlaceWarps * 32, smem, st>>>(idx, R, E, nchunks, P(L.chunk_base), P(L.offsets),
                                                       P(L.padded_offsets), P(L.perm), P(L.inv_perm),
                                                       P(L.pad_perm), P(L.pad_inv));
-  return cudaGetLastError();
-}
-
-cudaError_t launch_pair_table(const WsLayout& L, uint8_t* ws, cudaStream_t st) {
-  auto P = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
-  pair_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0));
   return cudaGetLastError();
 }
 
