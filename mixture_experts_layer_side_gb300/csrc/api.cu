@@ -106,7 +106,10 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   L.tile_expert = take(L.tile_capacity * 4);
   L.chunk_hist = take(L.nchunks * s.E * 4);
   L.chunk_base = take(L.nchunks * s.E * 4);
-  L.ring_flags = take(2 * L.tile_capacity * 4);
+  // ring flags: two halves (rows published, rows consumed) of 2 *
+  // tile_capacity walk positions each -- a CTA-pair ring's walk has two
+  // positions per unit, a solo unit's second one empty
+  L.ring_flags = take(4 * L.tile_capacity * 4);
   L.ring = take((size_t)L.ring_slots * M * I * 2);
   L.yk = take((size_t)R * H * 2);
   L.dhu = take(P * 2 * I * 2);
@@ -646,7 +649,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   MOK_TRY(reset_counters(w, L, st));
-  MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 2 * L.tile_capacity * 4, st));
+  MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 4 * L.tile_capacity * 4, st));
 
   const int M = L.minibatch_rows, S = L.ring_slots;
   const int bn2 = (s.H % 256 == 0) ? 256 : 128;
@@ -704,7 +707,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.bn = bn2;
     g.n_tiles = s.H / bn2;
     g.g1_tiles = s.I / 128;
-    g.m_tiles = (int)L.tile_capacity;
+    g.m_tiles = 2 * (int)L.tile_capacity;  // ring: where the consumed half of the flags starts
     g.counter = 0;
     {
       Phase ph(MOK_PHASE_FWD_GEMM, st, 1);
@@ -743,7 +746,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.bn = bn2;
     g.n_tiles = s.H / bn2;
     g.g1_tiles = s.I / 128;
-    g.m_tiles = (int)L.tile_capacity;
+    g.m_tiles = 2 * (int)L.tile_capacity;  // ring: where the consumed half of the flags starts
     g.counter = 0;
     const int grid = gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles));
     bool launched = false;
@@ -774,7 +777,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       const cudaError_t e = launch_gemm_pair(GM_FWD_RING, sm, gp, grid, st);
       if (e == cudaSuccess) {
         // the odd last tiles: a fresh ring walk (flags and tile counter)
-        MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 2 * L.tile_capacity * 4, st));
+        MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 4 * L.tile_capacity * 4, st));
         GemmParams gs = g;
         gs.fwd_sorted = 1;
         gs.ring_list = reinterpret_cast<const int32_t*>(w + L.pair_mb);
@@ -862,7 +865,7 @@ mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void
   uint8_t* w = static_cast<uint8_t*>(ws);
   // the whole header (error word, schedule totals, item counters) and the ring flags
   MOK_CUDA(cudaMemsetAsync(w + L.header, 0, kHeaderWords * 4, st));
-  MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 2 * L.tile_capacity * 4, st));
+  MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 4 * L.tile_capacity * 4, st));
   const int M = L.minibatch_rows, S = L.ring_slots;
   const int bn2 = (s.H % 256 == 0) ? 256 : 128;
   auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(w + off); };
@@ -901,7 +904,7 @@ mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void
   g.bn = bn2;
   g.n_tiles = s.H / bn2;
   g.g1_tiles = s.I / 128;
-  g.m_tiles = (int)L.tile_capacity;
+  g.m_tiles = 2 * (int)L.tile_capacity;  // ring: where the consumed half of the flags starts
   g.counter = 0;
   Phase ph(MOK_PHASE_FWD_FUSED, st, 1);
   MOK_CUDA(launch_gemm(GM_FWD_FUSED, maps, g, gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles)), st));

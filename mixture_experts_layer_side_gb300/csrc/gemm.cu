@@ -1893,10 +1893,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_arrive(&ctl->tempty[buf]);
         }
       };
-      if (is_ring<MODE>() && it.type == GM_FWD2 && !it.idle && warp == 2 && lane == 0) {
+      if (is_ring<MODE>() && it.type == GM_FWD2 && warp == 2 && lane == 0) {
         // the accumulator is complete, so every load of this tile's ring
-        // rows has landed: release the rows for reuse
-        red_release_gpu_add(&p.ring_flags[p.m_tiles + it.rp], 1u);
+        // rows has landed: release the rows for reuse.  The idle CTA of a
+        // solo pair releases its own walk position, 2u + 1 (its item names
+        // the leader's, 2u): no tile writes or reads that position's rows,
+        // but the GEMM1 that reuses its slot a ring later waits on it.
+        red_release_gpu_add(&p.ring_flags[p.m_tiles + it.rp + (it.idle ? 1 : 0)], 1u);
       }
       bool ok = true;
       if (is_ring<MODE>() && it.type == GM_FWD1 && !it.idle) {

@@ -58,7 +58,7 @@ struct GemmParams {
   int replay_keep;         // GEMM1 launch: stop before the last replay_keep minibatches
   __nv_bfloat16* ring;     // [ring_slots * ring_rows, I]
   int ring_rows, ring_slots;
-  uint32_t* ring_flags;    // [2 * tile_capacity]
+  uint32_t* ring_flags;    // [4 * tile_capacity]
   __nv_bfloat16* yk;       // [R, H]
   __nv_bfloat16* dhu;      // [pad, 2I]
   __nv_bfloat16* as;       // [pad, I]
@@ -121,9 +121,10 @@ struct GemmParams {
   uint8_t* ring_sf;           // GEMM1 epilogue: scales of a, tiled [ring rows/128][I/128][512 B]
   uint8_t* dhu_q;             // dA' epilogue: dh|du codes [pad, 2I] ...
   uint8_t* dhu_sf;            // ... and scales [pad, 2I/32]
-  // Ring launch: m_tiles holds the tile capacity; ring_flags[m] counts the
-  // epilogue warps (4 per column tile) that published GEMM1 rows of tile m,
-  // ring_flags[m_tiles + m] counts the GEMM2 column tiles that consumed them.
+  // Ring launch: m_tiles holds twice the tile capacity (the walk positions'
+  // bound); ring_flags[q] counts the epilogue warps (4 per column tile) that
+  // published GEMM1 rows of walk position q, ring_flags[m_tiles + q] the
+  // GEMM2 column tiles that consumed them.
 };
 
 size_t gemm_smem_bytes();

@@ -47,7 +47,7 @@ struct WsLayout {
   size_t header, counts, offsets, padded_offsets, perm, inv_perm, pad_perm, pad_inv, tile_expert;
   size_t chunk_hist, chunk_base;
   // forward
-  size_t ring_flags;  // uint32 [2 * tile_capacity]: GEMM1 / GEMM2 tiles done per M tile
+  size_t ring_flags;  // uint32 [4 * tile_capacity]: GEMM1 / GEMM2 tiles done per walk position
   size_t ring;        // bf16 [ring_slots * minibatch_rows, I]  (MXFP8: e4m3 codes)
   size_t ring_sf;     // MXFP8: u8 scales of the ring rows, tiled [ring rows/128][I/128][512 B]
   size_t yk;          // bf16 [R, H]: expert outputs (forward), dX parts (backward)
