@@ -105,13 +105,12 @@ typedef struct {
  *                 and dX GEMMs run one CTA per 128-row tile instead of
  *                 clusters of two CTAs sharing two tiles of one expert.
  *                 Bit 5 (MOK_DEBUG_SINGLE_CTA_RING): the BF16 forward ring
- *                 runs every tile on one CTA, in one launch.  By default it
- *                 runs in two launches, every expert wholly in one: experts
- *                 with an even number t of 128-row tiles, or t >= 5, on
- *                 clusters of two CTAs (two tiles of one expert per 256 x 256
- *                 tile; an odd last tile leaves one CTA idle), then experts
- *                 of 1 or 3 tiles on single CTAs; with replay = 1 it keeps
- *                 the one launch.
+ *                 runs every tile on one CTA, in one launch.  By default
+ *                 (T >= 1024, replay = 0) it runs in two launches, every
+ *                 expert wholly in one: experts of at least 8 tiles of 128
+ *                 rows on clusters of two CTAs (two tiles of one expert per
+ *                 256 x 256 tile; an odd last tile leaves one CTA idle), then
+ *                 the others on single CTAs.
  *                 Both forms read a token-sorted copy of x with plain TMA.
  *                 Bit 6 (MOK_DEBUG_GATHER_X_RING): the single-CTA ring
  *                 gathers token rows of x (MXFP8: of x's E4M3 codes) in its

@@ -280,6 +280,12 @@ int gemm_grid(long items) {
   return (int)(items < sms ? items : sms);
 }
 
+// The forward ring puts experts of at least this many 128-row tiles on CTA
+// pairs, the others on single CTAs: a pair launch holding only a few short
+// experts is bound by its critical path (measured on the mid-sized and
+// Kimi-shaped workloads), and long experts leave few solo pairs.
+constexpr int kRingPairTiles = 8;
+
 // Experts with at least this many padded rows have their BF16 weight
 // gradients computed on CTA pairs (cta_group::2, one 256 x 256 tile per
 // pair): their long K loops are bound by operand delivery, which the pair
@@ -342,20 +348,12 @@ void set_pair_table(GemmParams& g, const WsLayout& L, uint8_t* ws) {
 // A row-tiled launch on CTA pairs (pair_maps: weight boxes of 128 rows,
 // each CTA's half of the tile), else -- without pairs, or without clusters
 // of two on the device -- one CTA per tile (maps: boxes of bn rows).
-// With pairs the split table of launch_split_table decides: its pair units
-// run on CTA pairs, then its single-tile list on single CTAs (tile counter
-// `single_counter`), every expert wholly in one of the two launches.
+// With pairs, the units of the split table (every expert's tiles two at a
+// time, built with min_pair_tiles = 1, so no single tiles) run on CTA pairs.
 cudaError_t launch_rows(int mode, bool pairs, const TmapSet& pair_maps, const TmapSet& maps, const GemmParams& q,
-                        int grid, const WsLayout& L, uint8_t* ws, int single_counter, cudaStream_t st) {
+                        int grid, cudaStream_t st) {
   if (pairs) {
     const cudaError_t e = launch_gemm_pair(mode, pair_maps, q, grid, st);
-    if (e == cudaSuccess) {
-      GemmParams qs = q;
-      qs.ring_list = reinterpret_cast<const int32_t*>(ws + L.pair_mb);
-      qs.ring_count_word = kHdrSingles;
-      qs.counter = single_counter;
-      return launch_gemm(mode, maps, qs, grid, st);
-    }
     if (e != cudaErrorNotSupported) return e;
     (void)cudaGetLastError();
   }
@@ -751,20 +749,22 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     const int grid = gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles));
     bool launched = false;
     // The ring in two launches (unless single CTAs are asked for, or the
-    // context must keep the minibatches in one order for replay): the
-    // experts with an even number of tiles, or five and more, on CTA pairs
-    // (two tiles of one expert per 256 x 256 tile, an even number of tiles
-    // per minibatch), those of one or three tiles on single CTAs; every
-    // expert in one launch, so its weights stream once.  Both read the
-    // token-sorted copy of x with plain TMA.
+    // context must keep the minibatches in one order for replay, or no
+    // expert can reach kRingPairTiles tiles): the experts of at least
+    // kRingPairTiles tiles on CTA pairs (two tiles of one expert per
+    // 256 x 256 tile, an even number of tiles per minibatch), the others on
+    // single CTAs; every expert in one launch, so its weights stream once.
+    // Both read the token-sorted copy of x with plain TMA.
     const int Mt_pair = (M / kTileRows) & ~1;
-    if (!(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING) && !cfg->replay && bn2 == 256 && Mt_pair >= 2) {
+    const bool big_expert_possible = (int64_t)s.T >= (int64_t)kRingPairTiles * kTileRows;
+    if (!(cfg->debug_flags & MOK_DEBUG_SINGLE_CTA_RING) && !cfg->replay && bn2 == 256 && Mt_pair >= 2 &&
+        big_expert_possible) {
       __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
       {
         Phase ph(MOK_PHASE_FWD_SORT, st, 2);
         MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
         MOK_CUDA(cudaMemsetAsync(sorted_x_flag, 1, 1, st));
-        MOK_CUDA(launch_split_table(L, w, st));
+        MOK_CUDA(launch_split_table(L, w, kRingPairTiles, st));
       }
       TmapSet sm = maps;
       if (!map2d(&sm.m[0], srt, s.H, (uint64_t)L.pad_capacity, 128)) return MOK_ERR_CUDA;
@@ -1020,10 +1020,12 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.m_tile_end = (int)L.tile_capacity;
     q.counter = 0;
     {
-      Phase ph(MOK_PHASE_BWD_DA, st, 1 + (pairs_da || pairs_dx ? 1 : 0) + (pairs_da ? 1 : 0));
-      if (pairs_da || pairs_dx) MOK_CUDA(launch_split_table(L, w, st));
+      Phase ph(MOK_PHASE_BWD_DA, st, (pairs_da || pairs_dx) ? 2 : 1);
+      // every expert on pairs (an odd last tile a solo pair): measured faster
+      // for dA' and dX than splitting the short experts off onto single CTAs
+      if (pairs_da || pairs_dx) MOK_CUDA(launch_split_table(L, w, 1, st));
       if (pairs_da) set_pair_table(q, L, w);
-      MOK_CUDA(launch_rows(GM_BWD_DA, pairs_da, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), L, w, 8, st));
+      MOK_CUDA(launch_rows(GM_BWD_DA, pairs_da, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
     }
     Phase ph(MOK_PHASE_BWD_DS, st, 1);
     MOK_CUDA(launch_ds_reduce(s, L, w, dscores, q.n_tiles, st));
@@ -1047,8 +1049,8 @@ mok_status mok_backward(const mok_shape* shape, const mok_config* cfg, mok_preci
     q.counter = 1;
     if (pairs_dx) set_pair_table(q, L, w);
     {
-      Phase ph(MOK_PHASE_BWD_DX, st, pairs_dx ? 2 : 1);
-      MOK_CUDA(launch_rows(GM_BWD_DX, pairs_dx, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), L, w, 9, st));
+      Phase ph(MOK_PHASE_BWD_DX, st, 1);
+      MOK_CUDA(launch_rows(GM_BWD_DX, pairs_dx, mp, m, q, gemm_grid(L.tile_capacity * q.n_tiles), st));
     }
     Phase ph(MOK_PHASE_BWD_DX_COMBINE, st, 1);
     MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));

@@ -87,7 +87,7 @@ cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, 
                             cudaStream_t st);
 // the row tiles' split (forward ring, dA', dX): CTA-pair units (pair_m0,
 // header word kHdrPairs) and single tiles (pair_mb as the list, word kHdrSingles)
-cudaError_t launch_split_table(const WsLayout& L, uint8_t* ws, cudaStream_t st);
+cudaError_t launch_split_table(const WsLayout& L, uint8_t* ws, int min_pair_tiles, cudaStream_t st);
 cudaError_t launch_combine(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* yk,
                            const float* scores, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_ds_reduce(const mok_shape& s, const WsLayout& L, const uint8_t* ws, float* ds, int n_parts,

@@ -169,17 +169,17 @@ __global__ void __launch_bounds__(kPlaceWarps * 32)
 }
 
 // Split of the row tiles (forward ring, dA', dX) between a CTA-pair launch
-// and a single-CTA launch, every expert wholly in one of them (its weights then
-// stream from DRAM in one launch only).  An expert with t padded tiles goes
-// to the pairs when t is even, or odd and at least 5 (its last tile is then
-// a solo pair, an idle CTA for one tile in t + 1); experts of 1 or 3 tiles
-// run on single CTAs, where a solo would cost more than the pair saves.
-// pair_m0[j] = 2 * (first tile of unit j) + solo, single_list[q] = tile,
-// both in increasing tile order.  One block; integer work, exact.
+// and a single-CTA launch, every expert wholly in one of them (its weights
+// then stream from DRAM in one launch only).  An expert with t >= min_pair
+// padded tiles goes to the pairs, taken two at a time from its first tile
+// (an odd last tile is a solo pair: one idle CTA for one tile in t + 1);
+// the others run on single CTAs.  pair_m0[j] = 2 * (first tile of unit j)
+// + solo, single_list[q] = tile, both in increasing tile order.  One block;
+// integer work, exact.
 __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __restrict__ tile_expert,
                                                            const int32_t* __restrict__ poff, int32_t* __restrict__ hdr,
                                                            int32_t* __restrict__ pair_m0,
-                                                           int32_t* __restrict__ single_list) {
+                                                           int32_t* __restrict__ single_list, int min_pair) {
   __shared__ int warp_tot[32];
   __shared__ int tot;
   const int U = hdr[kHdrTiles];
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(1024) split_table_kernel(const int32_t* __rest
       const int first = poff[e] / kTileRows;
       const int t = (poff[e + 1] - poff[e]) / kTileRows;
       const int j = m - first;
-      const bool paired = t >= 2 && (!(t & 1) || t >= 5);
+      const bool paired = t >= min_pair;
       head = paired && !(j & 1);
       solo = head && j == t - 1;
       single = !paired;
@@ -232,10 +232,10 @@ cudaError_t launch_schedule(const mok_shape& s, const WsLayout& L, uint8_t* ws, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_table(const WsLayout& L, uint8_t* ws, cudaStream_t st) {
+cudaError_t launch_split_table(const WsLayout& L, uint8_t* ws, int min_pair_tiles, cudaStream_t st) {
   auto P = [&](size_t off) { return reinterpret_cast<int32_t*>(ws + off); };
   split_table_kernel<<<1, 1024, 0, st>>>(P(L.tile_expert), P(L.padded_offsets), P(L.header), P(L.pair_m0),
-                                         P(L.pair_mb));
+                                         P(L.pair_mb), min_pair_tiles);
   return cudaGetLastError();
 }
 

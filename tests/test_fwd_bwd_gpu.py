@@ -150,6 +150,12 @@ def test_backward_row_gemm_cta_pairs_match_single_cta(shape, routing, kw):
     ((1000, 512, 256, 6, 3), "uniform", dict(minibatch_rows=640, ring_slots=2)),
     ((4096, 256, 256, 16, 4), "zipf", dict(replay=True, minibatch_rows=256, ring_slots=2)),
     ((1024, 4096, 256, 24, 4), "hot", {}),
+    # experts of 9 tiles: pair units with a solo each, whose empty walk
+    # positions a later minibatch's GEMM1 reuses (small minibatches, 2 slots)
+    ((2200, 256, 128, 4, 2), "uniform", dict(minibatch_rows=640, ring_slots=2)),
+    ((2200, 256, 128, 4, 2), "uniform", dict(minibatch_rows=384, ring_slots=3)),
+    # one expert far above 8 tiles, the rest on single CTAs
+    ((4096, 512, 256, 40, 2), "hot", dict(minibatch_rows=1024, ring_slots=2)),
 ])
 def test_forward_ring_cta_pairs_match_single_cta(shape, routing, kw):
     """The forward ring split in two launches (each expert's tiles two at a
