@@ -312,7 +312,9 @@ mok_status mok_gemm_bf16(int32_t M, int32_t N, int32_t K, const void* A, int32_t
  * phases; mok_trace_read synchronises on them and returns, per phase, the
  * summed duration in ms and the number of times the phase ran since the
  * last read, then forgets them.  This is the library's only host-side
- * global state; enable it from one thread at a time.
+ * global state; enable it from one thread at a time.  Independently of
+ * this, every call opens an NVTX range per phase ("mok fwd gemm", ...) on
+ * the calling host thread, around the launches it issues for that phase.
  */
 enum {
   MOK_PHASE_SCHEDULE = 0,      /* histogram, scan, placement */

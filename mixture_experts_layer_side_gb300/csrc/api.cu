@@ -10,6 +10,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "gemm.cuh"
 
 namespace mok {
@@ -157,10 +159,20 @@ std::vector<TraceRec> g_trace;
 
 // Records an event pair around one phase of a call (when tracing is on) and
 // counts the phase's kernel launches.
+// Names of the phases, for the NVTX ranges each call opens around them
+// (host-side ranges: they mark when the launches were issued; a profiler
+// that follows NVTX into the device shows the kernels under them).
+const char* const kPhaseNames[MOK_NUM_PHASES] = {
+    "mok schedule",  "mok fwd gemm",   "mok fwd combine", "mok bwd dA'",      "mok bwd ds",
+    "mok bwd dX",    "mok bwd dX combine", "mok bwd dW1|dW3", "mok bwd dW2",   "mok mxfp8 quant",
+    "mok bwd sort",  "mok router fwd", "mok router bwd",  "mok bwd replay",   "mok fwd fused",
+    "mok fwd sort"};
+
 class Phase {
  public:
   Phase(int phase, cudaStream_t st, int kernels) : st_(st) {
     g_launches += kernels;
+    nvtxRangePushA(phase >= 0 && phase < MOK_NUM_PHASES ? kPhaseNames[phase] : "mok");
     std::lock_guard<std::mutex> lk(g_trace_mu);
     if (!g_trace_on) return;
     rec_.phase = phase;
@@ -169,6 +181,7 @@ class Phase {
     on_ = true;
   }
   ~Phase() {
+    nvtxRangePop();
     if (!on_) return;
     cudaEventRecord(rec_.b, st_);
     std::lock_guard<std::mutex> lk(g_trace_mu);
