@@ -60,6 +60,8 @@ def parse_args_from(argv):
     ap.add_argument("--workload", default="dsv3")
     ap.add_argument("--minibatch-rows", type=int, default=0)
     ap.add_argument("--ring-slots", type=int, default=0)
+    ap.add_argument("--overlap-sms", type=int, default=0,
+                    help="SMs of the short experts' ring launch beside the pair launch (0: the library's rule)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # MXFP8 workloads timed after the headline one (default run only)
@@ -336,6 +338,7 @@ def workload_config(args, shape, routing, prec, layer=None):
         cfg["ring_slots"] = args.ring_slots or 4
         if args.debug_flags:
             cfg["debug_flags"] = args.debug_flags
+        cfg["overlap_sms"] = args.overlap_sms or "library rule"
         cfg["replay"] = bool(args.replay)
         cfg["fused_forward"] = bool(args.fused)
         cfg["ctx_bytes"] = int(layer.ctx.numel())
@@ -463,7 +466,7 @@ def run_mok(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     inp = make_inputs(shape, routing, seed=1000 + rank, device=dev)
     layer = MoKLayer(shape, precision=prec, minibatch_rows=args.minibatch_rows, ring_slots=args.ring_slots,
-                     debug_flags=args.debug_flags, replay=args.replay, device=dev)
+                     debug_flags=args.debug_flags, replay=args.replay, overlap_sms=args.overlap_sms, device=dev)
     out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
     grads = layer.alloc_grads()
     stream = torch.cuda.current_stream()

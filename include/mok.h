@@ -117,6 +117,9 @@ typedef struct {
  *                 load path instead of reading a token-sorted copy with
  *                 plain TMA (in BF16 the backward's dW1|dW3 then sorts x
  *                 itself).
+ *                 Bit 7 (MOK_DEBUG_NO_OVERLAP): no two launches overlap (see
+ *                 overlap_sms): the forward ring's two launches run one
+ *                 after the other.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1: it holds [h|u] of the last ring_slots minibatches
@@ -130,6 +133,18 @@ typedef struct {
  *                 W1 and W3 then each point to TWO consecutive mok_mx, the
  *                 backward orientation (along I) followed by the forward
  *                 one (along H).
+ * overlap_sms     SMs given to the first launch of the overlapped pair, or
+ *                 0 for the default rule.  In the BF16 forward with the ring
+ *                 in two launches, the single-CTA launch of the short
+ *                 experts (bound by streaming their weights) and the
+ *                 CTA-pair launch of the long ones overlap on the caller's
+ *                 stream (programmatic dependent launch: the first lets the
+ *                 second start at once on the SMs it leaves free; the second
+ *                 takes each SM the first leaves and waits for it before it
+ *                 ends).  By default the first keeps the share of the SMs
+ *                 that its tiles make of both launches' tiles (a pair tile
+ *                 counted at 4/5 of a single one), all of them when there is
+ *                 no pair.  Must be >= 0.
  */
 typedef struct {
   int32_t minibatch_rows;
@@ -138,6 +153,7 @@ typedef struct {
   int32_t comm_sms;
   int32_t debug_flags;
   int32_t replay;
+  int32_t overlap_sms;
 } mok_config;
 
 #define MOK_DEBUG_SKIP_RING_SIGNAL 1
@@ -147,6 +163,7 @@ typedef struct {
 #define MOK_DEBUG_SINGLE_CTA_ROWS 16
 #define MOK_DEBUG_SINGLE_CTA_RING 32
 #define MOK_DEBUG_GATHER_X_RING 64
+#define MOK_DEBUG_NO_OVERLAP 128
 
 /* MXFP8 tensor: E4M3 codes plus E8M0 scales (see mok_mxfp8_quantize). */
 typedef struct {

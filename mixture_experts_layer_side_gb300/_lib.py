@@ -25,6 +25,7 @@ MOK_DEBUG_SINGLE_CTA_WGRAD = 8
 MOK_DEBUG_SINGLE_CTA_ROWS = 16
 MOK_DEBUG_SINGLE_CTA_RING = 32
 MOK_DEBUG_GATHER_X_RING = 64
+MOK_DEBUG_NO_OVERLAP = 128
 
 STATUS = {0: "MOK_OK", 1: "MOK_ERR_INVALID_ARG", 2: "MOK_ERR_UNSUPPORTED", 3: "MOK_ERR_WORKSPACE_TOO_SMALL",
           4: "MOK_ERR_CUDA", 5: "MOK_ERR_BAD_INDEX", 6: "MOK_ERR_TIMEOUT"}
@@ -56,7 +57,7 @@ class MokShape(ctypes.Structure):
 class MokConfig(ctypes.Structure):
     _fields_ = [("minibatch_rows", ctypes.c_int32), ("ring_slots", ctypes.c_int32),
                 ("capacity_mult", ctypes.c_float), ("comm_sms", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-                ("replay", ctypes.c_int32)]
+                ("replay", ctypes.c_int32), ("overlap_sms", ctypes.c_int32)]
 
 
 class MokMx(ctypes.Structure):
@@ -150,8 +151,8 @@ def shape_of(T, H, I, E, k):
     return MokShape(T, H, I, E, k)
 
 
-def config(minibatch_rows=0, ring_slots=0, capacity_mult=0.0, comm_sms=0, debug_flags=0, replay=0):
-    return MokConfig(minibatch_rows, ring_slots, capacity_mult, comm_sms, debug_flags, replay)
+def config(minibatch_rows=0, ring_slots=0, capacity_mult=0.0, comm_sms=0, debug_flags=0, replay=0, overlap_sms=0):
+    return MokConfig(minibatch_rows, ring_slots, capacity_mult, comm_sms, debug_flags, replay, overlap_sms)
 
 
 def mx(q, scale):

@@ -113,6 +113,10 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   // positions per unit, a solo unit's second one empty
   L.ring_flags = take(4 * L.tile_capacity * 4);
   L.ring = take((size_t)L.ring_slots * M * I * 2);
+  if (prec == MOK_BF16) {
+    L.ring_flags2 = take(4 * L.tile_capacity * 4);
+    L.ring2 = take((size_t)L.ring_slots * M * I * 2);
+  }
   L.yk = take((size_t)R * H * 2);
   L.dhu = take(P * 2 * I * 2);
   L.as = take(P * I * 2);
@@ -218,6 +222,7 @@ mok_status check_config(const mok_config* c) {
   if (c->ring_slots < 0 || c->ring_slots == 1) return MOK_ERR_INVALID_ARG;
   if (!(c->capacity_mult == 0.0f || c->capacity_mult >= 1.0f)) return MOK_ERR_INVALID_ARG;
   if (c->replay != 0 && c->replay != 1) return MOK_ERR_INVALID_ARG;
+  if (c->overlap_sms < 0) return MOK_ERR_INVALID_ARG;
   return MOK_OK;
 }
 
@@ -349,6 +354,22 @@ void base_params(GemmParams& g, const mok_shape& s, const WsLayout& L, uint8_t* 
   g.wg_rows_min = 0;
   g.wg_rows_max = INT_MAX;
   g.ring_count_word = kHdrTiles;  // a ring launch walks every tile unless given a list
+}
+
+// Whether launches may overlap (programmatic dependent launch).
+bool overlap(const mok_config& c) { return (c.debug_flags & MOK_DEBUG_NO_OVERLAP) == 0; }
+
+// Whether the device holds a cluster of two GEMM CTAs (the pair launches).
+bool pair_grid_available() {
+  static int device = -1;
+  static bool ok = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev != device) {
+    ok = gemm_pair_capacity() >= 2;
+    device = dev;
+  }
+  return ok;
 }
 
 // Whether the BF16 backward's dA' and dX run on CTA pairs.
@@ -661,6 +682,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   uint8_t* w = static_cast<uint8_t*>(ws);
   MOK_TRY(reset_counters(w, L, st));
   MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 4 * L.tile_capacity * 4, st));
+  if (prec == MOK_BF16) MOK_CUDA(cudaMemsetAsync(w + L.ring_flags2, 0, 4 * L.tile_capacity * 4, st));
 
   const int M = L.minibatch_rows, S = L.ring_slots;
   const int bn2 = (s.H % 256 == 0) ? 256 : 128;
@@ -786,20 +808,37 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       gp.pair_m0 = reinterpret_cast<const int32_t*>(w + L.pair_m0);
       gp.ring_count_word = kHdrPairs;
       gp.ring_rows = Mt_pair * kTileRows;
+      // the short experts' tiles: a ring walk of their own (ring, flags and
+      // tile counter), on single CTAs
+      GemmParams gs = g;
+      gs.fwd_sorted = 1;
+      gs.ring_list = reinterpret_cast<const int32_t*>(w + L.pair_mb);
+      gs.ring_count_word = kHdrSingles;
+      gs.counter = 7;
+      gs.ring = reinterpret_cast<__nv_bfloat16*>(w + L.ring2);
+      gs.ring_flags = reinterpret_cast<uint32_t*>(w + L.ring_flags2);
+      TmapSet ss = sm;
+      if (!map2d(&ss.m[3], gs.ring, s.I, (uint64_t)S * M, 128)) return MOK_ERR_CUDA;
       Phase ph(MOK_PHASE_FWD_GEMM, st, 2);
-      const cudaError_t e = launch_gemm_pair(GM_FWD_RING, sm, gp, grid, st);
-      if (e == cudaSuccess) {
-        // the odd last tiles: a fresh ring walk (flags and tile counter)
-        MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 4 * L.tile_capacity * 4, st));
-        GemmParams gs = g;
-        gs.fwd_sorted = 1;
-        gs.ring_list = reinterpret_cast<const int32_t*>(w + L.pair_mb);
-        gs.ring_count_word = kHdrSingles;
-        gs.counter = 7;
-        MOK_CUDA(launch_gemm(GM_FWD_RING, sm, gs, grid, st));
+      if (overlap(*cfg) && pair_grid_available()) {
+        // the single-CTA launch first, on its share of the SMs; the pair
+        // launch starts beside it at once and takes each SM it leaves
+        gs.pdl_trigger = 1;
+        gs.active_ctas = cfg->overlap_sms > 0 ? cfg->overlap_sms : -1;
+        MOK_CUDA(launch_gemm(GM_FWD_RING, ss, gs, grid, st));
+        gp.pdl_launch = 1;
+        gp.pdl_wait_end = 1;
+        MOK_CUDA(launch_gemm_pair(GM_FWD_RING, sm, gp, grid, st));
         launched = true;
-      } else if (e != cudaErrorNotSupported) {
-        return MOK_ERR_CUDA;
+      }
+      const cudaError_t e = launched ? cudaSuccess : launch_gemm_pair(GM_FWD_RING, sm, gp, grid, st);
+      if (e != cudaSuccess && e != cudaErrorNotSupported) return MOK_ERR_CUDA;
+      if (launched) {
+        // overlapped above
+      } else if (e == cudaSuccess) {
+        // one after the other: the pair launch, then the short experts
+        MOK_CUDA(launch_gemm(GM_FWD_RING, ss, gs, grid, st));
+        launched = true;
       } else {
         (void)cudaGetLastError();  // no cluster of two fits: all tiles on single CTAs below
         GemmParams ga = g;

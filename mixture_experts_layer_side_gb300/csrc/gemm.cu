@@ -1169,7 +1169,6 @@ __device__ void zero_empty_experts(const GemmParams& p, const Ctl* ctl, int gw, 
   }
 }
 
-
 // ---------------------------------------------------------------- single-launch forward
 // The schedule items and the combine phase of GM_FWD_FUSED.  The four
 // gather warps (128 threads, named barrier 1) run the schedule items; they
@@ -1506,6 +1505,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // no gathered operand)
   const uint32_t queue_consumers = PAIR ? 10u : gather_in_pipe ? 9u : 5u;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  if (p.pdl_trigger) griddep_launch_dependents();
+  if constexpr (MODE == GM_FWD_RING && !PAIR) {
+    if (p.active_ctas != 0) {
+      int n = p.active_ctas;
+      if (n < 0) {
+        const long a = p.hdr[kHdrSingles], b = 2l * p.hdr[kHdrPairs];
+        n = b == 0 ? (int)gridDim.x : (int)((5 * a * gridDim.x + 5 * a + 4 * b - 1) / (5 * a + 4 * b));
+      }
+      if ((int)blockIdx.x >= (n > 0 ? n : 1)) return;  // before any barrier or TMEM use
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSt; ++i) {
@@ -1969,6 +1979,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     else
       tmem_dealloc(tmem, 512);
   }
+  if (p.pdl_wait_end) griddep_wait();
 }
 
 template <int MODE, bool MX>
@@ -1983,7 +1994,22 @@ cudaError_t launch_mode(const TmapSet& maps, const GemmParams& p, int grid, cuda
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  gemm_kernel<MODE, MX, false><<<grid, kGemmThreads, smem, st>>>(maps, p);
+  if (!p.pdl_launch) {
+    gemm_kernel<MODE, MX, false><<<grid, kGemmThreads, smem, st>>>(maps, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_kernel<MODE, MX, false>, maps, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -1999,11 +2025,13 @@ cudaError_t launch_pair_mode(const TmapSet& maps, const GemmParams& p, int grid,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -2022,12 +2050,37 @@ cudaError_t launch_pair_mode(const TmapSet& maps, const GemmParams& p, int grid,
   const int g = (grid & ~1) < pair_grid ? (grid & ~1) : pair_grid;
   if (g < 2) return cudaErrorNotSupported;
   cfg.gridDim = dim3((unsigned)g, 1, 1);
+  cfg.numAttrs = p.pdl_launch ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, gemm_kernel<MODE, false, true>, maps, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int gemm_pair_capacity() {
+  const size_t smem = gemm_smem_bytes();
+  if (cudaFuncSetAttribute(gemm_kernel<GM_FWD_RING, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel<GM_FWD_RING, false, true>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return 2 * clusters;
+}
 
 size_t gemm_smem_bytes() {
   return 1024 + kStages * (kAStage + kBStage) + ((sizeof(Ctl) + 127) / 128) * 128 + 4 * kOutStage +

@@ -88,6 +88,20 @@ struct GemmParams {
   const int32_t* ring_list;
   int ring_count_word;
   int fwd_sorted;          // GEMM1 reads a token-sorted copy of x (plain TMA) instead of gathering
+  // Overlapped launches (programmatic dependent launch, one stream): a
+  // memory-bound launch on a few SMs sets pdl_trigger, so the next launch
+  // (pdl_launch: launched with programmatic stream serialisation, reading
+  // nothing the first one writes) starts on the other SMs at once and takes
+  // each SM the first one leaves; pdl_wait_end makes that second launch wait
+  // for the first before it exits, so the stream's later launches see both.
+  int pdl_trigger;
+  int pdl_wait_end;
+  int pdl_launch;          // host side: the launch attribute
+  // single-CTA ring launch beside a pair launch: CTAs at or above this index
+  // leave at once (0: none leave; -1: the share of the grid that matches
+  // this launch's tiles, hdr[kHdrSingles], against the pair launch's,
+  // 2 * hdr[kHdrPairs], each pair tile counted at 4/5 of a single one)
+  int active_ctas;
   // single-launch forward (GM_FWD_FUSED): the schedule's input and arrays
   // (written by its schedule items), and the combine's output
   const int32_t* topk_idx;
@@ -128,6 +142,8 @@ struct GemmParams {
 };
 
 size_t gemm_smem_bytes();
+// CTAs of the pair launches the device holds at once (0: no cluster of two fits).
+int gemm_pair_capacity();
 cudaError_t launch_gemm(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, int grid, cudaStream_t st);
 // BF16 launches on clusters of two CTAs that share each 256 x 256 tile

@@ -50,6 +50,8 @@ struct WsLayout {
   size_t ring_flags;  // uint32 [4 * tile_capacity]: GEMM1 / GEMM2 tiles done per walk position
   size_t ring;        // bf16 [ring_slots * minibatch_rows, I]  (MXFP8: e4m3 codes)
   size_t ring_sf;     // MXFP8: u8 scales of the ring rows, tiled [ring rows/128][I/128][512 B]
+  size_t ring_flags2, ring2;  // BF16: the flags and ring of the single-CTA ring launch that runs
+                              // beside the CTA-pair one (same sizes as ring_flags, ring)
   size_t yk;          // bf16 [R, H]: expert outputs (forward), dX parts (backward)
   // backward
   size_t dhu;         // bf16 [pad_capacity, 2I]

@@ -46,11 +46,11 @@ def quantize_weights(W1, W3, W2, stream=None):
 
 class MoKLayer:
     def __init__(self, shape: Shape, precision="bf16", minibatch_rows=0, ring_slots=0, debug_flags=0,
-                 replay=False, device="cuda"):
+                 replay=False, overlap_sms=0, device="cuda"):
         self.shape = shape
         self.cshape = _lib.shape_of(shape.T, shape.H, shape.I, shape.E, shape.k)
         self.cfg = _lib.config(minibatch_rows=minibatch_rows, ring_slots=ring_slots, debug_flags=debug_flags,
-                               replay=int(bool(replay)))
+                               replay=int(bool(replay)), overlap_sms=overlap_sms)
         self.prec = PRECISIONS[precision]
         self.device = torch.device(device)
         ws_bytes = _lib.mok_workspace_size(self.cshape, self.cfg, self.prec)

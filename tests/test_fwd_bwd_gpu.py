@@ -173,6 +173,33 @@ def test_forward_ring_cta_pairs_match_single_cta(shape, routing, kw):
         assert torch.equal(g_p[k], g_s[k]) and torch.equal(g_t[k], g_s[k]), k
 
 
+@pytest.mark.parametrize("shape,routing,kw", [
+    # long experts on pairs, short ones beside them, empty experts
+    ((4096, 256, 256, 32, 2), "zipf", {}),
+    # experts of 9 tiles (pair units with solos), small minibatches
+    ((2200, 256, 128, 4, 2), "uniform", dict(minibatch_rows=640, ring_slots=2)),
+    # one hot expert on pairs beside many short ones; empty experts
+    ((4096, 512, 256, 40, 2), "hot", dict(minibatch_rows=1024, ring_slots=2)),
+    # no expert reaches 8 tiles: the short-expert launch holds every tile
+    ((1024, 256, 256, 16, 2), "uniform", {}),
+    # every expert long: the short-expert launch finds no tile
+    ((4096, 256, 128, 2, 1), "uniform", {}),
+])
+@pytest.mark.parametrize("overlap_sms", [0, 1, 7])
+def test_overlapped_launches_match_one_after_another(shape, routing, kw, overlap_sms):
+    """The short experts' single-CTA ring launch overlapping the CTA-pair
+    ring launch on one stream (programmatic dependent launch) -- with the
+    library's SM share and with 1 and 7 SMs for the first launch -- against
+    the two launches one after the other (MOK_DEBUG_NO_OVERLAP): bitwise
+    equal outputs, and the backward from each bitwise equal."""
+    require_gpu()
+    _, out_o, g_o = run_layer(shape, routing, 21, overlap_sms=overlap_sms, **kw)
+    _, out_n, g_n = run_layer(shape, routing, 21, debug_flags=128, **kw)
+    assert torch.equal(out_o, out_n)
+    for k in g_o:
+        assert torch.equal(g_o[k], g_n[k]), k
+
+
 def _run_with_idx(shape, idx, seed):
     from mixture_experts_layer_side_gb300.inputs import Shape, make_inputs
     from mixture_experts_layer_side_gb300.layer import MoKLayer
