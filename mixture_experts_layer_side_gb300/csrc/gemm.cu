@@ -487,8 +487,7 @@ __device__ __forceinline__ uint32_t mx_stage_bytes(const GemmParams& p, int type
     case GM_FWD2: return kAStage + bn * 128 + 512u + 512u * bchunks;
     case GM_BWD_DA: return bn * 128 + 512u * bchunks + 512u + (p.rows_sorted ? (uint32_t)kAStage : 0u);
     case GM_BWD_DX: return kAStage + bn * 128 + 512u * bchunks + 512u;
-    case GM_WG13: return kAStage + 2u * 16384u + 512u + 1024u;
-    default: return kAStage + bn * 128 + 512u + 512u * bchunks;  // GM_WG2
+    default: return kAStage + bn * 128 + 512u + 512u * bchunks;  // GM_WG13, GM_WG2
   }
 }
 
@@ -1498,7 +1497,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // copies) take the gather warps out of the stage pipeline; those warps
   // write the empty experts' zero gradients instead.
   const bool gather_in_pipe = kGather && !PAIR && !(MODE == GM_DENSE && MX) && !(kWgrad && (MX || p.wg_sorted)) &&
-                              !(MODE == GM_BWD_DA && p.rows_sorted) &&
+                              !(MODE == GM_BWD_DA && p.rows_sorted) && !(MX && MODE == GM_BWD_DX) &&
                               !((MODE == GM_FWD_RING || MODE == GM_FWD1) && p.fwd_sorted);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
@@ -1812,7 +1811,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         if (lane == 0) {
           // the gather threads wrote part of this stage with cp.async: order
           // those writes before the tensor core's (async-proxy) reads
-          if (gathered || MX) fence_proxy_async_shared();
+          if (gathered || (MX && gather_in_pipe)) fence_proxy_async_shared();
           const uint32_t a0 = smem_u32(sA + stage * kAStage), b0 = smem_u32(sB + stage * kBSt);
           if constexpr (MX) {
             // stage scales into TMEM (columns 256 + 16 * stage): A at +0
