@@ -130,8 +130,8 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
     L.xq = take((size_t)s.T * H);
     L.xsf = take((size_t)s.T * (H / 32));
     L.xq_sorted = take(P * H);
-    L.wsf1 = take((size_t)s.E * H * I / 32);
-    L.wsf3 = take((size_t)s.E * H * I / 32);
+    L.wsf1 = take(2 * (size_t)s.E * H * I / 32);
+    L.wsf3 = L.wsf1 + (size_t)s.E * H * I / 32;
     L.wsf2 = take((size_t)s.E * I * H / 32);
     L.dhuq = take(P * 2 * I);
     L.dhusf = take(P * (2 * I / 32));
@@ -437,8 +437,8 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
       Phase ph(MOK_PHASE_BWD_REPLAY, st, srt ? 6 : 5);
       MOK_CUDA(launch_replay_copy(s, L, w, static_cast<const __nv_bfloat16*>(ctx), g.dhu, st));
       MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(x), 1, s.T, s.H, 1, w + L.xq, w + L.xsf, st));
-      MOK_CUDA(launch_tile_scales(f1->scale, s.E, s.H / 32, s.I, w + L.wsf1, st));
-      MOK_CUDA(launch_tile_scales(f3->scale, s.E, s.H / 32, s.I, w + L.wsf3, st));
+      MOK_CUDA(launch_tile_scales(f1->scale, s.E, s.H / 32, s.I, w + L.wsf1, st, 1, 2, 0));
+      MOK_CUDA(launch_tile_scales(f3->scale, s.E, s.H / 32, s.I, w + L.wsf1, st, 1, 2, 1));
       MOK_CUDA(launch_tile_row_scales(w + L.xsf, s.H / 32, reinterpret_cast<const int32_t*>(w + L.pad_perm), s.k,
                                       rows_used, L.pad_capacity, w + L.sfa_rows_t, st));
       if (srt) MOK_CUDA(launch_gather_code_rows(s, L, w, w + L.xq, w + L.xq_sorted, st));
@@ -457,8 +457,7 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     q.gq_src = w + L.xq;
     q.fwd_sorted = srt ? 1 : 0;
     q.sfa_tiled = w + L.sfa_rows_t;
-    q.sfb_tiled0 = w + L.wsf1;
-    q.sfb_tiled1 = w + L.wsf3;
+    q.sfb_tiled0 = w + L.wsf1;  // W1 | W3 interleaved
     q.nmaps = 3;
     q.bn = 256;
     q.n_tiles = s.I / 128;
@@ -501,7 +500,7 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
       Phase ph(MOK_PHASE_QUANT, st, sorted_codes ? 3 : 2);
       MOK_CUDA(launch_tile_row_scales(w + L.xsf, s.H / 32, reinterpret_cast<const int32_t*>(w + L.pad_perm), s.k,
                                       rows_used, L.pad_capacity, w + L.sfa_rows_t, st));
-      MOK_CUDA(launch_tile_scales_rows(q2.scale, s.E, s.I, s.H / 32, w + L.wsf2, st));
+      MOK_CUDA(launch_tile_scales_rows(q2.scale, s.E, s.I, s.H / 32, w + L.wsf2, st, bn_i / 128, bn_i / 128, 0));
       if (sorted_codes) MOK_CUDA(launch_gather_code_rows(s, L, w, w + L.xq, w + L.xq_sorted, st));
     }
     q.sfa_tiled = w + L.sfa_rows_t;
@@ -535,8 +534,8 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
       Phase ph(MOK_PHASE_QUANT, st, 3);
       MOK_CUDA(launch_tile_row_scales(w + L.dhusf, 2 * s.I / 32, nullptr, 1, rows_used, L.pad_capacity,
                                       w + L.sfa_rows_t, st));
-      MOK_CUDA(launch_tile_scales_rows(q1.scale, s.E, s.H, s.I / 32, w + L.wsf1, st));
-      MOK_CUDA(launch_tile_scales_rows(q3.scale, s.E, s.H, s.I / 32, w + L.wsf3, st));
+      MOK_CUDA(launch_tile_scales_rows(q1.scale, s.E, s.H, s.I / 32, w + L.wsf1, st, bn_h / 128, bn_h / 128, 0));
+      MOK_CUDA(launch_tile_scales_rows(q3.scale, s.E, s.H, s.I / 32, w + L.wsf3, st, bn_h / 128, bn_h / 128, 0));
     }
     q.sfa_tiled = w + L.sfa_rows_t;
     q.sfb_tiled0 = w + L.wsf1;
@@ -694,9 +693,9 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
       // x along H; forward weight scales tiled for the N-major B operands
       Phase ph(MOK_PHASE_QUANT, st, 4);
       MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(x), 1, s.T, s.H, 1, w + L.xq, w + L.xsf, st));
-      MOK_CUDA(launch_tile_scales(q1.scale, s.E, s.H / 32, s.I, w + L.wsf1, st));
-      MOK_CUDA(launch_tile_scales(q3.scale, s.E, s.H / 32, s.I, w + L.wsf3, st));
-      MOK_CUDA(launch_tile_scales(q2.scale, s.E, s.I / 32, s.H, w + L.wsf2, st));
+      MOK_CUDA(launch_tile_scales(q1.scale, s.E, s.H / 32, s.I, w + L.wsf1, st, 1, 2, 0));
+      MOK_CUDA(launch_tile_scales(q3.scale, s.E, s.H / 32, s.I, w + L.wsf1, st, 1, 2, 1));
+      MOK_CUDA(launch_tile_scales(q2.scale, s.E, s.I / 32, s.H, w + L.wsf2, st, bn2 / 128, bn2 / 128, 0));
     }
     const bool sorted_codes = !(cfg->debug_flags & MOK_DEBUG_GATHER_X_RING);
     {
@@ -721,8 +720,7 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
     g.debug_flags = cfg->debug_flags;
     g.gq_src = w + L.xq;
     g.sfa_tiled = w + L.sfa_rows_t;
-    g.sfb_tiled0 = w + L.wsf1;
-    g.sfb_tiled1 = w + L.wsf3;
+    g.sfb_tiled0 = w + L.wsf1;  // W1 | W3 interleaved
     g.sfb_tiled2 = w + L.wsf2;
     TmapSet maps;
     memset(&maps, 0, sizeof(maps));
@@ -1311,9 +1309,9 @@ mok_status mok_gemm_mxfp8(int32_t M, int32_t N, int32_t K, const uint8_t* Aq, co
   else
     MOK_CUDA(launch_tile_scales_rows(Asf, 1, M, K / 32, sfa_t, st));
   if (b_mn_major)
-    MOK_CUDA(launch_tile_scales(Bsf, 1, K / 32, N, sfb_t, st));
+    MOK_CUDA(launch_tile_scales(Bsf, 1, K / 32, N, sfb_t, st, bn / 128, bn / 128, 0));
   else
-    MOK_CUDA(launch_tile_scales_rows(Bsf, 1, N, K / 32, sfb_t, st));
+    MOK_CUDA(launch_tile_scales_rows(Bsf, 1, N, K / 32, sfb_t, st, bn / 128, bn / 128, 0));
   const int kernels = 3;
   TmapSet m;
   memset(&m, 0, sizeof(m));

@@ -509,17 +509,17 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     } else {
       tma_load_2d(b, &mp.m[1], bar, kk * 128, it.n * bn);
     }
-    for (int c = 0; c < bn / 128; ++c)
-      bulk_load(sfb + c * 512, p.sfb_tiled0 + ((long)(it.n * (bn / 128) + c) * kgroups + kk) * 512, 512, bar);
+    // B's scales grouped per bn-wide N tile: one load
+    bulk_load(sfb, p.sfb_tiled0 + ((long)it.n * kgroups + kk) * (bn / 128) * 512, (bn / 128) * 512, bar);
   } else if (type == GM_FWD1) {
     const int hg = p.H / 128;
     // A: x's codes in padded-row order, when GEMM1 does not gather them
     if (p.fwd_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
     tma_load_3d(b, &mp.m[1], bar, it.n * 128, kk * 128, it.e);
     tma_load_3d(b + 16384, &mp.m[2], bar, it.n * 128, kk * 128, it.e);
+    // W1's and W3's scale blocks interleaved: one load
     const long blk = ((long)it.e * (p.I / 128) + it.n) * hg + kk;
-    bulk_load(sfb, p.sfb_tiled0 + blk * 512, 512, bar);
-    bulk_load(sfb + 512, p.sfb_tiled1 + blk * 512, 512, bar);
+    bulk_load(sfb, p.sfb_tiled0 + blk * 1024, 1024, bar);
     // A (gathered x rows): its scales pre-tiled in padded-row order
     bulk_load(sfa, p.sfa_tiled + ((long)it.m * hg + kk) * 512, 512, bar);
   } else if (type == GM_FWD2) {
@@ -528,11 +528,11 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     tma_load_2d(a, &mp.m[mslot], bar, kk * 128, ring_row(p, it.rp * kTileRows));
     // a's scales, tiled by the GEMM1 epilogue next to the ring codes
     bulk_load(sfa, p.ring_sf + ((long)(ring_row(p, it.rp * kTileRows) >> 7) * (p.I / 128) + kk) * 512, 512, bar);
-    for (int c = 0; c < bn / 128; ++c) {
-      tma_load_3d(b + c * 16384, &mp.m[wmap], bar, it.n * bn + c * 128, kk * 128, it.e);
-      const long blk = ((long)it.e * (p.H / 128) + it.n * (bn / 128) + c) * (p.I / 128) + kk;
-      bulk_load(sfb + c * 512, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * 512, 512, bar);
-    }
+    for (int c = 0; c < bn / 128; ++c) tma_load_3d(b + c * 16384, &mp.m[wmap], bar, it.n * bn + c * 128, kk * 128, it.e);
+    // W2's scales grouped per bn-wide N tile: one load
+    const long blk = ((long)it.e * (p.H / bn) + it.n) * (p.I / 128) + kk;
+    bulk_load(sfb, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * (bn / 128) * 512, (bn / 128) * 512,
+              bar);
   } else if (type == GM_BWD_DA) {
     // A: dout's codes in padded-row order, when dA' does not gather them;
     // B = W2 along H (K-major); its scales, and those of the dout rows,
@@ -540,10 +540,8 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     if (p.rows_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
     tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
     bulk_load(sfa, p.sfa_tiled + ((long)it.m * (p.H / 128) + kk) * 512, 512, bar);
-    for (int c = 0; c < bn / 128; ++c) {
-      const long blk = ((long)it.e * (p.I / 128) + it.n * (bn / 128) + c) * (p.H / 128) + kk;
-      bulk_load(sfb + c * 512, p.sfb_tiled0 + blk * 512, 512, bar);
-    }
+    const long blk = ((long)it.e * (p.I / bn) + it.n) * (p.H / 128) + kk;
+    bulk_load(sfb, p.sfb_tiled0 + blk * (bn / 128) * 512, (bn / 128) * 512, bar);
   } else if (type == GM_BWD_DX) {
     // B = W1 then W3 along I (K-major); scales pre-tiled likewise
     tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
@@ -551,10 +549,8 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     const int ki = p.I / 128;
     const int kb = kk < ki ? kk : kk - ki;
     tma_load_3d(b, &mp.m[kk < ki ? 1 : 2], bar, kb * 128, it.n * bn, it.e);
-    for (int c = 0; c < bn / 128; ++c) {
-      const long blk = ((long)it.e * (p.H / 128) + it.n * (bn / 128) + c) * ki + kb;
-      bulk_load(sfb + c * 512, (kk < ki ? p.sfb_tiled0 : p.sfb_tiled1) + blk * 512, 512, bar);
-    }
+    const long blk = ((long)it.e * (p.H / bn) + it.n) * ki + kb;
+    bulk_load(sfb, (kk < ki ? p.sfb_tiled0 : p.sfb_tiled1) + blk * (bn / 128) * 512, (bn / 128) * 512, bar);
   } else if (type == GM_WG13 || type == GM_WG2) {
     // token-sorted operands quantised along the routed rows (K), M/N-major
     const int cols_a = (type == GM_WG13) ? p.H : p.I;
@@ -562,10 +558,9 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     const int rb = it.row0 / 128 + kk;
     tma_load_2d(a, &mp.m[0], bar, it.m * 128, it.row0 + kk * 128);
     bulk_load(sfa, p.sfa_tiled + ((long)rb * (cols_a / 128) + it.m) * 512, 512, bar);
-    for (int c = 0; c < bn / 128; ++c) {
-      tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, it.row0 + kk * 128);
-      bulk_load(sfb + c * 512, p.sfb_tiled0 + ((long)rb * (cols_b / 128) + it.n * (bn / 128) + c) * 512, 512, bar);
-    }
+    for (int c = 0; c < bn / 128; ++c) tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, it.row0 + kk * 128);
+    // the bn / 128 column blocks of B's scales are adjacent: one load
+    bulk_load(sfb, p.sfb_tiled0 + ((long)rb * (cols_b / 128) + it.n * (bn / 128)) * 512, (bn / 128) * 512, bar);
   }
 }
 

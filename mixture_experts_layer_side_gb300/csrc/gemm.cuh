@@ -125,12 +125,14 @@ struct GemmParams {
   const uint8_t* sfb_rows0;   // B scales (W2 along H; W1 along I)
   const uint8_t* sfb_rows1;   // B scales, second weight (W3 along I)
   long sfb_ld;
-  // M/N-major operands: scales pre-tiled into 512-byte blocks
-  // [..][MN/128][K/128] (see mxfp8.cu), loaded by the TMA producer.
+  // Scales pre-tiled into 512-byte blocks per 128 M/N x 128 K (see
+  // mxfp8.cu), loaded by the TMA producer one bulk load per operand per
+  // stage: weights' blocks grouped per bn-wide N tile (GEMM1: W1's and W3's
+  // interleaved in sfb_tiled0), activations' per 128 rows.
   const uint8_t* sfa_tiled;
   const uint8_t* sfb_tiled0;
-  const uint8_t* sfb_tiled1;
-  const uint8_t* sfb_tiled2;  // W2 in the ring launch (W1, W3 use tiled0/1)
+  const uint8_t* sfb_tiled1;  // dX: W3 (W1 in tiled0)
+  const uint8_t* sfb_tiled2;  // W2 in the ring launch (W1 | W3 in tiled0)
   const uint8_t* gq_src;      // gathered E4M3 rows (x or dout codes) [T, H]
   uint8_t* ring_sf;           // GEMM1 epilogue: scales of a, tiled [ring rows/128][I/128][512 B]
   uint8_t* dhu_q;             // dA' epilogue: dh|du codes [pad, 2I] ...

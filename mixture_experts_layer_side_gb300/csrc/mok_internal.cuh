@@ -66,7 +66,8 @@ struct WsLayout {
   size_t xq, xsf;     // x (forward) or dout (backward) along H: u8 [T, H], [T, H/32]
   size_t xq_sorted;   // those codes in padded-row order (GEMM1 / dA' A operand): u8 [pad_capacity, H]
   size_t sfa_rows_t;  // the A operand's scales in padded-row order, tiled: [pad/128][max(H,2I)/128][512]
-  size_t wsf1, wsf3, wsf2;  // forward weight scales tiled for the GEMMs
+  size_t wsf1, wsf3, wsf2;  // weight scales tiled for the GEMMs; wsf3 = wsf1 + one weight's scales, so
+                            // [wsf1, wsf3 end) holds W1's and W3's blocks interleaved (GEMM1)
   size_t dhuq, dhusf; // dh|du quantised along I: u8 [pad, 2I], [pad, 2I/32]
   size_t wqa, wsfa;   // weight gradients: sorted x / dout along rows, [pad, H] + tiled scales
   size_t wqb, wsfb;   // weight gradients: dh|du / s*a along rows, [pad, 2I] + tiled scales
@@ -100,9 +101,14 @@ cudaError_t launch_gather_code_rows(const mok_shape& s, const WsLayout& L, const
 // skip (device, optional): the launch does nothing while *skip != 0
 cudaError_t launch_gather_rows(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
                                __nv_bfloat16* xg, cudaStream_t st, const int32_t* skip = nullptr);
-cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st);
+// MXFP8 weight scales tiled for the GEMMs' bulk loads (see mxfp8.cu):
+// [batch][N / (128 g)][K/128][s x 512 B], N block nb at slot slot + nb % g.
+// From plain scales blocked along K = rows ([batch][K/32][N]) or along each
+// row of a K-major operand ([batch][N][K/32]).
+cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st,
+                               int g = 1, int s = 1, int slot = 0);
 cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_count, uint8_t* out,
-                                    cudaStream_t st);
+                                    cudaStream_t st, int g = 1, int s = 1, int slot = 0);
 cudaError_t launch_tile_row_scales(const uint8_t* sf, int kb_count, const int32_t* pad_perm, int k,
                                    const int32_t* rows_used, long rows_cap, uint8_t* out, cudaStream_t st);
 cudaError_t launch_replay_copy(const mok_shape& s, const WsLayout& L, const uint8_t* ws,

@@ -90,10 +90,20 @@ __global__ void quant_colblocks(const __nv_bfloat16* __restrict__ src, int batch
 
 __device__ __forceinline__ int sf_block_offset(int mn, int kb) { return mx_sf_offset(mn, kb); }
 
-// Plain scales [batch][K/32][N] (blocks along K = rows) -> tiled
-// [batch][N/128][K/128][512 B] (one block per 128 N x 128 K tile).
+// Tiled scale layout of a weight: 512-byte blocks, one per 128 N x 128 K
+// tile, grouped so that one bulk load brings what one stage of a GEMM tile
+// needs: [batch][N / (128 g)][K/128][s blocks], the block of N block nb at
+// slot `slot + nb % g` of its group.  g = s = 1: one block per group; g = s
+// = 2: the two 128-wide N blocks of a 256-wide N tile side by side; g = 1,
+// s = 2, slot 0 / 1: two weights' blocks interleaved (W1 | W3).
+__device__ __forceinline__ long tiled_block(long b, int nb, int kg, int n_blocks, int kg_count, int g, int s,
+                                            int slot) {
+  return (((b * (n_blocks / g) + nb / g) * kg_count + kg) * s + slot + nb % g) * 512;
+}
+
+// Plain scales [batch][K/32][N] (blocks along K = rows) -> the tiled layout.
 __global__ void tile_scales_kernel(const uint8_t* __restrict__ sf, int batch, int kb_count, int N,
-                                   uint8_t* __restrict__ out) {
+                                   uint8_t* __restrict__ out, int g, int s, int slot) {
   const int kg_count = kb_count / 4;
   const long n_words = (long)batch * kg_count * N;  // one 4-byte word per (batch, k group, n)
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n_words; i += (long)gridDim.x * blockDim.x) {
@@ -104,16 +114,16 @@ __global__ void tile_scales_kernel(const uint8_t* __restrict__ sf, int batch, in
     const uint8_t* src = sf + (b * kb_count + (long)kg * 4) * N + n;
     const uint32_t w = (uint32_t)src[0] | ((uint32_t)src[N] << 8) | ((uint32_t)src[2L * N] << 16) |
                        ((uint32_t)src[3L * N] << 24);
-    uint8_t* blk = out + ((b * (N / 128) + n / 128) * kg_count + kg) * 512;
+    uint8_t* blk = out + tiled_block(b, n / 128, kg, N / 128, kg_count, g, s, slot);
     *reinterpret_cast<uint32_t*>(blk + sf_block_offset(n & 127, 0)) = w;
   }
 }
 
 // Plain scales of a K-major operand [batch][N][K/32] (blocks along each
-// row) -> the same tiled [batch][N/128][K/128][512 B] layout: the four
-// scale bytes of (n, 128-wide K group) are contiguous in the source.
+// row) -> the same tiled layout: the four scale bytes of (n, 128-wide K
+// group) are contiguous in the source.
 __global__ void tile_scales_rows_kernel(const uint8_t* __restrict__ sf, int batch, int N, int kb_count,
-                                        uint8_t* __restrict__ out) {
+                                        uint8_t* __restrict__ out, int g, int s, int slot) {
   const int kg_count = kb_count / 4;
   const long n_words = (long)batch * N * kg_count;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n_words; i += (long)gridDim.x * blockDim.x) {
@@ -122,7 +132,7 @@ __global__ void tile_scales_rows_kernel(const uint8_t* __restrict__ sf, int batc
     const int n = (int)(bn % N);
     const long b = bn / N;
     const uint32_t w = *reinterpret_cast<const uint32_t*>(sf + bn * kb_count + (long)kg * 4);
-    uint8_t* blk = out + ((b * (N / 128) + n / 128) * kg_count + kg) * 512;
+    uint8_t* blk = out + tiled_block(b, n / 128, kg, N / 128, kg_count, g, s, slot);
     *reinterpret_cast<uint32_t*>(blk + sf_block_offset(n & 127, 0)) = w;
   }
 }
@@ -185,22 +195,25 @@ __global__ void quant_rows_tiled_kernel(const __nv_bfloat16* __restrict__ src, c
 
 }  // namespace
 
-cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st) {
+cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st,
+                               int g, int s, int slot) {
+  if (g < 1 || s < g || slot + g > s || (N / 128) % g) return cudaErrorInvalidValue;
   const long words = (long)batch * (kb_count / 4) * N;
   long grid = (words + 255) / 256;
   const long cap = (long)device_sm_count() * 32;
   if (grid > cap) grid = cap;
-  tile_scales_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, kb_count, N, out);
+  tile_scales_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, kb_count, N, out, g, s, slot);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_count, uint8_t* out,
-                                    cudaStream_t st) {
+                                    cudaStream_t st, int g, int s, int slot) {
+  if (g < 1 || s < g || slot + g > s || (N / 128) % g) return cudaErrorInvalidValue;
   const long words = (long)batch * N * (kb_count / 4);
   long grid = (words + 255) / 256;
   const long cap = (long)device_sm_count() * 32;
   if (grid > cap) grid = cap;
-  tile_scales_rows_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, N, kb_count, out);
+  tile_scales_rows_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, N, kb_count, out, g, s, slot);
   return cudaGetLastError();
 }
 
