@@ -118,8 +118,8 @@ typedef struct {
  *                 plain TMA (in BF16 the backward's dW1|dW3 then sorts x
  *                 itself).
  *                 Bit 7 (MOK_DEBUG_NO_OVERLAP): no two launches overlap (see
- *                 overlap_sms): the forward ring's two launches run one
- *                 after the other.
+ *                 overlap_sms): the forward ring's pair launch runs first,
+ *                 then the single-CTA one.
  *                 Results are bitwise the same in every mode.
  * replay          0: the forward context holds [h|u] of every routed row.
  *                 1: it holds [h|u] of the last ring_slots minibatches
