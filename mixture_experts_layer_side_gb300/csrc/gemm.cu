@@ -52,6 +52,7 @@ namespace {
 struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t sfready[kMaxStages];  // MXFP8: the stage's scales are in TMEM (written by the gather warps)
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t qfull[kQueue];
@@ -1494,10 +1495,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const bool gather_in_pipe = kGather && !PAIR && !(MODE == GM_DENSE && MX) && !(kWgrad && (MX || p.wg_sorted)) &&
                               !(MODE == GM_BWD_DA && p.rows_sorted) && !(MX && MODE == GM_BWD_DX) &&
                               !((MODE == GM_FWD_RING || MODE == GM_FWD1) && p.fwd_sorted);
+  // MXFP8 launches whose gather warps copy nothing: those warps move each
+  // stage's scale blocks from shared memory into TMEM with tcgen05.st
+  // (replicated over the four lane quarters, the layout tcgen05.cp
+  // .32x128b.warpx4 makes), so the MMA thread issues only MMAs; a
+  // per-stage barrier tells it the scales are in place (dense core 2,036 ->
+  // 2,217 TFLOP/s at 8192^3, Kimi-shaped dX 2% faster).  Weight-gradient
+  // launches keep those warps for the empty experts' zero stores, and the
+  // ring keeps the copies in the MMA thread (the hand-off made it 3% slower:
+  // its MMAs more often wait on a stage that has just landed).
+  const bool sf_writer = MX && !gather_in_pipe && !kWgrad && !is_ring<MODE>();
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)
-  const uint32_t queue_consumers = PAIR ? 10u : gather_in_pipe ? 9u : 5u;
+  const uint32_t queue_consumers = PAIR ? 10u : (gather_in_pipe || sf_writer) ? 9u : 5u;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   if (p.pdl_trigger) griddep_launch_dependents();
   if constexpr (MODE == GM_FWD_RING && !PAIR) {
@@ -1517,6 +1528,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       // gather thread when the gather warps take part
       mbar_init(&ctl->full[i], gather_in_pipe ? 129u : 1u);
       mbar_init(&ctl->empty[i], 1);
+      mbar_init(&ctl->sfready[i], 4);  // the four gather warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->tfull[i], 1);
@@ -1772,6 +1784,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       }
       // let this thread's copies land before the CTA can exit
       asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (sf_writer) {
+      // each lane writes, in its warp's lane quarter, the 16 bytes at
+      // lane * 16 of each 512-byte scale block: 4 columns (A), then 4 per
+      // 128 columns of the B tile
+      const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+      uint32_t stage = 0, phase = 0, qs = 0, qp = 0;
+      while (true) {
+        if (!mbar_wait(&ctl->qfull[qs], qp, wc)) break;
+        const int w = ctl->q[qs];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->qempty[qs]);
+        if (++qs == kQueue) { qs = 0; qp ^= 1; }
+        if (w < 0) break;
+        const Item it = decode<MODE, MX, PAIR>(p, ctl, w);
+        const int bchunks = item_bn(p, it.type) / 128;
+        bool ok = true;
+        for (int kk = 0; kk < it.k_iters; ++kk) {
+          if (!mbar_wait(&ctl->full[stage], phase, wc)) { ok = false; break; }
+          const uint8_t* sfs = sSF + stage * kSfStage + lane * 16;
+          const uint32_t col = tmem + lanes + 256u + (uint32_t)stage * 16u;
+          tmem_st4(col, *reinterpret_cast<const uint4*>(sfs));
+          for (int c = 0; c < bchunks; ++c)
+            tmem_st4(col + 4u + 4u * (uint32_t)c, *reinterpret_cast<const uint4*>(sfs + 512 + c * 512));
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->sfready[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
     }
     if (kWgrad && p.wg_rows_min == 0) zero_empty_experts<MODE>(p, ctl, warp - 6, lane);
   } else if (warp == 1) {
@@ -1802,6 +1845,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       bool ok = true;
       for (int kk = 0; kk < it.k_iters; ++kk) {
         if (!mbar_wait(&ctl->full[stage], phase, wc)) { ok = false; break; }
+        if (MX && sf_writer && !mbar_wait(&ctl->sfready[stage], phase, wc)) { ok = false; break; }
         tc_fence_after();
         if (lane == 0) {
           // the gather threads wrote part of this stage with cp.async: order
@@ -1812,10 +1856,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // stage scales into TMEM (columns 256 + 16 * stage): A at +0
             // (4 columns), B at +4 (4 columns per 128 N)
             const uint32_t sf_t = tmem + 256 + stage * 16;
-            const uint32_t sfa_s = smem_u32(sSF + stage * kSfStage);
-            tmem_cp_32x128b_warpx4(sf_t, sdesc_plain(sfa_s, 16, 128));
-            for (int c = 0; c < bn / 128; ++c)
-              tmem_cp_32x128b_warpx4(sf_t + 4 + 4 * c, sdesc_plain(sfa_s + 512 + c * 512, 16, 128));
+            if (!sf_writer) {
+              const uint32_t sfa_s = smem_u32(sSF + stage * kSfStage);
+              tmem_cp_32x128b_warpx4(sf_t, sdesc_plain(sfa_s, 16, 128));
+              for (int c = 0; c < bn / 128; ++c)
+                tmem_cp_32x128b_warpx4(sf_t + 4 + 4 * c, sdesc_plain(sfa_s + 512 + c * 512, 16, 128));
+            }
 #pragma unroll
             for (int k32 = 0; k32 < 4; ++k32) {
               const uint64_t ad = amn ? sdesc_sw128(a0 + k32 * 4096, 16384, 1024) : sdesc_sw128(a0 + k32 * 32, 16, 1024);
