@@ -860,8 +860,29 @@ __device__ void epi_scatter(const GemmParams& p, const Item& it, uint32_t tbase,
 //   ds partial = sum_i dA'_i a_i          (router-score gradient)
 //   dA = s dA',  dh = dA u sig(h) (1 + h (1 - sig(h))),  du = dA silu(h)
 //   A_s = s a  (the left operand of dW2)
-template <bool MX>
-__device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
+// MXFP8 keeps one accumulator, so this epilogue would hold up the next
+// tile's MMAs for all of its work: it first parks accumulator columns
+// [64, bn) unchanged (f32) in the TMEM columns no MMA or scale uses
+// (kParkCol.., 192 of them), works through columns [0, 64), hands the
+// accumulator back, and takes the rest from the parked copy while the next
+// tile's main loop runs.  The values are the same f32 bits either way.
+constexpr uint32_t kParkCol = 320;  // past the accumulator (0..255) and the stage scales (256..319)
+static_assert(256 + kStages * 16 <= kParkCol && kParkCol + 192 <= 512, "parked columns overlap or leave TMEM");
+
+template <bool MX, typename Release>
+__device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, int row, Release&& release) {
+  const uint32_t park = tbase + kParkCol;  // MXFP8: single accumulator at column 0
+  if constexpr (MX) {
+#pragma unroll 1
+    for (int c = 64; c < p.bn; c += 32) {
+      uint32_t r[32];
+      tmem_ld32_issue(tbase + c, r);
+      tmem_wait_ld();
+      tmem_regs_ready(r);
+      tmem_st32(park + (c - 64), r);
+    }
+    tmem_wait_st();
+  }
   const long prow = (long)it.row0 + row;
   const int f = p.pad_perm[prow];
   const float s = f >= 0 ? p.scores[f] : 0.0f;
@@ -897,7 +918,8 @@ __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, 
       }
     }
     float g[32];
-    tmem_ld32(tbase + c, g);
+    tmem_ld32((MX && c >= 64) ? park + (c - 64) : tbase + c, g);
+    if (MX && c == 32) release();  // columns [0, 64) are read: the rest is parked
     uint32_t dhw[16], duw[16], asw[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -1976,7 +1998,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           if constexpr (MX) epi_scatter_mx(p, it, tbase, row, p.bn, lane, stage_out, release_acc);
           else epi_scatter(p, it, tbase, row, p.bn);
           break;
-        case GM_BWD_DA: epi_bwd_da<MX>(p, it, tbase, row); break;
+        case GM_BWD_DA: epi_bwd_da<MX>(p, it, tbase, row, release_acc); break;
         default: epi_wgrad<MX && MODE == GM_WG13>(p, it, tbase, q, lane, stage_out, release_acc); break;
       }
       release_acc();
