@@ -1030,20 +1030,21 @@ __device__ __forceinline__ __nv_bfloat16* wgrad_base(const GemmParams& p, const 
 }
 
 // 64 columns at a time: two TMEM loads, one wait, then the coalesced store.
-// With EARLY the whole accumulator row is read first (the first 64 columns
-// into the staging buffer, the rest in registers as packed bf16), then
-// `release` hands the TMEM buffer back to the MMA warp, then the stores, so
-// the next tile's main loop runs while this tile's rows leave.  That pays
-// where the accumulator is single-buffered (MXFP8) and its 96 extra live
-// registers fit (measured on dW1 | dW3 only); elsewhere each 64 columns are
-// loaded and stored in turn and the caller releases the buffer after.
-template <int BN, bool EARLY, typename Release>
+// With PARKED (MXFP8: one accumulator, so this epilogue would otherwise hold
+// up the next tile's MMAs) the row is first rounded to bf16 64 columns at a
+// time -- the first 64 into the staging buffer, the rest packed into the
+// TMEM columns past the accumulator and the stage scales (kParkCol..) --
+// then `release` hands the accumulator back and the stores run from the
+// staging buffer and the parked copy while the next tile's main loop runs
+// (the same bf16 values either way).  Otherwise the caller releases the
+// accumulator after the stores.
+template <int BN, bool PARKED, typename Release>
 __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane,
                                             uint8_t* stage, Release&& release) {
   constexpr int kGroups = BN / 64;
   const int r0 = it.m * 128 + q * 32;  // first dW row of this warp
   const int col0 = it.n * BN;
-  if constexpr (!EARLY) {
+  if constexpr (!PARKED) {
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
       uint32_t w[32];
@@ -1054,32 +1055,41 @@ __device__ __forceinline__ void epi_wgrad_n(const GemmParams& p, const Item& it,
     }
     return;
   }
+  const uint32_t park = tbase + kParkCol;  // single accumulator at column 0
   {
     uint32_t w0[32];
     acc_load64_bf16(tbase, w0);
     stage_chunk64(stage, lane, w0);
   }
-  uint32_t w[kGroups - 1][32];
-#pragma unroll
-  for (int g = 1; g < kGroups; ++g) acc_load64_bf16(tbase + 64 * g, w[g - 1]);
+#pragma unroll 1
+  for (int g = 1; g < kGroups; ++g) {
+    uint32_t w[32];
+    acc_load64_bf16(tbase + 64 * g, w);
+    tmem_st32(park + 32 * (g - 1), w);
+  }
+  tmem_wait_st();
   release();
   long ld;
   __nv_bfloat16* base = wgrad_base(p, it, r0, col0, ld);
   flush_chunk64(stage, lane, [&](int rr) { return base + rr * ld; });
-#pragma unroll
+#pragma unroll 1
   for (int g = 1; g < kGroups; ++g) {
+    uint32_t w[32];
+    tmem_ld32_issue(park + 32 * (g - 1), w);
+    tmem_wait_ld();
+    tmem_regs_ready(w);
     base = wgrad_base(p, it, r0, col0 + 64 * g, ld);
-    store_chunk64_coalesced(stage, lane, w[g - 1], [&](int rr) { return base + rr * ld; });
+    store_chunk64_coalesced(stage, lane, w, [&](int rr) { return base + rr * ld; });
   }
 }
 
-template <bool EARLY, typename Release>
+template <bool PARKED, typename Release>
 __device__ void epi_wgrad(const GemmParams& p, const Item& it, uint32_t tbase, int q, int lane, uint8_t* stage,
                           Release&& release) {
   if (p.bn == 256)
-    epi_wgrad_n<256, EARLY>(p, it, tbase, q, lane, stage, release);
+    epi_wgrad_n<256, PARKED>(p, it, tbase, q, lane, stage, release);
   else
-    epi_wgrad_n<128, EARLY>(p, it, tbase, q, lane, stage, release);
+    epi_wgrad_n<128, PARKED>(p, it, tbase, q, lane, stage, release);
 }
 
 __device__ void epi_dense(const GemmParams& p, const Item& it, uint32_t tbase, int row) {
@@ -1999,7 +2009,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           else epi_scatter(p, it, tbase, row, p.bn);
           break;
         case GM_BWD_DA: epi_bwd_da<MX>(p, it, tbase, row, release_acc); break;
-        default: epi_wgrad<MX && MODE == GM_WG13>(p, it, tbase, q, lane, stage_out, release_acc); break;
+        default: epi_wgrad<MX>(p, it, tbase, q, lane, stage_out, release_acc); break;
       }
       release_acc();
       if (MODE == GM_FWD_FUSED && it.type == GM_FWD2) {
