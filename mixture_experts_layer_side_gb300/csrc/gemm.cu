@@ -703,29 +703,39 @@ __device__ __forceinline__ void acc_load32_bf16(uint32_t taddr, uint32_t* w16) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// MXFP8 launches keep one accumulator (TMEM columns 0..255) and the stage
+// scales (256..319); the epilogues park accumulator values in the columns
+// past those, so they can hand the accumulator back early.
+constexpr uint32_t kParkCol = 320;  // past the accumulator (0..255) and the stage scales (256..319)
+static_assert(256 + kStages * 16 <= kParkCol && kParkCol + 192 <= 512, "parked columns overlap or leave TMEM");
+
 // MXFP8 GEMM1 epilogue: as epi_fwd1, but a goes to the ring as E4M3 codes
 // with one scale per 32 intermediate columns (the K blocks of GEMM2).  The
-// MXFP8 accumulator is single-buffered (TMEM also holds the stage scales),
-// so the row's h and u are first read as the bf16 values the backward keeps
-// (128 registers), the accumulator is handed back (`release`), and only then
-// is a formed, quantised and stored: the same values, with the next tile's
-// main loop already running.
+// row's h and u are first read as the bf16 values the backward keeps (h
+// columns 0..63 into the staging buffer, the other 192 columns packed into
+// parked TMEM columns), the accumulator is handed back (`release`), and
+// only then is a formed, quantised and stored: the same values, with the
+// next tile's main loop already running.
 template <typename Release>
 __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase, int row, int lane, uint8_t* stage,
                             Release&& release) {
   const long prow = (long)it.row0 + row;
   const int i0 = it.n * 128;
   const long crow = p.ctx_ring ? (long)ring_row(p, (int)prow) : prow;
-  // h columns 0..63 parked in the staging buffer, the rest in registers
-  uint32_t hw1[32], uw[2][32];
+  // packed bf16 words parked from kParkCol: h 64..127 at +0, u 0..127 at +32
+  const uint32_t park = tbase + kParkCol;
   {
     uint32_t hw0[32];
     acc_load64_bf16(tbase, hw0);
     park64(stage, lane, hw0);
   }
-  acc_load64_bf16(tbase + 64, hw1);
-  acc_load64_bf16(tbase + 128, uw[0]);
-  acc_load64_bf16(tbase + 192, uw[1]);
+#pragma unroll 1
+  for (int g = 1; g < 4; ++g) {
+    uint32_t w[32];
+    acc_load64_bf16(tbase + 64 * g, w);
+    tmem_st32(park + 32 * (g - 1), w);
+  }
+  tmem_wait_st();
   release();
   __nv_bfloat16* hrow = p.ctx_hu + crow * 2 * p.I + i0;
   __nv_bfloat16* urow = hrow + p.I;
@@ -737,24 +747,23 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
   uint32_t* sword = reinterpret_cast<uint32_t*>(p.ring_sf + ((rr >> 7) * (p.I / 128) + it.n) * 512 +
                                                 mx_sf_offset((int)(rr & 127), 0));
   uint32_t scales = 0;
-  // columns 64..127 first, so their registers are free before the parked
-  // columns 0..63 are read back
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    // 32 columns = 16 packed words each of h and u
+    uint32_t h[16], u[16];
+    tmem_ld16_issue(park + 32 + 16 * c, u);
+    if (c >= 2) tmem_ld16_issue(park + 16 * (c - 2), h);
+    tmem_wait_ld();
+    tmem_regs_ready16(u);
+    if (c >= 2) {
+      tmem_regs_ready16(h);
+    } else {
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    const int c = (cc + 2) & 3;
-    const int o = (c & 1) * 16;  // 32 columns = 16 packed words
-    uint32_t h[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (c < 2) {
-        const uint4 v = unpark16(stage, lane, (c & 1) * 4 + i);
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = unpark16(stage, lane, c * 4 + i);
         h[4 * i] = v.x; h[4 * i + 1] = v.y; h[4 * i + 2] = v.z; h[4 * i + 3] = v.w;
-      } else {
-        h[4 * i] = hw1[o + 4 * i]; h[4 * i + 1] = hw1[o + 4 * i + 1];
-        h[4 * i + 2] = hw1[o + 4 * i + 2]; h[4 * i + 3] = hw1[o + 4 * i + 3];
       }
     }
-    const uint32_t* u = &uw[c >> 1][o];
     uint4* dh = reinterpret_cast<uint4*>(hrow + c * 32);
     uint4* du = reinterpret_cast<uint4*>(urow + c * 32);
 #pragma unroll
@@ -791,40 +800,45 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
 }
 
 // MXFP8 scatter (single-buffered accumulator): the whole row is read as
-// packed bf16 first (columns 0..63 parked in the staging buffer), the
-// accumulator handed back, then the row stored.
+// packed bf16 first (columns 0..63 parked in the staging buffer, the rest
+// in parked TMEM columns), the accumulator handed back, then the row
+// stored (padding rows load with the warp, store nothing).
 template <int BN, typename Release>
 __device__ void epi_scatter_mx_n(const GemmParams& p, const Item& it, uint32_t tbase, int row, int lane,
                                  uint8_t* stage, Release&& release) {
   constexpr int bn = BN;
   const int prow = it.row0 + row;
   const int f = p.pad_perm[prow];
-  uint32_t w[3][32];
+  const uint32_t park = tbase + kParkCol;
   {
     uint32_t w0[32];
     acc_load64_bf16(tbase, w0);
     park64(stage, lane, w0);
   }
-#pragma unroll
-  for (int g = 1; g < 4; ++g) {
-    if (g * 64 < bn) {
-      acc_load32_bf16(tbase + 64 * g, &w[g - 1][0]);
-      acc_load32_bf16(tbase + 64 * g + 32, &w[g - 1][16]);
-    }
+#pragma unroll 1
+  for (int g = 1; g < bn / 64; ++g) {
+    uint32_t w[32];
+    acc_load64_bf16(tbase + 64 * g, w);
+    tmem_st32(park + 32 * (g - 1), w);
   }
+  tmem_wait_st();
   release();
-  if (f < 0) return;
-  __nv_bfloat16* dst = p.yk + (long)f * p.H + it.n * bn;
-  uint4* d0 = reinterpret_cast<uint4*>(dst);
+  __nv_bfloat16* dst = p.yk + (long)(f < 0 ? 0 : f) * p.H + it.n * bn;
+  if (f >= 0) {
+    uint4* d0 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) d0[i] = unpark16(stage, lane, i);
-#pragma unroll
-  for (int g = 1; g < 4; ++g) {
-    if (g * 64 < bn) {
+    for (int i = 0; i < 8; ++i) d0[i] = unpark16(stage, lane, i);
+  }
+#pragma unroll 1
+  for (int g = 1; g < bn / 64; ++g) {
+    uint32_t w[32];
+    tmem_ld32_issue(park + 32 * (g - 1), w);
+    tmem_wait_ld();
+    tmem_regs_ready(w);
+    if (f >= 0) {
       uint4* d = reinterpret_cast<uint4*>(dst + 64 * g);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        d[i] = make_uint4(w[g - 1][4 * i], w[g - 1][4 * i + 1], w[g - 1][4 * i + 2], w[g - 1][4 * i + 3]);
+      for (int i = 0; i < 8; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
   }
 }
@@ -866,8 +880,6 @@ __device__ void epi_scatter(const GemmParams& p, const Item& it, uint32_t tbase,
 // (kParkCol.., 192 of them), works through columns [0, 64), hands the
 // accumulator back, and takes the rest from the parked copy while the next
 // tile's main loop runs.  The values are the same f32 bits either way.
-constexpr uint32_t kParkCol = 320;  // past the accumulator (0..255) and the stage scales (256..319)
-static_assert(256 + kStages * 16 <= kParkCol && kParkCol + 192 <= 512, "parked columns overlap or leave TMEM");
 
 template <bool MX, typename Release>
 __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, int row, Release&& release) {
