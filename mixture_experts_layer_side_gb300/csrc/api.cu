@@ -121,7 +121,7 @@ WsLayout ws_layout(const mok_shape& s, const mok_config& c, mok_precision prec, 
   L.dhu = take(P * 2 * I * 2);
   L.as = take(P * I * 2);
   L.dsp = take(P * (I / 128) * 4);
-  L.sorted = take(P * H * 2);
+  L.sorted = prec == MOK_BF16 ? take(P * H * 2) : 0;
   L.sorted2 = prec == MOK_BF16 ? take(P * H * 2) : 0;
   L.pair_m0 = take(L.tile_capacity * 4);
   L.pair_mb = take((L.tile_capacity + 2) * 4);
@@ -547,13 +547,15 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
     Phase ph(MOK_PHASE_BWD_DX_COMBINE, st, 1);
     MOK_CUDA(launch_combine(s, L, w, g.yk, nullptr, static_cast<__nv_bfloat16*>(dX), st));
   }
-  __nv_bfloat16* srt = reinterpret_cast<__nv_bfloat16*>(w + L.sorted);
+  // the weight gradients' token-row operands (x, dout) are gathered in
+  // padded-row order as they are quantised along the rows
+  const int32_t* pad_perm = reinterpret_cast<const int32_t*>(w + L.pad_perm);
   // dW1 | dW3: token-sorted x and dh|du, both quantised along the routed rows
   {
     {
-      Phase ph(MOK_PHASE_BWD_SORT, st, 3);
-      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(x), srt, st));
-      MOK_CUDA(launch_quant_rows_tiled(srt, rows_used, P, s.H, w + L.wqa, w + L.wsfa, st));
+      Phase ph(MOK_PHASE_BWD_SORT, st, 2);
+      MOK_CUDA(launch_quant_rows_gather(static_cast<const __nv_bfloat16*>(x), rows_used, P, s.H, pad_perm, s.k,
+                                        w + L.wqa, w + L.wsfa, st));
       MOK_CUDA(launch_quant_rows_tiled(g.dhu, rows_used, P, 2 * s.I, w + L.wqb, w + L.wsfb, st));
     }
     TmapSet m;
@@ -577,10 +579,10 @@ mok_status backward_mx(const mok_shape& s, const WsLayout& L, uint8_t* w, const 
   // dW2: s*a and token-sorted dout, both quantised along the routed rows
   {
     {
-      Phase ph(MOK_PHASE_BWD_SORT, st, 3);
+      Phase ph(MOK_PHASE_BWD_SORT, st, 2);
       MOK_CUDA(launch_quant_rows_tiled(g.as, rows_used, P, s.I, w + L.wqb, w + L.wsfb, st));
-      MOK_CUDA(launch_gather_rows(s, L, w, static_cast<const __nv_bfloat16*>(dout), srt, st));
-      MOK_CUDA(launch_quant_rows_tiled(srt, rows_used, P, s.H, w + L.wqa, w + L.wsfa, st));
+      MOK_CUDA(launch_quant_rows_gather(static_cast<const __nv_bfloat16*>(dout), rows_used, P, s.H, pad_perm, s.k,
+                                        w + L.wqa, w + L.wsfa, st));
     }
     TmapSet m;
     memset(&m, 0, sizeof(m));

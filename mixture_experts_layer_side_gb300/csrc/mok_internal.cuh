@@ -57,8 +57,7 @@ struct WsLayout {
   size_t dhu;         // bf16 [pad_capacity, 2I]
   size_t as;          // bf16 [pad_capacity, I]  s * a
   size_t dsp;         // f32  [pad_capacity, I/128] router-gradient partial sums
-  size_t sorted;      // bf16 [pad_capacity, H]: token-sorted x (the forward ring reads it; then dW1|dW3),
-                      // in MXFP8 also dout (dW2)
+  size_t sorted;      // BF16: [pad_capacity, H] token-sorted x (the forward ring reads it; then dW1|dW3)
   size_t sorted2;     // bf16 [pad_capacity, H]: BF16 token-sorted dout (dA', dW2)
   size_t pair_m0;     // int32 [tile_capacity]: CTA-pair units of dA' / dX / the ring (first M tile * 2 + solo)
   size_t pair_mb;     // int32 [tile_capacity + 2]: the list of tiles those launches run on single CTAs
@@ -123,6 +122,10 @@ cudaError_t launch_router_logit_grad(int T, int Tpad, int E, int Epad, int k, co
 cudaError_t launch_router_take_cols(int rows, int E, int Epad, const float* src, float* dst, cudaStream_t st);
 cudaError_t launch_quant_rows_tiled(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
                                     uint8_t* q, uint8_t* sf, cudaStream_t st);
+// The same codes and scales for the token rows pad_perm[p] / k of src [T, C]
+// in padded-row order (zeros for padding rows), without a sorted bf16 copy.
+cudaError_t launch_quant_rows_gather(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
+                                     const int32_t* pad_perm, int k, uint8_t* q, uint8_t* sf, cudaStream_t st);
 // Expert parallelism (ep.cu): source-side pack / combine / un-sort around the exchange
 cudaError_t launch_ep_pack(const mok_shape& s, const WsLayout& L, const uint8_t* ws, const __nv_bfloat16* x,
                            const float* scores, __nv_bfloat16* rows, float* s_rows, cudaStream_t st);
