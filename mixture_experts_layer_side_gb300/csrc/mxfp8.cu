@@ -101,24 +101,6 @@ __device__ __forceinline__ long tiled_block(long b, int nb, int kg, int n_blocks
   return (((b * (n_blocks / g) + nb / g) * kg_count + kg) * s + slot + nb % g) * 512;
 }
 
-// Plain scales [batch][K/32][N] (blocks along K = rows) -> the tiled layout.
-__global__ void tile_scales_kernel(const uint8_t* __restrict__ sf, int batch, int kb_count, int N,
-                                   uint8_t* __restrict__ out, int g, int s, int slot) {
-  const int kg_count = kb_count / 4;
-  const long n_words = (long)batch * kg_count * N;  // one 4-byte word per (batch, k group, n)
-  for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n_words; i += (long)gridDim.x * blockDim.x) {
-    const int n = (int)(i % N);
-    const long bg = i / N;
-    const int kg = (int)(bg % kg_count);
-    const long b = bg / kg_count;
-    const uint8_t* src = sf + (b * kb_count + (long)kg * 4) * N + n;
-    const uint32_t w = (uint32_t)src[0] | ((uint32_t)src[N] << 8) | ((uint32_t)src[2L * N] << 16) |
-                       ((uint32_t)src[3L * N] << 24);
-    uint8_t* blk = out + tiled_block(b, n / 128, kg, N / 128, kg_count, g, s, slot);
-    *reinterpret_cast<uint32_t*>(blk + sf_block_offset(n & 127, 0)) = w;
-  }
-}
-
 // Plain scales of a K-major operand [batch][N][K/32] (blocks along each
 // row) -> the same tiled layout: the four scale bytes of (n, 128-wide K
 // group) are contiguous in the source.
@@ -134,6 +116,67 @@ __global__ void tile_scales_rows_kernel(const uint8_t* __restrict__ sf, int batc
     const uint32_t w = *reinterpret_cast<const uint32_t*>(sf + bn * kb_count + (long)kg * 4);
     uint8_t* blk = out + tiled_block(b, n / 128, kg, N / 128, kg_count, g, s, slot);
     *reinterpret_cast<uint32_t*>(blk + sf_block_offset(n & 127, 0)) = w;
+  }
+}
+
+// The tilings with coalesced reads and writes: a CTA builds whole 512-byte
+// blocks in shared memory and writes them out in 16-byte pieces (one word
+// per thread, as tile_scales_rows_kernel does, scatters 4-byte stores over
+// each block; it stays for runs too long for shared memory).
+//   tile_scales_blocks_kernel: plain scales [batch][K/32][N] (blocks along
+//   K = rows); one CTA of 128 threads per block (b, 128 N, K group); thread
+//   n reads its four scale bytes from four rows of 128 contiguous bytes.
+__global__ void __launch_bounds__(128) tile_scales_blocks_kernel(const uint8_t* __restrict__ sf, int batch,
+                                                                 int kb_count, int N, uint8_t* __restrict__ out,
+                                                                 int g, int s, int slot) {
+  __shared__ uint32_t blk[128];
+  const int kg_count = kb_count / 4, nbs = N / 128;
+  const long nblocks = (long)batch * nbs * kg_count;
+  const int n = threadIdx.x;
+  for (long bi = blockIdx.x; bi < nblocks; bi += gridDim.x) {
+    const int kg = (int)(bi % kg_count);
+    const long bn = bi / kg_count;
+    const int nb = (int)(bn % nbs);
+    const long b = bn / nbs;
+    const uint8_t* src = sf + (b * kb_count + (long)kg * 4) * N + (long)nb * 128 + n;
+    const uint32_t w = (uint32_t)src[0] | ((uint32_t)src[N] << 8) | ((uint32_t)src[2L * N] << 16) |
+                       ((uint32_t)src[3L * N] << 24);
+    __syncthreads();  // the previous block is written out
+    blk[sf_block_offset(n, 0) / 4] = w;
+    __syncthreads();
+    if (n < 32)
+      reinterpret_cast<uint4*>(out + tiled_block(b, nb, kg, nbs, kg_count, g, s, slot))[n] =
+          reinterpret_cast<const uint4*>(blk)[n];
+  }
+}
+
+//   tile_scales_rows_blocks_kernel: one CTA of 256 threads per (b, 128 N):
+//   the 128 rows' kb_count scale bytes are one contiguous run (16-byte
+//   copies into shared memory), then every K group's block is written out.
+__global__ void __launch_bounds__(256) tile_scales_rows_blocks_kernel(const uint8_t* __restrict__ sf, int batch,
+                                                                      int N, int kb_count, uint8_t* __restrict__ out,
+                                                                      int g, int s, int slot) {
+  extern __shared__ __align__(16) uint8_t rows_s[];  // [128][kb_count]
+  const int kg_count = kb_count / 4, nbs = N / 128;
+  const long nrun = (long)batch * nbs;
+  const int run16 = 128 * kb_count / 16;
+  for (long bi = blockIdx.x; bi < nrun; bi += gridDim.x) {
+    const int nb = (int)(bi % nbs);
+    const long b = bi / nbs;
+    const uint4* src = reinterpret_cast<const uint4*>(sf + (b * N + (long)nb * 128) * kb_count);
+    __syncthreads();  // the previous run is written out
+    for (int i = threadIdx.x; i < run16; i += blockDim.x) reinterpret_cast<uint4*>(rows_s)[i] = src[i];
+    __syncthreads();
+    // piece l of K group kg: the words of rows l, l + 32, l + 64, l + 96
+    for (int i = threadIdx.x; i < kg_count * 32; i += blockDim.x) {
+      const int kg = i / 32, l = i % 32;
+      uint4 v;
+      v.x = *reinterpret_cast<const uint32_t*>(rows_s + (l)*kb_count + kg * 4);
+      v.y = *reinterpret_cast<const uint32_t*>(rows_s + (l + 32) * kb_count + kg * 4);
+      v.z = *reinterpret_cast<const uint32_t*>(rows_s + (l + 64) * kb_count + kg * 4);
+      v.w = *reinterpret_cast<const uint32_t*>(rows_s + (l + 96) * kb_count + kg * 4);
+      reinterpret_cast<uint4*>(out + tiled_block(b, nb, kg, nbs, kg_count, g, s, slot))[l] = v;
+    }
   }
 }
 
@@ -245,17 +288,26 @@ __global__ void __launch_bounds__(128) quant_rows_gather_kernel(const __nv_bfloa
 cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st,
                                int g, int s, int slot) {
   if (g < 1 || s < g || slot + g > s || (N / 128) % g) return cudaErrorInvalidValue;
-  const long words = (long)batch * (kb_count / 4) * N;
-  long grid = (words + 255) / 256;
-  const long cap = (long)device_sm_count() * 32;
+  const long blocks = (long)batch * (N / 128) * (kb_count / 4);
+  long grid = blocks;
+  const long cap = (long)device_sm_count() * 16;
   if (grid > cap) grid = cap;
-  tile_scales_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(sf, batch, kb_count, N, out, g, s, slot);
+  tile_scales_blocks_kernel<<<(int)(grid < 1 ? 1 : grid), 128, 0, st>>>(sf, batch, kb_count, N, out, g, s, slot);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tile_scales_rows(const uint8_t* sf, int batch, int N, int kb_count, uint8_t* out,
                                     cudaStream_t st, int g, int s, int slot) {
   if (g < 1 || s < g || slot + g > s || (N / 128) % g) return cudaErrorInvalidValue;
+  const size_t run = (size_t)128 * kb_count;
+  if (run <= 48 * 1024 && (reinterpret_cast<uintptr_t>(sf) & 15) == 0) {
+    long grid = (long)batch * (N / 128);
+    const long cap = (long)device_sm_count() * 8;
+    if (grid > cap) grid = cap;
+    tile_scales_rows_blocks_kernel<<<(int)(grid < 1 ? 1 : grid), 256, run, st>>>(sf, batch, N, kb_count, out, g, s,
+                                                                               slot);
+    return cudaGetLastError();
+  }
   const long words = (long)batch * N * (kb_count / 4);
   long grid = (words + 255) / 256;
   const long cap = (long)device_sm_count() * 32;
