@@ -238,48 +238,54 @@ __global__ void quant_rows_tiled_kernel(const __nv_bfloat16* __restrict__ src, c
 
 // The same quantisation of token rows gathered in padded-row order: padded
 // row p is row pad_perm[p] / k of src [T, C] (zeros for a padding row).  A
-// block takes a tile of 32 padded rows x 128 columns: the 32 source row
-// offsets go to shared memory first, then each thread issues the 32 loads
-// of its column at once (a padding row reads row 0 and is zeroed), so the
-// token-sorted bf16 rows are never stored.
-__global__ void __launch_bounds__(128) quant_rows_gather_kernel(const __nv_bfloat16* __restrict__ src,
+// CTA of 256 threads takes a tile of 32 padded rows x 512 columns, two
+// columns a thread: the 32 source row offsets go to shared memory first,
+// then each thread issues the 32 four-byte loads of its column pair at once
+// (a padding row reads row 0 and is zeroed), so each source row is read in
+// 1 KB runs and the token-sorted bf16 rows are never stored.
+__global__ void __launch_bounds__(256) quant_rows_gather_kernel(const __nv_bfloat16* __restrict__ src,
                                                                 const int32_t* __restrict__ rows_used, int C,
                                                                 const int32_t* __restrict__ pad_perm, int k,
                                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
   __shared__ long off[32];
   const int rbs = *rows_used / 32;
-  const int cch = C / 128;
+  const int cch = (C + 511) / 512;
   const long ntiles = (long)rbs * cch;
   for (long t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const int rb = (int)(t / cch);
-    const int c = (int)(t % cch) * 128 + threadIdx.x;
+    const int c = (int)(t % cch) * 512 + 2 * threadIdx.x;
     __syncthreads();  // the previous tile is done with off[]
     if (threadIdx.x < 32) {
       const int f = pad_perm[(long)rb * 32 + threadIdx.x];
       off[threadIdx.x] = f >= 0 ? (long)(f / k) * C : -1;
     }
     __syncthreads();
-    float v[32];
+    if (c >= C) continue;
+    float v0[32], v1[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
       const long o = off[r];
-      const float x = __bfloat162float(src[(o < 0 ? 0 : o) + c]);
-      v[r] = o < 0 ? 0.0f : x;
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + (o < 0 ? 0 : o) + c));
+      v0[r] = o < 0 ? 0.0f : x.x;
+      v1[r] = o < 0 ? 0.0f : x.y;
     }
-    float amax = 0.0f;
+    float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) amax = fmaxf(amax, fabsf(v[r]));
-    const int X = block_exponent(amax);
-    const float inv = exp2_int(-X);
+    for (int r = 0; r < 32; ++r) {
+      a0 = fmaxf(a0, fabsf(v0[r]));
+      a1 = fmaxf(a1, fabsf(v1[r]));
+    }
+    const int X0 = block_exponent(a0), X1 = block_exponent(a1);
+    const float i0 = exp2_int(-X0), i1 = exp2_int(-X1);
     const long base = (long)rb * 32 * C + c;
 #pragma unroll
-    for (int r = 0; r < 32; r += 2) {
-      const uint16_t pr = cvt_e4m3x2(v[r] * inv, v[r + 1] * inv);
-      q[base + (long)r * C] = (uint8_t)(pr & 0xFF);
-      q[base + (long)(r + 1) * C] = (uint8_t)(pr >> 8);
+    for (int r = 0; r < 32; ++r) {
+      const uint16_t pr = cvt_e4m3x2(v0[r] * i0, v1[r] * i1);
+      *reinterpret_cast<uint16_t*>(q + base + (long)r * C) = pr;
     }
     uint8_t* blk = sf + ((long)(rb / 4) * (C / 128) + c / 128) * 512;
-    blk[sf_block_offset(c & 127, rb & 3)] = (uint8_t)(X + 127);
+    blk[sf_block_offset(c & 127, rb & 3)] = (uint8_t)(X0 + 127);
+    blk[sf_block_offset((c + 1) & 127, rb & 3)] = (uint8_t)(X1 + 127);
   }
 }
 
@@ -328,11 +334,11 @@ cudaError_t launch_tile_row_scales(const uint8_t* sf, int kb_count, const int32_
 
 cudaError_t launch_quant_rows_gather(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
                                      const int32_t* pad_perm, int k, uint8_t* q, uint8_t* sf, cudaStream_t st) {
-  const long tiles = (rows_cap / 32) * (C / 128);
+  const long tiles = (rows_cap / 32) * ((C + 511) / 512);
   long grid = tiles;
-  const long cap = (long)device_sm_count() * 16;
+  const long cap = (long)device_sm_count() * 8;
   if (grid > cap) grid = cap;
-  quant_rows_gather_kernel<<<(int)(grid < 1 ? 1 : grid), 128, 0, st>>>(src, rows_used, C, pad_perm, k, q, sf);
+  quant_rows_gather_kernel<<<(int)(grid < 1 ? 1 : grid), 256, 0, st>>>(src, rows_used, C, pad_perm, k, q, sf);
   return cudaGetLastError();
 }
 
