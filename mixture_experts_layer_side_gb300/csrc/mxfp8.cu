@@ -210,29 +210,32 @@ __global__ void tile_row_scales_kernel(const uint8_t* __restrict__ sf, int kb_co
 // sf_block_offset(column % 128, (row / 32) % 4)).
 __global__ void quant_rows_tiled_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ rows_used,
                                         int C, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  // two columns a thread: four-byte loads, a warp reads 128 bytes of a row
   const int rows = *rows_used;
-  const long n = (long)(rows / 32) * C;
+  const int C2 = C / 2;
+  const long n = (long)(rows / 32) * C2;
   for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
-    const int c = (int)(i % C);
-    const int rb = (int)(i / C);
+    const int c = 2 * (int)(i % C2);
+    const int rb = (int)(i / C2);
     const long base = (long)rb * 32 * C + c;
-    float v[32];
-    float amax = 0.0f;
+    float v0[32], v1[32];
+    float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-      v[r] = __bfloat162float(src[base + (long)r * C]);
-      amax = fmaxf(amax, fabsf(v[r]));
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + base + (long)r * C));
+      v0[r] = x.x;
+      v1[r] = x.y;
+      a0 = fmaxf(a0, fabsf(x.x));
+      a1 = fmaxf(a1, fabsf(x.y));
     }
-    const int X = block_exponent(amax);
-    const float inv = exp2_int(-X);
+    const int X0 = block_exponent(a0), X1 = block_exponent(a1);
+    const float i0 = exp2_int(-X0), i1 = exp2_int(-X1);
 #pragma unroll
-    for (int r = 0; r < 32; r += 2) {
-      const uint16_t pr = cvt_e4m3x2(v[r] * inv, v[r + 1] * inv);
-      q[base + (long)r * C] = (uint8_t)(pr & 0xFF);
-      q[base + (long)(r + 1) * C] = (uint8_t)(pr >> 8);
-    }
+    for (int r = 0; r < 32; ++r)
+      *reinterpret_cast<uint16_t*>(q + base + (long)r * C) = cvt_e4m3x2(v0[r] * i0, v1[r] * i1);
     uint8_t* blk = sf + ((long)(rb / 4) * (C / 128) + c / 128) * 512;
-    blk[sf_block_offset(c & 127, rb & 3)] = (uint8_t)(X + 127);
+    blk[sf_block_offset(c & 127, rb & 3)] = (uint8_t)(X0 + 127);
+    blk[sf_block_offset((c + 1) & 127, rb & 3)] = (uint8_t)(X1 + 127);
   }
 }
 
@@ -344,7 +347,7 @@ cudaError_t launch_quant_rows_gather(const __nv_bfloat16* src, const int32_t* ro
 
 cudaError_t launch_quant_rows_tiled(const __nv_bfloat16* src, const int32_t* rows_used, long rows_cap, int C,
                                     uint8_t* q, uint8_t* sf, cudaStream_t st) {
-  const long n = (rows_cap / 32) * C;
+  const long n = (rows_cap / 32) * (C / 2);
   long grid = (n + 255) / 256;
   const long cap = (long)device_sm_count() * 32;
   if (grid > cap) grid = cap;
