@@ -150,6 +150,37 @@ __global__ void __launch_bounds__(128) tile_scales_blocks_kernel(const uint8_t* 
   }
 }
 
+//   tile_scales_run_kernel: the same for one CTA of 256 threads per (b,
+//   128 N) and every K group of it (all of its blocks in shared memory), so
+//   each thread has many independent loads in flight.
+__global__ void __launch_bounds__(256) tile_scales_run_kernel(const uint8_t* __restrict__ sf, int batch,
+                                                              int kb_count, int N, uint8_t* __restrict__ out, int g,
+                                                              int s, int slot) {
+  extern __shared__ __align__(16) uint32_t blks[];  // [kg_count][128 words]
+  const int kg_count = kb_count / 4, nbs = N / 128;
+  const long nrun = (long)batch * nbs;
+  for (long bi = blockIdx.x; bi < nrun; bi += gridDim.x) {
+    const int nb = (int)(bi % nbs);
+    const long b = bi / nbs;
+    const uint8_t* src0 = sf + b * kb_count * (long)N + (long)nb * 128;
+    __syncthreads();  // the previous run is written out
+#pragma unroll 4
+    for (int i = threadIdx.x; i < kg_count * 128; i += blockDim.x) {
+      const int kg = i >> 7, n = i & 127;
+      const uint8_t* src = src0 + (long)kg * 4 * N + n;
+      const uint32_t w = (uint32_t)src[0] | ((uint32_t)src[N] << 8) | ((uint32_t)src[2L * N] << 16) |
+                         ((uint32_t)src[3L * N] << 24);
+      blks[kg * 128 + sf_block_offset(n, 0) / 4] = w;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kg_count * 32; i += blockDim.x) {
+      const int kg = i >> 5, l = i & 31;
+      reinterpret_cast<uint4*>(out + tiled_block(b, nb, kg, nbs, kg_count, g, s, slot))[l] =
+          reinterpret_cast<const uint4*>(blks + kg * 128)[l];
+    }
+  }
+}
+
 //   tile_scales_rows_blocks_kernel: one CTA of 256 threads per (b, 128 N):
 //   the 128 rows' kb_count scale bytes are one contiguous run (16-byte
 //   copies into shared memory), then every K group's block is written out.
@@ -297,6 +328,14 @@ __global__ void __launch_bounds__(256) quant_rows_gather_kernel(const __nv_bfloa
 cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N, uint8_t* out, cudaStream_t st,
                                int g, int s, int slot) {
   if (g < 1 || s < g || slot + g > s || (N / 128) % g) return cudaErrorInvalidValue;
+  const size_t run = (size_t)(kb_count / 4) * 512;
+  if (run <= 48 * 1024) {
+    long grid = (long)batch * (N / 128);
+    const long cap = (long)device_sm_count() * 8;
+    if (grid > cap) grid = cap;
+    tile_scales_run_kernel<<<(int)(grid < 1 ? 1 : grid), 256, run, st>>>(sf, batch, kb_count, N, out, g, s, slot);
+    return cudaGetLastError();
+  }
   const long blocks = (long)batch * (N / 128) * (kb_count / 4);
   long grid = blocks;
   const long cap = (long)device_sm_count() * 16;
