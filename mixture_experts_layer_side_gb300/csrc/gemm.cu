@@ -53,6 +53,7 @@ struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t sfready[kMaxStages];  // MXFP8: the stage's scales are in TMEM (written by the gather warps)
+  uint64_t sffull[kMaxStages];   // MXFP8 with the scale writer: the stage's scale blocks are in smem
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t qfull[kQueue];
@@ -492,9 +493,14 @@ __device__ __forceinline__ uint32_t mx_stage_bytes(const GemmParams& p, int type
   }
 }
 
+// MXFP8 scale bytes of one stage: A's block (512 B) and B's blocks (512 B
+// per 128 columns of the tile)
+__device__ __forceinline__ uint32_t mx_sf_bytes(int bn) { return 512u * (1u + (uint32_t)bn / 128u); }
+
 template <int MODE>
 __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams& p, const Item& it, int kk, uint8_t* a,
-                                             uint8_t* b, uint8_t* sfa, uint8_t* sfb, uint64_t* bar) {
+                                             uint8_t* b, uint8_t* sfa, uint8_t* sfb, uint64_t* bar,
+                                             uint64_t* sfbar) {
   const int type = it.type;
   const int bn = item_bn(p, type);
   if (MODE == GM_DENSE) {
@@ -504,14 +510,14 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
       tma_load_2d(a, &mp.m[0], bar, it.m * 128, kk * 128);
     else
       tma_load_2d(a, &mp.m[0], bar, kk * 128, it.m * 128);
-    bulk_load(sfa, p.sfa_tiled + ((long)it.m * kgroups + kk) * 512, 512, bar);
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * kgroups + kk) * 512, 512, sfbar);
     if (p.b_mn) {
       for (int c = 0; c < bn / 128; ++c) tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, kk * 128);
     } else {
       tma_load_2d(b, &mp.m[1], bar, kk * 128, it.n * bn);
     }
     // B's scales grouped per bn-wide N tile: one load
-    bulk_load(sfb, p.sfb_tiled0 + ((long)it.n * kgroups + kk) * (bn / 128) * 512, (bn / 128) * 512, bar);
+    bulk_load(sfb, p.sfb_tiled0 + ((long)it.n * kgroups + kk) * (bn / 128) * 512, (bn / 128) * 512, sfbar);
   } else if (type == GM_FWD1) {
     const int hg = p.H / 128;
     // A: x's codes in padded-row order, when GEMM1 does not gather them
@@ -520,48 +526,48 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     tma_load_3d(b + 16384, &mp.m[2], bar, it.n * 128, kk * 128, it.e);
     // W1's and W3's scale blocks interleaved: one load
     const long blk = ((long)it.e * (p.I / 128) + it.n) * hg + kk;
-    bulk_load(sfb, p.sfb_tiled0 + blk * 1024, 1024, bar);
+    bulk_load(sfb, p.sfb_tiled0 + blk * 1024, 1024, sfbar);
     // A (gathered x rows): its scales pre-tiled in padded-row order
-    bulk_load(sfa, p.sfa_tiled + ((long)it.m * hg + kk) * 512, 512, bar);
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * hg + kk) * 512, 512, sfbar);
   } else if (type == GM_FWD2) {
     const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
     const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
     tma_load_2d(a, &mp.m[mslot], bar, kk * 128, ring_row(p, it.rp * kTileRows));
     // a's scales, tiled by the GEMM1 epilogue next to the ring codes
-    bulk_load(sfa, p.ring_sf + ((long)(ring_row(p, it.rp * kTileRows) >> 7) * (p.I / 128) + kk) * 512, 512, bar);
+    bulk_load(sfa, p.ring_sf + ((long)(ring_row(p, it.rp * kTileRows) >> 7) * (p.I / 128) + kk) * 512, 512, sfbar);
     for (int c = 0; c < bn / 128; ++c) tma_load_3d(b + c * 16384, &mp.m[wmap], bar, it.n * bn + c * 128, kk * 128, it.e);
     // W2's scales grouped per bn-wide N tile: one load
     const long blk = ((long)it.e * (p.H / bn) + it.n) * (p.I / 128) + kk;
     bulk_load(sfb, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * (bn / 128) * 512, (bn / 128) * 512,
-              bar);
+              sfbar);
   } else if (type == GM_BWD_DA) {
     // A: dout's codes in padded-row order, when dA' does not gather them;
     // B = W2 along H (K-major); its scales, and those of the dout rows,
     // pre-tiled per 128 rows x 128 K
     if (p.rows_sorted) tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
     tma_load_3d(b, &mp.m[1], bar, kk * 128, it.n * bn, it.e);
-    bulk_load(sfa, p.sfa_tiled + ((long)it.m * (p.H / 128) + kk) * 512, 512, bar);
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * (p.H / 128) + kk) * 512, 512, sfbar);
     const long blk = ((long)it.e * (p.I / bn) + it.n) * (p.H / 128) + kk;
-    bulk_load(sfb, p.sfb_tiled0 + blk * (bn / 128) * 512, (bn / 128) * 512, bar);
+    bulk_load(sfb, p.sfb_tiled0 + blk * (bn / 128) * 512, (bn / 128) * 512, sfbar);
   } else if (type == GM_BWD_DX) {
     // B = W1 then W3 along I (K-major); scales pre-tiled likewise
     tma_load_2d(a, &mp.m[0], bar, kk * 128, it.row0);
-    bulk_load(sfa, p.sfa_tiled + ((long)it.m * (2 * p.I / 128) + kk) * 512, 512, bar);
+    bulk_load(sfa, p.sfa_tiled + ((long)it.m * (2 * p.I / 128) + kk) * 512, 512, sfbar);
     const int ki = p.I / 128;
     const int kb = kk < ki ? kk : kk - ki;
     tma_load_3d(b, &mp.m[kk < ki ? 1 : 2], bar, kb * 128, it.n * bn, it.e);
     const long blk = ((long)it.e * (p.H / bn) + it.n) * ki + kb;
-    bulk_load(sfb, (kk < ki ? p.sfb_tiled0 : p.sfb_tiled1) + blk * (bn / 128) * 512, (bn / 128) * 512, bar);
+    bulk_load(sfb, (kk < ki ? p.sfb_tiled0 : p.sfb_tiled1) + blk * (bn / 128) * 512, (bn / 128) * 512, sfbar);
   } else if (type == GM_WG13 || type == GM_WG2) {
     // token-sorted operands quantised along the routed rows (K), M/N-major
     const int cols_a = (type == GM_WG13) ? p.H : p.I;
     const int cols_b = (type == GM_WG13) ? 2 * p.I : p.H;
     const int rb = it.row0 / 128 + kk;
     tma_load_2d(a, &mp.m[0], bar, it.m * 128, it.row0 + kk * 128);
-    bulk_load(sfa, p.sfa_tiled + ((long)rb * (cols_a / 128) + it.m) * 512, 512, bar);
+    bulk_load(sfa, p.sfa_tiled + ((long)rb * (cols_a / 128) + it.m) * 512, 512, sfbar);
     for (int c = 0; c < bn / 128; ++c) tma_load_2d(b + c * 16384, &mp.m[1], bar, it.n * bn + c * 128, it.row0 + kk * 128);
     // the bn / 128 column blocks of B's scales are adjacent: one load
-    bulk_load(sfb, p.sfb_tiled0 + ((long)rb * (cols_b / 128) + it.n * (bn / 128)) * 512, (bn / 128) * 512, bar);
+    bulk_load(sfb, p.sfb_tiled0 + ((long)rb * (cols_b / 128) + it.n * (bn / 128)) * 512, (bn / 128) * 512, sfbar);
   }
 }
 
@@ -1544,11 +1550,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // (replicated over the four lane quarters, the layout tcgen05.cp
   // .32x128b.warpx4 makes), so the MMA thread issues only MMAs; a
   // per-stage barrier tells it the scales are in place (dense core 2,036 ->
-  // 2,217 TFLOP/s at 8192^3, Kimi-shaped dX 2% faster).  Weight-gradient
-  // launches keep those warps for the empty experts' zero stores, and the
-  // ring keeps the copies in the MMA thread (the hand-off made it 3% slower:
-  // its MMAs more often wait on a stage that has just landed).
-  const bool sf_writer = MX && !gather_in_pipe && !kWgrad && !is_ring<MODE>();
+  // 2,217 TFLOP/s at 8192^3, Kimi-shaped dX 2% faster).  The scale blocks
+  // complete on a barrier of their own (sffull), so the writes overlap the
+  // operands' arrival; with one shared barrier the hand-off cost the ring
+  // 3%.  Weight-gradient launches with an empty expert keep those warps for
+  // the zero stores.
+  bool no_empty_expert = false;
+  if constexpr (MX && kWgrad) {
+    int ok = 1;
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) ok &= p.counts[e] > 0;
+    no_empty_expert = __syncthreads_and(ok) != 0;
+  }
+  const bool sf_writer = MX && !gather_in_pipe && (!kWgrad || no_empty_expert);
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)
@@ -1573,6 +1586,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       mbar_init(&ctl->full[i], gather_in_pipe ? 129u : 1u);
       mbar_init(&ctl->empty[i], 1);
       mbar_init(&ctl->sfready[i], 4);  // the four gather warps
+      mbar_init(&ctl->sffull[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->tfull[i], 1);
@@ -1748,13 +1762,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                                       : tma_stage_bytes(p, it.type, item_bn(p, it.type));
           for (int kk = 0; kk < it.k_iters; ++kk) {
             if (!mbar_wait(&ctl->empty[stage], phase ^ 1, wc)) { ok = false; break; }
-            mbar_arrive_expect_tx(&ctl->full[stage], bytes);
+            if (MX && sf_writer) {
+              // the scale blocks complete on a barrier of their own, so the
+              // gather warps move them into TMEM while the operands land
+              const uint32_t sfb = mx_sf_bytes(item_bn(p, it.type));
+              mbar_arrive_expect_tx(&ctl->full[stage], bytes - sfb);
+              mbar_arrive_expect_tx(&ctl->sffull[stage], sfb);
+            } else {
+              mbar_arrive_expect_tx(&ctl->full[stage], bytes);
+            }
             if constexpr (PAIR)
               tma_loads_pair<MODE>(maps, p, it, kk, 0, sA + stage * kAStage, sB + stage * kBSt,
                                    mapa_shared(&ctl->full[stage], 0));
             else if constexpr (MX)
               tma_loads_mx<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBSt, sSF + stage * kSfStage,
-                                 sSF + stage * kSfStage + 512, &ctl->full[stage]);
+                                 sSF + stage * kSfStage + 512, &ctl->full[stage],
+                                 sf_writer ? &ctl->sffull[stage] : &ctl->full[stage]);
             else
               tma_loads<MODE>(maps, p, it, kk, sA + stage * kAStage, sB + stage * kBSt, &ctl->full[stage]);
             ++issued;
@@ -1771,6 +1794,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           const uint32_t f = issued - j;
           const uint64_t spent = globaltimer() - t0;
           if (spent < kDrainNs) mbar_drain(&ctl->full[f % kSt], (f / kSt) & 1u, kDrainNs - spent);
+          if (MX && sf_writer) {
+            const uint64_t spent2 = globaltimer() - t0;
+            if (spent2 < kDrainNs) mbar_drain(&ctl->sffull[f % kSt], (f / kSt) & 1u, kDrainNs - spent2);
+          }
         }
       }
     }
@@ -1845,7 +1872,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int bchunks = item_bn(p, it.type) / 128;
         bool ok = true;
         for (int kk = 0; kk < it.k_iters; ++kk) {
-          if (!mbar_wait(&ctl->full[stage], phase, wc)) { ok = false; break; }
+          if (!mbar_wait(&ctl->sffull[stage], phase, wc)) { ok = false; break; }
           const uint8_t* sfs = sSF + stage * kSfStage + lane * 16;
           const uint32_t col = tmem + lanes + 256u + (uint32_t)stage * 16u;
           tmem_st4(col, *reinterpret_cast<const uint4*>(sfs));
