@@ -68,6 +68,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test with a suspend-time hint: a thread whose phase is not yet
+// complete is suspended until it completes or kSuspendNs pass.  Waiting
+// warps that poll without it take issue and shared-memory bandwidth from
+// the MMA thread: four such warps cut a block-scaled MMA loop from 621 to
+// 967 cycles per 128 x 256 x 128 step (measured; 646 with the hint).
+constexpr uint32_t kSuspendNs = 100000;  // 100 us
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Where a bounded wait reports: the CTA's own abort flag (shared memory),
 // the launch-wide abort word and the sticky error word (workspace header).
 struct WaitCtx {
@@ -93,8 +111,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((it & 3u) == 0) {
       if (wait_aborted(w)) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {
         wait_give_up(w);
@@ -108,7 +126,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 // used at exit to let copies already in flight land before the CTA leaves.
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_sleep(bar, parity))
     if (globaltimer() - t0 > limit_ns) return false;
   return true;
 }
@@ -150,14 +168,26 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // mbar_wait with cluster-scope acquire (the phase was completed by arrivals
 // from the other CTA of the pair, whose prior writes must be visible).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (mbar_try_wait_cluster_sleep(bar, parity)) return true;
+    if ((it & 3u) == 0) {
       if (wait_aborted(w)) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {
         wait_give_up(w);
