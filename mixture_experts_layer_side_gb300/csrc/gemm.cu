@@ -1545,23 +1545,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const bool gather_in_pipe = kGather && !PAIR && !(MODE == GM_DENSE && MX) && !(kWgrad && (MX || p.wg_sorted)) &&
                               !(MODE == GM_BWD_DA && p.rows_sorted) && !(MX && MODE == GM_BWD_DX) &&
                               !((MODE == GM_FWD_RING || MODE == GM_FWD1) && p.fwd_sorted);
-  // MXFP8 launches whose gather warps copy nothing: those warps move each
+  // The dense MXFP8 core's gather warps, which copy nothing, move each
   // stage's scale blocks from shared memory into TMEM with tcgen05.st
   // (replicated over the four lane quarters, the layout tcgen05.cp
-  // .32x128b.warpx4 makes), so the MMA thread issues only MMAs; a
-  // per-stage barrier tells it the scales are in place (dense core 2,036 ->
-  // 2,217 TFLOP/s at 8192^3, Kimi-shaped dX 2% faster).  The scale blocks
-  // complete on a barrier of their own (sffull), so the writes overlap the
-  // operands' arrival; with one shared barrier the hand-off cost the ring
-  // 3%.  Weight-gradient launches with an empty expert keep those warps for
-  // the zero stores.
-  bool no_empty_expert = false;
-  if constexpr (MX && kWgrad) {
-    int ok = 1;
-    for (int e = threadIdx.x; e < p.E; e += blockDim.x) ok &= p.counts[e] > 0;
-    no_empty_expert = __syncthreads_and(ok) != 0;
-  }
-  const bool sf_writer = MX && !gather_in_pipe && (!kWgrad || no_empty_expert);
+  // .32x128b.warpx4 makes), so its MMA thread issues only MMAs; the blocks
+  // complete on a barrier of their own (sffull) and a per-stage barrier
+  // (sfready) tells the MMA thread the scales are in place (dense core
+  // 2,004 -> 2,254 TFLOP/s at 8192^3).  The layer's GEMMs keep the copies
+  // in the MMA thread: with the hand-off their k-steps were slower (Kimi-
+  // shaped dA' 2.67 against 2.47 ms, dX 3.63 against 3.51).
+  const bool sf_writer = MX && MODE == GM_DENSE && !gather_in_pipe;
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)
