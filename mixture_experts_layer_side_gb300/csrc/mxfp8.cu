@@ -152,7 +152,10 @@ __global__ void __launch_bounds__(128) tile_scales_blocks_kernel(const uint8_t* 
 
 //   tile_scales_run_kernel: the same for one CTA of 256 threads per (b,
 //   128 N) and every K group of it (all of its blocks in shared memory), so
-//   each thread has many independent loads in flight.
+//   each thread has many independent loads in flight.  A thread takes four
+//   N columns of one K group: one 32-bit load from each of the group's four
+//   scale rows (a warp reads 128 contiguous bytes of a row), then a 4 x 4
+//   byte transpose in registers gives the four columns' words.
 __global__ void __launch_bounds__(256) tile_scales_run_kernel(const uint8_t* __restrict__ sf, int batch,
                                                               int kb_count, int N, uint8_t* __restrict__ out, int g,
                                                               int s, int slot) {
@@ -164,13 +167,22 @@ __global__ void __launch_bounds__(256) tile_scales_run_kernel(const uint8_t* __r
     const long b = bi / nbs;
     const uint8_t* src0 = sf + b * kb_count * (long)N + (long)nb * 128;
     __syncthreads();  // the previous run is written out
-#pragma unroll 4
-    for (int i = threadIdx.x; i < kg_count * 128; i += blockDim.x) {
-      const int kg = i >> 7, n = i & 127;
-      const uint8_t* src = src0 + (long)kg * 4 * N + n;
-      const uint32_t w = (uint32_t)src[0] | ((uint32_t)src[N] << 8) | ((uint32_t)src[2L * N] << 16) |
-                         ((uint32_t)src[3L * N] << 24);
-      blks[kg * 128 + sf_block_offset(n, 0) / 4] = w;
+#pragma unroll 2
+    for (int i = threadIdx.x; i < kg_count * 32; i += blockDim.x) {
+      const int kg = i >> 5, n4 = (i & 31) * 4;
+      const uint8_t* src = src0 + (long)kg * 4 * N + n4;
+      const uint32_t r0 = *reinterpret_cast<const uint32_t*>(src);
+      const uint32_t r1 = *reinterpret_cast<const uint32_t*>(src + N);
+      const uint32_t r2 = *reinterpret_cast<const uint32_t*>(src + 2L * N);
+      const uint32_t r3 = *reinterpret_cast<const uint32_t*>(src + 3L * N);
+      // column n4 + t: byte t of each row, K block j in byte j
+      const uint32_t lo01 = __byte_perm(r0, r1, 0x5140), hi01 = __byte_perm(r0, r1, 0x7362);
+      const uint32_t lo23 = __byte_perm(r2, r3, 0x5140), hi23 = __byte_perm(r2, r3, 0x7362);
+      uint32_t* blk = blks + kg * 128;
+      blk[sf_block_offset(n4 + 0, 0) / 4] = __byte_perm(lo01, lo23, 0x5410);
+      blk[sf_block_offset(n4 + 1, 0) / 4] = __byte_perm(lo01, lo23, 0x7632);
+      blk[sf_block_offset(n4 + 2, 0) / 4] = __byte_perm(hi01, hi23, 0x5410);
+      blk[sf_block_offset(n4 + 3, 0) / 4] = __byte_perm(hi01, hi23, 0x7632);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < kg_count * 32; i += blockDim.x) {
@@ -329,7 +341,7 @@ cudaError_t launch_tile_scales(const uint8_t* sf, int batch, int kb_count, int N
                                int g, int s, int slot) {
   if (g < 1 || s < g || slot + g > s || (N / 128) % g) return cudaErrorInvalidValue;
   const size_t run = (size_t)(kb_count / 4) * 512;
-  if (run <= 48 * 1024) {
+  if (run <= 48 * 1024 && (reinterpret_cast<uintptr_t>(sf) & 3) == 0) {
     long grid = (long)batch * (N / 128);
     const long cap = (long)device_sm_count() * 8;
     if (grid > cap) grid = cap;
