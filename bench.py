@@ -72,7 +72,8 @@ def parse_args_from(argv):
     # bounded-memory backward (forward context of ring_slots minibatches, GEMM1 recomputed)
     ap.add_argument("--replay", action="store_true")
     ap.add_argument("--fused", action="store_true",
-                    help="schedule + forward as one launch (mok_forward_fused, BF16)")
+                    help="schedule + forward as one launch (mok_forward_fused; MXFP8: after the "
+                         "routing-independent quantisation and scale tiling)")
     return ap.parse_args(argv)
 
 
@@ -476,9 +477,6 @@ def run_mok(args):
         w_fwd, w_bwd = wq["fwd"], wq["bwd"]
     else:
         w_fwd = w_bwd = (inp["W1"], inp["W3"], inp["W2"])
-
-    if args.fused and prec != "bf16":
-        raise SystemExit("--fused: the single-launch forward is BF16 only")
 
     def forward(x, idx, s, o):
         if args.fused:

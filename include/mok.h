@@ -243,20 +243,23 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
 /*
  * The schedule and the forward in one persistent launch ([MTP]: the layer
  * as a single kernel; the ring-token-buffer paragraph).  Same inputs as
- * mok_build_schedule followed by mok_forward (MOK_BF16 only), same results
- * bitwise -- the schedule arrays in the workspace (so mok_backward can
- * follow), out and ctx.  The launch's work items, taken in order from a
- * device counter, are: a histogram per 1,024 routed rows, the scan, the
- * placement per 1,024 routed rows and the ring's GEMM1 / GEMM2 tiles; each
- * waits (bounded) only on items before it.  A CTA that draws past the last
- * item combines tokens, taken from a second counter, once every GEMM2 row
- * is stored.
+ * mok_build_schedule followed by mok_forward (weights as for mok_forward
+ * in the given precision), same results bitwise -- the schedule arrays in
+ * the workspace (so mok_backward can follow), out and ctx.  The launch's
+ * work items, taken in order from a device counter, are: a histogram per
+ * 1,024 routed rows, the scan, the placement per 1,024 routed rows (MXFP8:
+ * also the placed rows' x scales, tiled for GEMM1) and the ring's GEMM1 /
+ * GEMM2 tiles; each waits (bounded) only on items before it.  A CTA that
+ * draws past the last item combines tokens, taken from a second counter,
+ * once every GEMM2 row is stored.  MXFP8: what does not depend on the
+ * routing -- x quantised along H, the weights' scales tiled -- runs as
+ * four small launches ahead of the persistent one.
  * Clears the workspace error word first; an id outside [0, E) records
  * MOK_ERR_BAD_INDEX as in mok_build_schedule.
  */
-mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void* ws, size_t ws_bytes,
-                             const int32_t* topk_idx, const void* x, const float* scores, const void* W1,
-                             const void* W3, const void* W2, void* out, void* ctx, void* stream);
+mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, mok_precision prec, void* ws,
+                             size_t ws_bytes, const int32_t* topk_idx, const void* x, const float* scores,
+                             const void* W1, const void* W3, const void* W2, void* out, void* ctx, void* stream);
 
 /*
  * Backward ([MoK] "Use the functional API": backward(config, workspace,

@@ -90,7 +90,7 @@ def _load():
         "mok_workspace_layout": (i32, [S, C, i32, ctypes.POINTER(MokLayout)]),
         "mok_build_schedule": (i32, [S, C, P, sz, P, P]),
         "mok_forward": (i32, [S, C, i32, P, sz, P, P, P, P, P, P, P, P]),
-        "mok_forward_fused": (i32, [S, C, P, sz, P, P, P, P, P, P, P, P, P]),
+        "mok_forward_fused": (i32, [S, C, i32, P, sz, P, P, P, P, P, P, P, P, P]),
         "mok_backward": (i32, [S, C, i32, P, sz, P, P, P, P, P, P, P, P, P, P, P, P, P]),
         "mok_mxfp8_quantize": (i32, [P, i32, i32, i32, i32, P, P, P]),
         "mok_gather_rows": (i32, [S, C, P, sz, P, P, P]),
@@ -198,8 +198,8 @@ def mok_forward(shape, cfg, prec, ws, x, scores, W1, W3, W2, out, ctx, stream=No
                         _stream(stream)), "mok_forward")
 
 
-def mok_forward_fused(shape, cfg, ws, idx, x, scores, W1, W3, W2, out, ctx, stream=None):
-    _ok(LIB.mok_forward_fused(ctypes.byref(shape), ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(),
+def mok_forward_fused(shape, cfg, prec, ws, idx, x, scores, W1, W3, W2, out, ctx, stream=None):
+    _ok(LIB.mok_forward_fused(ctypes.byref(shape), ctypes.byref(cfg), prec, _ptr(ws), ws.numel() * ws.element_size(),
                               _ptr(idx), _ptr(x), _ptr(scores), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(out),
                               _ptr(ctx), _stream(stream)), "mok_forward_fused")
 

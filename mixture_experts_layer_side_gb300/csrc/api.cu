@@ -904,14 +904,16 @@ mok_status mok_forward(const mok_shape* shape, const mok_config* cfg, mok_precis
   return MOK_OK;
 }
 
-mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void* ws, size_t ws_bytes,
-                             const int32_t* topk_idx, const void* x, const float* scores, const void* W1,
-                             const void* W3, const void* W2, void* out, void* ctx, void* stream) {
+mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, mok_precision prec, void* ws,
+                             size_t ws_bytes, const int32_t* topk_idx, const void* x, const float* scores,
+                             const void* W1, const void* W3, const void* W2, void* out, void* ctx, void* stream) {
   MOK_TRY(check_shape(shape));
   MOK_TRY(check_config(cfg));
+  MOK_TRY(check_prec(prec));
   if (!ws || !topk_idx || !x || !scores || !W1 || !W3 || !W2 || !out || !ctx) return MOK_ERR_INVALID_ARG;
+  if (prec == MOK_MXFP8 && (!mx_ok(W1) || !mx_ok(W3) || !mx_ok(W2))) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
-  const WsLayout L = ws_layout(s, *cfg, MOK_BF16, device_sm_count());
+  const WsLayout L = ws_layout(s, *cfg, prec, device_sm_count());
   if (ws_bytes < L.total) return MOK_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -920,6 +922,20 @@ mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void
   MOK_CUDA(cudaMemsetAsync(w + L.ring_flags, 0, 4 * L.tile_capacity * 4, st));
   const int M = L.minibatch_rows, S = L.ring_slots;
   const int bn2 = (s.H % 256 == 0) ? 256 : 128;
+  if (prec == MOK_MXFP8) {
+    const mok_mx &q1 = *as_mx(W1), &q3 = *as_mx(W3), &q2 = *as_mx(W2);
+    {
+      // what does not depend on the routing, ahead of the launch: x along H
+      // and the forward weight scales tiled; the tiled A scales cleared (the
+      // launch's placement items fill the routed rows')
+      Phase ph(MOK_PHASE_QUANT, st, 4);
+      MOK_CUDA(launch_mxfp8_quantize(static_cast<const __nv_bfloat16*>(x), 1, s.T, s.H, 1, w + L.xq, w + L.xsf, st));
+      MOK_CUDA(launch_tile_scales(q1.scale, s.E, s.H / 32, s.I, w + L.wsf1, st, 1, 2, 0));
+      MOK_CUDA(launch_tile_scales(q3.scale, s.E, s.H / 32, s.I, w + L.wsf1, st, 1, 2, 1));
+      MOK_CUDA(launch_tile_scales(q2.scale, s.E, s.I / 32, s.H, w + L.wsf2, st, bn2 / 128, bn2 / 128, 0));
+      MOK_CUDA(cudaMemsetAsync(w + L.sfa_rows_t, 0, (size_t)L.pad_capacity * (s.H / 32), st));
+    }
+  }
   auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(w + off); };
   GemmParams g;
   base_params(g, s, L, w);
@@ -948,10 +964,28 @@ mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void
   g.s_tile_expert = I32(L.tile_expert);
   TmapSet maps;
   memset(&maps, 0, sizeof(maps));
-  if (!map_gather(&maps.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
-  if (!map3d(&maps.m[1], W1, s.I, s.H, s.E, 64) || !map3d(&maps.m[2], W3, s.I, s.H, s.E, 64)) return MOK_ERR_CUDA;
-  if (!map2d(&maps.m[3], g.ring, s.I, (uint64_t)S * M, 128) || !map3d(&maps.m[4], W2, s.H, s.I, s.E, 64))
-    return MOK_ERR_CUDA;
+  if (prec == MOK_MXFP8) {
+    // GEMM1 gathers x's E4M3 rows by token; its A scales come tiled by the
+    // placement items, the weights' from the tilings above
+    const mok_mx &q1 = *as_mx(W1), &q3 = *as_mx(W3), &q2 = *as_mx(W2);
+    g.ring_sf = w + L.ring_sf;
+    g.gq_src = w + L.xq;
+    g.sfa_rows = w + L.xsf;
+    g.sfa_ld = s.H / 32;
+    g.sfa_tiled = w + L.sfa_rows_t;
+    g.sfb_tiled0 = w + L.wsf1;  // W1 | W3 interleaved
+    g.sfb_tiled2 = w + L.wsf2;
+    if (!map2d_u8(&maps.m[0], w + L.xq, s.H, s.T, 128, 128) ||  // a valid map for the prefetch
+        !map3d_u8(&maps.m[1], q1.q, s.I, s.H, s.E, 128) || !map3d_u8(&maps.m[2], q3.q, s.I, s.H, s.E, 128) ||
+        !map2d_u8(&maps.m[3], w + L.ring, s.I, (uint64_t)S * M, 128, 128) ||
+        !map3d_u8(&maps.m[4], q2.q, s.H, s.I, s.E, 128))
+      return MOK_ERR_CUDA;
+  } else {
+    if (!map_gather(&maps.m[0], x, s.H, s.T)) return MOK_ERR_CUDA;
+    if (!map3d(&maps.m[1], W1, s.I, s.H, s.E, 64) || !map3d(&maps.m[2], W3, s.I, s.H, s.E, 64)) return MOK_ERR_CUDA;
+    if (!map2d(&maps.m[3], g.ring, s.I, (uint64_t)S * M, 128) || !map3d(&maps.m[4], W2, s.H, s.I, s.E, 64))
+      return MOK_ERR_CUDA;
+  }
   g.nmaps = 5;
   g.bn = bn2;
   g.n_tiles = s.H / bn2;
@@ -959,7 +993,11 @@ mok_status mok_forward_fused(const mok_shape* shape, const mok_config* cfg, void
   g.m_tiles = 2 * (int)L.tile_capacity;  // ring: where the consumed half of the flags starts
   g.counter = 0;
   Phase ph(MOK_PHASE_FWD_FUSED, st, 1);
-  MOK_CUDA(launch_gemm(GM_FWD_FUSED, maps, g, gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles)), st));
+  const int grid = gemm_grid(L.tile_capacity * (g.g1_tiles + g.n_tiles));
+  if (prec == MOK_MXFP8)
+    MOK_CUDA(launch_gemm_mx(GM_FWD_FUSED, maps, g, grid, st));
+  else
+    MOK_CUDA(launch_gemm(GM_FWD_FUSED, maps, g, grid, st));
   return MOK_OK;
 }
 

@@ -530,15 +530,15 @@ __device__ __forceinline__ void tma_loads_mx(const TmapSet& mp, const GemmParams
     // A (gathered x rows): its scales pre-tiled in padded-row order
     bulk_load(sfa, p.sfa_tiled + ((long)it.m * hg + kk) * 512, 512, sfbar);
   } else if (type == GM_FWD2) {
-    const int mslot = (MODE == GM_FWD_RING) ? 3 : 0;
-    const int wmap = (MODE == GM_FWD_RING) ? 4 : 1;
+    const int mslot = is_ring<MODE>() ? 3 : 0;
+    const int wmap = is_ring<MODE>() ? 4 : 1;
     tma_load_2d(a, &mp.m[mslot], bar, kk * 128, ring_row(p, it.rp * kTileRows));
     // a's scales, tiled by the GEMM1 epilogue next to the ring codes
     bulk_load(sfa, p.ring_sf + ((long)(ring_row(p, it.rp * kTileRows) >> 7) * (p.I / 128) + kk) * 512, 512, sfbar);
     for (int c = 0; c < bn / 128; ++c) tma_load_3d(b + c * 16384, &mp.m[wmap], bar, it.n * bn + c * 128, kk * 128, it.e);
     // W2's scales grouped per bn-wide N tile: one load
     const long blk = ((long)it.e * (p.H / bn) + it.n) * (p.I / 128) + kk;
-    bulk_load(sfb, (MODE == GM_FWD_RING ? p.sfb_tiled2 : p.sfb_tiled0) + blk * (bn / 128) * 512, (bn / 128) * 512,
+    bulk_load(sfb, (is_ring<MODE>() ? p.sfb_tiled2 : p.sfb_tiled0) + blk * (bn / 128) * 512, (bn / 128) * 512,
               sfbar);
   } else if (type == GM_BWD_DA) {
     // A: dout's codes in padded-row order, when dA' does not gather them;
@@ -1333,7 +1333,11 @@ __device__ void fused_scan(const GemmParams& p, int* tot, int gt) {
 }
 
 // Places chunk c's rows (one warp; cursor: E ints of shared memory): rows of
-// one expert in increasing f, after the chunk's base.
+// one expert in increasing f, after the chunk's base.  MXFP8: also the row's
+// x scales (token f / k of sfa_rows, H / 32 bytes) into the tiled A-scale
+// layout GEMM1's TMA thread loads, [padded rows / 128][H / 128][512 B]
+// (padding rows keep the zeros the caller cleared them to).
+template <bool MX>
 __device__ void fused_place(const GemmParams& p, int c, int* cursor, int lane) {
   const int E = p.E, R = p.T * p.k;
   for (int e = lane; e < E; e += 32) cursor[e] = p.chunk_base[(size_t)c * E + e];
@@ -1361,12 +1365,21 @@ __device__ void fused_place(const GemmParams& p, int c, int* cursor, int lane) {
         p.s_inv_perm[f] = r;
         p.s_pad_perm[prow] = f;
         p.s_pad_inv[f] = prow;
+        if constexpr (MX) {
+          const uint8_t* src = p.sfa_rows + (long)(f / p.k) * p.sfa_ld;
+          uint8_t* dst = const_cast<uint8_t*>(p.sfa_tiled) + (long)(prow / kTileRows) * (p.H / 128) * 512 +
+                         mx_sf_offset(prow % kTileRows, 0);
+          for (int kg = 0; kg < p.H / 128; ++kg)
+            *reinterpret_cast<uint32_t*>(dst + (long)kg * 512) = *reinterpret_cast<const uint32_t*>(src + kg * 4);
+        }
       } else {
         p.s_inv_perm[f] = -1;
         p.s_pad_inv[f] = -1;
       }
     }
   }
+  // (MXFP8: the tiled scales are read by TMA, the async proxy)
+  if constexpr (MX) fence_proxy_async_global();
   __threadfence();
   __syncwarp();
   if (lane == 0) red_release_gpu_add(hdr_word(p, kHdrPlaceDone), 1u);
@@ -1481,6 +1494,7 @@ __device__ bool fused_combine_phase(const GemmParams& p, Ctl* ctl, uint8_t* stag
 
 // The gather warps' part of a schedule item or of the combine phase
 // (false: a bounded wait gave up).
+template <bool MX>
 __device__ bool fused_aux_gather(const GemmParams& p, Ctl* ctl, uint8_t* stages, const Item& it, int gt,
                                  const WaitCtx& wc) {
   const int lane = gt & 31;
@@ -1501,7 +1515,7 @@ __device__ bool fused_aux_gather(const GemmParams& p, Ctl* ctl, uint8_t* stages,
     if (gt < 32) {
       if (lane == 0) ok = wait_flag_geq(hdr_word(p, kHdrScanDone), 1u, wc);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (ok) fused_place(p, it.m, ctl->po, lane);
+      if (ok) fused_place<MX>(p, it.m, ctl->po, lane);
     }
   } else {
     ok = fused_combine_phase(p, ctl, stages, 6 + (gt >> 5), lane, wc);
@@ -1708,10 +1722,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // the ring's and the combine's items read the whole schedule:
             // acquire the place items' completions before publishing them
             sched_ready = true;
-            if (wait_flag_geq(hdr_word(p, kHdrPlaceDone), (uint32_t)p.nchunks, wc))
+            if (wait_flag_geq(hdr_word(p, kHdrPlaceDone), (uint32_t)p.nchunks, wc)) {
               num_items = fused_total(p);
-            else
+              // (MXFP8: this thread's TMA then reads the place items' tiled scales)
+              if constexpr (MX) fence_proxy_async_global();
+            } else {
               w = -1;
+            }
           }
           if (MODE == GM_FWD_FUSED && w >= num_items && num_items != INT_MAX && !combine_sent) {
             // past the last item: this CTA's combine phase, then the end
@@ -1813,7 +1830,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         bool ok = true;
         if constexpr (MODE == GM_FWD_FUSED) {
           if (it.type >= kItemCount) {
-            if (!fused_aux_gather(p, ctl, sA, it, gt, wc)) break;
+            if (!fused_aux_gather<MX>(p, ctl, sA, it, gt, wc)) break;
             continue;
           }
         }
@@ -2216,6 +2233,7 @@ cudaError_t launch_gemm_mx(int mode, const TmapSet& maps, const GemmParams& p, i
     case GM_WG13: return launch_mode<GM_WG13, true>(maps, p, grid, st);
     case GM_WG2: return launch_mode<GM_WG2, true>(maps, p, grid, st);
     case GM_FWD_RING: return launch_mode<GM_FWD_RING, true>(maps, p, grid, st);
+    case GM_FWD_FUSED: return launch_mode<GM_FWD_FUSED, true>(maps, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -72,11 +72,12 @@ class MoKLayer:
         return out
 
     def forward_fused(self, topk_idx, x, scores, W1, W3, W2, out=None, stream=None):
-        """Schedule and forward in one launch (BF16); backward may follow."""
+        """Schedule and forward in one launch (MXFP8: the routing-independent
+        quantisation and scale tiling ahead of it); backward may follow."""
         if out is None:
             out = torch.empty((self.shape.T, self.shape.H), dtype=torch.bfloat16, device=self.device)
-        _lib.mok_forward_fused(self.cshape, self.cfg, self.ws, topk_idx, x, scores, W1, W3, W2, out, self.ctx,
-                               stream)
+        _lib.mok_forward_fused(self.cshape, self.cfg, self.prec, self.ws, topk_idx, x, scores, W1, W3, W2, out,
+                               self.ctx, stream)
         return out
 
     def backward(self, x, scores, W1, W3, W2, dout, grads=None, stream=None):

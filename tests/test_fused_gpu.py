@@ -120,3 +120,50 @@ def test_fused_forward_full_size_dsv3():
         del layer
     assert torch.equal(outs[0], outs[1])
     assert not torch.isnan(outs[0].float()).any()
+
+
+def run_mx(shape, routing, seed, fused, inp=None, **kw):
+    from mixture_experts_layer_side_gb300.inputs import Shape, make_inputs
+    from mixture_experts_layer_side_gb300.layer import MoKLayer
+    S = Shape(*shape)
+    if inp is None:
+        inp = {k: v.cuda() for k, v in make_inputs(S, routing, seed=seed, device="cpu").items()}
+    layer = MoKLayer(S, precision="mxfp8", **kw)
+    wq = layer.quantize_weights(inp["W1"], inp["W3"], inp["W2"])
+    layer.ws.fill_(0x55)
+    layer.ctx.fill_(0x55)
+    out = torch.full((S.T, S.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    if fused:
+        layer.forward_fused(inp["idx"], inp["x"], inp["s"], *wq["fwd"], out=out)
+    else:
+        layer.build_schedule(inp["idx"])
+        layer.forward(inp["x"], inp["s"], *wq["fwd"], out=out)
+    layer.check()
+    sched = {n: a.clone() for n, a in layer.schedule_arrays().items()}
+    ctx = layer.ctx.clone()
+    # (the bounded-memory backward also takes W1 / W3 in the forward orientation)
+    grads = layer.backward(inp["x"], inp["s"], *wq["bwd_replay" if kw.get("replay") else "bwd"], inp["dout"])
+    layer.check()
+    return inp, out, sched, ctx, grads
+
+
+@pytest.mark.parametrize("shape,routing,kw", CASES)
+def test_mxfp8_fused_forward_is_bitwise_the_separate_launches(shape, routing, kw):
+    """MXFP8: the placement items tile the placed rows' x scales for GEMM1
+    and the ring gathers x's E4M3 rows by token; the separate launches read
+    a token-sorted code copy and a scale tiling kernel's output.  Same
+    schedule arrays, out, context and backward, bit for bit."""
+    require_gpu()
+    inp, out_f, sch_f, ctx_f, g_f = run_mx(shape, routing, 71, True, **kw)
+    _, out_s, sch_s, ctx_s, g_s = run_mx(shape, routing, 71, False, inp=inp, **kw)
+    for name in ("counts", "offsets", "padded_offsets", "perm", "inv_perm", "pad_inv"):
+        assert torch.equal(sch_f[name], sch_s[name]), name
+    used = int(sch_s["padded_offsets"][-1])
+    assert torch.equal(sch_f["pad_perm"][:used], sch_s["pad_perm"][:used])
+    assert torch.equal(out_f, out_s)
+    assert not torch.isnan(out_f.float()).any()
+    if not kw.get("replay"):
+        row_bytes = 2 * shape[2] * 2
+        assert torch.equal(ctx_f[:used * row_bytes], ctx_s[:used * row_bytes])
+    for k in g_s:
+        assert torch.equal(g_f[k], g_s[k]), k

@@ -81,12 +81,17 @@ def test_host_argument_checks(lib):
     # the single-launch forward: null pointers, workspace too small, bad
     # config, unsupported shape
     F = L.mok_forward_fused
-    assert F(S, C, None, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, None) == 1
-    assert F(S, C, fake, 1 << 30, None, fake, fake, fake, fake, fake, fake, fake, None) == 1
-    assert F(S, C, fake, 16, fake, fake, fake, fake, fake, fake, fake, fake, None) == 3
-    assert F(S, ctypes.byref(bad), fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, None) == 1
+    assert F(S, C, 0, None, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, None) == 1
+    assert F(S, C, 0, fake, 1 << 30, None, fake, fake, fake, fake, fake, fake, fake, None) == 1
+    assert F(S, C, 0, fake, 16, fake, fake, fake, fake, fake, fake, fake, fake, None) == 3
+    assert F(S, ctypes.byref(bad), 0, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, None) == 1
     odd = lib.shape_of(256, 100, 128, 8, 2)
-    assert F(ctypes.byref(odd), C, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, None) == 2
+    assert F(ctypes.byref(odd), C, 0, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, None) == 2
+    # an unknown precision; MXFP8 weights whose descriptors hold null pointers
+    assert F(S, C, 7, fake, 1 << 30, fake, fake, fake, fake, fake, fake, fake, fake, None) == 1
+    null_mx = lib.MokMx()
+    px = ctypes.cast(ctypes.pointer(null_mx), ctypes.c_void_p)
+    assert F(S, C, 1, fake, 1 << 30, fake, fake, fake, px, px, px, fake, fake, None) == 1
     assert L.mok_mxfp8_quantize(fake, 1, 48, 64, 0, fake, fake, None) == 2
     assert L.mok_mxfp8_quantize(fake, 1, 64, 48, 1, fake, fake, None) == 2
     # dense GEMM diagnostic: unsupported sizes
