@@ -723,20 +723,27 @@ static_assert(256 + kStages * 16 <= kParkCol && kParkCol + 192 <= 512, "parked c
 // only then is a formed, quantised and stored: the same values, with the
 // next tile's main loop already running.
 template <typename Release>
+// With split epilogues (hm 1 / 2: two warps per lane quarter, each taking
+// half of the row) the first warp takes h and u columns 0..63 (c = 0, 1),
+// the second 64..127 (c = 2, 3), which it parks without the staging
+// buffer; hm 0: one warp takes the whole row.
 __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase, int row, int lane, uint8_t* stage,
-                            Release&& release) {
+                            Release&& release, int hm = 0) {
   const long prow = (long)it.row0 + row;
   const int i0 = it.n * 128;
   const long crow = p.ctx_ring ? (long)ring_row(p, (int)prow) : prow;
+  const bool lo = hm != 2, hi = hm != 1;  // this warp's halves
   // packed bf16 words parked from kParkCol: h 64..127 at +0, u 0..127 at +32
   const uint32_t park = tbase + kParkCol;
-  {
+  if (lo) {
     uint32_t hw0[32];
     acc_load64_bf16(tbase, hw0);
     park64(stage, lane, hw0);
   }
 #pragma unroll 1
   for (int g = 1; g < 4; ++g) {
+    // g = 1: h 64..127, g = 2: u 0..63, g = 3: u 64..127
+    if (g == 2 ? !lo : !hi) continue;
     uint32_t w[32];
     acc_load64_bf16(tbase + 64 * g, w);
     tmem_st32(park + 32 * (g - 1), w);
@@ -755,6 +762,7 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
   uint32_t scales = 0;
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
+    if (c < 2 ? !lo : !hi) continue;
     // 32 columns = 16 packed words each of h and u
     uint32_t h[16], u[16];
     tmem_ld16_issue(park + 32 + 16 * c, u);
@@ -802,27 +810,36 @@ __device__ void epi_fwd1_mx(const GemmParams& p, const Item& it, uint32_t tbase,
     d[0] = make_uint4(q[0], q[1], q[2], q[3]);
     d[1] = make_uint4(q[4], q[5], q[6], q[7]);
   }
-  *sword = scales;
+  if (hm == 0)
+    *sword = scales;
+  else if (hm == 1)
+    reinterpret_cast<uint16_t*>(sword)[0] = (uint16_t)scales;
+  else
+    reinterpret_cast<uint16_t*>(sword)[1] = (uint16_t)(scales >> 16);
 }
 
 // MXFP8 scatter (single-buffered accumulator): the whole row is read as
 // packed bf16 first (columns 0..63 parked in the staging buffer, the rest
 // in parked TMEM columns), the accumulator handed back, then the row
 // stored (padding rows load with the warp, store nothing).
+// (hm 1 / 2: the first or the second half of the row's 64-column groups,
+// the staged group 0 in the first; hm 0: the whole row)
 template <int BN, typename Release>
 __device__ void epi_scatter_mx_n(const GemmParams& p, const Item& it, uint32_t tbase, int row, int lane,
-                                 uint8_t* stage, Release&& release) {
+                                 uint8_t* stage, Release&& release, int hm) {
   constexpr int bn = BN;
+  constexpr int kG = bn / 64;
+  const int g0 = hm == 2 ? kG / 2 : 0, g1 = hm == 1 ? kG / 2 : kG;
   const int prow = it.row0 + row;
   const int f = p.pad_perm[prow];
   const uint32_t park = tbase + kParkCol;
-  {
+  if (g0 == 0) {
     uint32_t w0[32];
     acc_load64_bf16(tbase, w0);
     park64(stage, lane, w0);
   }
 #pragma unroll 1
-  for (int g = 1; g < bn / 64; ++g) {
+  for (int g = g0 > 1 ? g0 : 1; g < g1; ++g) {
     uint32_t w[32];
     acc_load64_bf16(tbase + 64 * g, w);
     tmem_st32(park + 32 * (g - 1), w);
@@ -830,13 +847,13 @@ __device__ void epi_scatter_mx_n(const GemmParams& p, const Item& it, uint32_t t
   tmem_wait_st();
   release();
   __nv_bfloat16* dst = p.yk + (long)(f < 0 ? 0 : f) * p.H + it.n * bn;
-  if (f >= 0) {
+  if (f >= 0 && g0 == 0) {
     uint4* d0 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int i = 0; i < 8; ++i) d0[i] = unpark16(stage, lane, i);
   }
 #pragma unroll 1
-  for (int g = 1; g < bn / 64; ++g) {
+  for (int g = g0 > 1 ? g0 : 1; g < g1; ++g) {
     uint32_t w[32];
     tmem_ld32_issue(park + 32 * (g - 1), w);
     tmem_wait_ld();
@@ -851,11 +868,11 @@ __device__ void epi_scatter_mx_n(const GemmParams& p, const Item& it, uint32_t t
 
 template <typename Release>
 __device__ void epi_scatter_mx(const GemmParams& p, const Item& it, uint32_t tbase, int row, int bn, int lane,
-                               uint8_t* stage, Release&& release) {
+                               uint8_t* stage, Release&& release, int hm = 0) {
   if (bn == 256)
-    epi_scatter_mx_n<256>(p, it, tbase, row, lane, stage, release);
+    epi_scatter_mx_n<256>(p, it, tbase, row, lane, stage, release, hm);
   else
-    epi_scatter_mx_n<128>(p, it, tbase, row, lane, stage, release);
+    epi_scatter_mx_n<128>(p, it, tbase, row, lane, stage, release, hm);
 }
 
 // Scatter a tile row to token order: row f of dst (skipped for padding rows;
@@ -1569,10 +1586,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // in the MMA thread: with the hand-off their k-steps were slower (Kimi-
   // shaped dA' 2.67 against 2.47 ms, dX 3.63 against 3.51).
   const bool sf_writer = MX && MODE == GM_DENSE && !gather_in_pipe;
+  // MXFP8 ring and dX launches whose gather warps copy nothing split each
+  // tile's epilogue: warps 2-5 take the first half of every row's columns,
+  // warps 6-9 (the same lane quarters) the second, so the single
+  // accumulator goes back to the MMA thread in about half the time.
+  const bool epi_split = MX && !PAIR && !gather_in_pipe && !sf_writer && (MODE == GM_FWD_RING || MODE == GM_BWD_DX);
+  // epilogue warps per tile (each ring GEMM1 tile's warps publish its rows)
+  const uint32_t epi_warps = epi_split ? 8u : 4u;
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
   // by the other CTA's TMA producer and epilogue warps (pair launches have
   // no gathered operand)
-  const uint32_t queue_consumers = PAIR ? 10u : (gather_in_pipe || sf_writer) ? 9u : 5u;
+  const uint32_t queue_consumers = PAIR ? 10u : (gather_in_pipe || sf_writer || epi_split) ? 9u : 5u;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   if (p.pdl_trigger) griddep_launch_dependents();
   if constexpr (MODE == GM_FWD_RING && !PAIR) {
@@ -1598,7 +1622,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->tfull[i], 1);
       // the epilogue warps that read the accumulator (both CTAs of a pair)
-      mbar_init(&ctl->tempty[i], PAIR ? 8u : 4u);
+      mbar_init(&ctl->tempty[i], PAIR ? 8u : epi_warps);
     }
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(&ctl->qfull[i], 1);
@@ -1678,7 +1702,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           if (is_ring<MODE>() && it.type == GM_FWD2) {
             // this CTA loads the ring rows of its own tile: acquire their
             // GEMM1 completion itself, then order the async-proxy loads after it
-            ok = wait_flag_geq(&p.ring_flags[it.rp], 4u * (uint32_t)p.g1_tiles, wc);
+            ok = wait_flag_geq(&p.ring_flags[it.rp], epi_warps * (uint32_t)p.g1_tiles, wc);
             fence_proxy_async_global();
             if (!ok) break;
           }
@@ -1762,7 +1786,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // GEMM2 of a tile reads the ring rows GEMM1 wrote: wait until all
             // of its GEMM1 column tiles are published, then order the
             // async-proxy loads after the acquire
-            ok = wait_flag_geq(&p.ring_flags[it.rp], 4u * (uint32_t)p.g1_tiles, wc);
+            ok = wait_flag_geq(&p.ring_flags[it.rp], epi_warps * (uint32_t)p.g1_tiles, wc);
             fence_proxy_async_global();
             if (!ok) break;
           }
@@ -1814,7 +1838,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // lanes 1-31 skipped the producer loop: the warp reaches the final
     // barrier converged
     __syncwarp();
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && !epi_split) {
     // ---------------------------------------------------------------- gather producers
     if (gather_in_pipe) {
       const int gt = threadIdx.x - 192;
@@ -1984,7 +2008,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // ---------------------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    uint8_t* stage_out = sOut + (warp - 2) * kOutStage;
+    // split epilogues: warps 2-5 the first half of each row (hm 1), warps
+    // 6-9 the second (hm 2, no staging buffer); otherwise the whole row (0)
+    const int hm = epi_split ? (warp >= 6 ? 2 : 1) : 0;
+    uint8_t* stage_out = warp < 6 ? sOut + (warp - 2) * kOutStage : nullptr;
     uint32_t qs = 0, qp = 0, tcount = 0;
     while (true) {
       if (!(PAIR ? mbar_wait_cluster(&ctl->qfull[qs], qp, wc) : mbar_wait(&ctl->qfull[qs], qp, wc))) break;
@@ -2049,12 +2076,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         case -1: break;
         case GM_DENSE: epi_dense(p, it, tbase, row); break;
         case GM_FWD1:
-          if constexpr (MX) epi_fwd1_mx(p, it, tbase, row, lane, stage_out, release_acc);
+          if constexpr (MX) epi_fwd1_mx(p, it, tbase, row, lane, stage_out, release_acc, hm);
           else epi_fwd1(p, it, tbase, row);
           break;
         case GM_FWD2:
         case GM_BWD_DX:
-          if constexpr (MX) epi_scatter_mx(p, it, tbase, row, p.bn, lane, stage_out, release_acc);
+          if constexpr (MX) epi_scatter_mx(p, it, tbase, row, p.bn, lane, stage_out, release_acc, hm);
           else epi_scatter(p, it, tbase, row, p.bn);
           break;
         case GM_BWD_DA: epi_bwd_da<MX>(p, it, tbase, row, release_acc); break;
@@ -2073,7 +2100,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if (is_ring<MODE>() && it.type == GM_FWD1 && !it.idle) {
         // publish this warp's 32 ring rows of the tile to GEMM2 (another CTA,
         // read by TMA): each epilogue warp adds 1, so a tile is complete when
-        // its counter reaches 4 * (GEMM1 column tiles)
+        // its counter reaches (epilogue warps per tile) * (GEMM1 column tiles)
         fence_proxy_async_global();
         __syncwarp();
         if (lane == 0) {
