@@ -1586,11 +1586,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   // in the MMA thread: with the hand-off their k-steps were slower (Kimi-
   // shaped dA' 2.67 against 2.47 ms, dX 3.63 against 3.51).
   const bool sf_writer = MX && MODE == GM_DENSE && !gather_in_pipe;
-  // MXFP8 ring and dX launches whose gather warps copy nothing split each
-  // tile's epilogue: warps 2-5 take the first half of every row's columns,
-  // warps 6-9 (the same lane quarters) the second, so the single
-  // accumulator goes back to the MMA thread in about half the time.
-  const bool epi_split = MX && !PAIR && !gather_in_pipe && !sf_writer && (MODE == GM_FWD_RING || MODE == GM_BWD_DX);
+  // MXFP8 ring launches whose gather warps copy nothing split each tile's
+  // epilogue: warps 2-5 take the first half of every row's columns, warps
+  // 6-9 (the same lane quarters) the second, so the single accumulator goes
+  // back to the MMA thread in about half the time.  (dX's long K loop hides
+  // its light epilogue already; dA''s, bound by its global loads and stores,
+  // measured slower split.)
+  const bool epi_split = MX && !PAIR && !gather_in_pipe && !sf_writer && MODE == GM_FWD_RING;
   // epilogue warps per tile (each ring GEMM1 tile's warps publish its rows)
   const uint32_t epi_warps = epi_split ? 8u : 4u;
   // CTA pairs: the leader's queue is read by its MMA and epilogue warps and
