@@ -904,17 +904,23 @@ __device__ void epi_scatter(const GemmParams& p, const Item& it, uint32_t tbase,
 // accumulator back, and takes the rest from the parked copy while the next
 // tile's main loop runs.  The values are the same f32 bits either way.
 
+// MXFP8 dA': the accumulator goes back to the MMA thread once this many
+// columns are worked through (the rest parked in TMEM first).  Earlier
+// hand-backs measured slower: the epilogue's loads and stores beside the
+// next tile's MMAs slow those more than the accumulator wait costs.
+constexpr int kDaHandBack = 64;
+
 template <bool MX, typename Release>
 __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, int row, Release&& release) {
   const uint32_t park = tbase + kParkCol;  // MXFP8: single accumulator at column 0
   if constexpr (MX) {
 #pragma unroll 1
-    for (int c = 64; c < p.bn; c += 32) {
+    for (int c = kDaHandBack; c < p.bn; c += 32) {
       uint32_t r[32];
       tmem_ld32_issue(tbase + c, r);
       tmem_wait_ld();
       tmem_regs_ready(r);
-      tmem_st32(park + (c - 64), r);
+      tmem_st32(park + (c - kDaHandBack), r);
     }
     tmem_wait_st();
   }
@@ -953,8 +959,9 @@ __device__ void epi_bwd_da(const GemmParams& p, const Item& it, uint32_t tbase, 
       }
     }
     float g[32];
-    tmem_ld32((MX && c >= 64) ? park + (c - 64) : tbase + c, g);
-    if (MX && c == 32) release();  // columns [0, 64) are read: the rest is parked
+    tmem_ld32((MX && c >= kDaHandBack) ? park + (c - kDaHandBack) : tbase + c, g);
+    // columns [0, kDaHandBack) are read: the rest is parked
+    if (MX && c == kDaHandBack - 32) release();
     uint32_t dhw[16], duw[16], asw[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
