@@ -18,7 +18,11 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, then the fused
 //               per-mode work (SwiGLU, scatter to token order, SwiGLU
 //               backward with the router-score partial sums, weight-gradient
-//               stores).
+//               stores).  MXFP8 has one accumulator: its epilogues park what
+//               they still need in free TMEM columns and hand it back early;
+//               in the MXFP8 ring the otherwise idle warps 6..9 take half of
+//               each tile row.  In the dense MXFP8 core warps 6..9 move the
+//               stage scales into TMEM instead (tcgen05.st).
 // Weight-gradient launches read token-sorted operands with plain TMA (the
 // gather warps write the empty experts' zero gradients instead) and come in
 // two forms: single CTAs, and clusters of two CTAs sharing a 256 x 256 tile
@@ -52,8 +56,8 @@ namespace {
 struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t sfready[kMaxStages];  // MXFP8: the stage's scales are in TMEM (written by the gather warps)
-  uint64_t sffull[kMaxStages];   // MXFP8 with the scale writer: the stage's scale blocks are in smem
+  uint64_t sfready[kMaxStages];  // dense MXFP8 core: the stage's scales are in TMEM (written by the gather warps)
+  uint64_t sffull[kMaxStages];   // dense MXFP8 core: the stage's scale blocks are in smem
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t qfull[kQueue];
