@@ -167,3 +167,29 @@ def test_mxfp8_fused_forward_is_bitwise_the_separate_launches(shape, routing, kw
         assert torch.equal(ctx_f[:used * row_bytes], ctx_s[:used * row_bytes])
     for k in g_s:
         assert torch.equal(g_f[k], g_s[k]), k
+
+
+def test_mxfp8_fused_forward_full_size_kimi():
+    """Kimi-K2 shape in MXFP8: the single launch bitwise equal to the
+    separate launches (out and context)."""
+    require_gpu()
+    from mixture_experts_layer_side_gb300.inputs import WORKLOADS, make_inputs
+    from mixture_experts_layer_side_gb300.layer import MoKLayer
+    shape, routing, _ = WORKLOADS["kimi_mxfp8"]
+    inp = make_inputs(shape, routing, seed=1001, device="cuda")
+    res = []
+    for fused in (True, False):
+        layer = MoKLayer(shape, precision="mxfp8")
+        wq = layer.quantize_weights(inp["W1"], inp["W3"], inp["W2"])
+        if fused:
+            out = layer.forward_fused(inp["idx"], inp["x"], inp["s"], *wq["fwd"])
+        else:
+            layer.build_schedule(inp["idx"])
+            out = layer.forward(inp["x"], inp["s"], *wq["fwd"])
+        layer.check()
+        used = int(layer.schedule_arrays()["padded_offsets"][-1])
+        res.append((out, layer.ctx[:used * 2 * shape.I * 2].clone()))
+        del layer, wq
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][1], res[1][1])
+    assert not torch.isnan(res[0][0].float()).any()
