@@ -699,17 +699,6 @@ __device__ __forceinline__ uint4 unpark16(const uint8_t* stage, int lane, int i)
   return *reinterpret_cast<const uint4*>(stage + lane * 128 + ((i ^ (lane & 7)) << 4));
 }
 
-// 32 accumulator columns as 16 packed bf16 pairs (half the registers of
-// acc_load64_bf16 in flight).
-__device__ __forceinline__ void acc_load32_bf16(uint32_t taddr, uint32_t* w16) {
-  uint32_t r[32];
-  tmem_ld32_issue(taddr, r);
-  tmem_wait_ld();
-  tmem_regs_ready(r);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) w16[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
