@@ -75,6 +75,8 @@ CASES = [
     ("tiny", (256, 256, 128, 8, 2), "uniform", 1),
     ("ragged_zipf", (300, 256, 256, 6, 3), "zipf", 2),
     ("hot_empty", (512, 384, 128, 24, 4), "hot", 3),
+    # no expert empty and H = 384 (128-column dW2 tiles)
+    ("uniform_h384", (512, 384, 128, 6, 2), "uniform", 4),
     # degenerate and limit cases: one token and one expert; the largest
     # expert count (most experts empty); the largest top-k; every token on
     # one expert (top-1, one long weight-gradient K loop, seven empty experts)
